@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache decode hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch: host allocator work
+(block tables, slots, copy-on-write decisions), the ``pkv_write`` of the new
+tokens' keys and values, any ``pkv_block_copy``, and ``paged_attention_decode``
+(with its cross-partition combine), for every layer of the workload.
+
+Headline: the batched GQA decode workload (32 sequences, L ~ U{1..4096}, block
+16, 32 query / 8 KV heads, head dim 128, bf16).  Metric: KV-cache GB/s read
+(valid K and V rows) per step; query tokens/s alongside.  The other workloads
+are reported under "workloads".
+
+``--impl reference`` times the fp64 CPU oracle on the same workload instead.
+Multi-GPU (torchrun): every rank runs its own independent replica (weak
+scaling, no data-path collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = 2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ helpers
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(workload_tag):
+    """DRAM bytes per decode launch from the committed ncu summary, only if the
+    kernel source is unchanged since that capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    src = os.path.join(ROOT, "paged_kv_cache_276_gb300", "csrc", "decode.cu")
+    try:
+        rec = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("source_sha256") != sha:
+            return None
+        key = f"dram_bytes_per_launch[{workload_tag}]"
+        return float(rec[key]) if key in rec else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id():
+    """nvidia-smi identifier of the current CUDA device (UUID when torch exposes it)."""
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v for v in vis.split(",") if v.strip()]
+    return ids[torch.cuda.current_device()] if ids else str(torch.cuda.current_device())
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- our arm
+class Runner:
+    """Plans steps, times them on the device and end to end."""
+
+    def __init__(self, wnum, device, rank, block_size=None, q_len=None, steps_needed=8):
+        import torch
+        from paged_kv_cache_276_gb300 import inputs
+        from paged_kv_cache_276_gb300.workloads import DecodeSession
+        self.torch = torch
+        w = inputs.WORKLOADS[wnum]
+        self.w = w
+        # weak scaling: every rank owns an independent batch of the same shape
+        self.sess = DecodeSession(w, device, block_size=block_size, q_len=q_len, extra_steps=steps_needed + 2,
+                                  seed_salt=rank)
+        self.sess.apply_setup_copies()
+        self.device = device
+        self.rank = rank
+
+    def plan(self, n):
+        steps = self.sess.plan_steps(n)
+        toks = self.sess.new_token_tensors(n, seed=self.w.seed + 17 * self.rank)
+        return steps, toks
+
+    def time_device(self, warmup, steps, world):
+        """Per-step CUDA-event times with an L2 flush before every step (outside
+        the events); decode launches timed separately for the roofline."""
+        torch = self.torch
+        from paged_kv_cache_276_gb300 import native
+        sess = self.sess
+        plans, toks = self.plan(warmup + steps)
+        max_len = max(p.max_len for p in plans)
+        ws = sess.workspace(max_len)
+        out = torch.empty_like(toks[0][0])
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=self.device)
+        stream = torch.cuda.current_stream()
+        status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        step_ms, dec_ms = [], []
+        launches = 0
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_id()) as clocks:
+            for i in range(warmup + steps):
+                p = plans[i]
+                q, ks, vs = toks[i]
+                flush.fill_(float(i))
+                s0, s1 = ev(), ev()
+                dec = []
+                s0.record(stream)
+                for l in range(sess.layers):
+                    if p.cow_pairs is not None:
+                        native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
+                        launches += i >= warmup
+                    native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
+                    d0, d1 = ev(), ev()
+                    d0.record(stream)
+                    native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
+                                                  p.max_len, sess.scale, out, ws, sess.partition_size, status,
+                                                  stream)
+                    d1.record(stream)
+                    dec.append((d0, d1))
+                    nparts = math.ceil(p.max_len / sess.partition_size) if p.max_len else 1
+                    launches += (i >= warmup) * (2 + (nparts > 1))
+                s1.record(stream)
+                if i >= warmup:
+                    step_ms.append((s0, s1))
+                    dec_ms.extend(dec)
+            torch.cuda.synchronize()
+        barrier(world)
+        if status.item() != 0:
+            raise RuntimeError(f"device status {status.item()} during the benchmark")
+        step_t = [a.elapsed_time(b) for a, b in step_ms]
+        dec_t = [a.elapsed_time(b) for a, b in dec_ms]
+        timed = plans[warmup:]
+        kv_bytes = [sess.kv_bytes(p) for p in timed]
+        return {
+            "ms_per_step": sum(step_t) / len(step_t),
+            "step_ms_p10": float(np.percentile(step_t, 10)), "step_ms_p90": float(np.percentile(step_t, 90)),
+            "decode_ms_avg": sum(dec_t) / len(dec_t),
+            "kv_bytes_per_step": sum(kv_bytes) / len(kv_bytes),
+            "kv_bytes_per_decode": sum(kv_bytes) / len(kv_bytes) / sess.layers,
+            "query_tokens_per_step": sess.B * sess.q_len,
+            "launches": launches,
+            "clocks": clocks.summary(),
+        }
+
+    def time_e2e(self, steps):
+        """Same metric through the public API with host buffers: allocator work,
+        pinned host -> device copies of the step inputs, the kernels, and the
+        device -> host read of the outputs, all inside the timed region."""
+        torch = self.torch
+        from paged_kv_cache_276_gb300 import native
+        sess = self.sess
+        toks = sess.new_token_tensors(1, seed=self.w.seed + 5)
+        q_h = toks[0][0].cpu().pin_memory()
+        k_h = [t.cpu().pin_memory() for t in toks[0][1]]
+        v_h = [t.cpu().pin_memory() for t in toks[0][2]]
+        q_d = torch.empty_like(toks[0][0])
+        k_d = [torch.empty_like(t) for t in toks[0][1]]
+        v_d = [torch.empty_like(t) for t in toks[0][2]]
+        out_d = torch.empty_like(q_d)
+        out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+        ws = sess.workspace(int(sess.alloc.block_table(range(sess.B), sess.max_blocks)[1].max()) + steps + 8)
+        stream = torch.cuda.current_stream()
+        times, kv, h2d = [], [], 0
+        for i in range(steps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            # host allocator work of the step (public API), then the uploads
+            slots = np.empty(sess.B * sess.q_len, dtype=np.int64)
+            for s in range(sess.B):
+                slots[s * sess.q_len:(s + 1) * sess.q_len] = sess.alloc.seq_append(s, sess.q_len)
+            tables, lens = sess.alloc.block_table(range(sess.B), sess.max_blocks)
+            slots_h = torch.from_numpy(slots).pin_memory()
+            tables_h = torch.from_numpy(tables).pin_memory()
+            lens_h = torch.from_numpy(lens).pin_memory()
+            slots_d = slots_h.to(self.device, non_blocking=True)
+            tables_d = tables_h.to(self.device, non_blocking=True)
+            lens_d = lens_h.to(self.device, non_blocking=True)
+            q_d.copy_(q_h, non_blocking=True)
+            for l in range(sess.layers):
+                k_d[l].copy_(k_h[l], non_blocking=True)
+                v_d[l].copy_(v_h[l], non_blocking=True)
+            max_len = int(lens.max())
+            for l in range(sess.layers):
+                native.pkv_write(k_d[l], v_d[l], slots_d, sess.k_caches[l], sess.v_caches[l], None, stream)
+                native.paged_attention_decode(q_d, sess.k_caches[l], sess.v_caches[l], tables_d, lens_d, max_len,
+                                              sess.scale, out_d, ws, sess.partition_size, None, stream)
+            out_h.copy_(out_d, non_blocking=True)
+            torch.cuda.synchronize()
+            t1 = time.perf_counter()
+            if i:  # the first pass warms the pinned-memory paths
+                times.append((t1 - t0) * 1e3)
+                kv.append(int(lens.astype(np.int64).sum()) * 2 * sess.Hkv * sess.d * 2 * sess.layers)
+                h2d = (slots_h.numel() * 8 + tables_h.numel() * 4 + lens_h.numel() * 4 + q_h.numel() * 2
+                       + sum(t.numel() * 2 for t in k_h) + sum(t.numel() * 2 for t in v_h))
+        ms = sum(times) / len(times)
+        return {"ms_per_step": ms, "kv_bytes_per_step": sum(kv) / len(kv), "h2d": h2d,
+                "d2h": out_h.numel() * 2}
+
+
+def cpu_oracle_baseline(wnum, budget_s=12.0, reps=None, warmup=0):
+    """The fp64 oracle as it stands, on this host's cores: whole decode steps of
+    the workload (all sequences), repeated ``reps`` times or until ~budget_s
+    seconds have passed."""
+    from oracle import attention as OA
+    from paged_kv_cache_276_gb300 import inputs
+    w = inputs.WORKLOADS[wnum]
+    rng = inputs.rng_for(w)
+    lens = inputs.lengths(w, rng)
+    NB = inputs.pool_size(lens, w.block_size, 0.10)
+    tables, _ = inputs.permuted_tables(lens, w.block_size, NB, rng)
+    shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
+    kb = OA.as_bf16_bits(inputs.randn_bf16(shape, w.seed + 1))
+    vb = OA.as_bf16_bits(inputs.randn_bf16(shape, w.seed + 2))
+    qb = OA.as_bf16_bits(inputs.randn_bf16((len(lens), 1, w.num_q_heads, w.head_dim), w.seed + 3))
+    cores = OA.set_threads(os.cpu_count() or 1)
+
+    def one():
+        OA.paged_attention(qb, kb, vb, tables, lens, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                           head_dim=w.head_dim, block_size=w.block_size, scale=w.scale)
+
+    for _ in range(warmup):
+        one()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        one()
+        n += 1
+        el = time.perf_counter() - t0
+        if (reps is not None and n >= reps) or (reps is None and el >= budget_s):
+            break
+    kv = int(lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    return {"value": kv * n / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole decode steps of the workload ({len(lens)} sequences, {int(lens.sum())} tokens) "
+                      f"in {el:.1f} s, fp64, OpenMP over (sequence, KV head)",
+            "seconds": el, "reps": n, "query_tok_s": len(lens) * n / el}
+
+
+def workload_desc(wnum, bs=None, q_len=None):
+    from paged_kv_cache_276_gb300 import inputs
+    w = inputs.WORKLOADS[wnum]
+    bs = bs or w.block_size
+    q_len = q_len or w.q_len
+    lens = {1: "L=[17,33,64]", 2: "L~U{1..4096}", 3: "L=lognormal(median 512, sigma 1) clip [1,8192]",
+            4: "2048 shared prefix + U{0..512} suffix", 5: "L=32768"}[wnum]
+    return (f"{w.name}: {w.num_seqs} seqs, {lens}, block {bs}, {w.num_q_heads}q/{w.num_kv_heads}kv heads, "
+            f"d {w.head_dim}, {w.layers} layer(s), q_len {q_len}, bf16")
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from paged_kv_cache_276_gb300 import build
+    build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peak, peak_kind = measured_hbm_peak()
+
+    r = Runner(HEADLINE, device, rank, steps_needed=args.warmup + args.steps + 16)
+    dev_res = r.time_device(args.warmup, args.steps, world)
+    ms = max_over_ranks(dev_res["ms_per_step"], world)
+    total_bytes = dev_res["kv_bytes_per_step"] * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    e2e = r.time_e2e(max(3, min(args.steps, 10)))
+    e2e_ms = max_over_ranks(e2e["ms_per_step"], world)
+    e2e_value = e2e["kv_bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9
+    dec_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["decode_ms_avg"] * 1e-3) / 1e9
+    traffic = kernel_traffic("batched_gqa")
+    line = {
+        "metric": "paged decode attention KV-cache read bandwidth (valid K+V bytes / step time)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V/Q, seeded lengths and block placement)",
+        "config": {"workload": workload_desc(HEADLINE), "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "flushed before every step (write of 2x L2), outside the per-step CUDA events",
+                   "kv_bytes_per_step": int(dev_res["kv_bytes_per_step"]),
+                   "query_tokens_per_step": dev_res["query_tokens_per_step"],
+                   "step": "host allocator (precomputed) + pkv_write + paged_attention_decode (+combine)"},
+        "query_tok_s": round(dev_res["query_tokens_per_step"] * world / (ms * 1e-3), 1),
+        "step_ms_p10": round(dev_res["step_ms_p10"], 5), "step_ms_p90": round(dev_res["step_ms_p90"], 5),
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": "paged_attention_decode (decode_kernel + combine_kernel)",
+                     "kernel_ms_avg": round(dev_res["decode_ms_avg"], 5),
+                     "algorithmic_bytes_per_launch": int(dev_res["kv_bytes_per_decode"]),
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": dev_res["launches"],
+        "clocks": dev_res["clocks"],
+    }
+    if not args.no_workloads:
+        line["workloads"] = other_workloads(args, device, rank, world, peak)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_oracle_baseline(HEADLINE, budget_s=args.cpu_seconds)
+            line["cpu_baseline"]["value"] = round(line["cpu_baseline"]["value"], 4)
+        except Exception as e:  # reported, never fatal
+            line["cpu_baseline"] = {"error": repr(e)}
+    return line
+
+
+def other_workloads(args, device, rank, world, peak):
+    res = {}
+    cases = [(1, None, None), (3, None, None), (4, None, None), (5, 16, None), (5, 32, None), (5, 16, 16),
+             (5, 32, 16)]
+    for wnum, bs, q_len in cases:
+        tag = f"w{wnum}" + (f"_bs{bs}" if bs else "") + (f"_q{q_len}" if q_len else "")
+        try:
+            steps = 5 if wnum == 3 else 10
+            r = Runner(wnum, device, rank, block_size=bs, q_len=q_len, steps_needed=steps + 3)
+            d = r.time_device(3, steps, world)
+            ms = max_over_ranks(d["ms_per_step"], world)
+            dec = d["kv_bytes_per_decode"] / (d["decode_ms_avg"] * 1e-3) / 1e9
+            res[tag] = {"workload": workload_desc(wnum, bs, q_len), "ms_per_step": round(ms, 5),
+                        "kv_gbs_step": round(d["kv_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1),
+                        "decode_kernel_gbs": round(dec, 1), "decode_frac_of_peak": round(dec / peak, 4),
+                        "decode_ms_avg": round(d["decode_ms_avg"], 5),
+                        "query_tok_s": round(d["query_tokens_per_step"] * world / (ms * 1e-3), 1),
+                        "clocks_sm_mhz": d["clocks"]["sm_mhz"]}
+            if wnum == 4:
+                res[tag]["setup_cow_pairs"] = int(len(r.sess.setup_cow_pairs))
+            del r
+            import torch
+            torch.cuda.empty_cache()
+        except Exception as e:
+            res[tag] = {"error": repr(e)}
+            log(f"workload {tag} failed: {e!r}")
+    return res
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: W untimed and K timed whole decode steps
+    of the headline workload on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    cb = cpu_oracle_baseline(HEADLINE, reps=args.steps, warmup=args.warmup)
+    ms = cb["seconds"] * 1e3 / cb["reps"]
+    return {
+        "impl": "reference", "metric": "paged decode attention KV-cache read bandwidth (valid K+V bytes / step time)",
+        "value": round(cb["value"], 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": workload_desc(HEADLINE), "parallelism": "host cores (OpenMP)"},
+        "query_tok_s": round(cb["query_tok_s"], 3),
+        "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"], "value": round(cb["value"], 4),
+                         "unit": "GB/s"},
+        "e2e": {"value": round(cb["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-workloads", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3")
+        args.warmup = 3
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * pkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache library.
+ *
+ * The operation set follows the pages' statement of paged attention:
+ *   - the KV cache of a sequence lives in fixed-size blocks placed anywhere in
+ *     a pool, and a per-sequence block table keeps the logical order
+ *     (x321.org "The serving bottleneck is not just FLOPs", section
+ *     "PagedAttention borrows an operating-system trick");
+ *   - attention is softmax(Q K^T / sqrt(d_head)) V (same page, section "First
+ *     understand what the KV cache is storing"), here evaluated by a kernel
+ *     that follows the block mapping;
+ *   - blocks of an identical prefix are shared with copy-on-write
+ *     (praveentn.live "PagedAttention KV-cache constraint", section "What the
+ *     change bought").
+ *
+ * Conventions for every call
+ *   - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  Argument errors
+ *     are detected on the host before anything is enqueued; nothing is
+ *     launched when a call fails.
+ *   - Device pointers are owned by the caller.  The kernels allocate no
+ *     device memory; scratch space is passed in by the caller.
+ *   - Kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns after the launch, asynchronously.
+ *   - `d_status` (optional, may be NULL) is a device int32 that kernels OR
+ *     PKV_STATUS_* bits into when they meet an out-of-range index; the access
+ *     is skipped (reads as zero) instead of faulting.  The caller zeroes it
+ *     and reads it after synchronising.
+ *   - bf16 values are passed as their 16-bit patterns (pkv_bf16).  Tensors
+ *     are dense, row-major, with the shapes given below; device pointers must
+ *     be 16-byte aligned.
+ *   - KV cache layout: k_cache and v_cache are each
+ *     [num_blocks][num_kv_heads][block_size][head_dim] bf16, so one (block,
+ *     KV head) tile of block_size x head_dim values is contiguous.
+ *   - Slot encoding: slot = physical_block * block_size + offset_in_block;
+ *     a negative slot means "no token, skip".
+ *   - Grouped-query attention: query head g reads KV head
+ *     g / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;
+
+/* return codes */
+#define PKV_OK               0
+#define PKV_ERR_ARG         -1  /* null/misaligned pointer, bad size or shape    */
+#define PKV_ERR_OOM         -2  /* allocator: not enough free blocks             */
+#define PKV_ERR_RANGE       -3  /* index outside its table / pool                */
+#define PKV_ERR_UNSUPPORTED -4  /* valid but not compiled (head_dim, block, ...) */
+#define PKV_ERR_CUDA        -5  /* a CUDA runtime call failed                    */
+#define PKV_ERR_TIMEOUT     -6  /* reserved: a device wait gave up               */
+#define PKV_ERR_SHARED      -7  /* allocator: append into a shared partial block */
+#define PKV_ERR_WORKSPACE   -8  /* workspace too small                           */
+
+/* bits OR-ed into *d_status by kernels */
+#define PKV_STATUS_BAD_SLOT   1  /* pkv_write: slot >= num_blocks * block_size   */
+#define PKV_STATUS_BAD_BLOCK  2  /* block id outside [0, num_blocks)             */
+#define PKV_STATUS_BAD_LEN    4  /* seq_len < 0 or above the table's capacity    */
+#define PKV_STATUS_TIMEOUT    8  /* a bounded on-chip wait gave up               */
+
+/* Human-readable name of a return code (static storage). */
+const char *pkv_error_string(int code);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *pkv_last_cuda_error(void);
+
+/*
+ * pkv_write -- store the keys and values of new tokens into their cache slots.
+ *
+ * Pages: the cache keeps every past key and value and grows by one token per
+ * decode step (x321.org "The serving bottleneck is not just FLOPs", section
+ * "First understand what the KV cache is storing"); a request grows by taking
+ * more blocks (same page, "PagedAttention borrows an operating-system trick").
+ *
+ * For every token t < num_tokens with s = slot_mapping[t] >= 0 and every KV
+ * head h:  k_cache[s / block_size][h][s % block_size][:] = k[t][h][:]
+ *          v_cache[...same...]                          = v[t][h][:]
+ *   k, v          device, [num_tokens][num_kv_heads][head_dim] bf16 (read)
+ *   slot_mapping  device, [num_tokens] int64 (read)
+ *   k_cache/v_cache  device, layout above (written)
+ * Slots >= num_blocks*block_size set PKV_STATUS_BAD_SLOT and are skipped.
+ * Two tokens with the same slot race (undefined which one lands).
+ * head_dim must be a multiple of 8.  num_tokens == 0 is a no-op.
+ */
+int pkv_write(const pkv_bf16 *k, const pkv_bf16 *v, const int64_t *slot_mapping,
+              int num_tokens, pkv_bf16 *k_cache, pkv_bf16 *v_cache, int num_blocks,
+              int block_size, int num_kv_heads, int head_dim, int32_t *d_status,
+              void *stream);
+
+/*
+ * pkv_block_copy -- materialise copy-on-write: copy whole blocks.
+ *
+ * Pages: shared prefix blocks are referenced by several sequences and copied
+ * on write (praveentn.live "PagedAttention KV-cache constraint", section
+ * "What the change bought").
+ *
+ * For each pair i < num_pairs with (src, dst) = (pairs[2i], pairs[2i+1]):
+ *   k_cache[dst][:][:][:] = k_cache[src][:][:][:]; the same for v_cache.
+ *   src_dst_pairs  device, [num_pairs][2] int32 (read)
+ * An id outside [0, num_blocks) sets PKV_STATUS_BAD_BLOCK and skips the pair.
+ * The dst ids must be distinct and disjoint from the src ids (the allocator's
+ * copy-on-write pairs always are); otherwise the result is undefined.
+ */
+int pkv_block_copy(pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *src_dst_pairs,
+                   int num_pairs, int num_blocks, int block_size, int num_kv_heads,
+                   int head_dim, int32_t *d_status, void *stream);
+
+/*
+ * Bytes of caller-provided device workspace paged_attention_decode needs for
+ * these sizes (0 when no sequence can span more than one partition).
+ * partition_size: tokens per split-K partition, a multiple of block_size;
+ * 0 selects the default (512).  Returns 0 for invalid sizes as well; check
+ * the decode call's return code.
+ */
+size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads,
+                                      int head_dim, int max_seq_len, int partition_size);
+
+/*
+ * paged_attention_decode -- attention of the newest q_len tokens of each
+ * sequence over its block-paged KV cache.
+ *
+ * Pages: Attention(Q,K,V) = softmax(Q K^T / sqrt(d_head)) V (x321.org "The
+ * serving bottleneck is not just FLOPs", section "First understand what the KV
+ * cache is storing"), evaluated by a kernel that follows the block mapping
+ * (same page, "PagedAttention borrows an operating-system trick"; praveentn.live
+ * "PagedAttention KV-cache constraint", section "What it cost": an indirection
+ * on every attention step that needs a custom kernel).
+ *
+ * For sequence i with L = seq_lens[i], query row r < q_len and query head g:
+ *   keys visible: t < n = L - q_len + 1 + r (q_len = 1: all L keys; a longer
+ *   query chunk is causal inside the chunk), key/value row t of KV head
+ *   h = g / (num_q_heads/num_kv_heads) read from block
+ *   block_tables[i][t / block_size], offset t % block_size;
+ *   out[i][r][g][:] = sum_t softmax_t(scale * q[i][r][g].k_t) * v_t, rounded
+ *   to bf16 (round to nearest even).  n <= 0 gives zeros.
+ *   q, out        device, [num_seqs][q_len][num_q_heads][head_dim] bf16
+ *   block_tables  device, [num_seqs][max_blocks_per_seq] int32; entries past
+ *                 ceil(L / block_size) are never read
+ *   seq_lens      device, [num_seqs] int32, 0 <= L <= max_seq_len and
+ *                 L <= max_blocks_per_seq * block_size (else PKV_STATUS_BAD_LEN,
+ *                 and L is clamped)
+ *   max_seq_len   host upper bound of seq_lens; sizes the grid and workspace
+ *   partition_size tokens per split-K partition (0 = 512), a multiple of
+ *                 block_size; sequences longer than one partition are reduced
+ *                 across partitions with an exact log-sum-exp merge
+ *   workspace     device scratch of at least paged_attention_workspace_size(...)
+ *                 bytes (may be NULL when that size is 0); contents are not
+ *                 preserved between calls
+ * Supported: head_dim in {64, 128}; block_size in {16, 32}; q_len in {1, 16}
+ *   with q_len * num_q_heads / num_kv_heads <= 128 and, for q_len = 1,
+ *   num_q_heads / num_kv_heads <= 16.  Other sizes return PKV_ERR_UNSUPPORTED.
+ * Block ids outside [0, num_blocks) set PKV_STATUS_BAD_BLOCK; the block reads
+ * as zeros.
+ */
+int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                           const pkv_bf16 *v_cache, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                           int max_seq_len, int q_len, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, float scale,
+                           int partition_size, pkv_bf16 *out, void *workspace,
+                           size_t workspace_bytes, int32_t *d_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator: pool, block tables, refcounts, copy-on-write.
+ *
+ * Pages: a request grows by allocating more free blocks and returns them to
+ * the pool when it ends; every free block is interchangeable (x321.org "The
+ * serving bottleneck is not just FLOPs", "PagedAttention borrows an
+ * operating-system trick"; praveentn.live "PagedAttention KV-cache
+ * constraint", "What the change bought").  Blocks needed for L tokens:
+ * ceil(L / block_size) (chenhuiyu.github.io "A complete explanation from first
+ * principles", "Calculate a block-allocation example").
+ *
+ * Policy: free blocks form a LIFO stack that starts as [NB-1, ..., 1, 0]
+ * (block 0 is handed out first); blocks whose refcount falls to zero are
+ * pushed back in logical order.  Every failing call leaves the state
+ * unchanged.  Host memory only; one owner; not thread-safe.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_alloc pkv_alloc;
+
+int  pkv_alloc_create(int num_blocks, int block_size, pkv_alloc **out);
+void pkv_alloc_destroy(pkv_alloc *a);
+
+/* New empty sequence; PKV_ERR_ARG if seq_id exists. */
+int pkv_seq_add(pkv_alloc *a, int64_t seq_id);
+
+/* Append n_tokens >= 0 tokens: take ceil((len+n)/bs) - blocks new blocks and
+ * write the n slots (host, int64) of positions len .. len+n-1 to slots_out.
+ * PKV_ERR_OOM if too few blocks are free; PKV_ERR_SHARED if the tokens would
+ * land in a partially filled block whose refcount is above 1 (call
+ * pkv_seq_cow first). */
+int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_out);
+
+/* child := a new sequence sharing every block of parent (refcount + 1 each). */
+int pkv_seq_fork(pkv_alloc *a, int64_t parent, int64_t child);
+
+/* Give seq_id a private copy of logical block `logical_block` (-1: the block the
+ * next append writes into, none when the last block is full).  If that block's
+ * refcount is above 1: take a free block, lower the old refcount, repoint the
+ * table entry, write {src, dst} to pair_out and set *copied = 1; else set
+ * *copied = 0.  The caller then runs pkv_block_copy on the pairs. */
+int pkv_seq_cow(pkv_alloc *a, int64_t seq_id, int logical_block, int32_t *pair_out,
+                int *copied);
+
+/* Drop a sequence; blocks whose refcount reaches 0 return to the pool. */
+int pkv_seq_free(pkv_alloc *a, int64_t seq_id);
+
+/* Current length (tokens) of a sequence, or a negative error code. */
+int64_t pkv_seq_len(const pkv_alloc *a, int64_t seq_id);
+
+/* Host [n][max_blocks] table rows (-1 past each sequence's blocks) and int32
+ * lengths.  PKV_ERR_RANGE if a sequence has more than max_blocks blocks. */
+int pkv_block_table(const pkv_alloc *a, const int64_t *seq_ids, int n, int32_t *table_out,
+                    int max_blocks, int32_t *lens_out);
+
+int pkv_num_free(const pkv_alloc *a);
+/* Refcount of a block, or PKV_ERR_RANGE. */
+int pkv_refcount(const pkv_alloc *a, int block);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H */

@@ -1,0 +1,767 @@
+// Paged attention over a block-paged KV cache (paged_attention_decode).
+//
+// Math: out = softmax(scale * q K^T) V  (x321.org "The serving bottleneck is
+// not just FLOPs", section "First understand what the KV cache is storing"),
+// with K/V rows fetched through the per-sequence block table (same page,
+// "PagedAttention borrows an operating-system trick").
+//
+// Design (GB300, sm_103a):
+//   * grid = (partition, kv head, sequence).  A partition is `part_blocks`
+//     consecutive logical blocks of one sequence (split-K over the context).
+//   * one producer lane per CTA walks the block table and issues 2-D TMA tile
+//     loads (128-byte swizzle) of each (block, kv head) K and V tile into a
+//     ring of shared-memory stages guarded by mbarriers.  Each tile is
+//     block_size x head_dim contiguous bf16 in HBM.
+//   * consumer warps compute, per block, S^T = K Q^T and O^T += V^T P^T with
+//     warp-level bf16 MMA (m16n8k16): the keys of the block are the M
+//     dimension and the query heads of the GQA group are N, so every K/V byte
+//     is read once for the whole group.  Online softmax (running max / sum)
+//     in fp32, exp2 with log2(e) folded into the scale.
+//   * single-token decode: the 4 consumer warps take interleaved blocks and
+//     are merged in shared memory at the end; the 16-token chunk variant gives
+//     each of 8 consumer warps 16 query rows and all blocks.
+//   * a sequence that spans one partition writes bf16 output directly; longer
+//     ones write (max, sum, unnormalised O) partials that a second kernel
+//     merges exactly (log-sum-exp) into bf16.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "pkv.h"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDecodeWarps = 4;  // consumer warps, q_len = 1
+constexpr int kChunkWarps = 8;   // consumer warps, q_len = 16
+constexpr int kChunkLen = 16;
+constexpr int kDefaultPartition = 512;
+
+struct Params {
+  const __nv_bfloat16 *q;       // [B][q_len][Hq][D]
+  const int32_t *block_tables;  // [B][max_blocks]
+  const int32_t *seq_lens;      // [B]
+  __nv_bfloat16 *out;           // [B][q_len][Hq][D]
+  float *ws_o;                  // [B][q_len*Hq][P][D]   unnormalised partial outputs
+  float2 *ws_ml;                // [B][q_len*Hq][P]      (running max in log2 units, sum)
+  int32_t *status;
+  int max_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;         // query heads per KV head
+  int q_len;
+  int num_blocks;
+  int max_parts;     // P
+  int part_blocks;   // blocks per partition
+  int oob_row;       // a TMA row coordinate wholly outside the cache (reads zeros)
+  int active_warps;  // chunk kernel: consumer warps that own at least one real row
+  float scale_log2;  // scale * log2(e)
+};
+
+template <int D, int BS>
+struct Tile {
+  static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+  static_assert(BS % 16 == 0, "block_size must be a multiple of 16");
+  static constexpr int kHalves = D / 64;               // 128-byte-wide TMA boxes per row
+  static constexpr int kBoxBytes = BS * 128;           // one box: BS rows x 64 bf16
+  static constexpr int kTileBytes = kHalves * kBoxBytes;  // K (or V) of one block
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = (65536 / kStageBytes) < 8 ? (65536 / kStageBytes) : 8;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+};
+
+// Shared-memory address of the 16-byte chunk `dchunk` of tile row `row`,
+// matching the TMA 128-byte swizzle (chunk index XOR row mod 8 inside each
+// 1024-byte atom; every box starts 1024-byte aligned).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dchunk) {
+  return base + (dchunk >> 3) * (BS * 128) + row * 128 + ((((dchunk & 7) ^ (row & 7))) << 4);
+}
+
+template <int D, int NT>
+struct WarpAcc {
+  float m[NT][2];  // running max of the thread's two columns per n-tile (log2 units)
+  float l[NT][2];  // thread-partial running sum
+  float o[D / 16][NT][4];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int md = 0; md < D / 16; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
+    }
+  }
+};
+
+// One block of keys for one warp's columns.
+//   qf:    B fragments of Q^T (column = query row) per n-tile and 16-wide d step
+//   valid: keys of this block that hold tokens (1..BS)
+//   vis:   keys of this block visible to each of the thread's columns
+template <int D, int BS, int NT>
+__device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
+                                             const uint32_t (&qf)[NT][D / 16][2], uint32_t kbase,
+                                             uint32_t vbase, int valid, const int (&vis)[NT][2],
+                                             float scale_log2, int lane) {
+  constexpr int MT = BS / 16;
+  const int r8 = lane & 7, mi = lane >> 3;
+  const int g4 = lane >> 2, c4 = lane & 3;
+
+  // S^T[key][col] = K[key][:] . Q[col][:]
+  float sc[MT][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t a[4];
+      ldsm_x4(swz<BS>(kbase, mt * 16 + r8 + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+    }
+  }
+
+  // scale, mask, block max per column
+  float bmax[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) bmax[nt][0] = bmax[nt][1] = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int key = mt * 16 + g4 + (i >> 1) * 8;
+        const float s = key < vis[nt][i & 1] ? sc[mt][nt][i] * scale_log2 : -INFINITY;
+        sc[mt][nt][i] = s;
+        bmax[nt][i & 1] = fmaxf(bmax[nt][i & 1], s);
+      }
+  float msub[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float b = bmax[nt][e];
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 4));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 8));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 16));
+      const float mn = fmaxf(acc.m[nt][e], b);
+      const float alpha = mn == -INFINITY ? 1.f : exp2f(acc.m[nt][e] - mn);
+      msub[nt][e] = mn == -INFINITY ? 0.f : mn;
+      acc.m[nt][e] = mn;
+      acc.l[nt][e] *= alpha;
+#pragma unroll
+      for (int md = 0; md < D / 16; ++md) {
+        acc.o[md][nt][e] *= alpha;
+        acc.o[md][nt][e + 2] *= alpha;
+      }
+    }
+
+  // probabilities -> bf16 -> B fragments of P^T (movmatrix transposes the
+  // accumulator layout into the operand layout)
+  uint32_t pb[MT][NT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t lo = pack_bf16x2(exp2f(sc[mt][nt][0] - msub[nt][0]), exp2f(sc[mt][nt][1] - msub[nt][1]));
+      const uint32_t hi = pack_bf16x2(exp2f(sc[mt][nt][2] - msub[nt][0]), exp2f(sc[mt][nt][3] - msub[nt][1]));
+      // the running sum uses the same rounded weights as the P V product
+      const float2 flo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lo));
+      const float2 fhi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi));
+      acc.l[nt][0] += flo.x + fhi.x;
+      acc.l[nt][1] += flo.y + fhi.y;
+      pb[mt][nt][0] = movmatrix_trans(lo);
+      pb[mt][nt][1] = movmatrix_trans(hi);
+    }
+
+  // O^T[d][col] += V^T[d][key] P^T[key][col]
+#pragma unroll
+  for (int kt = 0; kt < MT; ++kt) {
+    const bool tail = valid < (kt + 1) * 16;  // warp-uniform
+    const int k0 = kt * 16 + 2 * c4;
+    const uint32_t m0 = (k0 < valid ? 0x0000FFFFu : 0u) | (k0 + 1 < valid ? 0xFFFF0000u : 0u);
+    const uint32_t m1 = (k0 + 8 < valid ? 0x0000FFFFu : 0u) | (k0 + 9 < valid ? 0xFFFF0000u : 0u);
+#pragma unroll
+    for (int md = 0; md < D / 16; ++md) {
+      uint32_t a[4];
+      ldsm_x4_trans(swz<BS>(vbase, kt * 16 + r8 + (mi >> 1) * 8, md * 2 + (mi & 1)), a);
+      if (tail) {  // slots past the sequence end were never written: keep NaNs out
+        a[0] &= m0;
+        a[1] &= m0;
+        a[2] &= m1;
+        a[3] &= m1;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc.o[md][nt], a, pb[kt][nt][0], pb[kt][nt][1]);
+    }
+  }
+}
+
+__device__ __forceinline__ int clamp_len(const Params &p, int seq, int block_size, bool report) {
+  int L = p.seq_lens[seq];
+  const long long cap_tbl = static_cast<long long>(p.max_blocks) * block_size;
+  const long long cap_grid = static_cast<long long>(p.max_parts) * p.part_blocks * block_size;
+  const long long cap = cap_tbl < cap_grid ? cap_tbl : cap_grid;
+  if (L < 0 || L > cap) {
+    if (report && p.status) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+    L = L < 0 ? 0 : static_cast<int>(cap);
+  }
+  return L;
+}
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Producer: walk this partition's block-table entries and stream K/V tiles
+// into the ring.  empty_parity_base lets several consumer warps release a
+// stage (count given at init).
+template <int D, int BS>
+__device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq,
+                        int h, int blk0, int nblk, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        volatile int *abort_flag) {
+  using T = Tile<D, BS>;
+  constexpr int S = T::kStages;
+  const uint64_t pol = l2_policy_evict_first();
+  const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
+  int issued = 0;
+  for (int j = 0; j < nblk; ++j) {
+    const int s = j % S;
+    if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) {
+      if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+      *abort_flag = 1;
+      break;
+    }
+    if (*abort_flag) break;
+    const int b = tbl[j];
+    int row;
+    if (b >= 0 && b < p.num_blocks) {
+      row = (b * p.num_kv_heads + h) * BS;
+    } else {
+      if (p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+      row = p.oob_row;  // zero fill
+    }
+    const uint32_t full = full0 + 8 * s;
+    mbar_arrive_expect_tx(full, T::kStageBytes);
+    const uint32_t kdst = ring + s * T::kStageBytes;
+    const uint32_t vdst = kdst + T::kTileBytes;
+#pragma unroll
+    for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(kdst + hf * T::kBoxBytes, tmk, hf * 64, row, full, pol);
+#pragma unroll
+    for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(vdst + hf * T::kBoxBytes, tmv, hf * 64, row, full, pol);
+    ++issued;
+  }
+  // never leave a copy in flight into this CTA's shared memory
+  for (int j = issued > S ? issued - S : 0; j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
+}
+
+// ------------------------------------------------------------- q_len = 1
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const Params p) {
+  using T = Tile<D, BS>;
+  constexpr int S = T::kStages;
+  constexpr int COLS = NT * 8;
+  constexpr int DP = D + 4;  // padded row of the merge buffer
+  static_assert(kDecodeWarps * COLS * DP * 4 + 2 * kDecodeWarps * COLS * 4 <= T::kRingBytes,
+                "merge buffer must fit in the ring");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * S);
+
+  const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
+  const int part_tokens = p.part_blocks * BS;
+  const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
+  if (part >= nparts) return;
+  const int blk0 = part * p.part_blocks;
+  const int nblk_seq = (L + BS - 1) / BS;
+  const int nblk = max(0, min(p.part_blocks, nblk_seq - blk0));
+
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kDecodeWarps && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  __syncthreads();
+
+  WarpAcc<D, NT> acc;
+  if (warp == kDecodeWarps) {
+    if (lane == 0) produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag);
+  } else {
+    const int g4 = lane >> 2, c4 = lane & 3;
+    uint32_t qf[NT][D / 16][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int col = nt * 8 + g4;
+      const bool real = col < p.group;
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          p.q + (static_cast<size_t>(seq) * p.num_q_heads + h * p.group + (real ? col : 0)) * D);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        qf[nt][ks][0] = real ? qrow[ks * 8 + c4] : 0u;
+        qf[nt][ks][1] = real ? qrow[ks * 8 + 4 + c4] : 0u;
+      }
+    }
+    acc.init();
+    for (int j = warp; j < nblk; j += kDecodeWarps) {
+      const int s = j % S;
+      if (!mbar_wait(full0 + 8 * s, (j / S) & 1)) {
+        if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const int valid = min(BS, L - (blk0 + j) * BS);
+      int vis[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) vis[nt][0] = vis[nt][1] = valid;
+      const uint32_t kb = ring + s * T::kStageBytes;
+      attend_block<D, BS, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (*abort_flag) break;
+    }
+  }
+  __syncthreads();  // ring drained: reuse it as the merge buffer
+
+  float *so = reinterpret_cast<float *>(smem);             // [warps][COLS][DP]
+  float *sm = so + kDecodeWarps * COLS * DP;               // [warps][COLS]
+  float *sl = sm + kDecodeWarps * COLS;                    // [warps][COLS]
+  if (warp < kDecodeWarps) {
+    const int g4 = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = acc.l[nt][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (g4 == 0) {
+          sm[warp * COLS + nt * 8 + 2 * c4 + e] = acc.m[nt][e];
+          sl[warp * COLS + nt * 8 + 2 * c4 + e] = l;
+        }
+      }
+#pragma unroll
+    for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          so[(warp * COLS + nt * 8 + 2 * c4 + (i & 1)) * DP + md * 16 + g4 + (i >> 1) * 8] = acc.o[md][nt][i];
+  }
+  __syncthreads();
+  if (*abort_flag) return;
+
+  const int rows = p.num_q_heads;  // q_len == 1
+  for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
+    const int col = idx / D, d = idx - col * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sm[w * COLS + col]);
+    float lt = 0.f, ot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float mw = sm[w * COLS + col];
+      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      lt += sl[w * COLS + col] * f;
+      ot += so[(w * COLS + col) * DP + d] * f;
+    }
+    const size_t row = static_cast<size_t>(seq) * rows + h * p.group + col;
+    if (nparts == 1) {
+      p.out[row * D + d] = __float2bfloat16_rn(lt > 0.f ? ot / lt : 0.f);
+    } else {
+      p.ws_o[(row * p.max_parts + part) * D + d] = ot;
+      if (d == 0) p.ws_ml[row * p.max_parts + part] = make_float2(M, lt);
+    }
+  }
+}
+
+// ------------------------------------------------- q_len = 16 causal chunk
+// Column c of the CTA is query row (r = c / G, g = c % G) of KV head h; warp w
+// owns columns [16w, 16w + 16).  Row r sees keys t < L - 16 + 1 + r.
+template <int D, int BS>
+__global__ void __launch_bounds__((kChunkWarps + 1) * 32)
+    chunk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                 const Params p) {
+  using T = Tile<D, BS>;
+  constexpr int S = T::kStages;
+  constexpr int NT = 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * S);
+
+  const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
+  const int part_tokens = p.part_blocks * BS;
+  const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
+  if (part >= nparts) return;
+  const int blk0 = part * p.part_blocks;
+  const int nblk_seq = (L + BS - 1) / BS;
+  const int nblk = max(0, min(p.part_blocks, nblk_seq - blk0));
+  const int ncols = kChunkLen * p.group;
+
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, p.active_warps);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kChunkWarps && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  __syncthreads();
+
+  if (warp == kChunkWarps) {
+    if (lane == 0) produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag);
+    return;
+  }
+  if (warp >= p.active_warps) return;
+
+  const int g4 = lane >> 2, c4 = lane & 3;
+  const int rows = kChunkLen * p.num_q_heads;
+  uint32_t qf[NT][D / 16][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = warp * 16 + nt * 8 + g4;
+    const bool real = col < ncols;
+    const int r = real ? col / p.group : 0, g = real ? col - (col / p.group) * p.group : 0;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        p.q + (static_cast<size_t>(seq) * rows + r * p.num_q_heads + h * p.group + g) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qf[nt][ks][0] = real ? qrow[ks * 8 + c4] : 0u;
+      qf[nt][ks][1] = real ? qrow[ks * 8 + 4 + c4] : 0u;
+    }
+  }
+  // keys visible to each of this thread's accumulator columns
+  int nvis[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = warp * 16 + nt * 8 + 2 * c4 + e;
+      nvis[nt][e] = col < ncols ? L - kChunkLen + 1 + col / p.group : 0;
+    }
+
+  WarpAcc<D, NT> acc;
+  acc.init();
+  bool ok = true;
+  for (int j = 0; j < nblk; ++j) {
+    const int s = j % S;
+    if (!mbar_wait(full0 + 8 * s, (j / S) & 1)) {
+      if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+      *abort_flag = 1;
+      ok = false;
+      break;
+    }
+    const int key0 = (blk0 + j) * BS;
+    const int valid = min(BS, L - key0);
+    int vis[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      vis[nt][0] = min(valid, nvis[nt][0] - key0);
+      vis[nt][1] = min(valid, nvis[nt][1] - key0);
+    }
+    const uint32_t kb = ring + s * T::kStageBytes;
+    attend_block<D, BS, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (*abort_flag) {
+      ok = false;
+      break;
+    }
+  }
+  if (!ok) return;
+
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = acc.l[nt][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      acc.l[nt][e] = l;
+    }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = warp * 16 + nt * 8 + 2 * c4 + e;
+      if (col >= ncols) continue;
+      const int r = col / p.group, g = col - r * p.group;
+      const size_t row = static_cast<size_t>(seq) * rows + r * p.num_q_heads + h * p.group + g;
+      const float l = acc.l[nt][e];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int md = 0; md < D / 16; ++md)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int d = md * 16 + g4 + hi * 8;
+          const float o = acc.o[md][nt][e + 2 * hi];
+          if (nparts == 1) {
+            p.out[row * D + d] = __float2bfloat16_rn(o * inv);
+          } else {
+            p.ws_o[(row * p.max_parts + part) * D + d] = o;
+          }
+        }
+      if (nparts > 1 && g4 == 0) p.ws_ml[row * p.max_parts + part] = make_float2(acc.m[nt][e], l);
+    }
+}
+
+// ---------------------------------------------- cross-partition combine
+// One warp per (sequence, query row): out = sum_p O_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
+                                                      int rows) {
+  constexpr int PER = D / 32;
+  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= total_rows) return;
+  const int seq = wg / rows;
+  const int L = clamp_len(p, seq, block_size, false);
+  const int part_tokens = p.part_blocks * block_size;
+  const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
+  if (nparts <= 1) return;
+  const float2 *ml = p.ws_ml + static_cast<size_t>(wg) * p.max_parts;
+  const float *o = p.ws_o + static_cast<size_t>(wg) * p.max_parts * D + lane * PER;
+  float M = -INFINITY;
+  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[i].x);
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
+  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+  float den = 0.f, accv[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) accv[k] = 0.f;
+  for (int i = 0; i < nparts; ++i) {
+    const float2 v = ml[i];
+    const float f = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+    den += v.y * f;
+    if constexpr (PER == 4) {
+      const float4 x = *reinterpret_cast<const float4 *>(o + static_cast<size_t>(i) * D);
+      accv[0] += f * x.x;
+      accv[1] += f * x.y;
+      accv[2] += f * x.z;
+      accv[3] += f * x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2 *>(o + static_cast<size_t>(i) * D);
+      accv[0] += f * x.x;
+      accv[1] += f * x.y;
+    }
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  __nv_bfloat16 *dst = p.out + static_cast<size_t>(wg) * D + lane * PER;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) dst[k] = __float2bfloat16_rn(accv[k] * inv);
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The cache as a 2-D bf16 tensor: rows = num_blocks * Hkv * block_size, each of
+// head_dim elements; a box is block_size rows x 64 elements (128 bytes).
+bool make_cache_map(CUtensorMap *map, const void *base, int head_dim, int block_size, long long rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_size)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int part_tokens = 0;
+  int max_parts = 0;
+  size_t ws_o_bytes = 0;
+  size_t ws_ml_bytes = 0;
+  size_t ws_bytes() const { return max_parts > 1 ? ws_o_bytes + ws_ml_bytes : 0; }
+};
+
+bool make_plan(int num_seqs, int q_len, int num_q_heads, int head_dim, int max_seq_len,
+               int partition_size, Plan *plan) {
+  if (num_seqs < 0 || q_len < 1 || num_q_heads < 1 || head_dim < 1 || max_seq_len < 0) return false;
+  const int part = partition_size == 0 ? kDefaultPartition : partition_size;
+  if (part < 1) return false;
+  plan->part_tokens = part;
+  const long long parts = max_seq_len > 0 ? (static_cast<long long>(max_seq_len) + part - 1) / part : 1;
+  if (parts > (1 << 20)) return false;
+  plan->max_parts = static_cast<int>(parts);
+  const size_t rows = static_cast<size_t>(num_seqs) * q_len * num_q_heads;
+  plan->ws_o_bytes = rows * plan->max_parts * head_dim * sizeof(float);
+  plan->ws_o_bytes = (plan->ws_o_bytes + 255) & ~size_t(255);
+  plan->ws_ml_bytes = rows * plan->max_parts * sizeof(float2);
+  return true;
+}
+
+template <int D, int BS>
+constexpr size_t smem_bytes() {
+  return Tile<D, BS>::kRingBytes + 2 * Tile<D, BS>::kStages * 8 + 16 + 1024;
+}
+
+template <typename K>
+cudaError_t raise_smem_limit(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+template <int D, int BS>
+int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int num_seqs, int q_len,
+           cudaStream_t stream) {
+  const dim3 grid(p.max_parts, p.num_kv_heads, num_seqs);
+  constexpr size_t smem = smem_bytes<D, BS>();
+  cudaError_t e;
+  if (q_len == 1) {
+    if (p.group <= 8) {
+      auto k = decode_kernel<D, BS, 1>;
+      if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+      k<<<grid, (kDecodeWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+    } else {
+      auto k = decode_kernel<D, BS, 2>;
+      if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+      k<<<grid, (kDecodeWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+    }
+  } else {
+    auto k = chunk_kernel<D, BS>;
+    if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+    k<<<grid, (kChunkWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+  }
+  int rc = check_launch();
+  if (rc != PKV_OK || p.max_parts <= 1) return rc;
+  const int rows = q_len * p.num_q_heads;
+  const int total = num_seqs * rows;
+  combine_kernel<D><<<(total + 3) / 4, 128, 0, stream>>>(p, BS, total, rows);
+  return check_launch();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads, int head_dim,
+                                      int max_seq_len, int partition_size) {
+  pkv::Plan plan;
+  if (!pkv::make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &plan)) return 0;
+  return plan.ws_bytes();
+}
+
+int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                           int num_seqs, int max_seq_len, int q_len, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, float scale, int partition_size,
+                           pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                           void *stream) {
+  using namespace pkv;
+  if (num_seqs < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_blocks < 0 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  if (q_len == 1) {
+    if (group > 16) return PKV_ERR_UNSUPPORTED;
+  } else if (q_len == kChunkLen) {
+    if (group * kChunkLen > kChunkWarps * 16) return PKV_ERR_UNSUPPORTED;
+  } else {
+    return q_len < 1 ? PKV_ERR_ARG : PKV_ERR_UNSUPPORTED;
+  }
+  if (partition_size < 0 || (partition_size != 0 && partition_size % block_size != 0)) return PKV_ERR_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PKV_ERR_ARG;
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+  if (rows + block_size >= (1ll << 31) || num_blocks == 0) return num_blocks == 0 ? PKV_ERR_ARG : PKV_ERR_UNSUPPORTED;
+
+  Plan plan;
+  if (!make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &plan)) return PKV_ERR_ARG;
+  if (plan.max_parts > 65535) return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes() > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes() || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  }
+
+  CUtensorMap tmk, tmv;
+  if (!make_cache_map(&tmk, k_cache, head_dim, block_size, rows) ||
+      !make_cache_map(&tmv, v_cache, head_dim, block_size, rows))
+    return PKV_ERR_CUDA;
+
+  Params p{};
+  p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  p.ws_o = plan.ws_bytes() ? static_cast<float *>(workspace) : nullptr;
+  p.ws_ml = plan.ws_bytes() ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.ws_o_bytes) : nullptr;
+  p.status = d_status;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.q_len = q_len;
+  p.num_blocks = num_blocks;
+  p.max_parts = plan.max_parts;
+  p.part_blocks = plan.part_tokens / block_size;
+  p.oob_row = static_cast<int>(rows);
+  p.active_warps = (group * kChunkLen + 15) / 16;
+  p.scale_log2 = scale * kLog2e;
+
+  cudaStream_t st = as_stream(stream);
+  if (head_dim == 128)
+    return block_size == 16 ? launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st)
+                            : launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st);
+  return block_size == 16 ? launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st)
+                          : launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,244 @@
+"""ctypes binding of libpkv.so: the C ABI declared in include/pkv.h, one Python
+function per C entry point with the same name.
+
+Argument marshalling only: shapes are read off the tensors, pointers and the
+current CUDA stream are passed through, return codes become exceptions.  Every
+step of the computation runs in the library's kernels.  There is no fallback:
+if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_ARG = -1
+PKV_ERR_OOM = -2
+PKV_ERR_RANGE = -3
+PKV_ERR_UNSUPPORTED = -4
+PKV_ERR_CUDA = -5
+PKV_ERR_TIMEOUT = -6
+PKV_ERR_SHARED = -7
+PKV_ERR_WORKSPACE = -8
+
+PKV_STATUS_BAD_SLOT = 1
+PKV_STATUS_BAD_BLOCK = 2
+PKV_STATUS_BAD_LEN = 4
+PKV_STATUS_TIMEOUT = 8
+
+_c_int, _c_i64, _c_ptr, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_float)
+
+# name -> (restype, argtypes); mirrors include/pkv.h
+SIGNATURES = {
+    "pkv_error_string": (ctypes.c_char_p, [_c_int]),
+    "pkv_last_cuda_error": (ctypes.c_char_p, []),
+    "pkv_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int,
+                           _c_int, _c_ptr, _c_ptr]),
+    "pkv_block_copy": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                _c_ptr, _c_ptr]),
+    "paged_attention_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "paged_attention_decode": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
+                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                        _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
+                                        _c_ptr]),
+    "pkv_alloc_create": (_c_int, [_c_int, _c_int, ctypes.POINTER(_c_ptr)]),
+    "pkv_alloc_destroy": (None, [_c_ptr]),
+    "pkv_seq_add": (_c_int, [_c_ptr, _c_i64]),
+    "pkv_seq_append": (_c_int, [_c_ptr, _c_i64, _c_int, _c_ptr]),
+    "pkv_seq_fork": (_c_int, [_c_ptr, _c_i64, _c_i64]),
+    "pkv_seq_cow": (_c_int, [_c_ptr, _c_i64, _c_int, _c_ptr, ctypes.POINTER(_c_int)]),
+    "pkv_seq_free": (_c_int, [_c_ptr, _c_i64]),
+    "pkv_seq_len": (_c_i64, [_c_ptr, _c_i64]),
+    "pkv_block_table": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_ptr, _c_int, _c_ptr]),
+    "pkv_num_free": (_c_int, [_c_ptr]),
+    "pkv_refcount": (_c_int, [_c_ptr, _c_int]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = f"{what} failed: {error_string(code)} ({code})"
+        if code == PKV_ERR_CUDA:
+            msg += f": {lib().pkv_last_cuda_error().decode()}"
+        super().__init__(msg)
+
+
+def lib():
+    """The loaded library; raises if it has not been built (no fallback path exists)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with `python -m paged_kv_cache_276_gb300.build`")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def error_string(code: int) -> str:
+    return lib().pkv_error_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != PKV_OK:
+        raise PkvError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+# --------------------------------------------------------------- kernels
+def pkv_write(k, v, slot_mapping, k_cache, v_cache, d_status=None, stream=None):
+    """k, v: [T, Hkv, d] bf16; slot_mapping: [T] int64; caches [NB, Hkv, bs, d] bf16 (device)."""
+    dev = k_cache.device
+    for t, n, dt in ((k, "k", torch.bfloat16), (v, "v", torch.bfloat16), (slot_mapping, "slot_mapping", torch.int64),
+                     (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    NB, Hkv, bs, d = k_cache.shape
+    T = slot_mapping.shape[0]
+    if k.shape != (T, Hkv, d) or v.shape != (T, Hkv, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between k/v and the caches")
+    _check(lib().pkv_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, d,
+                           _ptr(d_status), _stream(stream, dev)), "pkv_write")
+
+
+def pkv_block_copy(k_cache, v_cache, src_dst_pairs, d_status=None, stream=None):
+    """src_dst_pairs: [n, 2] int32 device tensor of (src, dst) block ids."""
+    dev = k_cache.device
+    _need(k_cache, torch.bfloat16, "k_cache", dev)
+    _need(v_cache, torch.bfloat16, "v_cache", dev)
+    _need(src_dst_pairs, torch.int32, "src_dst_pairs", dev)
+    NB, Hkv, bs, d = k_cache.shape
+    n = src_dst_pairs.numel() // 2
+    _check(lib().pkv_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs), n, NB, bs, Hkv, d,
+                                _ptr(d_status), _stream(stream, dev)), "pkv_block_copy")
+
+
+def paged_attention_workspace_size(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size=0):
+    return int(lib().paged_attention_workspace_size(num_seqs, q_len, num_q_heads, head_dim, max_seq_len,
+                                                    partition_size))
+
+
+def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, out,
+                           workspace=None, partition_size=0, d_status=None, stream=None):
+    """q, out: [B, q_len, Hq, d] bf16; caches [NB, Hkv, bs, d]; tables [B, max_blocks] int32; lens [B] int32."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (out, "out", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    B, q_len, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or seq_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().paged_attention_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+        int(max_seq_len), q_len, Hq, Hkv, d, bs, NB, float(scale), int(partition_size), _ptr(out),
+        _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_decode")
+
+
+# ------------------------------------------------------------- allocator
+class BlockAllocator:
+    """Host block manager (pkv_alloc_* / pkv_seq_* in the C ABI)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        h = ctypes.c_void_p()
+        _check(lib().pkv_alloc_create(num_blocks, block_size, ctypes.byref(h)), "pkv_alloc_create")
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            lib().pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def seq_add(self, seq_id: int):
+        _check(lib().pkv_seq_add(self._h, seq_id), "pkv_seq_add")
+
+    def seq_append(self, seq_id: int, n_tokens: int, out=None):
+        """Returns the n slots (int64 numpy array, or written into ``out``)."""
+        import numpy as np
+        slots = np.empty(n_tokens, dtype=np.int64) if out is None else out
+        _check(lib().pkv_seq_append(self._h, seq_id, n_tokens, slots.ctypes.data if n_tokens else None),
+               "pkv_seq_append")
+        return slots
+
+    def seq_fork(self, parent: int, child: int):
+        _check(lib().pkv_seq_fork(self._h, parent, child), "pkv_seq_fork")
+
+    def seq_cow(self, seq_id: int, logical_block: int = -1):
+        pair = (ctypes.c_int32 * 2)()
+        copied = ctypes.c_int()
+        _check(lib().pkv_seq_cow(self._h, seq_id, logical_block, pair, ctypes.byref(copied)), "pkv_seq_cow")
+        return (pair[0], pair[1]) if copied.value else None
+
+    def seq_free(self, seq_id: int):
+        _check(lib().pkv_seq_free(self._h, seq_id), "pkv_seq_free")
+
+    def seq_len(self, seq_id: int) -> int:
+        n = lib().pkv_seq_len(self._h, seq_id)
+        if n < 0:
+            raise PkvError(int(n), "pkv_seq_len")
+        return int(n)
+
+    def block_table(self, seq_ids, max_blocks: int):
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(list(seq_ids), dtype=np.int64))
+        table = np.empty((len(ids), max_blocks), dtype=np.int32)
+        lens = np.empty(len(ids), dtype=np.int32)
+        _check(lib().pkv_block_table(self._h, ids.ctypes.data, len(ids), table.ctypes.data, max_blocks,
+                                     lens.ctypes.data), "pkv_block_table")
+        return table, lens
+
+    def num_free(self) -> int:
+        return int(lib().pkv_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        rc = lib().pkv_refcount(self._h, block)
+        if rc < 0:
+            raise PkvError(rc, "pkv_refcount")
+        return int(rc)

@@ -1,0 +1,198 @@
+"""Decode workloads driven through the public API, as a serving step would use it.
+
+A ``DecodeSession`` owns the per-layer cache pools on the device, a block
+allocator (the native ``BlockAllocator``, or any object with the same methods),
+and the sequences.  ``plan_steps`` runs the allocator for a number of decode
+steps ahead of time and uploads each step's slot mapping, block tables and
+lengths, so timed steps start with every input resident in HBM.  ``run_step``
+is one pass of the hot path: for every layer, ``pkv_write`` the new tokens'
+K/V, then ``paged_attention_decode`` (plus ``pkv_block_copy`` for any
+copy-on-write pairs the step produced).
+
+Random numbers come from ``inputs``; this module does no attention, write or
+copy arithmetic itself.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import inputs, native
+from .inputs import Workload
+
+
+def permute_free_blocks(alloc, num_blocks: int, rng: np.random.Generator) -> np.ndarray:
+    """Leave the allocator's free stack in a random order using only its public calls.
+
+    Each block is taken by a throw-away one-token sequence, then the sequences
+    are freed in a random order; later allocations pop blocks in the reverse of
+    that order.  Returns the free order.
+    """
+    for b in range(num_blocks):
+        alloc.seq_add(-(b + 1))
+        alloc.seq_append(-(b + 1), 1)
+    order = rng.permutation(num_blocks)
+    for b in order:
+        alloc.seq_free(-(int(b) + 1))
+    return order
+
+
+@dataclass
+class StepInputs:
+    slots: torch.Tensor         # [B * q_len] int64, device
+    tables: torch.Tensor        # [B, max_blocks] int32, device
+    lens: torch.Tensor          # [B] int32, device
+    max_len: int
+    cow_pairs: torch.Tensor | None  # [n, 2] int32, device, or None
+    host_tables: np.ndarray
+    host_lens: np.ndarray
+
+
+class DecodeSession:
+    def __init__(self, w: Workload, device, allocator_factory=None, block_size: int | None = None,
+                 q_len: int | None = None, layers: int | None = None, seq_lens=None,
+                 extra_steps: int = 64, prefix_len: int | None = None, seed_salt: int = 0):
+        self.w = w
+        self.device = torch.device(device)
+        self.bs = block_size or w.block_size
+        self.q_len = q_len or w.q_len
+        self.layers = layers or w.layers
+        self.Hq, self.Hkv, self.d = w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.scale = w.scale
+        self.partition_size = w.partition_size
+        self.seed_salt = seed_salt  # offsets every tensor seed (independent replicas)
+        factory = allocator_factory or native.BlockAllocator
+        rng = inputs.rng_for(w)
+        target = np.asarray(inputs.lengths(w, rng) if seq_lens is None else seq_lens, dtype=np.int64)
+        self.B = len(target)
+        self.extra_steps = extra_steps
+        # tokens already cached before the first step; the step adds q_len more.
+        # Shared-prefix sampling: prefix + suffix are cached, the step generates
+        # the next token of every sample.
+        ctx = target.copy() if w.number == 4 else np.maximum(target - self.q_len, 0)
+        growth = self.q_len * extra_steps
+        if w.number == 4:
+            self._init_shared_prefix(factory, ctx, growth, prefix_len or w.extra["prefix"])
+        else:
+            if w.number == 1:
+                self.num_blocks = w.extra["pool"]
+            else:
+                used = sum(inputs.entries_to_fill(int(n) + growth, self.bs) for n in ctx)
+                frac = w.extra.get("pool_extra", 0.10)
+                self.num_blocks = int(np.ceil(used * (1 + frac)))
+            self.alloc = factory(self.num_blocks, self.bs)
+            permute_free_blocks(self.alloc, self.num_blocks, inputs.rng_for(w, salt=1))
+            for i, n in enumerate(ctx):
+                self.alloc.seq_add(i)
+                if n:
+                    self.alloc.seq_append(i, int(n))
+            self.setup_cow_pairs = np.zeros((0, 2), dtype=np.int32)
+        self.max_blocks = max(inputs.entries_to_fill(int(n) + growth, self.bs) for n in ctx) + 1
+        self.k_caches, self.v_caches = [], []
+        for layer in range(self.layers):
+            shape = (self.num_blocks, self.Hkv, self.bs, self.d)
+            base = w.seed * 100 + 2 * layer + 7777 * seed_salt
+            self.k_caches.append(inputs.randn_bf16(shape, base, self.device))
+            self.v_caches.append(inputs.randn_bf16(shape, base + 1, self.device))
+        self.step_index = 0
+
+    def _init_shared_prefix(self, factory, ctx, growth, prefix):
+        """64 prompts x 8 samples: the prefix blocks are shared by refcount, the
+        last prefix block is copied on write for each sample, suffixes follow."""
+        w = self.w
+        prompts, samples = w.extra["prompts"], w.extra["samples"]
+        assert prompts * samples == self.B
+        prefix_blocks = inputs.entries_to_fill(prefix, self.bs)
+        suffix_blocks = sum(inputs.entries_to_fill(int(n) + growth, self.bs) for n in ctx) \
+            - self.B * (prefix // self.bs)
+        self.num_blocks = prompts * prefix_blocks + self.B + suffix_blocks + self.B
+        self.alloc = factory(self.num_blocks, self.bs)
+        pairs = []
+        for p in range(prompts):
+            parent = 10 ** 9 + p
+            self.alloc.seq_add(parent)
+            self.alloc.seq_append(parent, prefix)
+            for s in range(samples):
+                self.alloc.seq_fork(parent, p * samples + s)
+            self.alloc.seq_free(parent)
+            if prefix % self.bs == 0:
+                # The prefix fills its last block, so no write would ever land in
+                # it; copy it on each sample's first write anyway, standing in for
+                # the partially filled last prefix block of the workload.
+                for s in range(samples):
+                    pair = self.alloc.seq_cow(p * samples + s, prefix_blocks - 1)
+                    if pair is not None:
+                        pairs.append(pair)
+        for i, n in enumerate(ctx):
+            extra = int(n) - prefix
+            if extra > 0:
+                pair = self.alloc.seq_cow(i)  # no-op unless the next write lands in a shared block
+                if pair is not None:
+                    pairs.append(pair)
+                self.alloc.seq_append(i, extra)
+        self.setup_cow_pairs = np.asarray(pairs, dtype=np.int32).reshape(-1, 2)
+
+    # ------------------------------------------------------------ planning
+    def plan_step(self) -> StepInputs:
+        """Allocator work of one step (host), then upload its inputs."""
+        slots = np.empty(self.B * self.q_len, dtype=np.int64)
+        pairs = []
+        for i in range(self.B):
+            pair = self.alloc.seq_cow(i)
+            if pair is not None:
+                pairs.append(pair)
+            slots[i * self.q_len:(i + 1) * self.q_len] = self.alloc.seq_append(i, self.q_len)
+        tables, lens = self.alloc.block_table(range(self.B), self.max_blocks)
+        tables = np.asarray(tables, dtype=np.int32)
+        lens = np.asarray(lens, dtype=np.int32)
+        dev = self.device
+        cow = torch.as_tensor(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), device=dev) if pairs else None
+        return StepInputs(torch.as_tensor(slots, device=dev), torch.as_tensor(tables, device=dev),
+                          torch.as_tensor(lens, device=dev), int(lens.max()) if len(lens) else 0, cow,
+                          tables, lens)
+
+    def plan_steps(self, n: int):
+        return [self.plan_step() for _ in range(n)]
+
+    def new_token_tensors(self, n_steps: int, seed: int):
+        """Per-step q [B, q_len, Hq, d] and new-token k, v [B*q_len, Hkv, d] (per layer)."""
+        out = []
+        for s in range(n_steps):
+            base = seed * 1000 + s * 97 + 7777 * self.seed_salt
+            q = inputs.randn_bf16((self.B, self.q_len, self.Hq, self.d), base, self.device)
+            ks = [inputs.randn_bf16((self.B * self.q_len, self.Hkv, self.d), base + 1 + 2 * l, self.device)
+                  for l in range(self.layers)]
+            vs = [inputs.randn_bf16((self.B * self.q_len, self.Hkv, self.d), base + 2 + 2 * l, self.device)
+                  for l in range(self.layers)]
+            out.append((q, ks, vs))
+        return out
+
+    def workspace(self, max_len: int):
+        n = native.paged_attention_workspace_size(self.B, self.q_len, self.Hq, self.d, max_len,
+                                                  self.partition_size)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=self.device) if n else None
+
+    def apply_setup_copies(self, d_status=None):
+        if len(self.setup_cow_pairs):
+            pairs = torch.as_tensor(self.setup_cow_pairs, device=self.device)
+            for l in range(self.layers):
+                native.pkv_block_copy(self.k_caches[l], self.v_caches[l], pairs, d_status=d_status)
+
+    # ------------------------------------------------------------ one step
+    def run_step(self, step: StepInputs, q, ks, vs, out, workspace, d_status=None, stream=None,
+                 per_layer_out=None):
+        """One pass of the hot path over every layer."""
+        for l in range(self.layers):
+            if step.cow_pairs is not None:
+                native.pkv_block_copy(self.k_caches[l], self.v_caches[l], step.cow_pairs, d_status, stream)
+            native.pkv_write(ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l], d_status, stream)
+            o = out if per_layer_out is None else per_layer_out[l]
+            native.paged_attention_decode(q, self.k_caches[l], self.v_caches[l], step.tables, step.lens,
+                                          step.max_len, self.scale, o, workspace, self.partition_size,
+                                          d_status, stream)
+
+    def kv_bytes(self, step: StepInputs) -> int:
+        """Valid K and V bytes one step's decodes read over all layers."""
+        return int(step.host_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.d * 2 * self.layers

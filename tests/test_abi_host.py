@@ -1,0 +1,203 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks and the host allocator work without a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, read_golden
+
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def native():
+    from paged_kv_cache_276_gb300 import build, native
+    build.build()
+    return native
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(p[a-z_]+)\s*\(", text)) - {"pkv_bf16"})
+
+
+def test_every_declared_symbol_is_exported(native):
+    names = declared_functions()
+    assert "paged_attention_decode" in names and "pkv_write" in names and "pkv_block_copy" in names
+    lib = native.lib()
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert set(names) == set(native.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_error_strings(native):
+    assert native.error_string(0) == "ok"
+    assert "shared" in native.error_string(native.PKV_ERR_SHARED)
+
+
+def test_workspace_size_host_only(native):
+    f = native.paged_attention_workspace_size
+    assert f(32, 1, 32, 128, 512, 512) == 0          # one partition: no scratch
+    n = f(32, 1, 32, 128, 4096, 512)
+    assert n >= 32 * 32 * 8 * 128 * 4 + 32 * 32 * 8 * 8
+    assert f(16, 16, 64, 128, 32768, 512) > f(16, 1, 64, 128, 32768, 512)
+    assert f(-1, 1, 1, 64, 1, 0) == 0
+
+
+def test_decode_rejects_bad_sizes_before_launch(native):
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails validation first
+    args = dict(q=fake, k=fake, v=fake, tbl=fake, maxb=4, lens=fake, B=2, maxlen=64, qlen=1, Hq=8, Hkv=2,
+                d=128, bs=16, NB=8, scale=0.1, part=0, out=fake, ws=None, wsb=0, st=None, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.paged_attention_decode(a["q"], a["k"], a["v"], a["tbl"], a["maxb"], a["lens"], a["B"],
+                                          a["maxlen"], a["qlen"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"],
+                                          a["scale"], a["part"], a["out"], a["ws"], a["wsb"], a["st"],
+                                          a["stream"])
+    assert call(d=96) == native.PKV_ERR_UNSUPPORTED
+    assert call(bs=8) == native.PKV_ERR_UNSUPPORTED
+    assert call(qlen=3) == native.PKV_ERR_UNSUPPORTED
+    assert call(Hq=7) == native.PKV_ERR_ARG
+    assert call(Hq=40, Hkv=2) == native.PKV_ERR_UNSUPPORTED       # group 20 > 16
+    assert call(qlen=16, Hq=32, Hkv=2) == native.PKV_ERR_UNSUPPORTED  # 16 x 16 rows > 128
+    assert call(part=24) == native.PKV_ERR_ARG                   # not a multiple of the block
+    assert call(maxlen=4096) == native.PKV_ERR_WORKSPACE          # 8 partitions, no scratch
+    assert call(scale=float("nan")) == native.PKV_ERR_ARG
+    assert call(q=ctypes.c_void_p((1 << 20) + 2)) == native.PKV_ERR_ARG  # misaligned
+    assert call(B=0) == native.PKV_OK                            # nothing to do, nothing launched
+
+
+def test_write_and_copy_reject_bad_sizes_before_launch(native):
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.pkv_write(fake, fake, fake, 4, fake, fake, 8, 16, 2, 12, None, None) == native.PKV_ERR_ARG
+    assert lib.pkv_write(fake, fake, fake, 0, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_OK
+    assert lib.pkv_write(None, fake, fake, 4, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
+    assert lib.pkv_block_copy(fake, fake, fake, -1, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
+    assert lib.pkv_block_copy(fake, fake, fake, 0, 8, 16, 2, 64, None, None) == native.PKV_OK
+
+
+# ------------------------------------------------------------- allocator
+def test_native_allocator_page_examples(native):
+    for length, block, blocks, _cap, unused, used_last, _o in read_golden("block_counts.txt"):
+        a = native.BlockAllocator(16, int(block))
+        a.seq_add(7)
+        slots = a.seq_append(7, int(length))
+        table, lens = a.block_table([7], 8)
+        nb = int((table[0] >= 0).sum())
+        assert nb == int(blocks) and lens[0] == int(length)
+        assert nb * int(block) - int(length) == int(unused)
+        assert int((slots // int(block) == table[0, nb - 1]).sum()) == int(used_last)
+        assert table[0, 0] == 0  # LIFO stack starts with block 0 on top
+
+
+def _kind(code):
+    from paged_kv_cache_276_gb300 import native
+    return {native.PKV_ERR_ARG: "arg", native.PKV_ERR_OOM: "oom", native.PKV_ERR_RANGE: "range",
+            native.PKV_ERR_SHARED: "shared"}[code]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_native_allocator_matches_oracle_bit_exact(native, seed):
+    """Same random sequence of add / append / fork / cow / free on both; every table, length,
+    refcount, free count, slot list and error kind must agree."""
+    from oracle.allocator import AllocError, OracleAllocator
+    rng = np.random.default_rng(seed)
+    NB, bs = 48, [4, 16, 8, 32][seed]
+    na = native.BlockAllocator(NB, bs)
+    oa = OracleAllocator(NB, bs)
+    live = []
+    next_id = 0
+    for step in range(600):
+        op = rng.choice(["add", "append", "append", "fork", "cow", "free", "bad"])
+        ids = list(oa.seqs)
+        res_o = res_n = None
+        err_o = err_n = None
+        if op == "add" or not ids:
+            sid = next_id if rng.random() > 0.05 or not ids else ids[0]  # sometimes a duplicate
+            next_id += 1
+            try:
+                oa.seq_add(sid)
+            except AllocError as e:
+                err_o = e.kind
+            try:
+                na.seq_add(sid)
+            except native.PkvError as e:
+                err_n = _kind(e.code)
+        elif op == "append":
+            sid = int(rng.choice(ids))
+            n = int(rng.integers(0, 3 * bs))
+            try:
+                res_o = oa.seq_append(sid, n)
+            except AllocError as e:
+                err_o = e.kind
+            try:
+                res_n = list(na.seq_append(sid, n))
+            except native.PkvError as e:
+                err_n = _kind(e.code)
+        elif op == "fork":
+            sid = int(rng.choice(ids))
+            child = next_id
+            next_id += 1
+            oa.seq_fork(sid, child)
+            na.seq_fork(sid, child)
+        elif op == "cow":
+            sid = int(rng.choice(ids))
+            nb = len(oa.seqs[sid]["blocks"])
+            logical = -1 if rng.random() < 0.5 or nb == 0 else int(rng.integers(0, nb + 1))
+            try:
+                res_o = oa.seq_cow(sid, logical)
+            except AllocError as e:
+                err_o = e.kind
+            try:
+                res_n = na.seq_cow(sid, logical)
+            except native.PkvError as e:
+                err_n = _kind(e.code)
+        elif op == "free":
+            sid = int(rng.choice(ids))
+            oa.seq_free(sid)
+            na.seq_free(sid)
+        else:  # unknown id
+            with pytest.raises(AllocError):
+                oa.seq_free(10 ** 9)
+            with pytest.raises(native.PkvError):
+                na.seq_free(10 ** 9)
+        assert err_o == err_n, (step, op, err_o, err_n)
+        if res_o is not None or res_n is not None:
+            assert (list(res_o) if isinstance(res_o, list) else res_o) == \
+                (list(res_n) if isinstance(res_n, list) else res_n), (step, op)
+        # full state comparison
+        ids = sorted(oa.seqs)
+        assert na.num_free() == oa.num_free()
+        if ids:
+            maxb = max(1, max(len(oa.seqs[i]["blocks"]) for i in ids))
+            t_o, l_o = oa.block_table(ids, maxb)
+            t_n, l_n = na.block_table(ids, maxb)
+            assert t_n.tolist() == t_o and l_n.tolist() == l_o
+        for b in range(NB):
+            assert na.refcount(b) == oa.refcount[b]
+        # invariants
+        assert sum(oa.refcount) == sum(len(oa.seqs[i]["blocks"]) for i in ids)
+        assert oa.num_free() + sum(1 for r in oa.refcount if r > 0) == NB
+    na.close()
+
+
+def test_native_allocator_oom_leaves_state_unchanged(native):
+    a = native.BlockAllocator(4, 16)
+    a.seq_add(1)
+    a.seq_append(1, 40)  # 3 blocks
+    before = (a.block_table([1], 8), a.num_free())
+    with pytest.raises(native.PkvError) as e:
+        a.seq_append(1, 40)  # needs 3 more, 1 free
+    assert e.value.code == native.PKV_ERR_OOM
+    after = (a.block_table([1], 8), a.num_free())
+    assert np.array_equal(before[0][0], after[0][0]) and before[1] == after[1] and a.seq_len(1) == 40
+    with pytest.raises(native.PkvError) as e:
+        a.block_table([1], 2)
+    assert e.value.code == native.PKV_ERR_RANGE

@@ -1,0 +1,321 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: bit-exact for pkv_write, pkv_block_copy and the bookkeeping; for the
+bf16-in / fp32-accumulate attention output against the fp64 oracle on the same
+bf16 inputs, |out - ref| <= 1e-2 + 1e-2 * |ref| elementwise.
+
+Oracle inputs never come from the CUDA path: tables and slots come from the
+oracle allocator or the seeded generators, caches are copied to the host
+before any kernel writes them, and the oracle applies its own write and copy
+to those host copies.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import cache_ops
+from oracle.allocator import OracleAllocator
+from paged_kv_cache_276_gb300 import inputs, native
+from paged_kv_cache_276_gb300.workloads import DecodeSession
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_276_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def bits(t):
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def assert_attention_close(got_bf16, ref, what=""):
+    got = got_bf16.detach().float().cpu().double().numpy()
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
+                           f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")
+
+
+def status_tensor():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def run_decode(q, kc, vc, tables, lens, scale, partition=0, max_len=None, status=None):
+    dev = kc.device
+    tables_d = torch.as_tensor(np.asarray(tables, dtype=np.int32), device=dev)
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device=dev)
+    B, q_len, Hq, d = q.shape
+    max_len = int(np.max(lens)) if max_len is None else max_len
+    n = native.paged_attention_workspace_size(B, q_len, Hq, d, max_len, partition)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev) if n else None
+    out = torch.full_like(q, float("nan"))
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max_len, scale, out, ws, partition, status)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_decode(q, kc, vc, tables, lens, w_or_dims, scale, q_len=1):
+    Hq, Hkv, d, bs = w_or_dims
+    return OA.paged_attention(bits(q), bits(kc), bits(vc), np.asarray(tables, dtype=np.int32),
+                              np.asarray(lens, dtype=np.int32), num_q_heads=Hq, num_kv_heads=Hkv,
+                              head_dim=d, block_size=bs, scale=scale, q_len=q_len)
+
+
+def random_case(lens, d, bs, Hq, Hkv, seed, q_len=1, spare=3):
+    rng = np.random.default_rng(seed)
+    NB = sum(inputs.entries_to_fill(n, bs) for n in lens) + spare
+    tables, _ = inputs.permuted_tables(lens, bs, NB, rng, max_blocks=max(1, max(inputs.entries_to_fill(n, bs) for n in lens)) + 2)
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), seed * 10 + 1, "cuda")
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), seed * 10 + 2, "cuda")
+    q = inputs.randn_bf16((len(lens), q_len, Hq, d), seed * 10 + 3, "cuda")
+    return q, kc, vc, tables
+
+
+# ------------------------------------------------------------------ write / copy
+@pytest.mark.parametrize("d,bs,Hkv", [(128, 16, 8), (64, 32, 2)])
+def test_pkv_write_bit_exact(d, bs, Hkv):
+    rng = np.random.default_rng(d + bs)
+    NB, T = 41, 300
+    slots = inputs.distinct_slots(T, NB * bs, rng, skip_fraction=0.1)
+    k = inputs.randn_bf16((T, Hkv, d), 5, "cuda")
+    v = inputs.randn_bf16((T, Hkv, d), 6, "cuda")
+    canary = torch.full((NB, Hkv, bs, d), 0.0, dtype=torch.bfloat16, device="cuda")
+    canary.view(torch.int16).fill_(0x7FC1)  # a NaN pattern: untouched slots must keep it bit for bit
+    kc, vc = canary.clone(), canary.clone()
+    kc_h, vc_h = bits(kc), bits(vc)
+    cache_ops.write(bits(k), bits(v), slots, kc_h, vc_h, bs)
+    st = status_tensor()
+    native.pkv_write(k, v, torch.as_tensor(slots, device="cuda"), kc, vc, st)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kc), kc_h) and np.array_equal(bits(vc), vc_h)
+    assert st.item() == 0
+
+
+def test_pkv_write_out_of_range_slot_sets_status_and_is_skipped():
+    NB, bs, Hkv, d = 4, 16, 2, 64
+    k = inputs.randn_bf16((3, Hkv, d), 1, "cuda")
+    kc = torch.zeros((NB, Hkv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = kc.clone()
+    st = status_tensor()
+    native.pkv_write(k, k, torch.tensor([5, NB * bs, -3], device="cuda"), kc, vc, st)
+    torch.cuda.synchronize()
+    assert st.item() & native.PKV_STATUS_BAD_SLOT
+    expect = np.zeros((NB, Hkv, bs, d), dtype=np.uint16)
+    cache_ops.write(bits(k)[:1], bits(k)[:1], np.array([5]), expect, expect.copy(), bs)
+    assert np.array_equal(bits(kc), expect)
+
+
+@pytest.mark.parametrize("d,bs,Hkv", [(128, 16, 8), (64, 32, 2)])
+def test_pkv_block_copy_bit_exact(d, bs, Hkv):
+    rng = np.random.default_rng(7)
+    NB = 60
+    perm = rng.permutation(NB)
+    pairs = np.stack([perm[:20], perm[20:40]], axis=1).astype(np.int32)
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), 11, "cuda")
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), 12, "cuda")
+    kc_h, vc_h = bits(kc), bits(vc)
+    cache_ops.block_copy(kc_h, vc_h, pairs)
+    st = status_tensor()
+    native.pkv_block_copy(kc, vc, torch.as_tensor(pairs, device="cuda"), st)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(kc), kc_h) and np.array_equal(bits(vc), vc_h)
+    assert st.item() == 0
+    bad = torch.tensor([[0, NB], [-1, 3]], dtype=torch.int32, device="cuda")
+    native.pkv_block_copy(kc, vc, bad, st)
+    torch.cuda.synchronize()
+    assert st.item() & native.PKV_STATUS_BAD_BLOCK
+    assert np.array_equal(bits(kc), kc_h)
+
+
+# ------------------------------------------------------------------ attention
+@pytest.mark.parametrize("d,bs,Hq,Hkv,lens,partition", [
+    (64, 16, 4, 2, [17, 33, 64], 0),                      # the tiny workload's shapes
+    (128, 16, 32, 8, [1, 15, 16, 17, 511, 512, 513, 1500], 512),
+    (128, 32, 64, 8, [1, 31, 32, 33, 700, 2049], 512),
+    (128, 16, 8, 8, [5, 100, 300], 32),                   # MHA, tiny partitions
+    (128, 16, 16, 1, [77, 1024], 64),                     # group 16 (two n-tiles)
+    (64, 32, 12, 4, [3, 64, 65, 1000], 96),
+    (128, 32, 8, 2, [40, 2000], 0),
+    (64, 16, 2, 1, [0, 1, 2, 1999], 128),                 # empty sequence gives zeros
+])
+def test_decode_matches_oracle(d, bs, Hq, Hkv, lens, partition):
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=d + bs + Hq + len(lens))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_decode(q, kc, vc, tables, lens, scale, partition, status=st)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale)
+    assert_attention_close(out, ref, f"d{d} bs{bs} {Hq}/{Hkv} part{partition}")
+    assert st.item() == 0
+
+
+@pytest.mark.parametrize("d,bs,Hq,Hkv,lens,partition", [
+    (128, 16, 64, 8, [16, 17, 40, 600], 512),     # 16 x 8 = 128 rows per KV head
+    (128, 32, 64, 8, [1000, 31], 128),
+    (64, 16, 8, 2, [3, 16, 100], 32),             # rows < 16: causal rows with nothing to see
+    (128, 16, 16, 8, [530], 64),
+])
+def test_chunked_causal_query_matches_oracle(d, bs, Hq, Hkv, lens, partition):
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=3 + d + bs + Hq, q_len=16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    out = run_decode(q, kc, vc, tables, lens, scale, partition)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale, q_len=16)
+    assert_attention_close(out, ref, "chunk")
+
+
+def test_partition_size_changes_little_and_placement_changes_nothing():
+    lens = [900, 2500, 4096, 37]
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=99)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale)
+    outs = {}
+    for part in (16, 64, 512, 4096):
+        outs[part] = run_decode(q, kc, vc, tables, lens, scale, part)
+        assert_attention_close(outs[part], ref, f"partition {part}")
+    # move every block to a new physical place: same logical content, same bits out
+    NB = kc.shape[0]
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(5))
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm.cuda()] = kc
+    vc2[perm.cuda()] = vc
+    tables2 = np.where(tables >= 0, perm.numpy()[np.maximum(tables, 0)], -1).astype(np.int32)
+    moved = run_decode(q, kc2, vc2, tables2, lens, scale, 512)
+    assert torch.equal(moved.view(torch.int16), outs[512].view(torch.int16))
+
+
+def test_bad_block_and_length_set_status_without_fault():
+    lens = [40, 70]
+    d, bs, Hq, Hkv = 128, 16, 8, 2
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=5)
+    scale = 0.1
+    bad = tables.copy()
+    bad[1, 2] = kc.shape[0] + 5
+    st = status_tensor()
+    out = run_decode(q, kc, vc, bad, lens, scale, status=st)
+    assert st.item() & native.PKV_STATUS_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    # sequence 0 is untouched by the bad entry of sequence 1
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale)
+    assert_attention_close(out[:1], ref[:1])
+    st.zero_()
+    too_long = [40, tables.shape[1] * bs + 1]
+    run_decode(q, kc, vc, tables, too_long, scale, max_len=max(too_long), status=st)
+    assert st.item() & native.PKV_STATUS_BAD_LEN
+
+
+def test_unwritten_tail_slots_never_leak_nan():
+    d, bs, Hq, Hkv = 128, 16, 8, 2
+    lens = [17, 3]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=8)
+    # poison every slot past each sequence's end with NaN bit patterns
+    for i, L in enumerate(lens):
+        last = tables[i, (L - 1) // bs]
+        off = L - ((L - 1) // bs) * bs
+        kc[last, :, off:].view(torch.int16).fill_(0x7FC1)
+        vc[last, :, off:].view(torch.int16).fill_(0x7FC1)
+    out = run_decode(q, kc, vc, tables, lens, 0.09)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.09)
+    assert_attention_close(out, ref, "nan tail")
+
+
+# ------------------------------------------------------------------ workloads
+def session_step_parity(w, n_check, block_size=None, q_len=None, layers=None, check_layers=(0,),
+                        prefix_len=None, seed=0):
+    """One full step of a workload on the GPU (in the launch configuration the
+    benchmark times), the oracle on sampled sequences and layers."""
+    sess = DecodeSession(w, "cuda", allocator_factory=OracleAllocator, block_size=block_size, q_len=q_len,
+                         layers=layers, extra_steps=1, prefix_len=prefix_len)
+    pre = {l: (bits(sess.k_caches[l]), bits(sess.v_caches[l])) for l in check_layers}
+    st = status_tensor()
+    sess.apply_setup_copies(st)
+    for l in check_layers:
+        cache_ops.block_copy(pre[l][0], pre[l][1], sess.setup_cow_pairs)
+    step = sess.plan_step()
+    (q, ks, vs), = sess.new_token_tensors(1, seed=w.seed + seed)
+    outs = [torch.empty_like(q) for _ in range(sess.layers)]
+    ws = sess.workspace(step.max_len)
+    sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rng = np.random.default_rng(w.seed)
+    order = np.argsort(step.host_lens)
+    pick = sorted(set([int(order[0]), int(order[-1])] + list(rng.choice(sess.B, n_check, replace=False))))
+    slots = step.slots.cpu().numpy()
+    for l in check_layers:
+        kh, vh = pre[l]
+        cache_ops.write(bits(ks[l]), bits(vs[l]), slots, kh, vh, sess.bs)
+        assert np.array_equal(bits(sess.k_caches[l]), kh), "pkv_write / block copy not bit-exact"
+        assert np.array_equal(bits(sess.v_caches[l]), vh)
+        ref = OA.paged_attention(bits(q[pick]), kh, vh, step.host_tables[pick], step.host_lens[pick],
+                                 num_q_heads=sess.Hq, num_kv_heads=sess.Hkv, head_dim=sess.d,
+                                 block_size=sess.bs, scale=sess.scale, q_len=sess.q_len)
+        assert_attention_close(outs[l][pick], ref, f"workload {w.number} layer {l}")
+    return sess, step
+
+
+def test_workload_tiny_full():
+    session_step_parity(inputs.WORKLOADS[1], n_check=2)
+
+
+def test_workload_batched_gqa_sampled():
+    session_step_parity(inputs.WORKLOADS[2], n_check=6)
+
+
+def test_workload_continuous_batching_sampled():
+    session_step_parity(inputs.WORKLOADS[3], n_check=4, check_layers=(0, 31))
+
+
+def test_workload_shared_prefix_sampled():
+    sess, _ = session_step_parity(inputs.WORKLOADS[4], n_check=4)
+    assert len(sess.setup_cow_pairs) == 64 * 7
+
+
+def test_workload_shared_prefix_partial_block_cow():
+    w = inputs.WORKLOADS[4]
+    sess, _ = session_step_parity(w, n_check=3, prefix_len=2043, seed=1)
+    assert len(sess.setup_cow_pairs) == 64 * 7
+
+
+@pytest.mark.parametrize("bs,q_len", [(16, 1), (32, 1), (16, 16), (32, 16)])
+def test_workload_long_context_sampled(bs, q_len):
+    session_step_parity(inputs.WORKLOADS[5], n_check=1 if q_len == 16 else 2, block_size=bs, q_len=q_len)
+
+
+def test_shared_prefix_layout_equals_private_copies_bit_exact():
+    """Refcounted shared blocks and fully private copies give identical bits."""
+    w = inputs.WORKLOADS[4]
+    sess = DecodeSession(w, "cuda", allocator_factory=OracleAllocator, extra_steps=1)
+    sess.apply_setup_copies()
+    step = sess.plan_step()
+    (q, ks, vs), = sess.new_token_tensors(1, seed=3)
+    sess.run_step(step, q, ks, vs, out := torch.empty_like(q), sess.workspace(step.max_len))
+    torch.cuda.synchronize()
+    # private layout: copy every sequence's blocks to fresh places, one owner each
+    kc, vc = sess.k_caches[0], sess.v_caches[0]
+    T = step.host_tables
+    used = [(i, j) for i in range(sess.B) for j in range(inputs.entries_to_fill(step.host_lens[i], sess.bs))]
+    kc2 = torch.empty((len(used) + 1,) + tuple(kc.shape[1:]), dtype=kc.dtype, device="cuda")
+    vc2 = torch.empty_like(kc2)
+    T2 = np.full_like(T, -1)
+    src = torch.as_tensor([T[i, j] for i, j in used], device="cuda", dtype=torch.long)
+    kc2[:len(used)] = kc[src]
+    vc2[:len(used)] = vc[src]
+    for n, (i, j) in enumerate(used):
+        T2[i, j] = n
+    out2 = run_decode(q, kc2, vc2, T2, step.host_lens, sess.scale, sess.partition_size, step.max_len)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
