@@ -167,6 +167,38 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                            int partition_size, pkv_bf16 *out, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, void *stream);
 
+/*
+ * paged_attention_decode_static_scratch -- paged_attention_decode without a
+ * caller-provided workspace and without allocating anything.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory: an engine that hands all of device memory to
+ * its own arena at start-up and allows no allocation afterwards, or a plugin
+ * whose host framework owns every allocation.  Arguments and results are those
+ * of paged_attention_decode minus workspace / workspace_bytes.
+ *
+ * The split-K scratch is a fixed array of PKV_STATIC_SCRATCH_BYTES inside the
+ * library; every GPU that loads the library keeps it until the process exits.
+ * Calls whose scratch need (paged_attention_workspace_size) is larger return
+ * PKV_ERR_WORKSPACE and launch nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture.  The call never invokes
+ * cudaMalloc, cudaFree or any other allocating routine.  All calls share the
+ * one array: calls whose kernels overlap on the GPU (different streams, or
+ * several host threads) race on it and give undefined results; serialise them.
+ * Nothing in the array needs to start at zero.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)  /* 8 MiB */
+
+int paged_attention_decode_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                          const pkv_bf16 *v_cache, const int32_t *block_tables,
+                                          int max_blocks_per_seq, const int32_t *seq_lens,
+                                          int num_seqs, int max_seq_len, int q_len,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, float scale,
+                                          int partition_size, pkv_bf16 *out, int32_t *d_status,
+                                          void *stream);
+
 /* ------------------------------------------------------------------------
  * Host block allocator: pool, block tables, refcounts, copy-on-write.
  *

@@ -765,3 +765,70 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of paged_attention_decode.
+//
+// Some callers cannot allocate device memory at all: an engine that carves all
+// of device memory into its own arena at start-up and forbids allocations
+// afterwards, or a plugin whose host framework owns every allocation and gives
+// the plugin no allocator.  For them the split-K scratch lives in this
+// fixed-size array, which every GPU that loads this library keeps until the
+// process exits.  Host code must not use the array's name as a device address
+// (on the host it is only a stand-in); the real address is looked up once per
+// device with cudaGetSymbolAddress, with that device current.
+namespace {
+
+constexpr size_t kStaticScratchBytes = PKV_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (set up on first use).
+int static_scratch_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    pkv::set_cuda_error(e);
+    return PKV_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess || !ptr) {
+      pkv::set_cuda_error(e);
+      return PKV_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_attention_decode_static_scratch(
+    const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+    int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+    int partition_size, pkv_bf16 *out, int32_t *d_status, void *stream) {
+  pkv::Plan plan;
+  if (!pkv::make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &plan))
+    return PKV_ERR_ARG;
+  if (plan.ws_bytes() > kStaticScratchBytes) return PKV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if (plan.ws_bytes() > 0) {
+    const int rc = static_scratch_address(&scratch);
+    if (rc != PKV_OK) return rc;
+  }
+  // No part of the scratch has to start at zero: every partial the combine
+  // step reads is written by the same call first.
+  return paged_attention_decode(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                max_seq_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                num_blocks, scale, partition_size, out, scratch,
+                                plan.ws_bytes() > 0 ? kStaticScratchBytes : 0, d_status, stream);
+}

@@ -48,6 +48,9 @@ SIGNATURES = {
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                         _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
                                         _c_ptr]),
+    "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
+                                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                                       _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, ctypes.POINTER(_c_ptr)]),
     "pkv_alloc_destroy": (None, [_c_ptr]),
     "pkv_seq_add": (_c_int, [_c_ptr, _c_i64]),
@@ -172,6 +175,26 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
         int(max_seq_len), q_len, Hq, Hkv, d, bs, NB, float(scale), int(partition_size), _ptr(out),
         _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_decode")
+
+
+STATIC_SCRATCH_BYTES = 8 << 20  # PKV_STATIC_SCRATCH_BYTES
+
+
+def paged_attention_decode_static_scratch(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, out,
+                                          partition_size=0, d_status=None, stream=None):
+    """paged_attention_decode for callers that cannot allocate: the split-K
+    scratch is the library's fixed array (see include/pkv.h)."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (out, "out", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    B, q_len, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    _check(lib().paged_attention_decode_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+        int(max_seq_len), q_len, Hq, Hkv, d, bs, NB, float(scale), int(partition_size), _ptr(out),
+        _ptr(d_status), _stream(stream, dev)), "paged_attention_decode_static_scratch")
 
 
 # ------------------------------------------------------------- allocator
