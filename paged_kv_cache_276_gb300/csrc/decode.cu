@@ -31,6 +31,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "internal.h"
 #include "pkv.h"
@@ -44,6 +45,7 @@ constexpr int kDecodeWarps = 4;  // consumer warps, q_len = 1
 constexpr int kChunkWarps = 8;   // consumer warps, q_len = 16
 constexpr int kChunkLen = 16;
 constexpr int kDefaultPartition = 512;
+constexpr float kRescaleSlack = 8.f;  // log2 units: weights stay below 256
 
 struct Params {
   const __nv_bfloat16 *q;       // [B][q_len][Hq][D]
@@ -102,6 +104,49 @@ struct WarpAcc {
   }
 };
 
+// Running-max update shared by the block steps.  The reference max moves only
+// when a column's block max exceeds it by more than kRescaleSlack (log2 units),
+// so most blocks skip rescaling the accumulators.  Exact: numerator and
+// denominator use the same reference, and every weight stays below
+// 2^kRescaleSlack.  bmax holds the thread's column maxima (reduced here over
+// the lanes sharing a column); msub receives the reference to subtract.
+template <int D, int NT>
+__device__ __forceinline__ void online_max_update(WarpAcc<D, NT> &acc, float (&bmax)[NT][2],
+                                                  float (&msub)[NT][2]) {
+  float alpha[NT][2];
+  bool rescale = false;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float b = bmax[nt][e];
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 4));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 8));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 16));
+      const float m = acc.m[nt][e];
+      alpha[nt][e] = 1.f;
+      if (b > m + kRescaleSlack) {  // also true while m is -inf and b finite
+        alpha[nt][e] = m == -INFINITY ? 0.f : exp2f(m - b);
+        acc.m[nt][e] = b;
+        rescale = true;
+      }
+      msub[nt][e] = acc.m[nt][e] == -INFINITY ? 0.f : acc.m[nt][e];
+    }
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        acc.l[nt][e] *= alpha[nt][e];
+#pragma unroll
+        for (int md = 0; md < D / 16; ++md) {
+          acc.o[md][nt][e] *= alpha[nt][e];
+          acc.o[md][nt][e + 2] *= alpha[nt][e];
+        }
+      }
+  }
+}
+
 // One block of keys for one warp's columns.
 //   qf:    B fragments of Q^T (column = query row) per n-tile and 16-wide d step
 //   valid: keys of this block that hold tokens (1..BS)
@@ -115,12 +160,15 @@ __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
   const int r8 = lane & 7, mi = lane >> 3;
   const int g4 = lane >> 2, c4 = lane & 3;
 
-  // S^T[key][col] = K[key][:] . Q[col][:]
-  float sc[MT][NT][4];
+  // S^T[key][col] = K[key][:] . Q[col][:]; even and odd d-steps accumulate in
+  // separate registers so the two MMA chains overlap
+  float sc[MT][NT][4], sc2[MT][NT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[mt][nt][i] = sc2[mt][nt][i] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
@@ -128,7 +176,10 @@ __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
       uint32_t a[4];
       ldsm_x4(swz<BS>(kbase, mt * 16 + r8 + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+      for (int nt = 0; nt < NT; ++nt) {
+        if (ks & 1) mma_bf16_16816(sc2[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+        else mma_bf16_16816(sc[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+      }
     }
   }
 
@@ -143,30 +194,12 @@ __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int key = mt * 16 + g4 + (i >> 1) * 8;
-        const float s = key < vis[nt][i & 1] ? sc[mt][nt][i] * scale_log2 : -INFINITY;
+        const float s = key < vis[nt][i & 1] ? (sc[mt][nt][i] + sc2[mt][nt][i]) * scale_log2 : -INFINITY;
         sc[mt][nt][i] = s;
         bmax[nt][i & 1] = fmaxf(bmax[nt][i & 1], s);
       }
   float msub[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float b = bmax[nt][e];
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 4));
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 8));
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 16));
-      const float mn = fmaxf(acc.m[nt][e], b);
-      const float alpha = mn == -INFINITY ? 1.f : exp2f(acc.m[nt][e] - mn);
-      msub[nt][e] = mn == -INFINITY ? 0.f : mn;
-      acc.m[nt][e] = mn;
-      acc.l[nt][e] *= alpha;
-#pragma unroll
-      for (int md = 0; md < D / 16; ++md) {
-        acc.o[md][nt][e] *= alpha;
-        acc.o[md][nt][e + 2] *= alpha;
-      }
-    }
+  online_max_update<D, NT>(acc, bmax, msub);
 
   // probabilities -> bf16 -> B fragments of P^T (movmatrix transposes the
   // accumulator layout into the operand layout)
@@ -225,46 +258,55 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Producer: walk this partition's block-table entries and stream K/V tiles
-// into the ring.  empty_parity_base lets several consumer warps release a
-// stage (count given at init).
+// Producer (one whole warp): walk this partition's block-table entries and
+// stream K/V tiles into the ring.  The warp reads 32 table entries with one
+// coalesced load and lane 0 issues the copies.  Stages are released by the
+// consumers through the empty barriers (count given at init).
 template <int D, int BS>
-__device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq,
-                        int h, int blk0, int nblk, uint32_t ring, uint32_t full0, uint32_t empty0,
-                        volatile int *abort_flag) {
+__device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq, int h,
+                        int blk0, int nblk, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        volatile int *abort_flag, int lane) {
   using T = Tile<D, BS>;
   constexpr int S = T::kStages;
   const uint64_t pol = l2_policy_evict_first();
   const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
-  int issued = 0;
+  int issued = 0, window = 0;
   for (int j = 0; j < nblk; ++j) {
+    if ((j & 31) == 0) window = j + lane < nblk ? tbl[j + lane] : -1;
+    const int b = __shfl_sync(0xffffffffu, window, j & 31);
     const int s = j % S;
-    if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) {
-      if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
-      *abort_flag = 1;
+    bool ok = true;
+    if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) ok = false;
+    const bool timed_out = __any_sync(0xffffffffu, !ok);
+    if (timed_out || __any_sync(0xffffffffu, *abort_flag != 0)) {  // warp-uniform decision
+      if (lane == 0) {
+        if (p.status && timed_out) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+        *abort_flag = 1;
+      }
       break;
     }
-    if (*abort_flag) break;
-    const int b = tbl[j];
-    int row;
-    if (b >= 0 && b < p.num_blocks) {
-      row = (b * p.num_kv_heads + h) * BS;
-    } else {
-      if (p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
-      row = p.oob_row;  // zero fill
+    if (lane == 0) {
+      int row;
+      if (b >= 0 && b < p.num_blocks) {
+        row = (b * p.num_kv_heads + h) * BS;
+      } else {
+        if (p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+        row = p.oob_row;  // zero fill
+      }
+      const uint32_t full = full0 + 8 * s;
+      mbar_arrive_expect_tx(full, T::kStageBytes);
+      const uint32_t kdst = ring + s * T::kStageBytes;
+      const uint32_t vdst = kdst + T::kTileBytes;
+#pragma unroll
+      for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(kdst + hf * T::kBoxBytes, tmk, hf * 64, row, full, pol);
+#pragma unroll
+      for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(vdst + hf * T::kBoxBytes, tmv, hf * 64, row, full, pol);
     }
-    const uint32_t full = full0 + 8 * s;
-    mbar_arrive_expect_tx(full, T::kStageBytes);
-    const uint32_t kdst = ring + s * T::kStageBytes;
-    const uint32_t vdst = kdst + T::kTileBytes;
-#pragma unroll
-    for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(kdst + hf * T::kBoxBytes, tmk, hf * 64, row, full, pol);
-#pragma unroll
-    for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(vdst + hf * T::kBoxBytes, tmv, hf * 64, row, full, pol);
     ++issued;
   }
   // never leave a copy in flight into this CTA's shared memory
-  for (int j = issued > S ? issued - S : 0; j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
+  if (lane == 0)
+    for (int j = issued > S ? issued - S : 0; j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
 }
 
 // ------------------------------------------------------------- q_len = 1
@@ -285,6 +327,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();  // inputs may come from the kernel launched just before
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
@@ -311,7 +354,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   WarpAcc<D, NT> acc;
   if (warp == kDecodeWarps) {
-    if (lane == 0) produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
     uint32_t qf[NT][D / 16][2];
@@ -418,6 +461,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
 
   const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();  // inputs may come from the kernel launched just before
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
@@ -444,7 +488,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   __syncthreads();
 
   if (warp == kChunkWarps) {
-    if (lane == 0) produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag, lane);
     return;
   }
   if (warp >= p.active_warps) return;
@@ -547,6 +591,7 @@ template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
                                                       int rows) {
   constexpr int PER = D / 32;
+  grid_dependency_wait();  // the partials come from the grid launched just before
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= total_rows) return;
@@ -652,6 +697,25 @@ cudaError_t raise_smem_limit(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
+// Launch with programmatic stream serialisation: the grid may start while the
+// previous kernel in the stream drains; it waits (griddepcontrol.wait) before
+// reading anything.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int D, int BS>
 int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int num_seqs, int q_len,
            cudaStream_t stream) {
@@ -662,23 +726,24 @@ int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int 
     if (p.group <= 8) {
       auto k = decode_kernel<D, BS, 1>;
       if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
-      k<<<grid, (kDecodeWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+      e = launch_pdl(k, grid, dim3((kDecodeWarps + 1) * 32), smem, stream, tmk, tmv, p);
     } else {
       auto k = decode_kernel<D, BS, 2>;
       if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
-      k<<<grid, (kDecodeWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+      e = launch_pdl(k, grid, dim3((kDecodeWarps + 1) * 32), smem, stream, tmk, tmv, p);
     }
   } else {
     auto k = chunk_kernel<D, BS>;
     if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
-    k<<<grid, (kChunkWarps + 1) * 32, smem, stream>>>(tmk, tmv, p);
+    e = launch_pdl(k, grid, dim3((kChunkWarps + 1) * 32), smem, stream, tmk, tmv, p);
   }
-  int rc = check_launch();
-  if (rc != PKV_OK || p.max_parts <= 1) return rc;
+  if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+  if (p.max_parts <= 1) return PKV_OK;
   const int rows = q_len * p.num_q_heads;
   const int total = num_seqs * rows;
-  combine_kernel<D><<<(total + 3) / 4, 128, 0, stream>>>(p, BS, total, rows);
-  return check_launch();
+  e = launch_pdl(combine_kernel<D>, dim3((total + 3) / 4), dim3(128), 0, stream, p, BS, total, rows);
+  if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 }  // namespace
