@@ -1,0 +1,582 @@
+// Chunked causal query (16 tokens) on the 5th-generation tensor cores.
+//
+// For one KV head the 16 query tokens x 8 query heads of the group form a
+// 128-row block Q (row r = token (r / 8), head (r % 8)).  Over each 64-key
+// tile of the paged cache:
+//     S  = Q K^T                     tcgen05.mma, M 128 x N 64 x K 128 -> TMEM
+//     P  = exp2(S * scale*log2e - m)  softmax warps, one query row per thread
+//     O += P V                       tcgen05.mma, M 128 x N 128 x K 64 -> TMEM
+// with the running max / sum of online softmax (x321.org "The serving
+// bottleneck is not just FLOPs", section "First understand what the KV cache
+// is storing"; the causal chunk follows the same page's section "Continuous
+// batching is the other half of the story" on chunked prefill).
+//
+// Persistent grid, one CTA per SM.  CTA c takes a contiguous range of the
+// (sequence, KV head, partition) items.  Consecutive items of the same
+// (sequence, KV head) accumulate into the same TMEM accumulator; at the end
+// of such a run the CTA writes one partial (max, sum, unnormalised O) into the
+// slot of the run's first partition and marks the run's other partitions
+// empty, and the split-K combine kernel merges the slots.  A sequence with a
+// single partition gets its bf16 output directly.
+//
+// Warp roles: 0-3 softmax + epilogue (thread = row), 4 TMA producer, 5 MMA
+// issuer (one lane) and tensor-memory owner.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "pkv.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kD = 128;          // head dim
+constexpr int kRows = 128;       // 16 tokens x 8 heads
+constexpr int kQLen = 16;
+constexpr int kGroup = 8;
+constexpr int kTileKeys = 64;    // keys per MMA tile
+constexpr int kStages = 4;       // K/V ring
+constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
+constexpr int kKVBytes = kTileKeys * kD * 2;     // 16 KiB each for K and V: [half][64 rows][128 B]
+constexpr int kStageBytes = 2 * kKVBytes;
+constexpr int kPBytes = kRows * 128;             // [128 rows][64 keys x 2 B]
+constexpr int kSmemQ = 0;
+constexpr int kSmemRing = kSmemQ + kQBytes;
+constexpr int kSmemP = kSmemRing + kStages * kStageBytes;
+constexpr int kSmemBars = kSmemP + 2 * kPBytes;
+constexpr int kTmemCols = 256;   // O: 128 columns, S: 2 x 64
+constexpr int kThreads = 6 * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
+
+// barrier indices (8 bytes each, after the P buffers)
+enum : int {
+  B_Q_FULL = 0, B_Q_FREE, B_O_FULL, B_O_FREE,
+  B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
+  B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1,
+  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_COUNT = B_KV_EMPTY0 + kStages
+};
+
+struct TcParams {
+  const int32_t *block_tables;
+  const int32_t *seq_lens;
+  __nv_bfloat16 *out;   // [B][16][Hq][128]
+  float *ws_o;          // [B * 16 * Hq][P][128]
+  float2 *ws_ml;        // [B * 16 * Hq][P]
+  int32_t *status;
+  int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
+  int part_tokens, max_parts, oob_row;
+  float scale_log2;
+};
+
+// Walks the (sequence, KV head, partition) items in order.
+struct ItemWalker {
+  int seq, head, part, nparts;
+  __device__ void seek(const int *prefix, int num_seqs, int hkv, int it) {
+    int lo = 0, hi = num_seqs;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= it) lo = mid; else hi = mid;
+    }
+    seq = lo;
+    nparts = (prefix[seq + 1] - prefix[seq]) / hkv;
+    const int off = it - prefix[seq];
+    head = off / nparts;
+    part = off - head * nparts;
+  }
+  __device__ void next(const int *prefix, int num_seqs, int hkv) {
+    if (++part < nparts) return;
+    part = 0;
+    if (++head < hkv) return;
+    head = 0;
+    if (++seq < num_seqs) nparts = (prefix[seq + 1] - prefix[seq]) / hkv;
+  }
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Bounded wait whose outcome every lane of the warp agrees on.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBars);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [B + 1] items before each sequence
+  int *lens = prefix + p.num_seqs + 1;                    // [B] clamped lengths
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = p.num_seqs, hkv = p.num_kv_heads;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+
+  grid_dependency_wait();
+
+  if (warp == 0) {  // items per sequence -> exclusive prefix
+    const int per = (B + 31) / 32;
+    const int lo = min(B, lane * per), hi = min(B, lo + per);
+    const int cap_tbl = p.max_blocks * BS, cap_grid = p.max_parts * p.part_tokens;
+    const int cap = cap_tbl < cap_grid ? cap_tbl : cap_grid;
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) {
+      int L = p.seq_lens[i];
+      if (L < 0 || L > cap) {
+        if (blockIdx.x == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+        L = L < 0 ? 0 : cap;
+      }
+      lens[i] = L;
+      const int n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
+      prefix[i + 1] = n;
+      sum += n;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      run += prefix[i + 1];
+      prefix[i + 1] = run;
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_FREE), 1);
+    mbar_init(bar(B_O_FULL), 1);
+    mbar_init(bar(B_O_FREE), kRows);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_S_FULL0 + i), 1);
+      mbar_init(bar(B_S_FREE0 + i), kRows);
+      mbar_init(bar(B_P_FULL0 + i), kRows);
+      mbar_init(bar(B_PV_DONE0 + i), 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_KV_FULL0 + s), 1);
+      mbar_init(bar(B_KV_EMPTY0 + s), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 5) {
+    tc::alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::relinquish();
+  }
+  if (threadIdx.x == 128) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int I = prefix[B];
+  const int it0 = static_cast<int>((static_cast<long long>(blockIdx.x) * I + gridDim.x - 1) / gridDim.x);
+  const int it1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * I + gridDim.x - 1) / gridDim.x);
+  const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing), sP = smem_u32(smem + kSmemP);
+  const uint32_t tO = tmem, tS0 = tmem + 128;
+
+  // key range of an item: [k_lo, k_hi)
+  auto item_keys = [&](const ItemWalker &w, int &k_lo, int &k_hi) {
+    const int L = lens[w.seq];
+    k_lo = w.part * p.part_tokens;
+    k_hi = min(L, k_lo + p.part_tokens);
+    if (k_hi < k_lo) k_hi = k_lo;
+  };
+
+  if (it0 < it1) {
+    if (warp == 4) {
+      // ------------------------------------------------------------ producer
+      const uint64_t pol = l2_policy_evict_first();
+      ItemWalker w;
+      w.seek(prefix, B, hkv, it0);
+      int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+      int tw_seq = -1, tw_base = 0, tw_val = -1;
+      for (int it = it0; it < it1 && !*abort_flag; ++it, w.next(prefix, B, hkv)) {
+        int k_lo, k_hi;
+        item_keys(w, k_lo, k_hi);
+        const bool new_run = w.seq != prev_seq || w.head != prev_head;
+        prev_seq = w.seq;
+        prev_head = w.head;
+        if (new_run && k_hi > k_lo) {  // a run with keys: load its queries
+          ++tpieces;
+          if (tpieces > 1 && !wait_warp(bar(B_Q_FREE), (tpieces - 2) & 1)) {
+            if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q_FULL), kQBytes);
+            for (int hf = 0; hf < 2; ++hf)
+              asm volatile(
+                  "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + hf * (kQBytes / 2)),
+                  "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(hf * 64), "r"(w.head * kGroup), "r"(w.seq * kQLen),
+                  "r"(bar(B_Q_FULL))
+                  : "memory");
+          }
+        }
+        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
+        for (int t = 0; t < ntile; ++t, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !wait_warp(bar(B_KV_EMPTY0 + s), ((g / kStages) - 1) & 1)) {
+            if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          const int blk_first = (k_lo + t * kTileKeys) / BS;
+          constexpr int kBlocks = kTileKeys / BS;
+          if (w.seq != tw_seq || blk_first < tw_base || blk_first + kBlocks > tw_base + 32) {
+            tw_seq = w.seq;
+            tw_base = blk_first;
+            const int e = blk_first + lane;
+            tw_val = e < p.max_blocks ? p.block_tables[static_cast<size_t>(w.seq) * p.max_blocks + e] : -1;
+          }
+          const int nblk_seq = ceil_div(lens[w.seq], BS);
+          int bids[kBlocks];
+#pragma unroll
+          for (int j = 0; j < kBlocks; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
+          if (lane == 0) {
+            const uint32_t st = sRing + s * kStageBytes;
+            mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), kStageBytes);
+#pragma unroll
+            for (int j = 0; j < kBlocks; ++j) {
+              const int b = bids[j];
+              int row;
+              if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
+                row = (b * hkv + w.head) * BS;
+              } else {
+                if (blk_first + j < nblk_seq && p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+                row = p.oob_row;  // past the sequence, or a bad id: zeros
+              }
+              for (int hf = 0; hf < 2; ++hf) {
+                tma_load_2d(st + hf * (kKVBytes / 2) + j * BS * 128, &tmk, hf * 64, row, bar(B_KV_FULL0 + s), pol);
+                tma_load_2d(st + kKVBytes + hf * (kKVBytes / 2) + j * BS * 128, &tmv, hf * 64, row,
+                            bar(B_KV_FULL0 + s), pol);
+              }
+            }
+          }
+        }
+      }
+      // never leave a copy in flight into this CTA's shared memory
+      if (lane == 0) {
+        for (int x = g > kStages ? g - kStages : 0; x < g; ++x)
+          mbar_wait(bar(B_KV_FULL0 + (x % kStages)), (x / kStages) & 1);
+        if (tpieces > 0) mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1);
+      }
+    } else if (warp == 5) {
+      // ------------------------------------------------------------- MMA
+      if (lane == 0) {
+        constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
+        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
+        ItemWalker w;
+        w.seek(prefix, B, hkv, it0);
+        int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+        // the tile whose P V product is still to be issued, with its run index
+        int pend = -1, pend_run = 0;
+        bool pend_first = false, pend_last = false;
+        bool ok = true;
+        auto issue_pv = [&](int x, int run, bool first, bool last) {
+          const int pb = x & 1;
+          if (!mbar_wait(bar(B_P_FULL0 + pb), (x >> 1) & 1)) return false;
+          // the first product of run j overwrites O: run j-1's epilogue must have read it
+          if (first && run > 1 && !mbar_wait(bar(B_O_FREE), (run - 2) & 1)) return false;
+          tc::fence_after();
+          const uint32_t pa = sP + pb * kPBytes;
+          const uint32_t vb = sRing + (x % kStages) * kStageBytes + kKVBytes;
+#pragma unroll
+          for (int ks = 0; ks < kTileKeys / 16; ++ks)
+            tc::mma(tO, tc::desc_sw128(pa + ks * 32, 16, 1024), tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024),
+                    kIdO, !(first && ks == 0));
+          tc::commit(bar(B_PV_DONE0 + pb));
+          tc::commit(bar(B_KV_EMPTY0 + (x % kStages)));
+          if (last) tc::commit(bar(B_O_FULL));
+          return true;
+        };
+        for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
+          int k_lo, k_hi;
+          item_keys(w, k_lo, k_hi);
+          const bool new_run = w.seq != prev_seq || w.head != prev_head;
+          prev_seq = w.seq;
+          prev_head = w.head;
+          ItemWalker nx = w;
+          nx.next(prefix, B, hkv);
+          const bool run_ends = it + 1 >= it1 || nx.seq != w.seq || nx.head != w.head;
+          const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
+          if (new_run && ntile > 0) {
+            ++tpieces;
+            if (!mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1)) { ok = false; break; }
+          }
+          for (int t = 0; t < ntile; ++t, ++g) {
+            const int s = g % kStages, sb = g & 1;
+            if (!mbar_wait(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+            if (g >= 2 && !mbar_wait(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
+            tc::fence_after();
+            const uint32_t kb = sRing + s * kStageBytes;
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks)
+              tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sQ + (ks >> 2) * (kQBytes / 2) + (ks & 3) * 32, 16, 1024),
+                      tc::desc_sw128(kb + (ks >> 2) * (kKVBytes / 2) + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
+            tc::commit(bar(B_S_FULL0 + sb));
+            const bool last_of_run = run_ends && t == ntile - 1;
+            if (last_of_run) tc::commit(bar(B_Q_FREE));  // the queries are only read by MMAs issued so far
+            if (pend >= 0 && !issue_pv(pend, pend_run, pend_first, pend_last)) { ok = false; break; }
+            pend = g;
+            pend_run = tpieces;
+            pend_first = new_run && t == 0;
+            pend_last = last_of_run;
+          }
+        }
+        if (ok && pend >= 0) ok = issue_pv(pend, pend_run, pend_first, pend_last);
+        if (!ok) {
+          if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+    } else {
+      // ------------------------------------------------------ softmax warps
+      const int r = threadIdx.x;                  // query row = TMEM lane
+      const int tok = r / kGroup, gh = r % kGroup;
+      const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+      ItemWalker w;
+      w.seek(prefix, B, hkv, it0);
+      int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+      float m = -INFINITY, l = 0.f;
+      int run_first_part = 0;
+      bool run_has_tiles = false;
+      bool ok = true;
+      for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
+        const int L = lens[w.seq];
+        int k_lo, k_hi;
+        item_keys(w, k_lo, k_hi);
+        if (w.seq != prev_seq || w.head != prev_head) {
+          prev_seq = w.seq;
+          prev_head = w.head;
+          m = -INFINITY;
+          l = 0.f;
+          run_first_part = w.part;
+          run_has_tiles = false;
+        }
+        const int limit = L - kQLen + 1 + tok;  // this row sees keys t < limit
+        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
+        for (int t = 0; t < ntile; ++t, ++g) {
+          const bool first_tile_of_run = !run_has_tiles;
+          if (first_tile_of_run) {
+            run_has_tiles = true;
+            ++tpieces;
+          }
+          const int sb = g & 1;
+          if (!wait_warp(bar(B_S_FULL0 + sb), (g >> 1) & 1)) { ok = false; break; }
+          tc::fence_after();
+          uint32_t sv[kTileKeys];
+          tc::ld32(tS0 + sb * kTileKeys + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tc::ld32(tS0 + sb * kTileKeys + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+          tc::wait_ld();
+          tc::fence_before();
+          mbar_arrive(bar(B_S_FREE0 + sb));
+          const int k0 = k_lo + t * kTileKeys;
+          const int vis = min(limit, k_hi) - k0;  // keys of this tile the row sees
+          float bm = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) {
+            const float s = c < vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+            sv[c] = __float_as_uint(s);
+            bm = fmaxf(bm, s);
+          }
+          // move the reference max only when a score passes it by more than
+          // kSlack (rare after a run's first tile); exact, since O and l share it
+          const bool move = bm > m + kSlack;
+          const bool scale_o = move && !first_tile_of_run && m != -INFINITY;
+          if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
+            // O must hold every earlier P V and none in flight: wait for the previous tile's
+            const int x = g - 1;
+            if (!wait_warp(bar(B_PV_DONE0 + (x & 1)), (x >> 1) & 1)) { ok = false; break; }
+            tc::fence_after();
+            const float alpha = scale_o ? exp2f(m - bm) : 1.f;
+#pragma unroll
+            for (int ch = 0; ch < kD / 32; ++ch) {
+              uint32_t ov[32];
+              tc::ld32(tO + lane_off + ch * 32, ov);
+              tc::wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+              tc::st32(tO + lane_off + ch * 32, ov);
+            }
+            tc::wait_st();
+          }
+          if (move) {
+            l = m == -INFINITY ? 0.f : l * exp2f(m - bm);
+            m = bm;
+          }
+          const float msub = m == -INFINITY ? 0.f : m;
+          // P buffer (g & 1) was last read by tile g - 2
+          if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
+          const uint32_t prow = sP + sb * kPBytes + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t packed =
+                  pack_bf16x2(exp2f(__uint_as_float(sv[c16 * 8 + 2 * j]) - msub),
+                              exp2f(__uint_as_float(sv[c16 * 8 + 2 * j + 1]) - msub));
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&packed));
+              l += f.x + f.y;
+              pk[j] = packed;
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c16 ^ (r & 7)) << 4)), "r"(pk[0]),
+                         "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                         : "memory");
+          }
+          // value rows past the sequence end were never written: zero them
+          const int exist = L - k0;
+          if (exist < kTileKeys) {
+            const int s = g % kStages;
+            if (!wait_warp(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+            const uint32_t vb = sRing + s * kStageBytes + kKVBytes;
+            const int first = exist < 0 ? 0 : exist;
+            for (int e = r; e < (kTileKeys - first) * 2 * 8; e += kRows) {  // 16-byte chunks
+              const int row = first + e / 16, rem = e % 16, hf = rem / 8, c = rem % 8;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + hf * (kKVBytes / 2) + row * 128 + c * 16),
+                           "r"(0u)
+                           : "memory");
+            }
+          }
+          fence_proxy_async_shared();
+          tc::fence_before();
+          mbar_arrive(bar(B_P_FULL0 + sb));
+        }
+        if (!ok) break;
+        // ---- end of a run: epilogue
+        ItemWalker nx = w;
+        nx.next(prefix, B, hkv);
+        const bool run_ends = it + 1 >= it1 || nx.seq != w.seq || nx.head != w.head;
+        if (!run_ends) continue;
+        const int nparts = w.nparts;
+        const size_t orow = (static_cast<size_t>(w.seq) * kQLen + tok) * p.num_q_heads + w.head * kGroup + gh;
+        if (run_has_tiles && !wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
+        tc::fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kD / 32; ++ch) {
+          uint32_t ov[32];
+          if (run_has_tiles) {
+            tc::ld32(tO + lane_off + ch * 32, ov);
+            tc::wait_ld();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = 0u;
+          }
+          if (nparts == 1) {
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 0]) * inv, __uint_as_float(ov[c8 * 8 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 2]) * inv, __uint_as_float(ov[c8 * 8 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 4]) * inv, __uint_as_float(ov[c8 * 8 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 6]) * inv, __uint_as_float(ov[c8 * 8 + 7]) * inv);
+              dst[c8] = v;
+            }
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + run_first_part) * kD + ch * 32);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              dst[c4] = make_float4(__uint_as_float(ov[c4 * 4]), __uint_as_float(ov[c4 * 4 + 1]),
+                                    __uint_as_float(ov[c4 * 4 + 2]), __uint_as_float(ov[c4 * 4 + 3]));
+          }
+        }
+        if (run_has_tiles) {
+          tc::fence_before();
+          mbar_arrive(bar(B_O_FREE));
+        }
+        if (nparts > 1) {
+          p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(m, l);
+          for (int q = run_first_part + 1; q <= w.part; ++q)  // merged into the run's first slot
+            p.ws_ml[orow * p.max_parts + q] = make_float2(-INFINITY, 0.f);
+        }
+      }
+      if (!ok) {
+        if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int part_tokens) {
+  return q_len == kQLen && head_dim == kD && num_q_heads == kGroup * num_kv_heads && num_seqs <= 2048 &&
+         (block_size == 16 || block_size == 32) && part_tokens % kTileKeys == 0;
+}
+
+int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
+  const int B = a.num_seqs;
+  CUtensorMap tmq, tmk, tmv;
+  // q viewed as [B*16][Hq][128]: box = 64 columns x 8 heads x 16 tokens
+  if (!make_tensor_map_3d(&tmq, a.q, kD, a.num_q_heads, static_cast<long long>(B) * kQLen, 64, kGroup, kQLen) ||
+      !make_tensor_map_2d(&tmk, a.k_cache, kD, a.rows, 64, a.block_size) ||
+      !make_tensor_map_2d(&tmv, a.v_cache, kD, a.rows, 64, a.block_size))
+    return PKV_ERR_CUDA;
+  TcParams p{};
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.out = reinterpret_cast<__nv_bfloat16 *>(a.out);
+  p.ws_o = a.ws_o;
+  p.ws_ml = static_cast<float2 *>(a.ws_ml);
+  p.status = a.status;
+  p.num_seqs = B;
+  p.max_blocks = a.max_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.num_blocks = a.num_blocks;
+  p.part_tokens = a.part_tokens;
+  p.max_parts = a.max_parts;
+  p.oob_row = static_cast<int>(a.rows);
+  p.scale_log2 = a.scale * kLog2e;
+  const size_t smem = 1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * static_cast<size_t>(B) + 1) * 4;
+  cudaError_t e;
+  void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) =
+      a.block_size == 16 ? chunk_tc_kernel<16> : chunk_tc_kernel<32>;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * 2048 + 1) * 4))) !=
+      cudaSuccess)
+    return set_cuda_error(e), PKV_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, tmq, tmk, tmv, p);
+  if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -614,7 +614,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_
   for (int k = 0; k < PER; ++k) accv[k] = 0.f;
   for (int i = 0; i < nparts; ++i) {
     const float2 v = ml[i];
-    const float f = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+    if (v.x == -INFINITY) continue;  // an empty slot: its O was never written
+    const float f = exp2f(v.x - M);
     den += v.y * f;
     if constexpr (PER == 4) {
       const float4 x = *reinterpret_cast<const float4 *>(o + static_cast<size_t>(i) * D);
@@ -747,6 +748,33 @@ int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int 
 }
 
 }  // namespace
+
+bool make_tensor_map_2d(void *map, const void *base, int dim0, long long dim1, int box0, int box1) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(dim0) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_3d(void *map, const void *base, int dim0, int dim1, long long dim2, int box0, int box1,
+                        int box2) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1),
+                        static_cast<cuuint64_t>(dim2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim0) * 2, static_cast<cuuint64_t>(dim0) * dim1 * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(static_cast<CUtensorMap *>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pkv
 
 extern "C" {
@@ -796,6 +824,48 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
     if (!workspace || workspace_bytes < plan.ws_bytes() || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   }
 
+  cudaStream_t st = as_stream(stream);
+  if (chunk_tc_supported(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, plan.part_tokens)) {
+    ChunkTcArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.ws_o = plan.ws_bytes() ? static_cast<float *>(workspace) : nullptr;
+    a.ws_ml = plan.ws_bytes() ? static_cast<char *>(workspace) + plan.ws_o_bytes : nullptr;
+    a.status = d_status;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.part_tokens = plan.part_tokens;
+    a.max_parts = plan.max_parts;
+    a.rows = rows;
+    a.scale = scale;
+    int rc = chunk_tc_launch(a, st);
+    if (rc != PKV_OK || plan.max_parts <= 1) return rc;
+    Params pc{};
+    pc.seq_lens = seq_lens;
+    pc.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    pc.ws_o = static_cast<float *>(workspace);
+    pc.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.ws_o_bytes);
+    pc.status = d_status;
+    pc.max_blocks = max_blocks_per_seq;
+    pc.max_parts = plan.max_parts;
+    pc.part_blocks = plan.part_tokens / block_size;
+    const int crows = q_len * num_q_heads, total = num_seqs * crows;
+    cudaError_t e = head_dim == 128
+                        ? launch_pdl(combine_kernel<128>, dim3((total + 3) / 4), dim3(128), 0, st, pc, block_size,
+                                     total, crows)
+                        : cudaErrorInvalidValue;
+    if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+    return PKV_OK;
+  }
+
   CUtensorMap tmk, tmv;
   if (!make_cache_map(&tmk, k_cache, head_dim, block_size, rows) ||
       !make_cache_map(&tmv, v_cache, head_dim, block_size, rows))
@@ -821,7 +891,6 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
   p.active_warps = (group * kChunkLen + 15) / 16;
   p.scale_log2 = scale * kLog2e;
 
-  cudaStream_t st = as_stream(stream);
   if (head_dim == 128)
     return block_size == 16 ? launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st)
                             : launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st);

@@ -176,6 +176,48 @@ def test_chunked_causal_query_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     assert_attention_close(out, ref, "chunk")
 
 
+@pytest.mark.parametrize("bs,lens,partition", [
+    (16, [16, 17, 40, 600, 64, 65, 1000], 512),
+    (32, [1000, 31, 2048, 3], 128),
+    (16, [0, 5, 15, 16, 200, 0, 130], 64),         # empty and shorter-than-chunk sequences
+    (16, [int(x) for x in np.random.default_rng(4).integers(1, 3000, size=40)], 256),  # many runs per CTA
+    (32, [4096, 4096, 100, 7], 64),
+])
+def test_chunk_tensor_core_path_matches_oracle(bs, lens, partition):
+    """16-token causal chunk with 8 query heads per KV head and head dim 128: the tcgen05 kernel."""
+    d, Hq, Hkv = 128, 64, 8
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=17 + bs + len(lens), q_len=16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_decode(q, kc, vc, tables, lens, scale, partition, status=st)
+    assert st.item() == 0
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale, q_len=16)
+    assert_attention_close(out, ref, "tcgen05 chunk")
+
+
+def test_chunk_tensor_core_rescales_running_max():
+    """Keys grow in magnitude block by block, so the running max keeps moving (rescale path)."""
+    d, bs, Hq, Hkv = 128, 16, 16, 2
+    lens = [1500, 700]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=3, q_len=16)
+    growth = torch.linspace(0.5, 6.0, kc.shape[0], device="cuda").view(-1, 1, 1, 1)
+    kc = (kc.float() * growth).to(torch.bfloat16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    out = run_decode(q, kc, vc, tables, lens, scale, 512)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale, q_len=16)
+    assert_attention_close(out, ref, "tcgen05 chunk rescale")
+
+
+def test_chunk_tensor_core_and_warp_mma_paths_agree():
+    d, bs, Hq, Hkv = 128, 16, 64, 8
+    lens = [900, 2500, 17]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=5, q_len=16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    a = run_decode(q, kc, vc, tables, lens, scale, 512).float()   # tcgen05
+    b = run_decode(q, kc, vc, tables, lens, scale, 496).float()   # not a multiple of 64: warp MMA
+    assert torch.allclose(a, b, atol=1e-2, rtol=1e-2)
+
+
 def test_partition_size_changes_little_and_placement_changes_nothing():
     lens = [900, 2500, 4096, 37]
     d, bs, Hq, Hkv = 128, 16, 32, 8
