@@ -19,8 +19,10 @@
 // empty, and the split-K combine kernel merges the slots.  A sequence with a
 // single partition gets its bf16 output directly.
 //
-// Warp roles: 0-3 softmax + epilogue (thread = row), 4 TMA producer, 5 MMA
-// issuer (one lane) and tensor-memory owner.
+// Warp roles: 0-7 softmax (thread = row; warps 0-3 take the even tiles of a
+// run, 4-7 the odd ones, each set with its own running max / sum and its own
+// TMEM accumulator, merged exactly at the end of the run by the even set),
+// 8 TMA producer, 9 MMA issuer (one lane) and tensor-memory owner.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -49,9 +51,11 @@ constexpr int kPBytes = kRows * 128;             // [128 rows][64 keys x 2 B]
 constexpr int kSmemQ = 0;
 constexpr int kSmemRing = kSmemQ + kQBytes;
 constexpr int kSmemP = kSmemRing + kStages * kStageBytes;
-constexpr int kSmemBars = kSmemP + 2 * kPBytes;
-constexpr int kTmemCols = 256;   // O: 128 columns, S: 2 x 64
-constexpr int kThreads = 6 * 32;
+constexpr int kSmemStats = kSmemP + 2 * kPBytes;  // float2 [2][128]: odd set's (max, sum) per run
+constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
+constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 
@@ -59,7 +63,7 @@ constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 enum : int {
   B_Q_FULL = 0, B_Q_FREE, B_O_FULL, B_O_FREE,
   B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
-  B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1,
+  B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0, B_STATS_FREE1,
   B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_COUNT = B_KV_EMPTY0 + kStages
 };
 
@@ -153,12 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) prefix[0] = 0;
   }
-  if (threadIdx.x == 32) {
+  if (threadIdx.x == 32 * kProducerWarp) {
     mbar_init(bar(B_Q_FULL), 1);
     mbar_init(bar(B_Q_FREE), 1);
     mbar_init(bar(B_O_FULL), 1);
     mbar_init(bar(B_O_FREE), kRows);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_STATS0 + i), kRows);
+      mbar_init(bar(B_STATS_FREE0 + i), kRows);
       mbar_init(bar(B_S_FULL0 + i), 1);
       mbar_init(bar(B_S_FREE0 + i), kRows);
       mbar_init(bar(B_P_FULL0 + i), kRows);
@@ -171,11 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
     tc::relinquish();
   }
-  if (threadIdx.x == 128) {
+  if (threadIdx.x == 32 * kProducerWarp + 1) {
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int it0 = static_cast<int>((static_cast<long long>(blockIdx.x) * I + gridDim.x - 1) / gridDim.x);
   const int it1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * I + gridDim.x - 1) / gridDim.x);
   const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing), sP = smem_u32(smem + kSmemP);
-  const uint32_t tO = tmem, tS0 = tmem + 128;
+  const uint32_t tS0 = tmem + 2 * kD;  // S buffers after the two accumulators
 
   // key range of an item: [k_lo, k_hi)
   auto item_keys = [&](const ItemWalker &w, int &k_lo, int &k_hi) {
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (it0 < it1) {
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
       // ------------------------------------------------------------ producer
       const uint64_t pol = l2_policy_evict_first();
       ItemWalker w;
@@ -278,30 +284,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(bar(B_KV_FULL0 + (x % kStages)), (x / kStages) & 1);
         if (tpieces > 0) mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1);
       }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------- MMA
       if (lane == 0) {
         constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
         constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
         ItemWalker w;
         w.seek(prefix, B, hkv, it0);
-        int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+        int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1, run_g0 = 0;
         // the tile whose P V product is still to be issued, with its run index
         int pend = -1, pend_run = 0;
         bool pend_first = false, pend_last = false;
         bool ok = true;
         auto issue_pv = [&](int x, int run, bool first, bool last) {
-          const int pb = x & 1;
+          const int pb = x & 1;  // the set (even / odd tiles): its P buffer and accumulator
           if (!mbar_wait(bar(B_P_FULL0 + pb), (x >> 1) & 1)) return false;
-          // the first product of run j overwrites O: run j-1's epilogue must have read it
+          // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
           if (first && run > 1 && !mbar_wait(bar(B_O_FREE), (run - 2) & 1)) return false;
           tc::fence_after();
           const uint32_t pa = sP + pb * kPBytes;
           const uint32_t vb = sRing + (x % kStages) * kStageBytes + kKVBytes;
 #pragma unroll
           for (int ks = 0; ks < kTileKeys / 16; ++ks)
-            tc::mma(tO, tc::desc_sw128(pa + ks * 32, 16, 1024), tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024),
-                    kIdO, !(first && ks == 0));
+            tc::mma(tmem + pb * kD, tc::desc_sw128(pa + ks * 32, 16, 1024),
+                    tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO, !(first && ks == 0));
           tc::commit(bar(B_PV_DONE0 + pb));
           tc::commit(bar(B_KV_EMPTY0 + (x % kStages)));
           if (last) tc::commit(bar(B_O_FULL));
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
           if (new_run && ntile > 0) {
             ++tpieces;
+            run_g0 = g;
             if (!mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1)) { ok = false; break; }
           }
           for (int t = 0; t < ntile; ++t, ++g) {
@@ -337,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pend >= 0 && !issue_pv(pend, pend_run, pend_first, pend_last)) { ok = false; break; }
             pend = g;
             pend_run = tpieces;
-            pend_first = new_run && t == 0;
+            pend_first = g - run_g0 < 2;  // the first tile of its set in this run
             pend_last = last_of_run;
           }
         }
@@ -349,37 +356,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------------ softmax warps
-      const int r = threadIdx.x;                  // query row = TMEM lane
+      const int set = warp >> 2;                  // 0: even tiles of a run, 1: odd tiles
+      const int r = threadIdx.x & (kRows - 1);    // query row = TMEM lane
       const int tok = r / kGroup, gh = r % kGroup;
-      const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tO = tmem + set * kD;        // this set's accumulator
+      float2 *stats = reinterpret_cast<float2 *>(smem + kSmemStats);
       ItemWalker w;
       w.seek(prefix, B, hkv, it0);
       int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
       float m = -INFINITY, l = 0.f;
       int run_first_part = 0;
-      bool run_has_tiles = false;
+      bool run_has_tiles = false, set_has_tiles = false;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
         const int L = lens[w.seq];
         int k_lo, k_hi;
         item_keys(w, k_lo, k_hi);
+        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
         if (w.seq != prev_seq || w.head != prev_head) {
           prev_seq = w.seq;
           prev_head = w.head;
           m = -INFINITY;
           l = 0.f;
           run_first_part = w.part;
-          run_has_tiles = false;
+          run_has_tiles = ntile > 0;  // only an empty sequence has none
+          set_has_tiles = false;
+          if (run_has_tiles) ++tpieces;
         }
         const int limit = L - kQLen + 1 + tok;  // this row sees keys t < limit
-        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
         for (int t = 0; t < ntile; ++t, ++g) {
-          const bool first_tile_of_run = !run_has_tiles;
-          if (first_tile_of_run) {
-            run_has_tiles = true;
-            ++tpieces;
-          }
-          const int sb = g & 1;
+          if ((g & 1) != set) continue;  // the other set's tile
+          const bool first_tile_of_set = !set_has_tiles;
+          set_has_tiles = true;
+          const int sb = set;
           if (!wait_warp(bar(B_S_FULL0 + sb), (g >> 1) & 1)) { ok = false; break; }
           tc::fence_after();
           uint32_t sv[kTileKeys];
@@ -393,18 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           float bm = -INFINITY;
 #pragma unroll
           for (int c = 0; c < kTileKeys; ++c) {
-            const float s = c < vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-            sv[c] = __float_as_uint(s);
-            bm = fmaxf(bm, s);
+            const float sc = c < vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+            sv[c] = __float_as_uint(sc);
+            bm = fmaxf(bm, sc);
           }
+          // this set's previous tile (g - 2) must be in the accumulator before a
+          // rescale, and its P buffer free before the new P is written
+          if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
           // move the reference max only when a score passes it by more than
-          // kSlack (rare after a run's first tile); exact, since O and l share it
+          // kSlack (rare after a set's first tile); exact, since O and l share it
           const bool move = bm > m + kSlack;
-          const bool scale_o = move && !first_tile_of_run && m != -INFINITY;
+          const bool scale_o = move && !first_tile_of_set && m != -INFINITY;
           if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
-            // O must hold every earlier P V and none in flight: wait for the previous tile's
-            const int x = g - 1;
-            if (!wait_warp(bar(B_PV_DONE0 + (x & 1)), (x >> 1) & 1)) { ok = false; break; }
             tc::fence_after();
             const float alpha = scale_o ? exp2f(m - bm) : 1.f;
 #pragma unroll
@@ -423,8 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = bm;
           }
           const float msub = m == -INFINITY ? 0.f : m;
-          // P buffer (g & 1) was last read by tile g - 2
-          if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
           const uint32_t prow = sP + sb * kPBytes + r * 128;
 #pragma unroll
           for (int c16 = 0; c16 < 8; ++c16) {
@@ -461,43 +469,77 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(B_P_FULL0 + sb));
         }
         if (!ok) break;
-        // ---- end of a run: epilogue
+        // ---- end of a run
         ItemWalker nx = w;
         nx.next(prefix, B, hkv);
         const bool run_ends = it + 1 >= it1 || nx.seq != w.seq || nx.head != w.head;
         if (!run_ends) continue;
+        const int rp = tpieces & 1;
+        if (set == 1) {  // the odd set hands its (max, sum) to the even set
+          if (run_has_tiles) {
+            // slot rp was last filled two runs ago: wait until the even set read it
+            const int use = (tpieces - 1) >> 1;
+            if (use > 0 && !wait_warp(bar(B_STATS_FREE0 + rp), (use - 1) & 1)) { ok = false; break; }
+            stats[rp * kRows + r] = make_float2(set_has_tiles ? m : -INFINITY, set_has_tiles ? l : 0.f);
+            mbar_arrive(bar(B_STATS0 + rp));
+          }
+          continue;
+        }
         const int nparts = w.nparts;
         const size_t orow = (static_cast<size_t>(w.seq) * kQLen + tok) * p.num_q_heads + w.head * kGroup + gh;
-        if (run_has_tiles && !wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
-        tc::fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float fa = 0.f, fb = 0.f, M = -INFINITY, lt = 0.f;
+        if (run_has_tiles) {
+          if (!wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
+          if (!wait_warp(bar(B_STATS0 + rp), ((tpieces - 1) >> 1) & 1)) { ok = false; break; }
+          tc::fence_after();
+          const float2 sb2 = stats[rp * kRows + r];
+          mbar_arrive(bar(B_STATS_FREE0 + rp));
+          const float ma = set_has_tiles ? m : -INFINITY, la = set_has_tiles ? l : 0.f;
+          M = fmaxf(ma, sb2.x);
+          fa = ma == -INFINITY ? 0.f : exp2f(ma - M);
+          fb = sb2.x == -INFINITY ? 0.f : exp2f(sb2.x - M);
+          lt = la * fa + sb2.y * fb;
+        }
+        // a set with no key for this row contributes nothing (its accumulator is not read)
+        const bool use_a = __any_sync(0xffffffffu, fa != 0.f), use_b = __any_sync(0xffffffffu, fb != 0.f);
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
         for (int ch = 0; ch < kD / 32; ++ch) {
-          uint32_t ov[32];
-          if (run_has_tiles) {
-            tc::ld32(tO + lane_off + ch * 32, ov);
-            tc::wait_ld();
-          } else {
+          float ov[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = 0u;
+          for (int c = 0; c < 32; ++c) ov[c] = 0.f;
+          if (use_a) {
+            uint32_t va[32];
+            tc::ld32(tmem + lane_off + ch * 32, va);
+            tc::wait_ld();
+            if (fa != 0.f)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] += fa * __uint_as_float(va[c]);
+          }
+          if (use_b) {
+            uint32_t vb2[32];
+            tc::ld32(tmem + kD + lane_off + ch * 32, vb2);
+            tc::wait_ld();
+            if (fb != 0.f)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(vb2[c]);
           }
           if (nparts == 1) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
               uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 0]) * inv, __uint_as_float(ov[c8 * 8 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 2]) * inv, __uint_as_float(ov[c8 * 8 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 4]) * inv, __uint_as_float(ov[c8 * 8 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 6]) * inv, __uint_as_float(ov[c8 * 8 + 7]) * inv);
+              v.x = pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
+              v.y = pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
+              v.z = pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
+              v.w = pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
               dst[c8] = v;
             }
           } else {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + run_first_part) * kD + ch * 32);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
-              dst[c4] = make_float4(__uint_as_float(ov[c4 * 4]), __uint_as_float(ov[c4 * 4 + 1]),
-                                    __uint_as_float(ov[c4 * 4 + 2]), __uint_as_float(ov[c4 * 4 + 3]));
+              dst[c4] = make_float4(ov[c4 * 4], ov[c4 * 4 + 1], ov[c4 * 4 + 2], ov[c4 * 4 + 3]);
           }
         }
         if (run_has_tiles) {
@@ -505,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(B_O_FREE));
         }
         if (nparts > 1) {
-          p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(m, l);
+          p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(M, lt);
           for (int q = run_first_part + 1; q <= w.part; ++q)  // merged into the run's first slot
             p.ws_ml[orow * p.max_parts + q] = make_float2(-INFINITY, 0.f);
         }
@@ -518,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }
@@ -557,6 +599,7 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.oob_row = static_cast<int>(a.rows);
   p.scale_log2 = a.scale * kLog2e;
   const size_t smem = 1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * static_cast<size_t>(B) + 1) * 4;
+  static_assert(1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * 2048 + 1) * 4 <= 227 * 1024, "shared memory");
   cudaError_t e;
   void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) =
       a.block_size == 16 ? chunk_tc_kernel<16> : chunk_tc_kernel<32>;
