@@ -107,7 +107,7 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 
 // Bounded wait whose outcome every lane of the warp agrees on.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+  return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity));
 }
 
 template <int BS>
@@ -196,12 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing), sP = smem_u32(smem + kSmemP);
   const uint32_t tS0 = tmem + 2 * kD;  // S buffers after the two accumulators
 
-  // key range of an item: [k_lo, k_hi)
-  auto item_keys = [&](const ItemWalker &w, int &k_lo, int &k_hi) {
-    const int L = lens[w.seq];
-    k_lo = w.part * p.part_tokens;
-    k_hi = min(L, k_lo + p.part_tokens);
-    if (k_hi < k_lo) k_hi = k_lo;
+  // key range of an item: [x, y)
+  auto item_keys = [&](const ItemWalker &w) {
+    const int lo = w.part * p.part_tokens;
+    return make_int2(lo, max(lo, min(lens[w.seq], lo + p.part_tokens)));
   };
 
   if (it0 < it1) {
@@ -213,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
       int tw_seq = -1, tw_base = 0, tw_val = -1;
       for (int it = it0; it < it1 && !*abort_flag; ++it, w.next(prefix, B, hkv)) {
-        int k_lo, k_hi;
-        item_keys(w, k_lo, k_hi);
+        const int2 kr = item_keys(w);
+        const int k_lo = kr.x, k_hi = kr.y;
         const bool new_run = w.seq != prev_seq || w.head != prev_head;
         prev_seq = w.seq;
         prev_head = w.head;
@@ -281,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // never leave a copy in flight into this CTA's shared memory
       if (lane == 0) {
         for (int x = g > kStages ? g - kStages : 0; x < g; ++x)
-          mbar_wait(bar(B_KV_FULL0 + (x % kStages)), (x / kStages) & 1);
-        if (tpieces > 0) mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1);
+          mbar_wait_sleep(bar(B_KV_FULL0 + (x % kStages)), (x / kStages) & 1);
+        if (tpieces > 0) mbar_wait_sleep(bar(B_Q_FULL), (tpieces - 1) & 1);
       }
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------- MMA
@@ -298,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         auto issue_pv = [&](int x, int run, bool first, bool last) {
           const int pb = x & 1;  // the set (even / odd tiles): its P buffer and accumulator
-          if (!mbar_wait(bar(B_P_FULL0 + pb), (x >> 1) & 1)) return false;
+          if (!mbar_wait_sleep(bar(B_P_FULL0 + pb), (x >> 1) & 1)) return false;
           // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
-          if (first && run > 1 && !mbar_wait(bar(B_O_FREE), (run - 2) & 1)) return false;
+          if (first && run > 1 && !mbar_wait_sleep(bar(B_O_FREE), (run - 2) & 1)) return false;
           tc::fence_after();
           const uint32_t pa = sP + pb * kPBytes;
           const uint32_t vb = sRing + (x % kStages) * kStageBytes + kKVBytes;
@@ -314,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
-          int k_lo, k_hi;
-          item_keys(w, k_lo, k_hi);
+          const int2 kr = item_keys(w);
+          const int k_lo = kr.x, k_hi = kr.y;
           const bool new_run = w.seq != prev_seq || w.head != prev_head;
           prev_seq = w.seq;
           prev_head = w.head;
@@ -326,12 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (new_run && ntile > 0) {
             ++tpieces;
             run_g0 = g;
-            if (!mbar_wait(bar(B_Q_FULL), (tpieces - 1) & 1)) { ok = false; break; }
+            if (!mbar_wait_sleep(bar(B_Q_FULL), (tpieces - 1) & 1)) { ok = false; break; }
           }
           for (int t = 0; t < ntile; ++t, ++g) {
             const int s = g % kStages, sb = g & 1;
-            if (!mbar_wait(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            if (g >= 2 && !mbar_wait(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
+            if (!mbar_wait_sleep(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+            if (g >= 2 && !mbar_wait_sleep(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
             tc::fence_after();
             const uint32_t kb = sRing + s * kStageBytes;
 #pragma unroll
@@ -371,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
         const int L = lens[w.seq];
-        int k_lo, k_hi;
-        item_keys(w, k_lo, k_hi);
+        const int2 kr = item_keys(w);
+        const int k_lo = kr.x, k_hi = kr.y;
         const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
         if (w.seq != prev_seq || w.head != prev_head) {
           prev_seq = w.seq;
@@ -400,13 +398,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(B_S_FREE0 + sb));
           const int k0 = k_lo + t * kTileKeys;
           const int vis = min(limit, k_hi) - k0;  // keys of this tile the row sees
-          float bm = -INFINITY;
+          float rm = -INFINITY;                    // max of the raw scores (the scale is > 0)
+          if (__all_sync(0xffffffffu, vis >= kTileKeys)) {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; ++c) {
-            const float sc = c < vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-            sv[c] = __float_as_uint(sc);
-            bm = fmaxf(bm, sc);
+            for (int c = 0; c < kTileKeys; ++c) rm = fmaxf(rm, __uint_as_float(sv[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < kTileKeys; ++c) {
+              const float sc = c < vis ? __uint_as_float(sv[c]) : -INFINITY;
+              sv[c] = __float_as_uint(sc);
+              rm = fmaxf(rm, sc);
+            }
           }
+          const float bm = rm * p.scale_log2;
           // this set's previous tile (g - 2) must be in the accumulator before a
           // rescale, and its P buffer free before the new P is written
           if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool scale_o = move && !first_tile_of_set && m != -INFINITY;
           if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
             tc::fence_after();
-            const float alpha = scale_o ? exp2f(m - bm) : 1.f;
+            const float alpha = scale_o ? fast_exp2(m - bm) : 1.f;
 #pragma unroll
             for (int ch = 0; ch < kD / 32; ++ch) {
               uint32_t ov[32];
@@ -434,14 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float msub = m == -INFINITY ? 0.f : m;
           const uint32_t prow = sP + sb * kPBytes + r * 128;
+          const float ks = p.scale_log2;
 #pragma unroll
           for (int c16 = 0; c16 < 8; ++c16) {
             uint32_t pk[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; ++j) {  // p = 2^(s * scale * log2e - m); masked keys hold -inf
               const uint32_t packed =
-                  pack_bf16x2(exp2f(__uint_as_float(sv[c16 * 8 + 2 * j]) - msub),
-                              exp2f(__uint_as_float(sv[c16 * 8 + 2 * j + 1]) - msub));
+                  pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sv[c16 * 8 + 2 * j]), ks, -msub)),
+                              fast_exp2(fmaf(__uint_as_float(sv[c16 * 8 + 2 * j + 1]), ks, -msub)));
               const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&packed));
               l += f.x + f.y;
               pk[j] = packed;
@@ -506,23 +511,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < kD / 32; ++ch) {
           float ov[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ov[c] = 0.f;
+          uint32_t tmp[32];
           if (use_a) {
-            uint32_t va[32];
-            tc::ld32(tmem + lane_off + ch * 32, va);
+            tc::ld32(tmem + lane_off + ch * 32, tmp);
             tc::wait_ld();
-            if (fa != 0.f)
 #pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] += fa * __uint_as_float(va[c]);
+            for (int c = 0; c < 32; ++c) ov[c] = fa != 0.f ? fa * __uint_as_float(tmp[c]) : 0.f;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = 0.f;
           }
           if (use_b) {
-            uint32_t vb2[32];
-            tc::ld32(tmem + kD + lane_off + ch * 32, vb2);
+            tc::ld32(tmem + kD + lane_off + ch * 32, tmp);
             tc::wait_ld();
             if (fb != 0.f)
 #pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(vb2[c]);
+              for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(tmp[c]);
           }
           if (nparts == 1) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
