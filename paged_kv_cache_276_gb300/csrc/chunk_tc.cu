@@ -43,17 +43,15 @@ constexpr int kRows = 128;       // 16 tokens x 8 heads
 constexpr int kQLen = 16;
 constexpr int kGroup = 8;
 constexpr int kTileKeys = 64;    // keys per MMA tile
-constexpr int kStages = 4;       // K/V ring
+constexpr int kStages = 5;       // K/V ring
 constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
 constexpr int kKVBytes = kTileKeys * kD * 2;     // 16 KiB each for K and V: [half][64 rows][128 B]
 constexpr int kStageBytes = 2 * kKVBytes;
-constexpr int kPBytes = kRows * 128;             // [128 rows][64 keys x 2 B]
 constexpr int kSmemQ = 0;
 constexpr int kSmemRing = kSmemQ + kQBytes;
-constexpr int kSmemP = kSmemRing + kStages * kStageBytes;
-constexpr int kSmemStats = kSmemP + 2 * kPBytes;  // float2 [2][128]: odd set's (max, sum) per run
+constexpr int kSmemStats = kSmemRing + kStages * kStageBytes;  // float2 [2][128]: odd set's (max, sum) per run
 constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
-constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64
+constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64, P: 2 x 32
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kThreads = 10 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -193,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int I = prefix[B];
   const int it0 = static_cast<int>((static_cast<long long>(blockIdx.x) * I + gridDim.x - 1) / gridDim.x);
   const int it1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * I + gridDim.x - 1) / gridDim.x);
-  const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing), sP = smem_u32(smem + kSmemP);
-  const uint32_t tS0 = tmem + 2 * kD;  // S buffers after the two accumulators
+  const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing);
+  const uint32_t tS0 = tmem + 2 * kD;        // S buffers after the two accumulators
+  const uint32_t tP0 = tS0 + 2 * kTileKeys;  // P (bf16 pairs per column) after the S buffers
 
   // key range of an item: [x, y)
   auto item_keys = [&](const ItemWalker &w) {
@@ -300,12 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
           if (first && run > 1 && !mbar_wait_sleep(bar(B_O_FREE), (run - 2) & 1)) return false;
           tc::fence_after();
-          const uint32_t pa = sP + pb * kPBytes;
+          const uint32_t pa = tP0 + pb * (kTileKeys / 2);
           const uint32_t vb = sRing + (x % kStages) * kStageBytes + kKVBytes;
 #pragma unroll
-          for (int ks = 0; ks < kTileKeys / 16; ++ks)
-            tc::mma(tmem + pb * kD, tc::desc_sw128(pa + ks * 32, 16, 1024),
-                    tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO, !(first && ks == 0));
+          for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
+            tc::mma_ta(tmem + pb * kD, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO,
+                       !(first && ks == 0));
           tc::commit(bar(B_PV_DONE0 + pb));
           tc::commit(bar(B_KV_EMPTY0 + (x % kStages)));
           if (last) tc::commit(bar(B_O_FULL));
@@ -437,24 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = bm;
           }
           const float msub = m == -INFINITY ? 0.f : m;
-          const uint32_t prow = sP + sb * kPBytes + r * 128;
           const float ks = p.scale_log2;
+          uint32_t pk[kTileKeys / 2];  // P row: two bf16 per tensor-memory column
 #pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {  // p = 2^(s * scale * log2e - m); masked keys hold -inf
-              const uint32_t packed =
-                  pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sv[c16 * 8 + 2 * j]), ks, -msub)),
-                              fast_exp2(fmaf(__uint_as_float(sv[c16 * 8 + 2 * j + 1]), ks, -msub)));
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&packed));
-              l += f.x + f.y;
-              pk[j] = packed;
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((c16 ^ (r & 7)) << 4)), "r"(pk[0]),
-                         "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                         : "memory");
+          for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys hold -inf
+            pk[c] = pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sv[2 * c]), ks, -msub)),
+                                fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), ks, -msub)));
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[c]));
+            l += f.x + f.y;
           }
+          tc::st32(tP0 + sb * (kTileKeys / 2) + lane_off, pk);
+          tc::wait_st();
           // value rows past the sequence end were never written: zero them
           const int exist = L - k0;
           if (exist < kTileKeys) {
