@@ -253,25 +253,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           int bids[kBlocks];
 #pragma unroll
           for (int j = 0; j < kBlocks; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
-          if (lane == 0) {
-            const uint32_t st = sRing + s * kStageBytes;
-            mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), kStageBytes);
-#pragma unroll
-            for (int j = 0; j < kBlocks; ++j) {
-              const int b = bids[j];
-              int row;
-              if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
-                row = (b * hkv + w.head) * BS;
-              } else {
-                if (blk_first + j < nblk_seq && p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
-                row = p.oob_row;  // past the sequence, or a bad id: zeros
-              }
-              for (int hf = 0; hf < 2; ++hf) {
-                tma_load_2d(st + hf * (kKVBytes / 2) + j * BS * 128, &tmk, hf * 64, row, bar(B_KV_FULL0 + s), pol);
-                tma_load_2d(st + kKVBytes + hf * (kKVBytes / 2) + j * BS * 128, &tmv, hf * 64, row,
-                            bar(B_KV_FULL0 + s), pol);
-              }
+          const uint32_t st = sRing + s * kStageBytes;
+          if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), kStageBytes);
+          // one lane per (block, K/V, half): the box copies go out in parallel
+          if (lane < kBlocks * 4) {
+            const int j = lane >> 2, kv = (lane >> 1) & 1, hf = lane & 1;
+            const int b = bids[j];
+            int row;
+            if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
+              row = (b * hkv + w.head) * BS;
+            } else {
+              if (blk_first + j < nblk_seq && p.status && kv == 0 && hf == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+              row = p.oob_row;  // past the sequence, or a bad id: zeros
             }
+            tma_load_2d(st + kv * kKVBytes + hf * (kKVBytes / 2) + j * BS * 128, kv ? &tmv : &tmk, hf * 64, row,
+                        bar(B_KV_FULL0 + s), pol);
           }
         }
       }
