@@ -320,6 +320,10 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   constexpr int DP = D + 4;  // padded row of the merge buffer
   static_assert(kDecodeWarps * COLS * DP * 4 + 2 * kDecodeWarps * COLS * 4 <= T::kRingBytes,
                 "merge buffer must fit in the ring");
+  // Block j goes to stage j % S and to consumer warp j % kDecodeWarps.  Every
+  // use of a stage must go to the same warp, else a warp could wait on a
+  // stage two phases ahead of the barrier and pass the parity test early.
+  static_assert(S % kDecodeWarps == 0, "ring stages must be a multiple of the consumer warps");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
