@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = 2
 FALLBACK_HBM_GBS = 6800.0
+DEFAULT_PARTITION = 768  # the library's split-K partition when the caller passes 0
 
 
 def log(*a):
@@ -222,8 +223,8 @@ class Runner:
                                                   stream)
                     d1.record(stream)
                     dec.append((d0, d1))
-                    nparts = math.ceil(p.max_len / sess.partition_size) if p.max_len else 1
-                    launches += (i >= warmup) * (2 + (nparts > 1))
+                    nparts = math.ceil(p.max_len / (sess.partition_size or DEFAULT_PARTITION)) if p.max_len else 1
+                    launches += (i >= warmup) * (2 + (nparts > 1))  # write, decode, cross-partition combine
                 s1.record(stream)
                 if i >= warmup:
                     step_ms.append((s0, s1))

@@ -116,7 +116,7 @@ int pkv_block_copy(pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *src_dst_
  * Bytes of caller-provided device workspace paged_attention_decode needs for
  * these sizes (0 when no sequence can span more than one partition).
  * partition_size: tokens per split-K partition, a multiple of block_size;
- * 0 selects the default (512).  Returns 0 for invalid sizes as well; check
+ * 0 selects the default (768).  Returns 0 for invalid sizes as well; check
  * the decode call's return code.
  */
 size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads,
@@ -147,7 +147,7 @@ size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads,
  *                 L <= max_blocks_per_seq * block_size (else PKV_STATUS_BAD_LEN,
  *                 and L is clamped)
  *   max_seq_len   host upper bound of seq_lens; sizes the grid and workspace
- *   partition_size tokens per split-K partition (0 = 512), a multiple of
+ *   partition_size tokens per split-K partition (0 = 768), a multiple of
  *                 block_size; sequences longer than one partition are reduced
  *                 across partitions with an exact log-sum-exp merge
  *   workspace     device scratch of at least paged_attention_workspace_size(...)
