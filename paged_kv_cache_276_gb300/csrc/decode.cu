@@ -44,7 +44,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kDecodeWarps = 4;  // consumer warps, q_len = 1
 constexpr int kChunkWarps = 8;   // consumer warps, q_len = 16
 constexpr int kChunkLen = 16;
-constexpr int kDefaultPartition = 512;
+constexpr int kDefaultPartition = 768;
 constexpr float kRescaleSlack = 8.f;  // log2 units: weights stay below 256
 
 struct Params {
