@@ -591,6 +591,9 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
 
 // ---------------------------------------------- cross-partition combine
 // One warp per (sequence, query row): out = sum_p O_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+// The partitions' (max, sum) pairs are read by the lanes in parallel and each
+// lane then issues every partition's slice of O at once, so the merge costs a
+// few memory round trips instead of two per partition.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
                                                       int rows) {
@@ -608,31 +611,49 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_
   const float *o = p.ws_o + static_cast<size_t>(wg) * p.max_parts * D + lane * PER;
   float M = -INFINITY;
   for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[i].x);
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 4));
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 8));
-  M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float den = 0.f, accv[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) accv[k] = 0.f;
-  for (int i = 0; i < nparts; ++i) {
-    const float2 v = ml[i];
-    if (v.x == -INFINITY) continue;  // an empty slot: its O was never written
-    const float f = exp2f(v.x - M);
-    den += v.y * f;
-    if constexpr (PER == 4) {
-      const float4 x = *reinterpret_cast<const float4 *>(o + static_cast<size_t>(i) * D);
-      accv[0] += f * x.x;
-      accv[1] += f * x.y;
-      accv[2] += f * x.z;
-      accv[3] += f * x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2 *>(o + static_cast<size_t>(i) * D);
-      accv[0] += f * x.x;
-      accv[1] += f * x.y;
+  for (int base = 0; base < nparts; base += 32) {
+    // lane i holds the weight of partition base + i (0 for an empty slot)
+    const int i = base + lane;
+    float f = 0.f;
+    if (i < nparts) {
+      const float2 v = ml[i];
+      f = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+      den += v.y * f;
+    }
+    const int cnt = min(32, nparts - base);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float w[8];
+      float x[8][PER];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // eight independent loads in flight
+        w[j] = __shfl_sync(0xffffffffu, f, (j0 + j) & 31);
+        const bool use = j0 + j < cnt && w[j] != 0.f;  // an empty slot's O is never read
+#pragma unroll
+        for (int k = 0; k < PER; ++k) x[j][k] = 0.f;
+        if (use) {
+          const float *src = o + static_cast<size_t>(base + j0 + j) * D;
+          if constexpr (PER == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            x[j][0] = t.x; x[j][1] = t.y; x[j][2] = t.z; x[j][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            x[j][0] = t.x; x[j][1] = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int k = 0; k < PER; ++k) accv[k] += w[j] * x[j][k];
     }
   }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
   const float inv = den > 0.f ? 1.f / den : 0.f;
   __nv_bfloat16 *dst = p.out + static_cast<size_t>(wg) * D + lane * PER;
 #pragma unroll
