@@ -32,6 +32,9 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     int64_t total, uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
     int block_size, int num_kv_heads, int chunks, int32_t *status) {
+  // the attention grid queued behind this one may become resident now (it
+  // waits for this grid's writes before it reads the cache)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t per_token = static_cast<int64_t>(num_kv_heads) * chunks;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -61,6 +64,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
 __global__ void __launch_bounds__(256) block_copy_kernel(
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, const int32_t *__restrict__ pairs,
     int num_pairs, int num_blocks, int64_t chunks_per_block, int32_t *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int pr = blockIdx.y; pr < num_pairs; pr += gridDim.y) {
     const int src = pairs[2 * pr];
     const int dst = pairs[2 * pr + 1];

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = p.num_seqs, hkv = p.num_kv_heads;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
+  grid_launch_dependents();  // the merge grid may become resident; it waits for our results
   grid_dependency_wait();
 
   if (warp == 0) {  // items per sequence -> exclusive prefix

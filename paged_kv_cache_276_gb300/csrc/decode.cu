@@ -331,6 +331,9 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Let the merge grid queued behind this one become resident now; it still
+  // waits for this whole grid's results before it reads anything.
+  grid_launch_dependents();
   grid_dependency_wait();  // inputs may come from the kernel launched just before
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
@@ -465,6 +468,9 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
 
   const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Let the merge grid queued behind this one become resident now; it still
+  // waits for this whole grid's results before it reads anything.
+  grid_launch_dependents();
   grid_dependency_wait();  // inputs may come from the kernel launched just before
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
@@ -598,6 +604,7 @@ template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
                                                       int rows) {
   constexpr int PER = D / 32;
+  grid_launch_dependents();
   grid_dependency_wait();  // the partials come from the grid launched just before
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
