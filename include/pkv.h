@@ -142,7 +142,8 @@ size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads,
  *   to bf16 (round to nearest even).  n <= 0 gives zeros.
  *   q, out        device, [num_seqs][q_len][num_q_heads][head_dim] bf16
  *   block_tables  device, [num_seqs][max_blocks_per_seq] int32; entries past
- *                 ceil(L / block_size) are never read
+ *                 ceil(L / block_size) are never used (any value; the kernel
+ *                 may read up to 32 of them before it knows L)
  *   seq_lens      device, [num_seqs] int32, 0 <= L <= max_seq_len and
  *                 L <= max_blocks_per_seq * block_size (else PKV_STATUS_BAD_LEN,
  *                 and L is clamped)

@@ -35,17 +35,18 @@
 
 #include "internal.h"
 #include "pkv.h"
+#include "attend.cuh"
 #include "ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+using namespace attend;
+
 constexpr int kDecodeWarps = 4;  // consumer warps, q_len = 1
 constexpr int kChunkWarps = 8;   // consumer warps, q_len = 16
 constexpr int kChunkLen = 16;
 constexpr int kDefaultPartition = 768;
-constexpr float kRescaleSlack = 8.f;  // log2 units: weights stay below 256
 
 struct Params {
   const __nv_bfloat16 *q;       // [B][q_len][Hq][D]
@@ -80,168 +81,6 @@ struct Tile {
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
 
-// Shared-memory address of the 16-byte chunk `dchunk` of tile row `row`,
-// matching the TMA 128-byte swizzle (chunk index XOR row mod 8 inside each
-// 1024-byte atom; every box starts 1024-byte aligned).
-template <int BS>
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dchunk) {
-  return base + (dchunk >> 3) * (BS * 128) + row * 128 + ((((dchunk & 7) ^ (row & 7))) << 4);
-}
-
-template <int D, int NT>
-struct WarpAcc {
-  float m[NT][2];  // running max of the thread's two columns per n-tile (log2 units)
-  float l[NT][2];  // thread-partial running sum
-  float o[D / 16][NT][4];
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m[nt][0] = m[nt][1] = -INFINITY;
-      l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-      for (int md = 0; md < D / 16; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
-    }
-  }
-};
-
-// Running-max update shared by the block steps.  The reference max moves only
-// when a column's block max exceeds it by more than kRescaleSlack (log2 units),
-// so most blocks skip rescaling the accumulators.  Exact: numerator and
-// denominator use the same reference, and every weight stays below
-// 2^kRescaleSlack.  bmax holds the thread's column maxima (reduced here over
-// the lanes sharing a column); msub receives the reference to subtract.
-template <int D, int NT>
-__device__ __forceinline__ void online_max_update(WarpAcc<D, NT> &acc, float (&bmax)[NT][2],
-                                                  float (&msub)[NT][2]) {
-  float alpha[NT][2];
-  bool rescale = false;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float b = bmax[nt][e];
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 4));
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 8));
-      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, 16));
-      const float m = acc.m[nt][e];
-      alpha[nt][e] = 1.f;
-      if (b > m + kRescaleSlack) {  // also true while m is -inf and b finite
-        alpha[nt][e] = m == -INFINITY ? 0.f : exp2f(m - b);
-        acc.m[nt][e] = b;
-        rescale = true;
-      }
-      msub[nt][e] = acc.m[nt][e] == -INFINITY ? 0.f : acc.m[nt][e];
-    }
-  if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        acc.l[nt][e] *= alpha[nt][e];
-#pragma unroll
-        for (int md = 0; md < D / 16; ++md) {
-          acc.o[md][nt][e] *= alpha[nt][e];
-          acc.o[md][nt][e + 2] *= alpha[nt][e];
-        }
-      }
-  }
-}
-
-// One block of keys for one warp's columns.
-//   qf:    B fragments of Q^T (column = query row) per n-tile and 16-wide d step
-//   valid: keys of this block that hold tokens (1..BS)
-//   vis:   keys of this block visible to each of the thread's columns
-template <int D, int BS, int NT>
-__device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
-                                             const uint32_t (&qf)[NT][D / 16][2], uint32_t kbase,
-                                             uint32_t vbase, int valid, const int (&vis)[NT][2],
-                                             float scale_log2, int lane) {
-  constexpr int MT = BS / 16;
-  const int r8 = lane & 7, mi = lane >> 3;
-  const int g4 = lane >> 2, c4 = lane & 3;
-
-  // S^T[key][col] = K[key][:] . Q[col][:]; even and odd d-steps accumulate in
-  // separate registers so the two MMA chains overlap
-  float sc[MT][NT][4], sc2[MT][NT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc[mt][nt][i] = sc2[mt][nt][i] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      uint32_t a[4];
-      ldsm_x4(swz<BS>(kbase, mt * 16 + r8 + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if (ks & 1) mma_bf16_16816(sc2[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-        else mma_bf16_16816(sc[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-      }
-    }
-  }
-
-  // scale, mask, block max per column
-  float bmax[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) bmax[nt][0] = bmax[nt][1] = -INFINITY;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int key = mt * 16 + g4 + (i >> 1) * 8;
-        const float s = key < vis[nt][i & 1] ? (sc[mt][nt][i] + sc2[mt][nt][i]) * scale_log2 : -INFINITY;
-        sc[mt][nt][i] = s;
-        bmax[nt][i & 1] = fmaxf(bmax[nt][i & 1], s);
-      }
-  float msub[NT][2];
-  online_max_update<D, NT>(acc, bmax, msub);
-
-  // probabilities -> bf16 -> B fragments of P^T (movmatrix transposes the
-  // accumulator layout into the operand layout)
-  uint32_t pb[MT][NT][2];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t lo = pack_bf16x2(exp2f(sc[mt][nt][0] - msub[nt][0]), exp2f(sc[mt][nt][1] - msub[nt][1]));
-      const uint32_t hi = pack_bf16x2(exp2f(sc[mt][nt][2] - msub[nt][0]), exp2f(sc[mt][nt][3] - msub[nt][1]));
-      // the running sum uses the same rounded weights as the P V product
-      const float2 flo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lo));
-      const float2 fhi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi));
-      acc.l[nt][0] += flo.x + fhi.x;
-      acc.l[nt][1] += flo.y + fhi.y;
-      pb[mt][nt][0] = movmatrix_trans(lo);
-      pb[mt][nt][1] = movmatrix_trans(hi);
-    }
-
-  // O^T[d][col] += V^T[d][key] P^T[key][col]
-#pragma unroll
-  for (int kt = 0; kt < MT; ++kt) {
-    const bool tail = valid < (kt + 1) * 16;  // warp-uniform
-    const int k0 = kt * 16 + 2 * c4;
-    const uint32_t m0 = (k0 < valid ? 0x0000FFFFu : 0u) | (k0 + 1 < valid ? 0xFFFF0000u : 0u);
-    const uint32_t m1 = (k0 + 8 < valid ? 0x0000FFFFu : 0u) | (k0 + 9 < valid ? 0xFFFF0000u : 0u);
-#pragma unroll
-    for (int md = 0; md < D / 16; ++md) {
-      uint32_t a[4];
-      ldsm_x4_trans(swz<BS>(vbase, kt * 16 + r8 + (mi >> 1) * 8, md * 2 + (mi & 1)), a);
-      if (tail) {  // slots past the sequence end were never written: keep NaNs out
-        a[0] &= m0;
-        a[1] &= m0;
-        a[2] &= m1;
-        a[3] &= m1;
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc.o[md][nt], a, pb[kt][nt][0], pb[kt][nt][1]);
-    }
-  }
-}
-
 __device__ __forceinline__ int clamp_len(const Params &p, int seq, int block_size, bool report) {
   int L = p.seq_lens[seq];
   const long long cap_tbl = static_cast<long long>(p.max_blocks) * block_size;
@@ -258,13 +97,21 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// The first 32 block-table entries of a partition (lane i: entry blk0 + i),
+// read before the sequence length is known so that the two loads overlap;
+// entries past the sequence's end are dropped by the producer unused.
+__device__ __forceinline__ int first_window(const Params &p, int seq, int part, int lane) {
+  const int e = part * p.part_blocks + lane;
+  return e < p.max_blocks ? p.block_tables[static_cast<size_t>(seq) * p.max_blocks + e] : -1;
+}
+
 // Producer (one whole warp): walk this partition's block-table entries and
 // stream K/V tiles into the ring.  The warp reads 32 table entries with one
 // coalesced load and lane 0 issues the copies.  Stages are released by the
 // consumers through the empty barriers (count given at init).
 template <int D, int BS>
 __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq, int h,
-                        int blk0, int nblk, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        int blk0, int nblk, int window0, uint32_t ring, uint32_t full0, uint32_t empty0,
                         volatile int *abort_flag, int lane) {
   using T = Tile<D, BS>;
   constexpr int S = T::kStages;
@@ -272,7 +119,7 @@ __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Pa
   const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
   int issued = 0, window = 0;
   for (int j = 0; j < nblk; ++j) {
-    if ((j & 31) == 0) window = j + lane < nblk ? tbl[j + lane] : -1;
+    if ((j & 31) == 0) window = j + lane < nblk ? (j == 0 ? window0 : tbl[j + lane]) : -1;
     const int b = __shfl_sync(0xffffffffu, window, j & 31);
     const int s = j % S;
     bool ok = true;
@@ -335,6 +182,8 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   // waits for this whole grid's results before it reads anything.
   grid_launch_dependents();
   grid_dependency_wait();  // inputs may come from the kernel launched just before
+  // the producer's first 32 block-table entries load while the length does
+  const int window0 = warp == kDecodeWarps ? first_window(p, seq, part, lane) : -1;
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
@@ -361,7 +210,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   WarpAcc<D, NT> acc;
   if (warp == kDecodeWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, window0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
     uint32_t qf[NT][D / 16][2];
@@ -472,6 +321,8 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   // waits for this whole grid's results before it reads anything.
   grid_launch_dependents();
   grid_dependency_wait();  // inputs may come from the kernel launched just before
+  // the producer's first 32 block-table entries load while the length does
+  const int window0 = warp == kChunkWarps ? first_window(p, seq, part, lane) : -1;
   const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
   const int part_tokens = p.part_blocks * BS;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
@@ -498,7 +349,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   __syncthreads();
 
   if (warp == kChunkWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, window0, ring, full0, empty0, abort_flag, lane);
     return;
   }
   if (warp >= p.active_warps) return;

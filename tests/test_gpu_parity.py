@@ -240,6 +240,90 @@ def test_partition_size_changes_little_and_placement_changes_nothing():
     assert torch.equal(moved.view(torch.int16), outs[512].view(torch.int16))
 
 
+# ------------------------------------------------ the library's default schedule
+# partition_size 0: 768-token partitions, chosen by the library.
+@pytest.mark.parametrize("d,bs,Hq,Hkv,lens", [
+    (128, 16, 32, 8, [int(x) for x in np.random.default_rng(7).integers(0, 3000, size=37)]),  # mixed, empties
+    (128, 32, 64, 8, [1, 31, 32, 33, 700, 2049, 0, 5000]),
+    (64, 16, 8, 1, [40000]),                 # one sequence over 53 partitions
+    (64, 32, 6, 2, [17, 33, 64]),            # one partition each: no merge
+    (128, 16, 8, 8, [300, 1, 4095, 16, 17]),  # one query head per KV head
+    (128, 16, 16, 2, [0, 0, 0]),             # nothing to read: zeros
+])
+def test_default_schedule_matches_oracle(d, bs, Hq, Hkv, lens):
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=41 + d + bs + Hq + len(lens))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_decode(q, kc, vc, tables, lens, scale, 0, status=st)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale)
+    assert_attention_close(out, ref, f"default d{d} bs{bs} {Hq}/{Hkv}")
+    assert st.item() == 0
+
+
+def test_default_schedule_is_the_768_token_partition_and_placement_changes_nothing():
+    lens = [900, 2500, 4096, 37, 1, 1500]
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=77)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    bal = run_decode(q, kc, vc, tables, lens, scale, 0)
+    grid = run_decode(q, kc, vc, tables, lens, scale, 768)
+    assert torch.equal(bal.view(torch.int16), grid.view(torch.int16))
+    NB = kc.shape[0]
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(9))
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm.cuda()] = kc
+    vc2[perm.cuda()] = vc
+    tables2 = np.where(tables >= 0, perm.numpy()[np.maximum(tables, 0)], -1).astype(np.int32)
+    moved = run_decode(q, kc2, vc2, tables2, lens, scale, 0)
+    assert torch.equal(moved.view(torch.int16), bal.view(torch.int16))
+
+
+def test_default_schedule_reuses_a_dirty_workspace():
+    """The workspace starts as random bytes and is reused by successive calls
+    with different batches: nothing in it needs clearing."""
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    n = native.paged_attention_workspace_size(64, 1, Hq, d, 6000, 0)
+    ws = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(31)
+    for call in range(4):
+        lens = [int(x) for x in rng.integers(1, 6000, size=int(rng.integers(3, 64)))]
+        q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=200 + call)
+        out = torch.full_like(q, float("nan"))
+        native.paged_attention_decode(q, kc, vc, torch.as_tensor(tables, device="cuda"),
+                                      torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda"),
+                                      max(lens), 0.09, out, ws, 0)
+        torch.cuda.synchronize()
+        ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.09)
+        assert_attention_close(out, ref, f"call {call}")
+
+
+def test_default_schedule_at_the_edges():
+    """4100 sequences, a group of 16, and no workspace for a batch that fits one
+    partition per sequence."""
+    rng = np.random.default_rng(12)
+    lens = [int(x) for x in rng.integers(0, 40, size=4100)]
+    d, bs, Hq, Hkv = 64, 16, 4, 2
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=13)
+    out = run_decode(q, kc, vc, tables, lens, 0.125, 0)
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.125)
+    assert_attention_close(out, ref, "4100 sequences")
+    lens = [77, 1024, 3000]
+    q, kc, vc, tables = random_case(lens, 128, 16, 16, 1, seed=14)
+    out = run_decode(q, kc, vc, tables, lens, 0.09, 0)
+    ref = oracle_decode(q, kc, vc, tables, lens, (16, 1, 128, 16), 0.09)
+    assert_attention_close(out, ref, "group 16")
+    lens = [100, 700, 768]  # one 768-token partition each: no workspace needed
+    q, kc, vc, tables = random_case(lens, 128, 16, 32, 8, seed=15)
+    out = torch.full_like(q, float("nan"))
+    native.paged_attention_decode(q, kc, vc, torch.as_tensor(tables, device="cuda"),
+                                  torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda"), 768, 0.09,
+                                  out, None, 0)
+    torch.cuda.synchronize()
+    ref = oracle_decode(q, kc, vc, tables, lens, (32, 8, 128, 16), 0.09)
+    assert_attention_close(out, ref, "no workspace")
+
+
 def test_bad_block_and_length_set_status_without_fault():
     lens = [40, 70]
     d, bs, Hq, Hkv = 128, 16, 8, 2
