@@ -403,12 +403,20 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def other_workloads(args, device, rank, world, peak):
+WORKLOAD_CASES = [(1, None, None), (3, None, None), (4, None, None), (5, 16, None), (5, 32, None), (5, 16, 16),
+                  (5, 32, 16)]
+
+
+def case_tag(wnum, bs, q_len):
+    return f"w{wnum}" + (f"_bs{bs}" if bs else "") + (f"_q{q_len}" if q_len else "")
+
+
+def other_workloads(args, device, rank, world, peak, only=None):
     res = {}
-    cases = [(1, None, None), (3, None, None), (4, None, None), (5, 16, None), (5, 32, None), (5, 16, 16),
-             (5, 32, 16)]
-    for wnum, bs, q_len in cases:
-        tag = f"w{wnum}" + (f"_bs{bs}" if bs else "") + (f"_q{q_len}" if q_len else "")
+    for wnum, bs, q_len in WORKLOAD_CASES:
+        tag = case_tag(wnum, bs, q_len)
+        if only is not None and tag != only:
+            continue
         try:
             steps = 5 if wnum == 3 else 10
             r = Runner(wnum, device, rank, block_size=bs, q_len=q_len, steps_needed=steps + 3)
@@ -462,6 +470,8 @@ def main():
     ap.add_argument("--no-workloads", action="store_true", help="headline only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default=None, choices=[case_tag(*c) for c in WORKLOAD_CASES],
+                    help="time only this secondary workload (for profiling runs; no headline line)")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")
@@ -477,6 +487,13 @@ def main():
             dist.init_process_group("gloo")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload:
+        import torch
+        from paged_kv_cache_276_gb300 import build
+        build.build()
+        torch.cuda.set_device(local)
+        line = {"workloads": other_workloads(args, torch.device("cuda", local), rank, world, measured_hbm_peak()[0],
+                                             only=args.workload)}
     else:
         line = run_ours(args, rank, world, local)
     if rank == 0 and line is not None:
