@@ -394,18 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(B_S_FREE0 + sb));
           const int k0 = k_lo + t * kTileKeys;
           const int vis = min(limit, k_hi) - k0;  // keys of this tile the row sees
-          float rm = -INFINITY;                    // max of the raw scores (the scale is > 0)
-          if (__all_sync(0xffffffffu, vis >= kTileKeys)) {
+          if (!__all_sync(0xffffffffu, vis >= kTileKeys)) {
 #pragma unroll
-            for (int c = 0; c < kTileKeys; ++c) rm = fmaxf(rm, __uint_as_float(sv[c]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < kTileKeys; ++c) {
-              const float sc = c < vis ? __uint_as_float(sv[c]) : -INFINITY;
-              sv[c] = __float_as_uint(sc);
-              rm = fmaxf(rm, sc);
-            }
+            for (int c = 0; c < kTileKeys; ++c)
+              if (c >= vis) sv[c] = __float_as_uint(-INFINITY);
           }
+          // max of the raw scores (the scale is > 0): eight short chains of 3-input maxima
+          float mx[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
+          const float rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
           const float bm = rm * p.scale_log2;
           // this set's previous tile (g - 2) must be in the accumulator before a
           // rescale, and its P buffer free before the new P is written
@@ -433,14 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = bm;
           }
           const float msub = m == -INFINITY ? 0.f : m;
-          const float ks = p.scale_log2;
+          const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+          const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
           uint32_t pk[kTileKeys / 2];  // P row: two bf16 per tensor-memory column
+          uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
 #pragma unroll
           for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys hold -inf
-            pk[c] = pack_bf16x2(fast_exp2(fmaf(__uint_as_float(sv[2 * c]), ks, -msub)),
-                                fast_exp2(fmaf(__uint_as_float(sv[2 * c + 1]), ks, -msub)));
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&pk[c]));
-            l += f.x + f.y;
+            float x0, x1;
+            f32x2_split(ffma2(f32x2_bits(sv[2 * c], sv[2 * c + 1]), ks2, nm2), x0, x1);
+            pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+            // the running sum uses the same rounded weights as the P V product
+            ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
+          }
+          {
+            float a0, a1, b0, b1, c0, c1, d0, d1;
+            f32x2_split(ls[0], a0, a1);
+            f32x2_split(ls[1], b0, b1);
+            f32x2_split(ls[2], c0, c1);
+            f32x2_split(ls[3], d0, d1);
+            l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
           }
           tc::st32(tP0 + sb * (kTileKeys / 2) + lane_off, pk);
           tc::wait_st();
