@@ -198,8 +198,15 @@ class Runner:
         flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=self.device)
         stream = torch.cuda.current_stream()
         status = torch.zeros(1, dtype=torch.int32, device=self.device)
-        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-        step_ms, dec_ms = [], []
+        # every event is created (recorded once) before the timed loop; the
+        # library records `dm` itself right after the main decode kernel
+        pool = []
+        for _ in range((warmup + 2 * steps) * (3 * sess.layers + 2)):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            pool.append(e)
+        ev = pool.pop
+        step_ms, dec_ms, main_ms = [], [], []
         launches = 0
         barrier(world)
         torch.cuda.synchronize()
@@ -230,17 +237,39 @@ class Runner:
                     step_ms.append((s0, s1))
                     dec_ms.extend(dec)
             torch.cuda.synchronize()
+            # Main-kernel pass: the timed steps again (same slots, same values,
+            # so the writes change nothing), each decode call handed an event
+            # that the library records right after its main kernel.  Kept out
+            # of the steps above: the event stops the merge kernel from
+            # launching early behind the main kernel.
+            for i in range(warmup, warmup + steps):
+                p = plans[i]
+                q, ks, vs = toks[i]
+                flush.fill_(float(i))
+                for l in range(sess.layers):
+                    if p.cow_pairs is not None:
+                        native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
+                    native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
+                    d0, dm = ev(), ev()
+                    d0.record(stream)
+                    native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
+                                                  p.max_len, sess.scale, out, ws, sess.partition_size, status,
+                                                  stream, main_done_event=dm)
+                    main_ms.append((d0, dm))
+            torch.cuda.synchronize()
         barrier(world)
         if status.item() != 0:
             raise RuntimeError(f"device status {status.item()} during the benchmark")
         step_t = [a.elapsed_time(b) for a, b in step_ms]
         dec_t = [a.elapsed_time(b) for a, b in dec_ms]
+        main_t = [a.elapsed_time(b) for a, b in main_ms]
         timed = plans[warmup:]
         kv_bytes = [sess.kv_bytes(p) for p in timed]
         return {
             "ms_per_step": sum(step_t) / len(step_t),
             "step_ms_p10": float(np.percentile(step_t, 10)), "step_ms_p90": float(np.percentile(step_t, 90)),
             "decode_ms_avg": sum(dec_t) / len(dec_t),
+            "main_ms_avg": sum(main_t) / len(main_t),
             "kv_bytes_per_step": sum(kv_bytes) / len(kv_bytes),
             "kv_bytes_per_decode": sum(kv_bytes) / len(kv_bytes) / sess.layers,
             "query_tokens_per_step": sess.B * sess.q_len,
@@ -367,7 +396,10 @@ def run_ours(args, rank, world, local):
     e2e = r.time_e2e(max(3, min(args.steps, 10)))
     e2e_ms = max_over_ranks(e2e["ms_per_step"], world)
     e2e_value = e2e["kv_bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9
-    dec_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["decode_ms_avg"] * 1e-3) / 1e9
+    # the dominant kernel: paged_attention_decode's main kernel, timed from an
+    # event before the call to the event the library records right after it
+    main_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["main_ms_avg"] * 1e-3) / 1e9
+    op_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["decode_ms_avg"] * 1e-3) / 1e9
     traffic = kernel_traffic("batched_gqa")
     line = {
         "metric": "paged decode attention KV-cache read bandwidth (valid K+V bytes / step time)",
@@ -381,12 +413,15 @@ def run_ours(args, rank, world, local):
                    "step": "host allocator (precomputed) + pkv_write + paged_attention_decode (+combine)"},
         "query_tok_s": round(dev_res["query_tokens_per_step"] * world / (ms * 1e-3), 1),
         "step_ms_p10": round(dev_res["step_ms_p10"], 5), "step_ms_p90": round(dev_res["step_ms_p90"], 5),
-        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(dec_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "paged_attention_decode (decode_kernel + combine_kernel)",
-                     "kernel_ms_avg": round(dev_res["decode_ms_avg"], 5),
+        "roofline": {"bound": "hbm", "achieved": round(main_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(main_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": "decode_kernel (main kernel of paged_attention_decode)",
+                     "kernel_ms_avg": round(dev_res["main_ms_avg"], 5),
                      "algorithmic_bytes_per_launch": int(dev_res["kv_bytes_per_decode"]),
-                     "traffic": traffic},
+                     "traffic": traffic,
+                     "whole_call": {"kernels": "decode_kernel + cross-partition combine_kernel",
+                                    "ms_avg": round(dev_res["decode_ms_avg"], 5), "achieved": round(op_gbs, 1),
+                                    "frac": round(op_gbs / peak, 4)}},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": dev_res["launches"],
@@ -422,10 +457,13 @@ def other_workloads(args, device, rank, world, peak, only=None):
             r = Runner(wnum, device, rank, block_size=bs, q_len=q_len, steps_needed=steps + 3)
             d = r.time_device(3, steps, world)
             ms = max_over_ranks(d["ms_per_step"], world)
-            dec = d["kv_bytes_per_decode"] / (d["decode_ms_avg"] * 1e-3) / 1e9
+            dec = d["kv_bytes_per_decode"] / (d["main_ms_avg"] * 1e-3) / 1e9
+            op = d["kv_bytes_per_decode"] / (d["decode_ms_avg"] * 1e-3) / 1e9
             res[tag] = {"workload": workload_desc(wnum, bs, q_len), "ms_per_step": round(ms, 5),
                         "kv_gbs_step": round(d["kv_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1),
                         "decode_kernel_gbs": round(dec, 1), "decode_frac_of_peak": round(dec / peak, 4),
+                        "decode_kernel_ms_avg": round(d["main_ms_avg"], 5),
+                        "decode_call_gbs": round(op, 1), "decode_call_frac_of_peak": round(op / peak, 4),
                         "decode_ms_avg": round(d["decode_ms_avg"], 5),
                         "query_tok_s": round(d["query_tokens_per_step"] * world / (ms * 1e-3), 1),
                         "clocks_sm_mhz": d["clocks"]["sm_mhz"]}

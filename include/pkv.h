@@ -169,6 +169,28 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                            size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
+ * paged_attention_decode_ex -- paged_attention_decode that also marks, for
+ * measurement, where its main kernel ends.
+ *
+ * The pages have no counterpart to this call.  A decode is one main kernel
+ * (the paged attention itself) followed, when a sequence spans more than one
+ * partition, by the cross-partition merge.  main_done_event, when not NULL,
+ * is a cudaEvent_t created by the caller; it is recorded on `stream` right
+ * after the main kernel is enqueued and before the merge, so that the elapsed
+ * time from an event recorded before the call to it is the main kernel's.
+ * Everything else is paged_attention_decode's, which is this call with NULL.
+ * A failing record returns PKV_ERR_CUDA.
+ */
+int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                              const pkv_bf16 *v_cache, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                              int max_seq_len, int q_len, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, int num_blocks, float scale,
+                              int partition_size, pkv_bf16 *out, void *workspace,
+                              size_t workspace_bytes, int32_t *d_status, void *stream,
+                              void *main_done_event);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace and without allocating anything.
  *

@@ -602,7 +602,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 template <int D, int BS>
 int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int num_seqs, int q_len,
-           cudaStream_t stream) {
+           cudaStream_t stream, cudaEvent_t main_done) {
   const dim3 grid(p.max_parts, p.num_kv_heads, num_seqs);
   constexpr size_t smem = smem_bytes<D, BS>();
   cudaError_t e;
@@ -621,6 +621,7 @@ int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int 
     if ((e = raise_smem_limit(k, smem)) != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
     e = launch_pdl(k, grid, dim3((kChunkWarps + 1) * 32), smem, stream, tmk, tmv, p);
   }
+  if (e == cudaSuccess && main_done) e = cudaEventRecord(main_done, stream);
   if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
   if (p.max_parts <= 1) return PKV_OK;
   const int rows = q_len * p.num_q_heads;
@@ -675,7 +676,19 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
                            int head_dim, int block_size, int num_blocks, float scale, int partition_size,
                            pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
                            void *stream) {
+  return paged_attention_decode_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                   max_seq_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                   scale, partition_size, out, workspace, workspace_bytes, d_status, stream, nullptr);
+}
+
+int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                              int num_seqs, int max_seq_len, int q_len, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, int num_blocks, float scale, int partition_size,
+                              pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                              void *stream, void *main_done_event) {
   using namespace pkv;
+  cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   if (num_seqs < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -730,6 +743,10 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
     a.rows = rows;
     a.scale = scale;
     int rc = chunk_tc_launch(a, st);
+    if (rc == PKV_OK && main_done) {
+      const cudaError_t er = cudaEventRecord(main_done, st);
+      if (er != cudaSuccess) return set_cuda_error(er), PKV_ERR_CUDA;
+    }
     if (rc != PKV_OK || plan.max_parts <= 1) return rc;
     Params pc{};
     pc.seq_lens = seq_lens;
@@ -775,10 +792,10 @@ int paged_attention_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv
   p.scale_log2 = scale * kLog2e;
 
   if (head_dim == 128)
-    return block_size == 16 ? launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st)
-                            : launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st);
-  return block_size == 16 ? launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st)
-                          : launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st);
+    return block_size == 16 ? launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done)
+                            : launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+  return block_size == 16 ? launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done)
+                          : launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
 }
 
 }  // extern "C"

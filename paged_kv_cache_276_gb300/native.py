@@ -48,6 +48,10 @@ SIGNATURES = {
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                         _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
                                         _c_ptr]),
+    "paged_attention_decode_ex": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
+                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                           _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
+                                           _c_ptr, _c_ptr]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -158,8 +162,11 @@ def paged_attention_workspace_size(num_seqs, q_len, num_q_heads, head_dim, max_s
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_len, scale, out,
-                           workspace=None, partition_size=0, d_status=None, stream=None):
-    """q, out: [B, q_len, Hq, d] bf16; caches [NB, Hkv, bs, d]; tables [B, max_blocks] int32; lens [B] int32."""
+                           workspace=None, partition_size=0, d_status=None, stream=None, main_done_event=None):
+    """q, out: [B, q_len, Hq, d] bf16; caches [NB, Hkv, bs, d]; tables [B, max_blocks] int32; lens [B] int32.
+
+    main_done_event (a torch.cuda.Event or None): recorded right after the main
+    kernel, before the cross-partition merge (paged_attention_decode_ex)."""
     dev = k_cache.device
     for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
                      (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
@@ -171,10 +178,16 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_
             or seq_lens.shape != (B,):
         raise ValueError("shape mismatch")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib().paged_attention_decode(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
-        int(max_seq_len), q_len, Hq, Hkv, d, bs, NB, float(scale), int(partition_size), _ptr(out),
-        _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_decode")
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+            int(max_seq_len), q_len, Hq, Hkv, d, bs, NB, float(scale), int(partition_size), _ptr(out),
+            _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev))
+    if main_done_event is None:
+        _check(lib().paged_attention_decode(*args), "paged_attention_decode")
+    else:
+        handle = main_done_event.cuda_event
+        if not handle:
+            raise ValueError("main_done_event: record the torch.cuda.Event once before passing it")
+        _check(lib().paged_attention_decode_ex(*args, ctypes.c_void_p(handle)), "paged_attention_decode_ex")
 
 
 STATIC_SCRATCH_BYTES = 8 << 20  # PKV_STATIC_SCRATCH_BYTES

@@ -324,6 +324,31 @@ def test_default_schedule_at_the_edges():
     assert_attention_close(out, ref, "no workspace")
 
 
+def test_decode_ex_marks_the_main_kernel_and_changes_nothing():
+    """paged_attention_decode_ex records its event between the main kernel and
+    the merge; the output is bit for bit paged_attention_decode's."""
+    lens = [900, 2500, 37, 1500]
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=61)
+    tables_d = torch.as_tensor(tables, device="cuda")
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    n = native.paged_attention_workspace_size(len(lens), 1, Hq, d, max(lens), 512)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    a = torch.empty_like(q)
+    b = torch.empty_like(q)
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max(lens), 0.09, a, ws, 512)
+    e0, em, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    for e in (e0, em, e1):
+        e.record()
+    e0.record()
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max(lens), 0.09, b, ws, 512, main_done_event=em)
+    e1.record()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    t_main, t_all = e0.elapsed_time(em), e0.elapsed_time(e1)
+    assert 0 < t_main <= t_all
+
+
 def test_bad_block_and_length_set_status_without_fault():
     lens = [40, 70]
     d, bs, Hq, Hkv = 128, 16, 8, 2
