@@ -52,11 +52,22 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def decode_kernel_source_sha():
+    """sha256 of the device code the decode kernel is built from: decode.cu up to
+    its host section, then attend.cuh and ptx.cuh."""
+    csrc = os.path.join(ROOT, "paged_kv_cache_276_gb300", "csrc")
+    text = open(os.path.join(csrc, "decode.cu"), "rb").read()
+    cut = text.find(b"// ------------------------------------------------------------------ host")
+    h = hashlib.sha256(text[:cut] if cut >= 0 else text)
+    for name in ("attend.cuh", "ptx.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
 def kernel_traffic(workload_tag):
     """DRAM bytes per decode launch from the committed ncu summary, only if the
-    kernel source is unchanged since that capture (else None)."""
+    kernel's device code is unchanged since that capture (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
-    src = os.path.join(ROOT, "paged_kv_cache_276_gb300", "csrc", "decode.cu")
     try:
         rec = {}
         with open(path) as f:
@@ -64,7 +75,7 @@ def kernel_traffic(workload_tag):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     rec[k.strip()] = v.strip()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = decode_kernel_source_sha()
         if rec.get("source_sha256") != sha:
             return None
         key = f"dram_bytes_per_launch[{workload_tag}]"
@@ -165,7 +176,7 @@ def barrier(world):
 class Runner:
     """Plans steps, times them on the device and end to end."""
 
-    def __init__(self, wnum, device, rank, block_size=None, q_len=None, steps_needed=8):
+    def __init__(self, wnum, device, rank, block_size=None, q_len=None, steps_needed=8, layers=None):
         import torch
         from paged_kv_cache_276_gb300 import inputs
         from paged_kv_cache_276_gb300.workloads import DecodeSession
@@ -174,7 +185,7 @@ class Runner:
         self.w = w
         # weak scaling: every rank owns an independent batch of the same shape
         self.sess = DecodeSession(w, device, block_size=block_size, q_len=q_len, extra_steps=steps_needed + 2,
-                                  seed_salt=rank)
+                                  seed_salt=rank, layers=layers)
         self.sess.apply_setup_copies()
         self.device = device
         self.rank = rank
@@ -478,6 +489,47 @@ def other_workloads(args, device, rank, world, peak, only=None):
     return res
 
 
+def block_sweep(device, peak):
+    """Block-size trade-off: decode bandwidth at block 16/32/64/128 on the
+    batched and mixed length distributions (one layer each), and the memory
+    simulation (paged at block 8..128 versus one contiguous reservation per
+    request) on request streams drawn from the same distributions."""
+    import torch
+    from paged_kv_cache_276_gb300 import inputs, waste
+    out = {"decode": {}, "memory": {}}
+    for wnum in (2, 3):
+        for bs in (16, 32, 64, 128):
+            tag = f"w{wnum}_bs{bs}"
+            try:
+                r = Runner(wnum, device, 0, block_size=bs, steps_needed=16, layers=1)
+                d = r.time_device(3, 10, 1)
+                main = d["kv_bytes_per_decode"] / (d["main_ms_avg"] * 1e-3) / 1e9
+                call = d["kv_bytes_per_decode"] / (d["decode_ms_avg"] * 1e-3) / 1e9
+                out["decode"][tag] = {"decode_kernel_gbs": round(main, 1), "frac": round(main / peak, 4),
+                                      "decode_call_gbs": round(call, 1), "call_frac": round(call / peak, 4)}
+                del r
+                torch.cuda.empty_cache()
+            except Exception as e:
+                out["decode"][tag] = {"error": repr(e)}
+    for wnum, n, reserve in ((2, 256, 4096), (3, 512, 8192)):
+        w = inputs.WORKLOADS[wnum]
+        rng = np.random.default_rng(w.seed + 31)
+        finals = np.concatenate([inputs.lengths(w, rng) for _ in range(-(-n // w.num_seqs))])[:n]
+        prompts, finals = waste.request_stream(finals, rng)
+        cap = 16 * reserve
+        rows = {}
+        c = waste.simulate(prompts, finals, cap, "contiguous", reserve=reserve)
+        rows["contiguous"] = c
+        for bs in (8, 16, 32, 64, 128):
+            rows[f"paged_bs{bs}"] = waste.simulate(prompts, finals, cap, "paged", block_size=bs)
+        out["memory"][f"w{wnum}"] = {
+            "requests": n, "capacity_tokens": cap, "contiguous_reservation": reserve,
+            **{k: {"token_state_fraction": round(v.token_state_fraction, 4), "utilisation": round(v.utilisation, 4),
+                   "mean_running": round(v.mean_running, 2), "tokens_per_step": round(v.tokens_per_step, 2),
+                   "steps": v.steps, "preemptions": v.preemptions} for k, v in rows.items()}}
+    return out
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: W untimed and K timed whole decode steps
     of the headline workload on this host's cores (rank 0 only)."""
@@ -510,6 +562,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default=None, choices=[case_tag(*c) for c in WORKLOAD_CASES],
                     help="time only this secondary workload (for profiling runs; no headline line)")
+    ap.add_argument("--block-sweep", action="store_true",
+                    help="block-size trade-off: decode GB/s at block 16..128 and the memory simulation")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")
@@ -525,6 +579,12 @@ def main():
             dist.init_process_group("gloo")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.block_sweep:
+        import torch
+        from paged_kv_cache_276_gb300 import build
+        build.build()
+        torch.cuda.set_device(local)
+        line = {"block_sweep": block_sweep(torch.device("cuda", local), measured_hbm_peak()[0])}
     elif args.workload:
         import torch
         from paged_kv_cache_276_gb300 import build

@@ -154,7 +154,7 @@ size_t paged_attention_workspace_size(int num_seqs, int q_len, int num_q_heads,
  *   workspace     device scratch of at least paged_attention_workspace_size(...)
  *                 bytes (may be NULL when that size is 0); contents are not
  *                 preserved between calls
- * Supported: head_dim in {64, 128}; block_size in {16, 32}; q_len in {1, 16}
+ * Supported: head_dim in {64, 128}; block_size in {16, 32, 64, 128}; q_len in {1, 16}
  *   with q_len * num_q_heads / num_kv_heads <= 128 and, for q_len = 1,
  *   num_q_heads / num_kv_heads <= 16.  Other sizes return PKV_ERR_UNSUPPORTED.
  * Block ids outside [0, num_blocks) set PKV_STATUS_BAD_BLOCK; the block reads

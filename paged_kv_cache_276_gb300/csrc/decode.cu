@@ -69,6 +69,17 @@ struct Params {
   float scale_log2;  // scale * log2(e)
 };
 
+// A block is staged as one or more "units" of consecutive token rows: the
+// whole block for block sizes 16 and 32, 32-row pieces for 64 and 128 (whole
+// tiles would leave too few ring stages for four consumer warps; 32 rows make
+// the same TMA boxes as block 32, which streams best).
+template <int BS>
+struct Unit {
+  static_assert(BS == 16 || BS == 32 || BS == 64 || BS == 128, "block size 16, 32, 64 or 128");
+  static constexpr int kRows = BS <= 32 ? BS : 32;
+  static constexpr int kPerBlock = BS / kRows;
+};
+
 template <int D, int BS>
 struct Tile {
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
@@ -111,16 +122,19 @@ __device__ __forceinline__ int first_window(const Params &p, int seq, int part, 
 // consumers through the empty barriers (count given at init).
 template <int D, int BS>
 __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq, int h,
-                        int blk0, int nblk, int window0, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        int blk0, int nunit, int window0, uint32_t ring, uint32_t full0, uint32_t empty0,
                         volatile int *abort_flag, int lane) {
-  using T = Tile<D, BS>;
+  using U = Unit<BS>;
+  using T = Tile<D, U::kRows>;
   constexpr int S = T::kStages;
   const uint64_t pol = l2_policy_evict_first();
   const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
+  const int nblk = (nunit + U::kPerBlock - 1) / U::kPerBlock;
   int issued = 0, window = 0;
-  for (int j = 0; j < nblk; ++j) {
-    if ((j & 31) == 0) window = j + lane < nblk ? (j == 0 ? window0 : tbl[j + lane]) : -1;
-    const int b = __shfl_sync(0xffffffffu, window, j & 31);
+  for (int j = 0; j < nunit; ++j) {
+    const int e = j / U::kPerBlock, piece = j - e * U::kPerBlock;  // table entry, unit within the block
+    if (piece == 0 && (e & 31) == 0) window = e + lane < nblk ? (e == 0 ? window0 : tbl[e + lane]) : -1;
+    const int b = __shfl_sync(0xffffffffu, window, e & 31);
     const int s = j % S;
     bool ok = true;
     if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) ok = false;
@@ -135,7 +149,7 @@ __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Pa
     if (lane == 0) {
       int row;
       if (b >= 0 && b < p.num_blocks) {
-        row = (b * p.num_kv_heads + h) * BS;
+        row = (b * p.num_kv_heads + h) * BS + piece * U::kRows;
       } else {
         if (p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
         row = p.oob_row;  // zero fill
@@ -161,7 +175,8 @@ template <int D, int BS, int NT>
 __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const Params p) {
-  using T = Tile<D, BS>;
+  using U = Unit<BS>;
+  using T = Tile<D, U::kRows>;
   constexpr int S = T::kStages;
   constexpr int COLS = NT * 8;
   constexpr int DP = D + 4;  // padded row of the merge buffer
@@ -189,8 +204,9 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
   if (part >= nparts) return;
   const int blk0 = part * p.part_blocks;
-  const int nblk_seq = (L + BS - 1) / BS;
-  const int nblk = max(0, min(p.part_blocks, nblk_seq - blk0));
+  const int tok0 = blk0 * BS;  // first key of the partition
+  const int ntok = max(0, min(L, tok0 + p.part_blocks * BS) - tok0);
+  const int nunit = (ntok + U::kRows - 1) / U::kRows;
 
   const uint32_t ring = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
@@ -210,7 +226,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   WarpAcc<D, NT> acc;
   if (warp == kDecodeWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, window0, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
     uint32_t qf[NT][D / 16][2];
@@ -227,19 +243,19 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
       }
     }
     acc.init();
-    for (int j = warp; j < nblk; j += kDecodeWarps) {
+    for (int j = warp; j < nunit; j += kDecodeWarps) {
       const int s = j % S;
       if (!mbar_wait(full0 + 8 * s, (j / S) & 1)) {
         if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
         *abort_flag = 1;
         break;
       }
-      const int valid = min(BS, L - (blk0 + j) * BS);
+      const int valid = min(U::kRows, L - (tok0 + j * U::kRows));
       int vis[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) vis[nt][0] = vis[nt][1] = valid;
       const uint32_t kb = ring + s * T::kStageBytes;
-      attend_block<D, BS, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+      attend_block<D, U::kRows, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
       if (*abort_flag) break;
@@ -307,7 +323,8 @@ template <int D, int BS>
 __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
     chunk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Params p) {
-  using T = Tile<D, BS>;
+  using U = Unit<BS>;
+  using T = Tile<D, U::kRows>;
   constexpr int S = T::kStages;
   constexpr int NT = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -328,8 +345,9 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
   if (part >= nparts) return;
   const int blk0 = part * p.part_blocks;
-  const int nblk_seq = (L + BS - 1) / BS;
-  const int nblk = max(0, min(p.part_blocks, nblk_seq - blk0));
+  const int tok0 = blk0 * BS;  // first key of the partition
+  const int ntok = max(0, min(L, tok0 + p.part_blocks * BS) - tok0);
+  const int nunit = (ntok + U::kRows - 1) / U::kRows;
   const int ncols = kChunkLen * p.group;
 
   const uint32_t ring = smem_u32(smem);
@@ -349,7 +367,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   __syncthreads();
 
   if (warp == kChunkWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nblk, window0, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
     return;
   }
   if (warp >= p.active_warps) return;
@@ -383,7 +401,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   WarpAcc<D, NT> acc;
   acc.init();
   bool ok = true;
-  for (int j = 0; j < nblk; ++j) {
+  for (int j = 0; j < nunit; ++j) {
     const int s = j % S;
     if (!mbar_wait(full0 + 8 * s, (j / S) & 1)) {
       if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
@@ -391,8 +409,8 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
       ok = false;
       break;
     }
-    const int key0 = (blk0 + j) * BS;
-    const int valid = min(BS, L - key0);
+    const int key0 = tok0 + j * U::kRows;
+    const int valid = min(U::kRows, L - key0);
     int vis[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
       vis[nt][1] = min(valid, nvis[nt][1] - key0);
     }
     const uint32_t kb = ring + s * T::kStageBytes;
-    attend_block<D, BS, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+    attend_block<D, U::kRows, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     if (*abort_flag) {
@@ -534,13 +552,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The cache as a 2-D bf16 tensor: rows = num_blocks * Hkv * block_size, each of
-// head_dim elements; a box is block_size rows x 64 elements (128 bytes).
-bool make_cache_map(CUtensorMap *map, const void *base, int head_dim, int block_size, long long rows) {
+// head_dim elements; a box is box_rows rows x 64 elements (128 bytes).
+bool make_cache_map(CUtensorMap *map, const void *base, int head_dim, int box_rows, long long rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_size)};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -573,7 +591,8 @@ bool make_plan(int num_seqs, int q_len, int num_q_heads, int head_dim, int max_s
 
 template <int D, int BS>
 constexpr size_t smem_bytes() {
-  return Tile<D, BS>::kRingBytes + 2 * Tile<D, BS>::kStages * 8 + 16 + 1024;
+  using T = Tile<D, Unit<BS>::kRows>;
+  return T::kRingBytes + 2 * T::kStages * 8 + 16 + 1024;
 }
 
 template <typename K>
@@ -694,7 +713,7 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
     return PKV_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PKV_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
   if (q_len == 1) {
     if (group > 16) return PKV_ERR_UNSUPPORTED;
@@ -767,8 +786,9 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   }
 
   CUtensorMap tmk, tmv;
-  if (!make_cache_map(&tmk, k_cache, head_dim, block_size, rows) ||
-      !make_cache_map(&tmv, v_cache, head_dim, block_size, rows))
+  const int tile_rows = block_size <= 32 ? block_size : 32;  // the kernels' Unit<BS>::kRows
+  if (!make_cache_map(&tmk, k_cache, head_dim, tile_rows, rows) ||
+      !make_cache_map(&tmv, v_cache, head_dim, tile_rows, rows))
     return PKV_ERR_CUDA;
 
   Params p{};
@@ -791,11 +811,16 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   p.active_warps = (group * kChunkLen + 15) / 16;
   p.scale_log2 = scale * kLog2e;
 
-  if (head_dim == 128)
-    return block_size == 16 ? launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done)
-                            : launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-  return block_size == 16 ? launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done)
-                          : launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+  switch (head_dim * 1000 + block_size) {
+    case 128016: return launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 128032: return launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 128064: return launch<128, 64>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 128128: return launch<128, 128>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 64016: return launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 64032: return launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 64064: return launch<64, 64>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    default: return launch<64, 128>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+  }
 }
 
 }  // extern "C"

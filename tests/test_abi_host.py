@@ -62,6 +62,7 @@ def test_decode_rejects_bad_sizes_before_launch(native):
                                           a["stream"])
     assert call(d=96) == native.PKV_ERR_UNSUPPORTED
     assert call(bs=8) == native.PKV_ERR_UNSUPPORTED
+    assert call(bs=256) == native.PKV_ERR_UNSUPPORTED
     assert call(qlen=3) == native.PKV_ERR_UNSUPPORTED
     assert call(Hq=7) == native.PKV_ERR_ARG
     assert call(Hq=40, Hkv=2) == native.PKV_ERR_UNSUPPORTED       # group 20 > 16

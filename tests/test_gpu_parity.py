@@ -151,6 +151,9 @@ def test_pkv_block_copy_bit_exact(d, bs, Hkv):
     (64, 32, 12, 4, [3, 64, 65, 1000], 96),
     (128, 32, 8, 2, [40, 2000], 0),
     (64, 16, 2, 1, [0, 1, 2, 1999], 128),                 # empty sequence gives zeros
+    (128, 64, 32, 8, [1, 63, 64, 65, 700, 2049], 512),    # block 64: staged as 16-row units
+    (64, 128, 8, 2, [5, 127, 128, 129, 1500], 256),       # block 128
+    (128, 128, 16, 1, [77, 1024, 0], 0),                  # block 128, group 16, default partition
 ])
 def test_decode_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=d + bs + Hq + len(lens))
@@ -167,6 +170,8 @@ def test_decode_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     (128, 32, 64, 8, [1000, 31], 128),
     (64, 16, 8, 2, [3, 16, 100], 32),             # rows < 16: causal rows with nothing to see
     (128, 16, 16, 8, [530], 64),
+    (128, 64, 64, 8, [100, 700, 16], 512),        # block 64: warp-MMA chunk kernel
+    (64, 128, 8, 2, [1000, 3], 256),              # block 128
 ])
 def test_chunked_causal_query_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=3 + d + bs + Hq, q_len=16)
