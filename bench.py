@@ -530,6 +530,42 @@ def block_sweep(device, peak):
     return out
 
 
+def swap_bench(device):
+    """Bandwidth of pkv_swap_out / pkv_swap_in: whole blocks (block 16, 8 KV
+    heads, head dim 128: 64 KiB of K and V each) between a device pool and
+    page-locked host buffers, CUDA events around each call, 2 x L2 of cache
+    flushed before each."""
+    import torch
+    from paged_kv_cache_276_gb300 import inputs, native
+    NB, Hkv, bs, d = 8192, 8, 16, 128
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), 5, device)
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), 6, device)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+    res = {}
+    for n in (256, 2048):
+        ids = torch.as_tensor(np.random.default_rng(n).permutation(NB)[:n].astype(np.int32), device=device)
+        hk = torch.empty((n, Hkv, bs, d), dtype=torch.bfloat16).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        nbytes = 2 * n * Hkv * bs * d * 2
+        for name, call in (("out", lambda: native.pkv_swap_out(kc, vc, ids, hk, hv)),
+                           ("in", lambda: native.pkv_swap_in(hk, hv, ids, kc, vc))):
+            for _ in range(3):
+                call()
+            ts = []
+            for _ in range(10):
+                flush.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            ms = float(np.median(ts))
+            res[f"{name}_{n}_blocks"] = {"bytes": nbytes, "ms": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1)}
+    return res
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: W untimed and K timed whole decode steps
     of the headline workload on this host's cores (rank 0 only)."""
@@ -562,6 +598,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default=None, choices=[case_tag(*c) for c in WORKLOAD_CASES],
                     help="time only this secondary workload (for profiling runs; no headline line)")
+    ap.add_argument("--swap", action="store_true", help="bandwidth of the block swap-out / swap-in copies")
     ap.add_argument("--block-sweep", action="store_true",
                     help="block-size trade-off: decode GB/s at block 16..128 and the memory simulation")
     args = ap.parse_args()
@@ -579,6 +616,12 @@ def main():
             dist.init_process_group("gloo")
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.swap:
+        import torch
+        from paged_kv_cache_276_gb300 import build
+        build.build()
+        torch.cuda.set_device(local)
+        line = {"swap": swap_bench(torch.device("cuda", local))}
     elif args.block_sweep:
         import torch
         from paged_kv_cache_276_gb300 import build

@@ -222,6 +222,30 @@ int paged_attention_decode_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_c
                                           int partition_size, pkv_bf16 *out, int32_t *d_status,
                                           void *stream);
 
+/*
+ * pkv_swap_out / pkv_swap_in -- move whole blocks between the device caches
+ * and page-locked host memory (the data side of pkv_seq_swap_out / _in).
+ *
+ * Pages: praveentn.live "PagedAttention KV-cache constraint", "What it cost"
+ * (swapping blocks when memory runs out).  For i < n, with b = block_ids[i]:
+ *   out:  host_k[i][:][:][:] = k_cache[b][:][:][:]   (same for v)
+ *   in:   k_cache[b][:][:][:] = host_k[i][:][:][:]   (same for v)
+ *   block_ids       device, [n] int32; ids outside [0, num_blocks) set
+ *                   PKV_STATUS_BAD_BLOCK and are skipped
+ *   host_k, host_v  page-locked host memory (cudaHostAlloc / cudaMallocHost /
+ *                   cudaHostRegister), [n][num_kv_heads][block_size][head_dim]
+ *                   bf16, 16-byte aligned; the kernel reads or writes it
+ *                   directly through unified addressing.  Pageable memory is
+ *                   refused (PKV_ERR_ARG).
+ * Bit-exact copies; the ids of one call must be distinct for pkv_swap_in.
+ */
+int pkv_swap_out(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_ids, int n,
+                 pkv_bf16 *host_k, pkv_bf16 *host_v, int num_blocks, int block_size, int num_kv_heads,
+                 int head_dim, int32_t *d_status, void *stream);
+int pkv_swap_in(const pkv_bf16 *host_k, const pkv_bf16 *host_v, const int32_t *block_ids, int n,
+                pkv_bf16 *k_cache, pkv_bf16 *v_cache, int num_blocks, int block_size, int num_kv_heads,
+                int head_dim, int32_t *d_status, void *stream);
+
 /* ------------------------------------------------------------------------
  * Host block allocator: pool, block tables, refcounts, copy-on-write.
  *
@@ -266,6 +290,23 @@ int pkv_seq_cow(pkv_alloc *a, int64_t seq_id, int logical_block, int32_t *pair_o
 
 /* Drop a sequence; blocks whose refcount reaches 0 return to the pool. */
 int pkv_seq_free(pkv_alloc *a, int64_t seq_id);
+
+/* Swap a resident sequence out (praveentn.live "PagedAttention KV-cache
+ * constraint", "What it cost": under memory pressure blocks are swapped or
+ * recomputed).  Writes its block ids in logical order (ceil(len / block_size)
+ * of them; PKV_ERR_RANGE if more than max_blocks) to blocks_out and *n_out,
+ * then releases them like pkv_seq_free does.  The caller copies those blocks
+ * to host memory with pkv_swap_out, enqueued before anything that writes into
+ * them again.  The sequence keeps its id and length but holds no block until
+ * pkv_seq_swap_in: append, fork, cow and block_table refuse it (PKV_ERR_ARG);
+ * pkv_seq_free drops it.  A shared block stays resident for its other owners;
+ * the swapped sequence comes back with private copies. */
+int pkv_seq_swap_out(pkv_alloc *a, int64_t seq_id, int32_t *blocks_out, int max_blocks, int *n_out);
+
+/* Bring a swapped-out sequence back: take ceil(len / block_size) free blocks
+ * as its new table (logical order), written to blocks_out and *n_out for the
+ * caller's pkv_swap_in.  PKV_ERR_OOM, state unchanged, if too few are free. */
+int pkv_seq_swap_in(pkv_alloc *a, int64_t seq_id, int32_t *blocks_out, int max_blocks, int *n_out);
 
 /* Current length (tokens) of a sequence, or a negative error code. */
 int64_t pkv_seq_len(const pkv_alloc *a, int64_t seq_id);

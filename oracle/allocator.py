@@ -12,7 +12,9 @@ What the pages fix:
   "PagedAttention borrows an operating-system trick");
 * blocks holding an identical prefix may be referenced by several sequences
   and are copied on write (praveentn.live "PagedAttention KV-cache
-  constraint", section "What the change bought").
+  constraint", section "What the change bought");
+* under memory pressure a sequence's blocks are swapped out to host memory
+  and back (same page, "What it cost").
 
 Readings of ours where the pages leave the policy open:
 * free blocks form a LIFO stack that starts as [NB-1, ..., 1, 0] (top last),
@@ -20,7 +22,10 @@ Readings of ours where the pages leave the policy open:
   pushed back in logical order;
 * an append that would write into a partially filled block with refcount > 1
   is refused ("shared"); the caller first asks for the copy-on-write;
-* a failed call (out of blocks, bad id) leaves the state unchanged.
+* a failed call (out of blocks, bad id) leaves the state unchanged;
+* a swapped-out sequence keeps its id and length, releases its blocks like a
+  free does, refuses append / fork / cow / table until it is swapped back in,
+  and comes back with fresh private blocks in logical order.
 """
 from __future__ import annotations
 
@@ -50,16 +55,19 @@ class OracleAllocator:
             n += 1
         return n
 
-    def _get(self, seq_id: int) -> dict:
+    def _get(self, seq_id: int, resident: bool = True) -> dict:
         if seq_id not in self.seqs:
             raise AllocError("arg", f"unknown sequence {seq_id}")
-        return self.seqs[seq_id]
+        s = self.seqs[seq_id]
+        if resident and s["swapped"]:
+            raise AllocError("arg", f"sequence {seq_id} is swapped out")
+        return s
 
     # -- operations --------------------------------------------------------
     def seq_add(self, seq_id: int) -> None:
         if seq_id in self.seqs:
             raise AllocError("arg", f"sequence {seq_id} exists")
-        self.seqs[seq_id] = {"blocks": [], "len": 0}
+        self.seqs[seq_id] = {"blocks": [], "len": 0, "swapped": False}
 
     def seq_append(self, seq_id: int, n_tokens: int) -> list[int]:
         s = self._get(seq_id)
@@ -93,7 +101,7 @@ class OracleAllocator:
             raise AllocError("arg", f"sequence {child} exists")
         for b in p["blocks"]:
             self.refcount[b] += 1
-        self.seqs[child] = {"blocks": list(p["blocks"]), "len": p["len"]}
+        self.seqs[child] = {"blocks": list(p["blocks"]), "len": p["len"], "swapped": False}
 
     def seq_cow(self, seq_id: int, logical: int = -1):
         """Give ``seq_id`` a private copy of one shared block.
@@ -121,12 +129,43 @@ class OracleAllocator:
         return (old, new)
 
     def seq_free(self, seq_id: int) -> None:
-        s = self._get(seq_id)
+        s = self._get(seq_id, resident=False)
         for b in s["blocks"]:
             self.refcount[b] -= 1
             if self.refcount[b] == 0:
                 self.free.append(b)
         del self.seqs[seq_id]
+
+    def seq_swap_out(self, seq_id: int, max_blocks: int) -> list[int]:
+        """Release the sequence's blocks (returned in logical order for the copy out)."""
+        s = self._get(seq_id)
+        if len(s["blocks"]) > max_blocks:
+            raise AllocError("range", f"sequence {seq_id} has more than {max_blocks} blocks")
+        out = list(s["blocks"])
+        for b in out:
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free.append(b)
+        s["blocks"] = []
+        s["swapped"] = True
+        return out
+
+    def seq_swap_in(self, seq_id: int, max_blocks: int) -> list[int]:
+        """Fresh blocks for a swapped-out sequence (logical order), for the copy in."""
+        s = self._get(seq_id, resident=False)
+        if not s["swapped"]:
+            raise AllocError("arg", f"sequence {seq_id} is resident")
+        need = self._blocks_for(s["len"])
+        if need > max_blocks:
+            raise AllocError("range", f"sequence {seq_id} needs more than {max_blocks} blocks")
+        if need > len(self.free):
+            raise AllocError("oom", f"need {need} blocks, {len(self.free)} free")
+        for _ in range(need):
+            b = self.free.pop()
+            self.refcount[b] = 1
+            s["blocks"].append(b)
+        s["swapped"] = False
+        return list(s["blocks"])
 
     def block_table(self, seq_ids, max_blocks: int):
         """Rows of physical ids (-1 past each sequence's blocks) and lengths."""

@@ -13,6 +13,9 @@ shared with the CUDA path.
 * ``block_copy``: the copy that materialises copy-on-write of a shared block
   (praveentn.live "PagedAttention KV-cache constraint", section "What the
   change bought": blocks of an identical prefix are shared with copy-on-write).
+* ``swap_out`` / ``swap_in``: whole blocks to and from a host buffer, the data
+  side of swapping blocks out under memory pressure (same page, "What it
+  cost").
 
 Arrays are numpy; bf16 values are carried as their uint16 bit patterns, so
 every operation here is an exact bit copy.
@@ -50,3 +53,27 @@ def block_copy(k_cache, v_cache, src_dst_pairs):
             raise IndexError(f"pair ({src}, {dst}) is outside a pool of {num_blocks} blocks")
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
+
+
+def swap_out(k_cache, v_cache, block_ids):
+    """Host copies of the listed blocks: returns (k, v), each [n, Hkv, bs, d]."""
+    num_blocks = k_cache.shape[0]
+    ids = [int(b) for b in np.asarray(block_ids).reshape(-1)]
+    k = np.empty((len(ids),) + k_cache.shape[1:], dtype=k_cache.dtype)
+    v = np.empty_like(k)
+    for i, b in enumerate(ids):
+        if not 0 <= b < num_blocks:
+            raise IndexError(f"block {b} is outside a pool of {num_blocks} blocks")
+        k[i] = k_cache[b]
+        v[i] = v_cache[b]
+    return k, v
+
+
+def swap_in(k, v, block_ids, k_cache, v_cache):
+    """In place: block block_ids[i] of the caches := k[i], v[i]."""
+    num_blocks = k_cache.shape[0]
+    for i, b in enumerate(int(x) for x in np.asarray(block_ids).reshape(-1)):
+        if not 0 <= b < num_blocks:
+            raise IndexError(f"block {b} is outside a pool of {num_blocks} blocks")
+        k_cache[b] = k[i]
+        v_cache[b] = v[i]

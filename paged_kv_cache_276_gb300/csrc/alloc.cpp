@@ -5,7 +5,9 @@
 // to the pool on finish (x321.org "The serving bottleneck is not just FLOPs",
 // section "PagedAttention borrows an operating-system trick") and
 // reference-counted sharing with copy-on-write (praveentn.live "PagedAttention
-// KV-cache constraint", section "What the change bought").
+// KV-cache constraint", section "What the change bought"); under memory
+// pressure a sequence's blocks can be swapped out to host memory and back
+// (same page, "What it cost").
 //
 // Every mutating call validates first and mutates last, so a failing call
 // leaves the state unchanged.
@@ -22,6 +24,7 @@ namespace {
 struct Sequence {
   std::vector<int32_t> blocks;  // logical -> physical
   int64_t len = 0;              // tokens stored
+  bool swapped = false;         // blocks released to the pool, contents held by the caller
 };
 
 }  // namespace
@@ -70,7 +73,7 @@ int pkv_seq_add(pkv_alloc *a, int64_t seq_id) {
 int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_out) {
   if (!a || n_tokens < 0) return PKV_ERR_ARG;
   Sequence *s = a->find(seq_id);
-  if (!s) return PKV_ERR_ARG;
+  if (!s || s->swapped) return PKV_ERR_ARG;
   if (n_tokens == 0) return PKV_OK;
   if (!slots_out) return PKV_ERR_ARG;
   const int64_t bs = a->block_size;
@@ -96,7 +99,7 @@ int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_ou
 int pkv_seq_fork(pkv_alloc *a, int64_t parent, int64_t child) {
   if (!a) return PKV_ERR_ARG;
   const Sequence *p = a->find(parent);
-  if (!p || a->find(child)) return PKV_ERR_ARG;
+  if (!p || p->swapped || a->find(child)) return PKV_ERR_ARG;
   Sequence c = *p;  // copy before the map may rehash
   for (int32_t b : c.blocks) a->refcount[b] += 1;
   a->seqs.emplace(child, std::move(c));
@@ -106,7 +109,7 @@ int pkv_seq_fork(pkv_alloc *a, int64_t parent, int64_t child) {
 int pkv_seq_cow(pkv_alloc *a, int64_t seq_id, int logical_block, int32_t *pair_out, int *copied) {
   if (!a || !pair_out || !copied) return PKV_ERR_ARG;
   Sequence *s = a->find(seq_id);
-  if (!s) return PKV_ERR_ARG;
+  if (!s || s->swapped) return PKV_ERR_ARG;
   *copied = 0;
   int64_t logical = logical_block;
   if (logical == -1) {
@@ -139,6 +142,43 @@ int pkv_seq_free(pkv_alloc *a, int64_t seq_id) {
   return PKV_OK;
 }
 
+int pkv_seq_swap_out(pkv_alloc *a, int64_t seq_id, int32_t *blocks_out, int max_blocks, int *n_out) {
+  if (!a || !n_out || max_blocks < 0) return PKV_ERR_ARG;
+  Sequence *s = a->find(seq_id);
+  if (!s || s->swapped) return PKV_ERR_ARG;
+  const int64_t nb = static_cast<int64_t>(s->blocks.size());
+  if (nb > max_blocks) return PKV_ERR_RANGE;
+  if (nb > 0 && !blocks_out) return PKV_ERR_ARG;
+  for (int64_t i = 0; i < nb; ++i) blocks_out[i] = s->blocks[i];
+  for (int32_t b : s->blocks) {
+    if (--a->refcount[b] == 0) a->free_stack.push_back(b);
+  }
+  s->blocks.clear();
+  s->swapped = true;
+  *n_out = static_cast<int>(nb);
+  return PKV_OK;
+}
+
+int pkv_seq_swap_in(pkv_alloc *a, int64_t seq_id, int32_t *blocks_out, int max_blocks, int *n_out) {
+  if (!a || !n_out || max_blocks < 0) return PKV_ERR_ARG;
+  Sequence *s = a->find(seq_id);
+  if (!s || !s->swapped) return PKV_ERR_ARG;
+  const int64_t nb = a->blocks_for(s->len);
+  if (nb > max_blocks) return PKV_ERR_RANGE;
+  if (nb > 0 && !blocks_out) return PKV_ERR_ARG;
+  if (nb > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+  for (int64_t i = 0; i < nb; ++i) {
+    const int32_t b = a->free_stack.back();
+    a->free_stack.pop_back();
+    a->refcount[b] = 1;
+    s->blocks.push_back(b);
+    blocks_out[i] = b;
+  }
+  s->swapped = false;
+  *n_out = static_cast<int>(nb);
+  return PKV_OK;
+}
+
 int64_t pkv_seq_len(const pkv_alloc *a, int64_t seq_id) {
   if (!a) return PKV_ERR_ARG;
   const Sequence *s = a->find(seq_id);
@@ -151,7 +191,7 @@ int pkv_block_table(const pkv_alloc *a, const int64_t *seq_ids, int n, int32_t *
     return PKV_ERR_ARG;
   for (int i = 0; i < n; ++i) {  // validate everything before writing
     const Sequence *s = a->find(seq_ids[i]);
-    if (!s) return PKV_ERR_ARG;
+    if (!s || s->swapped) return PKV_ERR_ARG;
     if (static_cast<int64_t>(s->blocks.size()) > max_blocks) return PKV_ERR_RANGE;
     if (s->len > INT32_MAX) return PKV_ERR_RANGE;
   }

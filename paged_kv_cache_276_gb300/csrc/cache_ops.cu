@@ -1,6 +1,7 @@
-// Slot write (pkv_write) and copy-on-write block copy (pkv_block_copy).
+// Slot write (pkv_write), copy-on-write block copy (pkv_block_copy) and block
+// swap to and from page-locked host memory (pkv_swap_out / pkv_swap_in).
 //
-// Both are pure data movement: 16-byte vector loads and stores, coalesced
+// All are pure data movement: 16-byte vector loads and stores, coalesced
 // along head_dim, grid-stride loops sized to the SM count.
 #include <cstdio>
 #include <cuda_runtime.h>
@@ -92,6 +93,77 @@ __global__ void __launch_bounds__(256) block_copy_kernel(
   }
 }
 
+// Whole blocks between the caches and a host buffer of n blocks: blockIdx.y
+// walks the listed blocks, the x threads stride over a block's 16-byte chunks
+// (all heads, slots and dims), K and V together.  to_host: cache -> buffer.
+__global__ void __launch_bounds__(256) swap_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                                   uint4 *__restrict__ buf_k, uint4 *__restrict__ buf_v,
+                                                   const int32_t *__restrict__ ids, int n, int num_blocks,
+                                                   int64_t chunks_per_block, int to_host, int32_t *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = blockIdx.y; i < n; i += gridDim.y) {
+    const int b = ids[i];
+    if (b < 0 || b >= num_blocks) {
+      if (blockIdx.x == 0 && threadIdx.x == 0 && status) atomicOr(status, PKV_STATUS_BAD_BLOCK);
+      continue;
+    }
+    uint4 *ck = k_cache + static_cast<int64_t>(b) * chunks_per_block;
+    uint4 *cv = v_cache + static_cast<int64_t>(b) * chunks_per_block;
+    uint4 *hk = buf_k + static_cast<int64_t>(i) * chunks_per_block;
+    uint4 *hv = buf_v + static_cast<int64_t>(i) * chunks_per_block;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t c = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; c < chunks_per_block;
+         c += stride) {
+      if (to_host) {
+        const uint4 a = ck[c], d = cv[c];
+        hk[c] = a;
+        hv[c] = d;
+      } else {
+        const uint4 a = hk[c], d = hv[c];
+        ck[c] = a;
+        cv[c] = d;
+      }
+    }
+  }
+}
+
+// Device address of a buffer the caller says is page-locked host memory (or
+// device memory); nullptr for pageable memory the device cannot address.
+void *device_view(const void *p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of a failed query
+    return nullptr;
+  }
+  if (attr.type != cudaMemoryTypeHost && attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return nullptr;
+  return attr.devicePointer;
+}
+
+int swap_blocks(const void *k_cache, const void *v_cache, const int32_t *block_ids, int n, const void *host_k,
+                const void *host_v, int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                int32_t *d_status, void *stream, bool to_host) {
+  if (n < 0 || num_blocks < 0 || block_size < 1 || num_kv_heads < 1 || head_dim < 8 || head_dim % 8 != 0)
+    return PKV_ERR_ARG;
+  if (n == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !block_ids || !host_k || !host_v) return PKV_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(host_k) || !aligned16(host_v) ||
+      (reinterpret_cast<uintptr_t>(block_ids) & 3u))
+    return PKV_ERR_ARG;
+  void *dk = device_view(host_k), *dv = device_view(host_v);
+  if (!dk || !dv) return PKV_ERR_ARG;
+  const int64_t chunks_per_block = static_cast<int64_t>(num_kv_heads) * block_size * head_dim / 8;
+  const int threads = 256;
+  int64_t gx = (chunks_per_block + threads - 1) / threads;
+  if (gx > 32) gx = 32;
+  const int gy = n < 65535 ? n : 65535;
+  swap_kernel<<<dim3(static_cast<unsigned>(gx), gy), threads, 0, as_stream(stream)>>>(
+      reinterpret_cast<uint4 *>(const_cast<void *>(k_cache)), reinterpret_cast<uint4 *>(const_cast<void *>(v_cache)),
+      reinterpret_cast<uint4 *>(dk), reinterpret_cast<uint4 *>(dv), block_ids, n, num_blocks, chunks_per_block,
+      to_host ? 1 : 0, d_status);
+  return check_launch();
+}
+
 }  // namespace
 
 void set_cuda_error(cudaError_t e) {
@@ -167,6 +239,20 @@ int pkv_block_copy(pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *src_dst_
       reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), src_dst_pairs,
       num_pairs, num_blocks, chunks_per_block, d_status);
   return pkv::check_launch();
+}
+
+int pkv_swap_out(const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_ids, int n,
+                 pkv_bf16 *host_k, pkv_bf16 *host_v, int num_blocks, int block_size, int num_kv_heads,
+                 int head_dim, int32_t *d_status, void *stream) {
+  return pkv::swap_blocks(k_cache, v_cache, block_ids, n, host_k, host_v, num_blocks, block_size, num_kv_heads,
+                          head_dim, d_status, stream, true);
+}
+
+int pkv_swap_in(const pkv_bf16 *host_k, const pkv_bf16 *host_v, const int32_t *block_ids, int n,
+                pkv_bf16 *k_cache, pkv_bf16 *v_cache, int num_blocks, int block_size, int num_kv_heads,
+                int head_dim, int32_t *d_status, void *stream) {
+  return pkv::swap_blocks(k_cache, v_cache, block_ids, n, host_k, host_v, num_blocks, block_size, num_kv_heads,
+                          head_dim, d_status, stream, false);
 }
 
 }  // extern "C"

@@ -55,6 +55,12 @@ SIGNATURES = {
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
+    "pkv_swap_out": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
+                              _c_ptr, _c_ptr]),
+    "pkv_swap_in": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
+                             _c_ptr, _c_ptr]),
+    "pkv_seq_swap_out": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
+    "pkv_seq_swap_in": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, ctypes.POINTER(_c_ptr)]),
     "pkv_alloc_destroy": (None, [_c_ptr]),
     "pkv_seq_add": (_c_int, [_c_ptr, _c_i64]),
@@ -190,6 +196,35 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_
         _check(lib().paged_attention_decode_ex(*args, ctypes.c_void_p(handle)), "paged_attention_decode_ex")
 
 
+def _swap_check(k_cache, v_cache, block_ids, host_k, host_v):
+    dev = k_cache.device
+    for t, n, dt in ((k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
+                     (block_ids, "block_ids", torch.int32)):
+        _need(t, dt, n, dev)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device.type != "cpu" or not t.is_pinned():
+            raise ValueError(f"{n}: contiguous pinned host bf16 tensor expected")
+    NB, Hkv, bs, d = k_cache.shape
+    n = block_ids.numel()
+    if v_cache.shape != k_cache.shape or host_k.shape != (n, Hkv, bs, d) or host_v.shape != host_k.shape:
+        raise ValueError("shape mismatch")
+    return NB, Hkv, bs, d, n, dev
+
+
+def pkv_swap_out(k_cache, v_cache, block_ids, host_k, host_v, d_status=None, stream=None):
+    """host_k/v[i] = cache[block_ids[i]]; host buffers pinned [n, Hkv, bs, d] bf16."""
+    NB, Hkv, bs, d, n, dev = _swap_check(k_cache, v_cache, block_ids, host_k, host_v)
+    _check(lib().pkv_swap_out(_ptr(k_cache), _ptr(v_cache), _ptr(block_ids), n, _ptr(host_k), _ptr(host_v), NB, bs,
+                              Hkv, d, _ptr(d_status), _stream(stream, dev)), "pkv_swap_out")
+
+
+def pkv_swap_in(host_k, host_v, block_ids, k_cache, v_cache, d_status=None, stream=None):
+    """cache[block_ids[i]] = host_k/v[i]."""
+    NB, Hkv, bs, d, n, dev = _swap_check(k_cache, v_cache, block_ids, host_k, host_v)
+    _check(lib().pkv_swap_in(_ptr(host_k), _ptr(host_v), _ptr(block_ids), n, _ptr(k_cache), _ptr(v_cache), NB, bs,
+                             Hkv, d, _ptr(d_status), _stream(stream, dev)), "pkv_swap_in")
+
+
 STATIC_SCRATCH_BYTES = 8 << 20  # PKV_STATIC_SCRATCH_BYTES
 
 
@@ -254,6 +289,21 @@ class BlockAllocator:
 
     def seq_free(self, seq_id: int):
         _check(lib().pkv_seq_free(self._h, seq_id), "pkv_seq_free")
+
+    def _swap(self, fn, name, seq_id: int, max_blocks: int):
+        import numpy as np
+        out = np.empty(max(1, max_blocks), dtype=np.int32)
+        n = ctypes.c_int()
+        _check(fn(self._h, seq_id, out.ctypes.data, max_blocks, ctypes.byref(n)), name)
+        return out[:n.value].copy()
+
+    def seq_swap_out(self, seq_id: int, max_blocks: int = 1 << 16):
+        """Release the sequence's blocks; returns their ids in logical order (int32)."""
+        return self._swap(lib().pkv_seq_swap_out, "pkv_seq_swap_out", seq_id, max_blocks)
+
+    def seq_swap_in(self, seq_id: int, max_blocks: int = 1 << 16):
+        """New blocks for a swapped-out sequence, in logical order (int32)."""
+        return self._swap(lib().pkv_seq_swap_in, "pkv_seq_swap_in", seq_id, max_blocks)
 
     def seq_len(self, seq_id: int) -> int:
         n = lib().pkv_seq_len(self._h, seq_id)

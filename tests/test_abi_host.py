@@ -116,7 +116,7 @@ def test_native_allocator_matches_oracle_bit_exact(native, seed):
     live = []
     next_id = 0
     for step in range(600):
-        op = rng.choice(["add", "append", "append", "fork", "cow", "free", "bad"])
+        op = rng.choice(["add", "append", "append", "fork", "cow", "free", "bad", "swap_out", "swap_in"])
         ids = list(oa.seqs)
         res_o = res_n = None
         err_o = err_n = None
@@ -146,8 +146,14 @@ def test_native_allocator_matches_oracle_bit_exact(native, seed):
             sid = int(rng.choice(ids))
             child = next_id
             next_id += 1
-            oa.seq_fork(sid, child)
-            na.seq_fork(sid, child)
+            try:
+                oa.seq_fork(sid, child)
+            except AllocError as e:
+                err_o = e.kind
+            try:
+                na.seq_fork(sid, child)
+            except native.PkvError as e:
+                err_n = _kind(e.code)
         elif op == "cow":
             sid = int(rng.choice(ids))
             nb = len(oa.seqs[sid]["blocks"])
@@ -164,6 +170,18 @@ def test_native_allocator_matches_oracle_bit_exact(native, seed):
             sid = int(rng.choice(ids))
             oa.seq_free(sid)
             na.seq_free(sid)
+        elif op in ("swap_out", "swap_in"):
+            sid = int(rng.choice(ids))
+            f_o = oa.seq_swap_out if op == "swap_out" else oa.seq_swap_in
+            f_n = na.seq_swap_out if op == "swap_out" else na.seq_swap_in
+            try:
+                res_o = f_o(sid, 64)
+            except AllocError as e:
+                err_o = e.kind
+            try:
+                res_n = list(f_n(sid, 64))
+            except native.PkvError as e:
+                err_n = _kind(e.code)
         else:  # unknown id
             with pytest.raises(AllocError):
                 oa.seq_free(10 ** 9)
@@ -173,8 +191,8 @@ def test_native_allocator_matches_oracle_bit_exact(native, seed):
         if res_o is not None or res_n is not None:
             assert (list(res_o) if isinstance(res_o, list) else res_o) == \
                 (list(res_n) if isinstance(res_n, list) else res_n), (step, op)
-        # full state comparison
-        ids = sorted(oa.seqs)
+        # full state comparison (swapped-out sequences have no table)
+        ids = sorted(i for i in oa.seqs if not oa.seqs[i]["swapped"])
         assert na.num_free() == oa.num_free()
         if ids:
             maxb = max(1, max(len(oa.seqs[i]["blocks"]) for i in ids))
@@ -183,8 +201,10 @@ def test_native_allocator_matches_oracle_bit_exact(native, seed):
             assert t_n.tolist() == t_o and l_n.tolist() == l_o
         for b in range(NB):
             assert na.refcount(b) == oa.refcount[b]
+        for i in oa.seqs:
+            assert na.seq_len(i) == oa.seqs[i]["len"]
         # invariants
-        assert sum(oa.refcount) == sum(len(oa.seqs[i]["blocks"]) for i in ids)
+        assert sum(oa.refcount) == sum(len(oa.seqs[i]["blocks"]) for i in oa.seqs)
         assert oa.num_free() + sum(1 for r in oa.refcount if r > 0) == NB
     na.close()
 
@@ -202,3 +222,47 @@ def test_native_allocator_oom_leaves_state_unchanged(native):
     with pytest.raises(native.PkvError) as e:
         a.block_table([1], 2)
     assert e.value.code == native.PKV_ERR_RANGE
+
+
+def test_swapped_sequence_is_refused_until_swapped_back(native):
+    a = native.BlockAllocator(8, 16)
+    a.seq_add(1)
+    a.seq_append(1, 40)  # blocks 0, 1, 2
+    a.seq_fork(1, 2)      # shared with sequence 2
+    out = a.seq_swap_out(1)
+    assert out.tolist() == [0, 1, 2] and a.seq_len(1) == 40 and a.num_free() == 5  # still held by 2
+    for call in (lambda: a.seq_append(1, 1), lambda: a.seq_fork(1, 3), lambda: a.seq_cow(1),
+                 lambda: a.block_table([1], 8), lambda: a.seq_swap_out(1)):
+        with pytest.raises(native.PkvError) as e:
+            call()
+        assert e.value.code == native.PKV_ERR_ARG
+    a.seq_free(2)  # the shared blocks return to the pool
+    assert a.num_free() == 8
+    back = a.seq_swap_in(1)
+    assert len(back) == 3 and a.num_free() == 5
+    table, lens = a.block_table([1], 4)
+    assert table[0, :3].tolist() == back.tolist() and lens[0] == 40
+    with pytest.raises(native.PkvError):
+        a.seq_swap_in(1)  # resident again
+    a.close()
+    b = native.BlockAllocator(2, 16)
+    b.seq_add(7)
+    b.seq_append(7, 20)
+    b.seq_swap_out(7)
+    b.seq_add(8)
+    b.seq_append(8, 17)
+    with pytest.raises(native.PkvError) as e:
+        b.seq_swap_in(7)  # needs 2 blocks, none free
+    assert e.value.code == native.PKV_ERR_OOM
+    b.seq_free(8)
+    assert len(b.seq_swap_in(7)) == 2
+    b.close()
+
+
+def test_swap_copies_reject_bad_arguments_before_launch(native):
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.pkv_swap_out(fake, fake, fake, 0, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_OK
+    assert lib.pkv_swap_out(fake, fake, fake, -1, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
+    assert lib.pkv_swap_in(fake, fake, None, 3, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
+    assert lib.pkv_swap_in(fake, fake, fake, 3, fake, fake, 8, 16, 2, 60, None, None) == native.PKV_ERR_ARG

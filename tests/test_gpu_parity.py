@@ -141,6 +141,79 @@ def test_pkv_block_copy_bit_exact(d, bs, Hkv):
     assert np.array_equal(bits(kc), kc_h)
 
 
+# ------------------------------------------------------------------ swap out / in
+@pytest.mark.parametrize("d,bs,Hkv", [(128, 16, 8), (64, 32, 2)])
+def test_swap_out_and_in_bit_exact(d, bs, Hkv):
+    NB = 40
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), 71, "cuda")
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), 72, "cuda")
+    k_h, v_h = bits(kc), bits(vc)
+    ids = np.array([5, 0, 39, 17, 18, 2], dtype=np.int32)
+    ids_d = torch.as_tensor(ids, device="cuda")
+    hk = torch.empty((len(ids), Hkv, bs, d), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    st = status_tensor()
+    native.pkv_swap_out(kc, vc, ids_d, hk, hv, st)
+    torch.cuda.synchronize()
+    ek, ev = cache_ops.swap_out(k_h, v_h, ids)
+    assert np.array_equal(hk.view(torch.int16).numpy().view(np.uint16), ek)
+    assert np.array_equal(hv.view(torch.int16).numpy().view(np.uint16), ev)
+    # back into other blocks
+    dst = np.array([30, 31, 1, 3, 4, 6], dtype=np.int32)
+    native.pkv_swap_in(hk, hv, torch.as_tensor(dst, device="cuda"), kc, vc, st)
+    torch.cuda.synchronize()
+    cache_ops.swap_in(ek, ev, dst, k_h, v_h)
+    assert np.array_equal(bits(kc), k_h) and np.array_equal(bits(vc), v_h)
+    assert st.item() == 0
+    bad = torch.as_tensor(np.array([2, NB + 3], dtype=np.int32), device="cuda")
+    hk2 = torch.zeros((2, Hkv, bs, d), dtype=torch.bfloat16).pin_memory()
+    hv2 = torch.zeros_like(hk2).pin_memory()
+    native.pkv_swap_out(kc, vc, bad, hk2, hv2, st)
+    torch.cuda.synchronize()
+    assert st.item() & native.PKV_STATUS_BAD_BLOCK
+    assert np.array_equal(hk2[0].view(torch.int16).numpy().view(np.uint16), k_h[2])
+    assert not hk2[1].view(torch.int16).any()  # skipped
+
+
+def test_decode_after_a_swap_round_trip_is_bit_identical():
+    """Swap one sequence out, let other writes reuse its blocks, swap it back
+    into fresh blocks: the decode gives the same bits as before."""
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    NB = 100
+    alloc = native.BlockAllocator(NB, bs)
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), 81, "cuda")
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), 82, "cuda")
+    lens = [300, 700, 45]
+    for i, n in enumerate(lens):
+        alloc.seq_add(i)
+        alloc.seq_append(i, n)
+    q = inputs.randn_bf16((3, 1, Hq, d), 83, "cuda")
+
+    def decode():
+        table, ln = alloc.block_table(range(3), 48)
+        return run_decode(q, kc, vc, table, ln, 0.09, 512)
+
+    before = decode()
+    out_ids = alloc.seq_swap_out(1)
+    hk = torch.empty((len(out_ids), Hkv, bs, d), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    native.pkv_swap_out(kc, vc, torch.as_tensor(out_ids, device="cuda"), hk, hv)
+    # another sequence takes the freed blocks and overwrites them
+    alloc.seq_add(9)
+    slots = alloc.seq_append(9, 700)
+    junk = inputs.randn_bf16((700, Hkv, d), 84, "cuda")
+    native.pkv_write(junk, junk, torch.as_tensor(slots, device="cuda"), kc, vc)
+    alloc.seq_free(9)
+    alloc.seq_add(10)
+    alloc.seq_append(10, 5 * bs)  # holds the top of the free stack, so sequence 1 lands elsewhere
+    in_ids = alloc.seq_swap_in(1)
+    assert set(in_ids.tolist()) != set(out_ids.tolist())
+    native.pkv_swap_in(hk, hv, torch.as_tensor(in_ids, device="cuda"), kc, vc)
+    after = decode()
+    assert torch.equal(after.view(torch.int16), before.view(torch.int16))
+    alloc.close()
+
+
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("d,bs,Hq,Hkv,lens,partition", [
     (64, 16, 4, 2, [17, 33, 64], 0),                      # the tiny workload's shapes
