@@ -306,21 +306,26 @@ class Runner:
         out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
         ws = sess.workspace(int(sess.alloc.block_table(range(sess.B), sess.max_blocks)[1].max()) + steps + 8)
         stream = torch.cuda.current_stream()
+        # page-locked staging that the allocator fills in place every step
+        seq_ids = np.arange(sess.B, dtype=np.int64)
+        slots_h = torch.empty(sess.B * sess.q_len, dtype=torch.int64).pin_memory()
+        tables_h = torch.empty((sess.B, sess.max_blocks), dtype=torch.int32).pin_memory()
+        lens_h = torch.empty(sess.B, dtype=torch.int32).pin_memory()
+        slots_d = torch.empty(sess.B * sess.q_len, dtype=torch.int64, device=self.device)
+        tables_d = torch.empty((sess.B, sess.max_blocks), dtype=torch.int32, device=self.device)
+        lens_d = torch.empty(sess.B, dtype=torch.int32, device=self.device)
+        slots_np, tables_np, lens_np = slots_h.numpy(), tables_h.numpy(), lens_h.numpy()
         times, kv, h2d = [], [], 0
         for i in range(steps + 1):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            # host allocator work of the step (public API), then the uploads
-            slots = np.empty(sess.B * sess.q_len, dtype=np.int64)
-            for s in range(sess.B):
-                slots[s * sess.q_len:(s + 1) * sess.q_len] = sess.alloc.seq_append(s, sess.q_len)
-            tables, lens = sess.alloc.block_table(range(sess.B), sess.max_blocks)
-            slots_h = torch.from_numpy(slots).pin_memory()
-            tables_h = torch.from_numpy(tables).pin_memory()
-            lens_h = torch.from_numpy(lens).pin_memory()
-            slots_d = slots_h.to(self.device, non_blocking=True)
-            tables_d = tables_h.to(self.device, non_blocking=True)
-            lens_d = lens_h.to(self.device, non_blocking=True)
+            # host allocator work of the step (public API, one call each), then the uploads
+            sess.alloc.seq_append_batch(seq_ids, sess.q_len, out=slots_np)
+            sess.alloc.block_table(seq_ids, sess.max_blocks, table_out=tables_np, lens_out=lens_np)
+            slots_d.copy_(slots_h, non_blocking=True)
+            tables_d.copy_(tables_h, non_blocking=True)
+            lens_d.copy_(lens_h, non_blocking=True)
+            lens = lens_np
             q_d.copy_(q_h, non_blocking=True)
             for l in range(sess.layers):
                 k_d[l].copy_(k_h[l], non_blocking=True)

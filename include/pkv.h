@@ -277,6 +277,13 @@ int pkv_seq_add(pkv_alloc *a, int64_t seq_id);
  * pkv_seq_cow first). */
 int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_out);
 
+/* pkv_seq_append for n distinct sequences at once, n_tokens each: the slots of
+ * sequence i go to slots_out[i * n_tokens ...].  All or nothing: every check
+ * (ids, shared partial blocks, enough free blocks for all) runs before any
+ * sequence changes, so a failing call leaves the state unchanged; the blocks
+ * are then taken in the order of seq_ids, exactly as n single appends would. */
+int pkv_seq_append_batch(pkv_alloc *a, const int64_t *seq_ids, int n, int n_tokens, int64_t *slots_out);
+
 /* child := a new sequence sharing every block of parent (refcount + 1 each). */
 int pkv_seq_fork(pkv_alloc *a, int64_t parent, int64_t child);
 

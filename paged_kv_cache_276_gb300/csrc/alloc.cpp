@@ -96,6 +96,29 @@ int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_ou
   return PKV_OK;
 }
 
+int pkv_seq_append_batch(pkv_alloc *a, const int64_t *seq_ids, int n, int n_tokens, int64_t *slots_out) {
+  if (!a || n < 0 || n_tokens < 0) return PKV_ERR_ARG;
+  if (n == 0 || n_tokens == 0) return PKV_OK;
+  if (!seq_ids || !slots_out) return PKV_ERR_ARG;
+  // validate all, and count the blocks all of them need, before changing anything
+  const int64_t bs = a->block_size;
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    const Sequence *s = a->find(seq_ids[i]);
+    if (!s || s->swapped) return PKV_ERR_ARG;
+    for (int j = 0; j < i; ++j)
+      if (seq_ids[j] == seq_ids[i]) return PKV_ERR_ARG;  // each sequence once
+    if (s->len % bs != 0 && a->refcount[s->blocks.back()] > 1) return PKV_ERR_SHARED;
+    need += a->blocks_for(s->len + n_tokens) - static_cast<int64_t>(s->blocks.size());
+  }
+  if (need > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+  for (int i = 0; i < n; ++i) {
+    const int rc = pkv_seq_append(a, seq_ids[i], n_tokens, slots_out + static_cast<size_t>(i) * n_tokens);
+    if (rc != PKV_OK) return rc;  // cannot happen after the checks above
+  }
+  return PKV_OK;
+}
+
 int pkv_seq_fork(pkv_alloc *a, int64_t parent, int64_t child) {
   if (!a) return PKV_ERR_ARG;
   const Sequence *p = a->find(parent);

@@ -59,6 +59,7 @@ SIGNATURES = {
                               _c_ptr, _c_ptr]),
     "pkv_swap_in": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
                              _c_ptr, _c_ptr]),
+    "pkv_seq_append_batch": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_ptr]),
     "pkv_seq_swap_out": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
     "pkv_seq_swap_in": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, ctypes.POINTER(_c_ptr)]),
@@ -278,6 +279,19 @@ class BlockAllocator:
                "pkv_seq_append")
         return slots
 
+    def seq_append_batch(self, seq_ids, n_tokens: int, out=None):
+        """Append n_tokens to each listed sequence; returns (or fills ``out`` with)
+        the int64 slots, sequence by sequence.  ``seq_ids`` and ``out`` may be
+        numpy arrays (``out`` for instance a view of pinned memory)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        slots = np.empty(len(ids) * n_tokens, dtype=np.int64) if out is None else out
+        if slots.dtype != np.int64 or not slots.flags.c_contiguous or slots.size < len(ids) * n_tokens:
+            raise ValueError("out: contiguous int64 array of len(seq_ids) * n_tokens expected")
+        _check(lib().pkv_seq_append_batch(self._h, ids.ctypes.data, len(ids), n_tokens, slots.ctypes.data),
+               "pkv_seq_append_batch")
+        return slots
+
     def seq_fork(self, parent: int, child: int):
         _check(lib().pkv_seq_fork(self._h, parent, child), "pkv_seq_fork")
 
@@ -311,11 +325,17 @@ class BlockAllocator:
             raise PkvError(int(n), "pkv_seq_len")
         return int(n)
 
-    def block_table(self, seq_ids, max_blocks: int):
+    def block_table(self, seq_ids, max_blocks: int, table_out=None, lens_out=None):
+        """[n, max_blocks] int32 table rows and [n] int32 lengths (or written into
+        ``table_out`` / ``lens_out``, e.g. views of pinned memory)."""
         import numpy as np
-        ids = np.ascontiguousarray(np.asarray(list(seq_ids), dtype=np.int64))
-        table = np.empty((len(ids), max_blocks), dtype=np.int32)
-        lens = np.empty(len(ids), dtype=np.int32)
+        ids = np.ascontiguousarray(np.asarray(list(seq_ids) if not isinstance(seq_ids, np.ndarray) else seq_ids,
+                                              dtype=np.int64))
+        table = np.empty((len(ids), max_blocks), dtype=np.int32) if table_out is None else table_out
+        lens = np.empty(len(ids), dtype=np.int32) if lens_out is None else lens_out
+        if (table.dtype != np.int32 or lens.dtype != np.int32 or not table.flags.c_contiguous
+                or table.shape != (len(ids), max_blocks) or lens.shape != (len(ids),)):
+            raise ValueError("table_out / lens_out: contiguous int32 [n, max_blocks] / [n] expected")
         _check(lib().pkv_block_table(self._h, ids.ctypes.data, len(ids), table.ctypes.data, max_blocks,
                                      lens.ctypes.data), "pkv_block_table")
         return table, lens

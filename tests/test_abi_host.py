@@ -266,3 +266,35 @@ def test_swap_copies_reject_bad_arguments_before_launch(native):
     assert lib.pkv_swap_out(fake, fake, fake, -1, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
     assert lib.pkv_swap_in(fake, fake, None, 3, fake, fake, 8, 16, 2, 64, None, None) == native.PKV_ERR_ARG
     assert lib.pkv_swap_in(fake, fake, fake, 3, fake, fake, 8, 16, 2, 60, None, None) == native.PKV_ERR_ARG
+
+
+def test_batched_append_equals_single_appends_and_is_all_or_nothing(native):
+    rng = np.random.default_rng(3)
+    a = native.BlockAllocator(64, 16)
+    b = native.BlockAllocator(64, 16)
+    for x in (a, b):
+        for i in range(6):
+            x.seq_add(i)
+            x.seq_append(i, int(rng.integers(0, 40)) if x is a else 0)
+    # give b the same lengths as a
+    b.close()
+    b = native.BlockAllocator(64, 16)
+    for i in range(6):
+        b.seq_add(i)
+        b.seq_append(i, a.seq_len(i))
+    ids = [4, 0, 5, 2]
+    got = a.seq_append_batch(ids, 3)
+    want = np.concatenate([b.seq_append(i, 3) for i in ids])
+    assert got.tolist() == want.tolist()
+    assert a.block_table(range(6), 8)[0].tolist() == b.block_table(range(6), 8)[0].tolist()
+    before = (a.block_table(range(6), 8)[0].copy(), a.num_free())
+    for bad in ([1, 1], [1, 99]):
+        with pytest.raises(native.PkvError) as e:
+            a.seq_append_batch(bad, 2)
+        assert e.value.code == native.PKV_ERR_ARG
+    with pytest.raises(native.PkvError) as e:
+        a.seq_append_batch([0, 1, 2, 3, 4, 5], 200)  # more blocks than free in total
+    assert e.value.code == native.PKV_ERR_OOM
+    assert np.array_equal(a.block_table(range(6), 8)[0], before[0]) and a.num_free() == before[1]
+    a.close()
+    b.close()
