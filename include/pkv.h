@@ -277,6 +277,25 @@ int pkv_seq_add(pkv_alloc *a, int64_t seq_id);
  * pkv_seq_cow first). */
 int pkv_seq_append(pkv_alloc *a, int64_t seq_id, int n_tokens, int64_t *slots_out);
 
+/* Append n_tokens tokens with their ids (prefix caching).  Like pkv_seq_append,
+ * except that a whole block of this call whose token prefix (every token from
+ * the start of the sequence through the end of the block) matches a
+ * registered block exactly is not stored again: the sequence's table points to
+ * that block (its refcount + 1), the block's tokens get slot -1 (pkv_write
+ * skips them) and count in *cached_out.  Every block this sequence fills is
+ * registered under its prefix unless the prefix already names a block.
+ * Registered blocks nobody holds stay cached and count as free; a block is
+ * taken from the free stack first, else the least recently released cached
+ * block is evicted.  Prefix caching follows a sequence while all its tokens
+ * come through this call (fork and copy-on-write keep it); pkv_seq_append or a
+ * swap-in ends it for that sequence.  Errors as pkv_seq_append; all lookups
+ * are made before any block is taken, and a failing call changes nothing. */
+int pkv_seq_append_tokens(pkv_alloc *a, int64_t seq_id, const int32_t *token_ids, int n_tokens,
+                          int64_t *slots_out, int *cached_out);
+
+/* Registered (content-addressed) blocks, and those of them nobody holds. */
+int pkv_prefix_cache_stats(const pkv_alloc *a, int64_t *registered_blocks, int64_t *evictable_blocks);
+
 /* pkv_seq_append for n distinct sequences at once, n_tokens each: the slots of
  * sequence i go to slots_out[i * n_tokens ...].  All or nothing: every check
  * (ids, shared partial blocks, enough free blocks for all) runs before any
@@ -323,6 +342,7 @@ int64_t pkv_seq_len(const pkv_alloc *a, int64_t seq_id);
 int pkv_block_table(const pkv_alloc *a, const int64_t *seq_ids, int n, int32_t *table_out,
                     int max_blocks, int32_t *lens_out);
 
+/* Blocks that can be handed out: the free stack plus the cached blocks nobody holds. */
 int pkv_num_free(const pkv_alloc *a);
 /* Refcount of a block, or PKV_ERR_RANGE. */
 int pkv_refcount(const pkv_alloc *a, int block);

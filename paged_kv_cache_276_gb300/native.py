@@ -60,6 +60,8 @@ SIGNATURES = {
     "pkv_swap_in": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
                              _c_ptr, _c_ptr]),
     "pkv_seq_append_batch": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_ptr]),
+    "pkv_seq_append_tokens": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, _c_ptr, ctypes.POINTER(_c_int)]),
+    "pkv_prefix_cache_stats": (_c_int, [_c_ptr, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "pkv_seq_swap_out": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
     "pkv_seq_swap_in": (_c_int, [_c_ptr, ctypes.c_int64, _c_ptr, _c_int, ctypes.POINTER(_c_int)]),
     "pkv_alloc_create": (_c_int, [_c_int, _c_int, ctypes.POINTER(_c_ptr)]),
@@ -291,6 +293,24 @@ class BlockAllocator:
         _check(lib().pkv_seq_append_batch(self._h, ids.ctypes.data, len(ids), n_tokens, slots.ctypes.data),
                "pkv_seq_append_batch")
         return slots
+
+    def seq_append_tokens(self, seq_id: int, token_ids):
+        """Append tokens with their ids; returns (slots int64, cached token count).
+        Slots of tokens found in the prefix cache are -1."""
+        import numpy as np
+        toks = np.ascontiguousarray(np.asarray(token_ids, dtype=np.int32))
+        slots = np.empty(len(toks), dtype=np.int64)
+        cached = ctypes.c_int()
+        _check(lib().pkv_seq_append_tokens(self._h, seq_id, toks.ctypes.data if len(toks) else None, len(toks),
+                                           slots.ctypes.data if len(toks) else None, ctypes.byref(cached)),
+               "pkv_seq_append_tokens")
+        return slots, cached.value
+
+    def prefix_cache_stats(self):
+        """(registered blocks, of which nobody holds)."""
+        r, e = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pkv_prefix_cache_stats(self._h, ctypes.byref(r), ctypes.byref(e)), "pkv_prefix_cache_stats")
+        return r.value, e.value
 
     def seq_fork(self, parent: int, child: int):
         _check(lib().pkv_seq_fork(self._h, parent, child), "pkv_seq_fork")

@@ -214,6 +214,55 @@ def test_decode_after_a_swap_round_trip_is_bit_identical():
     alloc.close()
 
 
+def test_decode_over_prefix_cached_blocks_equals_private_storage():
+    """Sequence B shares its first blocks with A through the prefix cache (their
+    slots come back -1 and pkv_write skips them); its decode is bit for bit the
+    decode of the same tokens stored privately."""
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    NB, P = 64, 96
+    kv_k = inputs.randn_bf16((3, P, Hkv, d), 91, "cuda")  # K / V of token id t at position p
+    kv_v = inputs.randn_bf16((3, P, Hkv, d), 92, "cuda")
+
+    def store(alloc, kc, vc, sid, toks, cached_ok):
+        slots, cached = alloc.seq_append_tokens(sid, toks)
+        if not cached_ok:
+            assert cached == 0
+        start = alloc.seq_len(sid) - len(toks)
+        pos = torch.arange(start, start + len(toks), device="cuda")
+        tid = torch.as_tensor(np.asarray(toks, dtype=np.int64), device="cuda")
+        native.pkv_write(kv_k[tid, pos].contiguous(), kv_v[tid, pos].contiguous(),
+                         torch.as_tensor(slots, device="cuda"), kc, vc)
+        return cached
+
+    rng = np.random.default_rng(17)
+    prompt = rng.integers(0, 3, size=40).tolist()
+    tail_a, tail_b = rng.integers(0, 3, size=9).tolist(), rng.integers(0, 3, size=21).tolist()
+    q = inputs.randn_bf16((1, 1, Hq, d), 93, "cuda")
+    # shared: A stores the prompt, B finds its two full blocks
+    a = native.BlockAllocator(NB, bs)
+    kc = torch.zeros((NB, Hkv, bs, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    a.seq_add(0)
+    store(a, kc, vc, 0, prompt + tail_a, False)
+    a.seq_add(1)
+    assert store(a, kc, vc, 1, prompt + tail_b, True) == 32
+    t1, l1 = a.block_table([1], 8)
+    t0, _ = a.block_table([0], 8)
+    assert t1[0, :2].tolist() == t0[0, :2].tolist()
+    shared = run_decode(q, kc, vc, t1, l1, 0.09, 512)
+    # private: B alone in a fresh pool
+    b = native.BlockAllocator(NB, bs)
+    kc2 = torch.zeros_like(kc)
+    vc2 = torch.zeros_like(kc)
+    b.seq_add(1)
+    store(b, kc2, vc2, 1, prompt + tail_b, False)
+    t2, l2 = b.block_table([1], 8)
+    private = run_decode(q, kc2, vc2, t2, l2, 0.09, 512)
+    assert torch.equal(shared.view(torch.int16), private.view(torch.int16))
+    a.close()
+    b.close()
+
+
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("d,bs,Hq,Hkv,lens,partition", [
     (64, 16, 4, 2, [17, 33, 64], 0),                      # the tiny workload's shapes
