@@ -111,3 +111,40 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, *, num_q_heads,
     if rc != 0:
         raise ValueError(f"oracle_paged_attention failed with code {rc}")
     return out
+
+
+def paged_attention_varlen(q, k_cache, v_cache, block_tables, seq_lens, q_start, *, num_q_heads,
+                           num_kv_heads, head_dim, block_size, scale):
+    """fp64 paged attention of a chunk of new tokens per sequence (chunked prefill).
+
+    The pages' scheduler splits a long prompt into chunks and runs them in the
+    same step as single-token decodes (x321.org "The serving bottleneck is not
+    just FLOPs", section "Continuous batching is the other half of the story").
+    Sequence i owns query rows q_start[i] .. q_start[i+1]-1 of q (bf16
+    [total_q, Hq, d]); they are its newest c_i = q_start[i+1] - q_start[i]
+    tokens, so row r < c_i sees keys t < seq_lens[i] - c_i + 1 + r, the causal
+    rule of ``paged_attention`` with q_len = c_i.  Each sequence is one call of
+    that function on its own rows; rows with no visible key are zero.
+    Returns float64 [total_q, Hq, d].
+    """
+    qb = as_bf16_bits(q)
+    qs = np.asarray(q_start, dtype=np.int64).reshape(-1)
+    sl = np.asarray(seq_lens, dtype=np.int32).reshape(-1)
+    bt = np.asarray(block_tables, dtype=np.int32)
+    B = int(sl.shape[0])
+    if qs.shape[0] != B + 1 or qs[0] != 0 or np.any(np.diff(qs) < 0):
+        raise ValueError("q_start must be [num_seqs + 1], start at 0 and never decrease")
+    total = int(qs[-1])
+    qb = qb.reshape(-1, num_q_heads, head_dim)
+    if qb.shape[0] != total:
+        raise ValueError("q must hold q_start[-1] rows")
+    out = np.zeros((total, num_q_heads, head_dim), dtype=np.float64)
+    for i in range(B):
+        lo, hi = int(qs[i]), int(qs[i + 1])
+        if hi == lo:
+            continue
+        out[lo:hi] = paged_attention(qb[lo:hi][None], k_cache, v_cache, bt[i:i + 1], sl[i:i + 1],
+                                     num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                                     head_dim=head_dim, block_size=block_size, scale=scale,
+                                     q_len=hi - lo)[0]
+    return out
