@@ -64,6 +64,7 @@ typedef uint16_t pkv_bf16;
 #define PKV_STATUS_BAD_BLOCK  2  /* block id outside [0, num_blocks)             */
 #define PKV_STATUS_BAD_LEN    4  /* seq_len < 0 or above the table's capacity    */
 #define PKV_STATUS_TIMEOUT    8  /* a bounded on-chip wait gave up               */
+#define PKV_STATUS_BAD_QSTART 16 /* prefill: q_start entry out of order or range */
 
 /* Human-readable name of a return code (static storage). */
 const char *pkv_error_string(int code);
@@ -189,6 +190,46 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               int partition_size, pkv_bf16 *out, void *workspace,
                               size_t workspace_bytes, int32_t *d_status, void *stream,
                               void *main_done_event);
+
+/*
+ * paged_attention_prefill -- attention of a chunk of new tokens per sequence,
+ * each sequence with its own chunk length (chunked prefill).
+ *
+ * Pages: the scheduler splits a long prompt into chunks and runs them in the
+ * same step as the decodes of other requests; the prompt side is the
+ * compute-heavy phase (x321.org "The serving bottleneck is not just FLOPs",
+ * section "Continuous batching is the other half of the story").  The chunk's
+ * keys and values are in the cache already (pkv_write before this call), so a
+ * chunk attends over the paged cache exactly like paged_attention_decode's
+ * causal chunk, and a decode is a chunk of one token.
+ *
+ * Sequence i owns query rows q_start[i] .. q_start[i+1]-1, its newest
+ * c = q_start[i+1] - q_start[i] tokens.  With L = seq_lens[i], row
+ * q_start[i] + r (r < c) and query head g see keys t < n = L - c + 1 + r of KV
+ * head g / (num_q_heads/num_kv_heads); out = sum_t softmax_t(scale * q.k_t) v_t
+ * rounded to bf16; n <= 0 gives zeros.
+ *   q, out        device, [total_q][num_q_heads][128] bf16
+ *   q_start       device, [num_seqs + 1] int32, never decreasing, within
+ *                 [0, total_q] (normally q_start[0] = 0 and q_start[num_seqs] =
+ *                 total_q).  A sequence whose pair of entries breaks this sets
+ *                 PKV_STATUS_BAD_QSTART and gets no rows; rows of out that no
+ *                 sequence owns are not written.
+ *   block_tables, seq_lens, k_cache, v_cache, num_blocks, block_size, scale:
+ *                 as paged_attention_decode (L <= max_blocks_per_seq *
+ *                 block_size, else PKV_STATUS_BAD_LEN and L is clamped)
+ * No workspace: every query tile of 128 / G tokens x G heads
+ * (G = num_q_heads / num_kv_heads) is one unit of work over all the keys it
+ * sees, on the tensor cores.
+ * Supported: head_dim 128; G in {1, 2, 4, 8, 16}; block_size in {16, 32, 64,
+ * 128}; num_seqs <= 1024.  Other sizes return PKV_ERR_UNSUPPORTED.
+ * total_q == 0 or num_seqs == 0 is a no-op.
+ */
+int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *seq_lens, const int32_t *q_start, int num_seqs,
+                            int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, pkv_bf16 *out,
+                            int32_t *d_status, void *stream);
 
 /*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a

@@ -1,23 +1,33 @@
-// Chunked causal query (16 tokens) on the 5th-generation tensor cores.
+// Causal query chunks on the 5th-generation tensor cores: the 16-token chunk
+// of a decode step, and prompt chunks of any length (chunked prefill).
 //
-// For one KV head the 16 query tokens x 8 query heads of the group form a
-// 128-row block Q (row r = token (r / 8), head (r % 8)).  Over each 64-key
-// tile of the paged cache:
+// For one KV head, a query tile of 128 rows holds 128 / G tokens x the G query
+// heads of the group (row r = token r / G, head r % G).  Over each 64-key tile
+// of the paged cache:
 //     S  = Q K^T                     tcgen05.mma, M 128 x N 64 x K 128 -> TMEM
 //     P  = exp2(S * scale*log2e - m)  softmax warps, one query row per thread
 //     O += P V                       tcgen05.mma, M 128 x N 128 x K 64 -> TMEM
 // with the running max / sum of online softmax (x321.org "The serving
 // bottleneck is not just FLOPs", section "First understand what the KV cache
-// is storing"; the causal chunk follows the same page's section "Continuous
-// batching is the other half of the story" on chunked prefill).
+// is storing"; the causal chunk and chunked prefill follow the same page's
+// section "Continuous batching is the other half of the story").
 //
-// Persistent grid, one CTA per SM.  CTA c takes a contiguous range of the
-// (sequence, KV head, partition) items.  Consecutive items of the same
-// (sequence, KV head) accumulate into the same TMEM accumulator; at the end
-// of such a run the CTA writes one partial (max, sum, unnormalised O) into the
-// slot of the run's first partition and marks the run's other partitions
-// empty, and the split-K combine kernel merges the slots.  A sequence with a
-// single partition gets its bf16 output directly.
+// Two schedules drive the same pipeline (persistent grid, one CTA per SM):
+//  * decode chunk (16 tokens, G = 8: one query tile per sequence and KV head).
+//    The (sequence, KV head, partition) items split each sequence's keys into
+//    partitions and CTA c takes a contiguous range of them.  Consecutive items
+//    of the same (sequence, KV head) accumulate into the same TMEM
+//    accumulator; at the end of such a run the CTA writes one partial (max,
+//    sum, unnormalised O) into the slot of the run's first partition and marks
+//    the run's other partitions empty, and the split-K combine kernel merges
+//    the slots.  A sequence with a single partition gets its bf16 output
+//    directly.
+//  * prefill (a chunk of its own length per sequence).  One item per
+//    (sequence, KV head, query tile), covering every key the tile's last token
+//    sees; items of one (sequence, KV head) are numbered together, longest
+//    first, and CTA c takes items c, c + grid, c + 2 grid, ...  The CTAs that
+//    run at the same time then sweep the same keys, so the re-reads hit L2.
+//    Every item writes its bf16 output directly; no workspace.
 //
 // Warp roles: 0-7 softmax (thread = row; warps 0-3 take the even tiles of a
 // run, 4-7 the odd ones, each set with its own running max / sum and its own
@@ -27,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 
@@ -39,45 +50,65 @@ namespace pkv {
 namespace {
 
 constexpr int kD = 128;          // head dim
-constexpr int kRows = 128;       // 16 tokens x 8 heads
-constexpr int kQLen = 16;
-constexpr int kGroup = 8;
+constexpr int kRows = 128;       // query rows per tile (tokens x group heads)
+constexpr int kQLen = 16;        // decode chunk: tokens
+constexpr int kGroup = 8;        // decode chunk: query heads per KV head
 constexpr int kTileKeys = 64;    // keys per MMA tile
-constexpr int kStages = 5;       // K/V ring
+constexpr int kMaxStages = 5;    // K/V ring (at most)
 constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
 constexpr int kKVBytes = kTileKeys * kD * 2;     // 16 KiB each for K and V: [half][64 rows][128 B]
 constexpr int kStageBytes = 2 * kKVBytes;
-constexpr int kSmemQ = 0;
-constexpr int kSmemRing = kSmemQ + kQBytes;
-constexpr int kSmemStats = kSmemRing + kStages * kStageBytes;  // float2 [2][128]: odd set's (max, sum) per run
-constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
 constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64, P: 2 x 32
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kThreads = 10 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 
-// barrier indices (8 bytes each, after the P buffers)
+// barrier indices (8 bytes each)
 enum : int {
-  B_Q_FULL = 0, B_Q_FREE, B_O_FULL, B_O_FREE,
+  B_Q_FULL0 = 0, B_Q_FULL1, B_Q_FREE0, B_Q_FREE1, B_O_FULL, B_O_FREE,
   B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
   B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0, B_STATS_FREE1,
-  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kStages, B_COUNT = B_KV_EMPTY0 + kStages
+  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kMaxStages, B_COUNT = B_KV_EMPTY0 + kMaxStages
 };
+
+// Shared-memory plan of each schedule.  Prefill double-buffers the query tile
+// (items are short runs, so the next tile loads while the current one is
+// still in flight) and gives up one K/V stage for it.
+template <bool kPrefill>
+struct Layout {
+  static constexpr int kStages = kPrefill ? 4 : 5;
+  static constexpr int kQBufs = kPrefill ? 2 : 1;
+  static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
+  static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
+  static constexpr int kSmemRing = kQBufs * kQBytes;
+  static constexpr int kSmemStats = kSmemRing + kStages * kStageBytes;  // float2 [2][128]: odd set's (max, sum)
+  static constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
+  static constexpr int kSmemSeq = kSmemBars + B_COUNT * 8 + 16;  // after the TMEM slot and the abort flag
+  static constexpr size_t bytes(int num_seqs) {
+    return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 1) * 4;
+  }
+};
+static_assert(Layout<false>::bytes(Layout<false>::kMaxSeqs) <= 227 * 1024, "shared memory");
+static_assert(Layout<true>::bytes(Layout<true>::kMaxSeqs) <= 227 * 1024, "shared memory");
+static_assert(Layout<false>::kStages <= kMaxStages && Layout<true>::kStages <= kMaxStages, "stages");
 
 struct TcParams {
   const int32_t *block_tables;
   const int32_t *seq_lens;
-  __nv_bfloat16 *out;   // [B][16][Hq][128]
-  float *ws_o;          // [B * 16 * Hq][P][128]
-  float2 *ws_ml;        // [B * 16 * Hq][P]
+  const int32_t *q_start;  // prefill: [B + 1] first query row of each sequence
+  __nv_bfloat16 *out;      // decode chunk: [B][16][Hq][128]; prefill: [total_q][Hq][128]
+  float *ws_o;             // decode chunk: [B * 16 * Hq][P][128]
+  float2 *ws_ml;           // decode chunk: [B * 16 * Hq][P]
   int32_t *status;
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
   int part_tokens, max_parts, oob_row;
+  int total_q, lg_group;   // prefill: query rows, log2 of the group size
   float scale_log2;
 };
 
-// Walks the (sequence, KV head, partition) items in order.
+// Walks (sequence, KV head, sub-item) in order; the sub-items of a sequence are
+// its partitions (decode chunk) or its query tiles (prefill).
 struct ItemWalker {
   int seq, head, part, nparts;
   __device__ void seek(const int *prefix, int num_seqs, int hkv, int it) {
@@ -103,22 +134,112 @@ struct ItemWalker {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Decode chunk: CTA c takes items [range_first(c), range_first(c + 1)).
+__device__ __forceinline__ int range_first(unsigned c, int total) {
+  return static_cast<int>((static_cast<long long>(c) * total + gridDim.x - 1) / gridDim.x);
+}
+
+// Per-sequence values kept in shared memory.
+struct SeqTab {
+  const int *prefix;  // [B + 1] items before each sequence
+  const int *lens;    // [B] clamped lengths
+  const int *qs;      // prefill: [B] first query row
+  const int *qc;      // prefill: [B] chunk length (0 for a bad q_start entry)
+};
+
+// One work item: a query tile against the keys [k_lo, k_hi) of one sequence
+// and KV head.  A run is a maximal sequence of items sharing one accumulator.
+struct Item {
+  int seq, head, qt, part, nparts, k_lo, k_hi;
+  bool run_begin, run_end;
+};
+
+// The items of this CTA in order (every role walks the same sequence).
+template <bool kPrefill>
+struct Sched {
+  int it, end, step;
+  ItemWalker w;
+  Item x;
+
+  __device__ void begin(const TcParams &p, const SeqTab &t, int total_items) {
+    if (kPrefill) {
+      it = blockIdx.x;
+      end = total_items;
+      step = gridDim.x;
+    } else {
+      it = range_first(blockIdx.x, total_items);
+      end = range_first(blockIdx.x + 1, total_items);
+      step = 1;
+    }
+    if (it < end) {
+      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+      fill(p, t, true);
+    }
+  }
+  __device__ bool valid() const { return it < end; }
+  __device__ void advance(const TcParams &p, const SeqTab &t) {
+    it += step;
+    if (it >= end) return;
+    if (kPrefill) {
+      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+      fill(p, t, true);
+    } else {
+      const int s0 = w.seq, h0 = w.head;
+      w.next(t.prefix, p.num_seqs, p.num_kv_heads);
+      fill(p, t, w.seq != s0 || w.head != h0);
+    }
+  }
+  __device__ void fill(const TcParams &p, const SeqTab &t, bool begins) {
+    const int L = t.lens[w.seq];
+    x.seq = w.seq;
+    x.head = w.head;
+    x.run_begin = begins;
+    if (kPrefill) {
+      const int c = t.qc[w.seq];
+      const int tile_tok = kRows >> p.lg_group;
+      x.qt = w.nparts - 1 - w.part;  // longest first
+      x.part = 0;
+      x.nparts = 1;
+      x.k_lo = 0;
+      x.k_hi = min(L, max(0, L - c + min(c, tile_tok * (x.qt + 1))));
+      x.run_end = true;
+    } else {
+      x.qt = 0;
+      x.part = w.part;
+      x.nparts = w.nparts;
+      x.k_lo = w.part * p.part_tokens;
+      x.k_hi = max(x.k_lo, min(L, x.k_lo + p.part_tokens));
+      ItemWalker nx = w;
+      nx.next(t.prefix, p.num_seqs, p.num_kv_heads);
+      x.run_end = it + 1 >= end || nx.seq != w.seq || nx.head != w.head;
+    }
+  }
+};
+
 // Bounded wait whose outcome every lane of the warp agrees on.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity));
 }
 
-template <int BS>
+template <int BS, bool kPrefill>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+  using Lay = Layout<kPrefill>;
+  constexpr int kStages = Lay::kStages, kQBufs = Lay::kQBufs;
+  // one TMA box per block of the tile (a 128-token block: the tile's half of it)
+  constexpr int kBoxRows = BS < kTileKeys ? BS : kTileKeys;
+  constexpr int kBoxes = kTileKeys / kBoxRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBars);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kSmemBars);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *prefix = reinterpret_cast<int *>(tmem_slot + 4);  // [B + 1] items before each sequence
-  int *lens = prefix + p.num_seqs + 1;                    // [B] clamped lengths
+  int *prefix = reinterpret_cast<int *>(smem + Lay::kSmemSeq);  // [B + 1]
+  int *lens = prefix + p.num_seqs + 1;                          // [B]
+  int *qs = lens + p.num_seqs;                                  // prefill: [B]
+  int *qc = qs + p.num_seqs;                                    // prefill: [B]
+  const SeqTab tab{prefix, lens, qs, qc};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs, hkv = p.num_kv_heads;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -130,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per = (B + 31) / 32;
     const int lo = min(B, lane * per), hi = min(B, lo + per);
     const int cap_tbl = p.max_blocks * BS, cap_grid = p.max_parts * p.part_tokens;
-    const int cap = cap_tbl < cap_grid ? cap_tbl : cap_grid;
+    const int cap = kPrefill || cap_tbl < cap_grid ? cap_tbl : cap_grid;
+    const int tile_tok = kRows >> p.lg_group;
     int sum = 0;
     for (int i = lo; i < hi; ++i) {
       int L = p.seq_lens[i];
@@ -139,7 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         L = L < 0 ? 0 : cap;
       }
       lens[i] = L;
-      const int n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
+      int n;
+      if (kPrefill) {
+        const int a = p.q_start[i], b = p.q_start[i + 1];
+        int c = b - a;
+        if (a < 0 || c < 0 || b > p.total_q) {
+          if (blockIdx.x == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_QSTART);
+          c = 0;
+        }
+        qs[i] = a;
+        qc[i] = c;
+        n = ceil_div(c, tile_tok) * hkv;
+      } else {
+        n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
+      }
       prefix[i + 1] = n;
       sum += n;
     }
@@ -157,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) prefix[0] = 0;
   }
   if (threadIdx.x == 32 * kProducerWarp) {
-    mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_FREE), 1);
+    for (int i = 0; i < kQBufs; ++i) {
+      mbar_init(bar(B_Q_FULL0 + i), 1);
+      mbar_init(bar(B_Q_FREE0 + i), 1);
+    }
     mbar_init(bar(B_O_FULL), 1);
     mbar_init(bar(B_O_FREE), kRows);
     for (int i = 0; i < 2; ++i) {
@@ -190,51 +327,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   const int I = prefix[B];
-  const int it0 = static_cast<int>((static_cast<long long>(blockIdx.x) * I + gridDim.x - 1) / gridDim.x);
-  const int it1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * I + gridDim.x - 1) / gridDim.x);
-  const uint32_t sQ = smem_u32(smem + kSmemQ), sRing = smem_u32(smem + kSmemRing);
+  const uint32_t sQ = smem_u32(smem), sRing = smem_u32(smem + Lay::kSmemRing);
   const uint32_t tS0 = tmem + 2 * kD;        // S buffers after the two accumulators
   const uint32_t tP0 = tS0 + 2 * kTileKeys;  // P (bf16 pairs per column) after the S buffers
+  const bool has_work = kPrefill ? static_cast<int>(blockIdx.x) < I
+                                 : range_first(blockIdx.x, I) < range_first(blockIdx.x + 1, I);
 
-  // key range of an item: [x, y)
-  auto item_keys = [&](const ItemWalker &w) {
-    const int lo = w.part * p.part_tokens;
-    return make_int2(lo, max(lo, min(lens[w.seq], lo + p.part_tokens)));
-  };
-
-  if (it0 < it1) {
+  if (has_work) {
     if (warp == kProducerWarp) {
       // ------------------------------------------------------------ producer
-      const uint64_t pol = l2_policy_evict_first();
-      ItemWalker w;
-      w.seek(prefix, B, hkv, it0);
-      int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+      // decode: every key is read once; prefill: the CTAs beside this one read them too
+      const uint64_t pol = kPrefill ? l2_policy_evict_normal() : l2_policy_evict_first();
+      Sched<kPrefill> sc;
+      sc.begin(p, tab, I);
+      int g = 0, tpieces = 0;
       int tw_seq = -1, tw_base = 0, tw_val = -1;
-      for (int it = it0; it < it1 && !*abort_flag; ++it, w.next(prefix, B, hkv)) {
-        const int2 kr = item_keys(w);
-        const int k_lo = kr.x, k_hi = kr.y;
-        const bool new_run = w.seq != prev_seq || w.head != prev_head;
-        prev_seq = w.seq;
-        prev_head = w.head;
-        if (new_run && k_hi > k_lo) {  // a run with keys: load its queries
-          ++tpieces;
-          if (tpieces > 1 && !wait_warp(bar(B_Q_FREE), (tpieces - 2) & 1)) {
+      for (; sc.valid() && !*abort_flag; sc.advance(p, tab)) {
+        const Item &x = sc.x;
+        if (x.run_begin && x.k_hi > x.k_lo) {  // a run with keys: load its queries
+          const int qi = tpieces++, qb = qi % kQBufs, use = qi / kQBufs;
+          if (use > 0 && !wait_warp(bar(B_Q_FREE0 + qb), (use - 1) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
             *abort_flag = 1;
             break;
           }
           if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_Q_FULL), kQBytes);
+            const int gsz = 1 << p.lg_group;
+            const int qz = kPrefill ? qs[x.seq] + (kRows >> p.lg_group) * x.qt : x.seq * kQLen;
+            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kQBytes);
             for (int hf = 0; hf < 2; ++hf)
               asm volatile(
                   "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + hf * (kQBytes / 2)),
-                  "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(hf * 64), "r"(w.head * kGroup), "r"(w.seq * kQLen),
-                  "r"(bar(B_Q_FULL))
+                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + qb * kQBytes + hf * (kQBytes / 2)),
+                  "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(hf * 64), "r"(x.head * gsz), "r"(qz),
+                  "r"(bar(B_Q_FULL0 + qb))
                   : "memory");
           }
         }
-        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
+        const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
+        const int nblk_seq = ceil_div(lens[x.seq], BS);
         for (int t = 0; t < ntile; ++t, ++g) {
           const int s = g % kStages;
           if (g >= kStages && !wait_warp(bar(B_KV_EMPTY0 + s), ((g / kStages) - 1) & 1)) {
@@ -242,86 +373,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             break;
           }
-          const int blk_first = (k_lo + t * kTileKeys) / BS;
-          constexpr int kBlocks = kTileKeys / BS;
-          if (w.seq != tw_seq || blk_first < tw_base || blk_first + kBlocks > tw_base + 32) {
-            tw_seq = w.seq;
+          const int k0 = x.k_lo + t * kTileKeys;
+          const int blk_first = k0 / BS;
+          if (x.seq != tw_seq || blk_first < tw_base || blk_first + kBoxes > tw_base + 32) {
+            tw_seq = x.seq;
             tw_base = blk_first;
             const int e = blk_first + lane;
-            tw_val = e < p.max_blocks ? p.block_tables[static_cast<size_t>(w.seq) * p.max_blocks + e] : -1;
+            tw_val = e < p.max_blocks ? p.block_tables[static_cast<size_t>(x.seq) * p.max_blocks + e] : -1;
           }
-          const int nblk_seq = ceil_div(lens[w.seq], BS);
-          int bids[kBlocks];
+          int bids[kBoxes];
 #pragma unroll
-          for (int j = 0; j < kBlocks; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
+          for (int j = 0; j < kBoxes; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
           const uint32_t st = sRing + s * kStageBytes;
           if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), kStageBytes);
-          // one lane per (block, K/V, half): the box copies go out in parallel
-          if (lane < kBlocks * 4) {
+          // one lane per (box, K/V, half): the box copies go out in parallel
+          if (lane < kBoxes * 4) {
             const int j = lane >> 2, kv = (lane >> 1) & 1, hf = lane & 1;
             const int b = bids[j];
             int row;
             if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
-              row = (b * hkv + w.head) * BS;
+              row = (b * hkv + x.head) * BS + k0 % BS;
             } else {
               if (blk_first + j < nblk_seq && p.status && kv == 0 && hf == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
               row = p.oob_row;  // past the sequence, or a bad id: zeros
             }
-            tma_load_2d(st + kv * kKVBytes + hf * (kKVBytes / 2) + j * BS * 128, kv ? &tmv : &tmk, hf * 64, row,
-                        bar(B_KV_FULL0 + s), pol);
+            tma_load_2d(st + kv * kKVBytes + hf * (kKVBytes / 2) + j * kBoxRows * 128, kv ? &tmv : &tmk, hf * 64,
+                        row, bar(B_KV_FULL0 + s), pol);
           }
         }
       }
       // never leave a copy in flight into this CTA's shared memory
       if (lane == 0) {
-        for (int x = g > kStages ? g - kStages : 0; x < g; ++x)
-          mbar_wait_sleep(bar(B_KV_FULL0 + (x % kStages)), (x / kStages) & 1);
-        if (tpieces > 0) mbar_wait_sleep(bar(B_Q_FULL), (tpieces - 1) & 1);
+        for (int y = g > kStages ? g - kStages : 0; y < g; ++y)
+          mbar_wait_sleep(bar(B_KV_FULL0 + (y % kStages)), (y / kStages) & 1);
+        for (int qi = tpieces > kQBufs ? tpieces - kQBufs : 0; qi < tpieces; ++qi)
+          mbar_wait_sleep(bar(B_Q_FULL0 + qi % kQBufs), (qi / kQBufs) & 1);
       }
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------------------- MMA
       if (lane == 0) {
         constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
         constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
-        ItemWalker w;
-        w.seek(prefix, B, hkv, it0);
-        int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1, run_g0 = 0;
+        Sched<kPrefill> sc;
+        sc.begin(p, tab, I);
+        int g = 0, tpieces = 0, run_g0 = 0;
         // the tile whose P V product is still to be issued, with its run index
         int pend = -1, pend_run = 0;
         bool pend_first = false, pend_last = false;
         bool ok = true;
-        auto issue_pv = [&](int x, int run, bool first, bool last) {
-          const int pb = x & 1;  // the set (even / odd tiles): its P buffer and accumulator
-          if (!mbar_wait_sleep(bar(B_P_FULL0 + pb), (x >> 1) & 1)) return false;
+        auto issue_pv = [&](int y, int run, bool first, bool last) {
+          const int pb = y & 1;  // the set (even / odd tiles): its P buffer and accumulator
+          if (!mbar_wait_sleep(bar(B_P_FULL0 + pb), (y >> 1) & 1)) return false;
           // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
           if (first && run > 1 && !mbar_wait_sleep(bar(B_O_FREE), (run - 2) & 1)) return false;
           tc::fence_after();
           const uint32_t pa = tP0 + pb * (kTileKeys / 2);
-          const uint32_t vb = sRing + (x % kStages) * kStageBytes + kKVBytes;
+          const uint32_t vb = sRing + (y % kStages) * kStageBytes + kKVBytes;
 #pragma unroll
           for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
             tc::mma_ta(tmem + pb * kD, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO,
                        !(first && ks == 0));
           tc::commit(bar(B_PV_DONE0 + pb));
-          tc::commit(bar(B_KV_EMPTY0 + (x % kStages)));
+          tc::commit(bar(B_KV_EMPTY0 + (y % kStages)));
           if (last) tc::commit(bar(B_O_FULL));
           return true;
         };
-        for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
-          const int2 kr = item_keys(w);
-          const int k_lo = kr.x, k_hi = kr.y;
-          const bool new_run = w.seq != prev_seq || w.head != prev_head;
-          prev_seq = w.seq;
-          prev_head = w.head;
-          ItemWalker nx = w;
-          nx.next(prefix, B, hkv);
-          const bool run_ends = it + 1 >= it1 || nx.seq != w.seq || nx.head != w.head;
-          const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
-          if (new_run && ntile > 0) {
-            ++tpieces;
+        for (; sc.valid() && ok; sc.advance(p, tab)) {
+          const Item &x = sc.x;
+          const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
+          int qb = 0;
+          if (x.run_begin && ntile > 0) {
+            const int qi = tpieces++;
+            qb = qi % kQBufs;
             run_g0 = g;
-            if (!mbar_wait_sleep(bar(B_Q_FULL), (tpieces - 1) & 1)) { ok = false; break; }
+            if (!mbar_wait_sleep(bar(B_Q_FULL0 + qb), (qi / kQBufs) & 1)) { ok = false; break; }
+          } else if (tpieces > 0) {
+            qb = (tpieces - 1) % kQBufs;
           }
+          const uint32_t sq = sQ + qb * kQBytes;
           for (int t = 0; t < ntile; ++t, ++g) {
             const int s = g % kStages, sb = g & 1;
             if (!mbar_wait_sleep(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
@@ -330,11 +459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t kb = sRing + s * kStageBytes;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks)
-              tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sQ + (ks >> 2) * (kQBytes / 2) + (ks & 3) * 32, 16, 1024),
+              tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * (kQBytes / 2) + (ks & 3) * 32, 16, 1024),
                       tc::desc_sw128(kb + (ks >> 2) * (kKVBytes / 2) + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
             tc::commit(bar(B_S_FULL0 + sb));
-            const bool last_of_run = run_ends && t == ntile - 1;
-            if (last_of_run) tc::commit(bar(B_Q_FREE));  // the queries are only read by MMAs issued so far
+            const bool last_of_run = x.run_end && t == ntile - 1;
+            if (last_of_run) tc::commit(bar(B_Q_FREE0 + qb));  // the queries are only read by MMAs issued so far
             if (pend >= 0 && !issue_pv(pend, pend_run, pend_first, pend_last)) { ok = false; break; }
             pend = g;
             pend_run = tpieces;
@@ -352,33 +481,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ softmax warps
       const int set = warp >> 2;                  // 0: even tiles of a run, 1: odd tiles
       const int r = threadIdx.x & (kRows - 1);    // query row = TMEM lane
-      const int tok = r / kGroup, gh = r % kGroup;
+      const int tok = r >> p.lg_group, gh = r & ((1 << p.lg_group) - 1);
+      const int tile_tok = kRows >> p.lg_group;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tO = tmem + set * kD;        // this set's accumulator
-      float2 *stats = reinterpret_cast<float2 *>(smem + kSmemStats);
-      ItemWalker w;
-      w.seek(prefix, B, hkv, it0);
-      int g = 0, tpieces = 0, prev_seq = -1, prev_head = -1;
+      float2 *stats = reinterpret_cast<float2 *>(smem + Lay::kSmemStats);
+      Sched<kPrefill> sc;
+      sc.begin(p, tab, I);
+      int g = 0, tpieces = 0;
       float m = -INFINITY, l = 0.f;
       int run_first_part = 0;
       bool run_has_tiles = false, set_has_tiles = false;
       bool ok = true;
-      for (int it = it0; it < it1 && ok; ++it, w.next(prefix, B, hkv)) {
-        const int L = lens[w.seq];
-        const int2 kr = item_keys(w);
-        const int k_lo = kr.x, k_hi = kr.y;
-        const int ntile = ceil_div(k_hi - k_lo, kTileKeys);
-        if (w.seq != prev_seq || w.head != prev_head) {
-          prev_seq = w.seq;
-          prev_head = w.head;
+      for (; sc.valid() && ok; sc.advance(p, tab)) {
+        const Item &x = sc.x;
+        const int L = lens[x.seq];
+        const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
+        if (x.run_begin) {
           m = -INFINITY;
           l = 0.f;
-          run_first_part = w.part;
-          run_has_tiles = ntile > 0;  // only an empty sequence has none
+          run_first_part = x.part;
+          run_has_tiles = ntile > 0;
           set_has_tiles = false;
           if (run_has_tiles) ++tpieces;
         }
-        const int limit = L - kQLen + 1 + tok;  // this row sees keys t < limit
+        // this row's token within the chunk, and the keys it sees: t < limit
+        int row_tok, limit;
+        bool row_valid;
+        if (kPrefill) {
+          const int c = qc[x.seq];
+          row_tok = tile_tok * x.qt + tok;
+          row_valid = row_tok < c;
+          limit = row_valid ? L - c + 1 + row_tok : 0;
+        } else {
+          row_tok = tok;
+          row_valid = true;
+          limit = L - kQLen + 1 + tok;
+        }
         for (int t = 0; t < ntile; ++t, ++g) {
           if ((g & 1) != set) continue;  // the other set's tile
           const bool first_tile_of_set = !set_has_tiles;
@@ -392,27 +531,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::wait_ld();
           tc::fence_before();
           mbar_arrive(bar(B_S_FREE0 + sb));
-          const int k0 = k_lo + t * kTileKeys;
-          const int vis = min(limit, k_hi) - k0;  // keys of this tile the row sees
+          // a negative scale turns the largest score into the smallest: take minima then
+          const bool neg = p.scale_log2 < 0.f;
+          const uint32_t masked = __float_as_uint(neg ? INFINITY : -INFINITY);
+          const int k0 = x.k_lo + t * kTileKeys;
+          const int vis = min(limit, x.k_hi) - k0;  // keys of this tile the row sees
           if (!__all_sync(0xffffffffu, vis >= kTileKeys)) {
 #pragma unroll
             for (int c = 0; c < kTileKeys; ++c)
-              if (c >= vis) sv[c] = __float_as_uint(-INFINITY);
+              if (c >= vis) sv[c] = masked;
           }
-          // max of the raw scores (the scale is > 0): eight short chains of 3-input maxima
-          float mx[8];
+          // the extreme raw score (its product with the scale is the largest
+          // scaled score): eight short chains of 3-input maxima (minima)
+          float rm;
+          if (!neg) {
+            float mx[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
+            for (int q = 0; q < 8; ++q)
+              mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
+            for (int q = 0; q < 8; ++q)
+              mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+            for (int q = 0; q < 8; ++q)
+              mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
 #pragma unroll
-          for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
-          const float rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
+            rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          } else {
+            float mn[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              mn[q] = fmin3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mn[q] = fminf(mn[q], __uint_as_float(sv[q + 56]));
+            rm = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
+          }
           const float bm = rm * p.scale_log2;
           // this set's previous tile (g - 2) must be in the accumulator before a
           // rescale, and its P buffer free before the new P is written
@@ -445,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[kTileKeys / 2];  // P row: two bf16 per tensor-memory column
           uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
 #pragma unroll
-          for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys hold -inf
+          for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys give 2^-inf
             float x0, x1;
             f32x2_split(ffma2(f32x2_bits(sv[2 * c], sv[2 * c + 1]), ks2, nm2), x0, x1);
             pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
@@ -482,10 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // ---- end of a run
-        ItemWalker nx = w;
-        nx.next(prefix, B, hkv);
-        const bool run_ends = it + 1 >= it1 || nx.seq != w.seq || nx.head != w.head;
-        if (!run_ends) continue;
+        if (!x.run_end) continue;
         const int rp = tpieces & 1;
         if (set == 1) {  // the odd set hands its (max, sum) to the even set
           if (run_has_tiles) {
@@ -497,8 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        const int nparts = w.nparts;
-        const size_t orow = (static_cast<size_t>(w.seq) * kQLen + tok) * p.num_q_heads + w.head * kGroup + gh;
+        const int nparts = x.nparts;
+        const size_t orow =
+            kPrefill ? static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + (x.head << p.lg_group) + gh
+                     : (static_cast<size_t>(x.seq) * kQLen + tok) * p.num_q_heads + x.head * kGroup + gh;
         float fa = 0.f, fb = 0.f, M = -INFINITY, lt = 0.f;
         if (run_has_tiles) {
           if (!wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
@@ -535,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(tmp[c]);
           }
+          if (!row_valid) continue;  // a row past the chunk's end (prefill): nothing to store
           if (nparts == 1) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
 #pragma unroll
@@ -557,9 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before();
           mbar_arrive(bar(B_O_FREE));
         }
-        if (nparts > 1) {
+        if (!kPrefill && nparts > 1) {
           p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(M, lt);
-          for (int q = run_first_part + 1; q <= w.part; ++q)  // merged into the run's first slot
+          for (int q = run_first_part + 1; q <= x.part; ++q)  // merged into the run's first slot
             p.ws_ml[orow * p.max_parts + q] = make_float2(-INFINITY, 0.f);
         }
       }
@@ -577,21 +737,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <bool kPrefill>
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+
+template <bool kPrefill>
+KernelFn<kPrefill> pick_kernel(int block_size) {
+  switch (block_size) {
+    case 16: return chunk_tc_kernel<16, kPrefill>;
+    case 32: return chunk_tc_kernel<32, kPrefill>;
+    case 64: return chunk_tc_kernel<64, kPrefill>;
+    default: return chunk_tc_kernel<128, kPrefill>;
+  }
+}
+
+template <bool kPrefill>
+int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
+              int block_size, cudaStream_t stream) {
+  using Lay = Layout<kPrefill>;
+  const KernelFn<kPrefill> kernel = pick_kernel<kPrefill>(block_size);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(Lay::bytes(Lay::kMaxSeqs)))) != cudaSuccess)
+    return set_cuda_error(e), PKV_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Lay::bytes(p.num_seqs);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, tmq, tmk, tmv, p);
+  if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+// The kernels compare raw scores before scaling them; a zero scale would turn
+// the masked -inf scores into NaN, so it runs as the smallest normal float,
+// whose products with finite scores round to the same weights (all 1).
+float kernel_scale_log2(float scale) { return (scale == 0.f ? FLT_MIN : scale) * kLog2e; }
+
 }  // namespace
 
 bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                         int part_tokens) {
-  return q_len == kQLen && head_dim == kD && num_q_heads == kGroup * num_kv_heads && num_seqs <= 2048 &&
-         (block_size == 16 || block_size == 32) && part_tokens % kTileKeys == 0;
+  return q_len == kQLen && head_dim == kD && num_q_heads == kGroup * num_kv_heads &&
+         num_seqs <= Layout<false>::kMaxSeqs &&
+         (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128) &&
+         part_tokens % kTileKeys == 0 && part_tokens % block_size == 0;
 }
 
 int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   const int B = a.num_seqs;
+  const int box_rows = a.block_size < kTileKeys ? a.block_size : kTileKeys;
   CUtensorMap tmq, tmk, tmv;
   // q viewed as [B*16][Hq][128]: box = 64 columns x 8 heads x 16 tokens
   if (!make_tensor_map_3d(&tmq, a.q, kD, a.num_q_heads, static_cast<long long>(B) * kQLen, 64, kGroup, kQLen) ||
-      !make_tensor_map_2d(&tmk, a.k_cache, kD, a.rows, 64, a.block_size) ||
-      !make_tensor_map_2d(&tmv, a.v_cache, kD, a.rows, 64, a.block_size))
+      !make_tensor_map_2d(&tmk, a.k_cache, kD, a.rows, 64, box_rows) ||
+      !make_tensor_map_2d(&tmv, a.v_cache, kD, a.rows, 64, box_rows))
     return PKV_ERR_CUDA;
   TcParams p{};
   p.block_tables = a.block_tables;
@@ -608,29 +813,66 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.part_tokens = a.part_tokens;
   p.max_parts = a.max_parts;
   p.oob_row = static_cast<int>(a.rows);
-  p.scale_log2 = a.scale * kLog2e;
-  const size_t smem = 1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * static_cast<size_t>(B) + 1) * 4;
-  static_assert(1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * 2048 + 1) * 4 <= 227 * 1024, "shared memory");
-  cudaError_t e;
-  void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) =
-      a.block_size == 16 ? chunk_tc_kernel<16> : chunk_tc_kernel<32>;
-  if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(1024 + kSmemBars + B_COUNT * 8 + 16 + (2 * 2048 + 1) * 4))) !=
-      cudaSuccess)
-    return set_cuda_error(e), PKV_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, tmq, tmk, tmv, p);
-  if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
-  return PKV_OK;
+  p.lg_group = 3;
+  p.scale_log2 = kernel_scale_log2(a.scale);
+  return launch_tc<false>(tmq, tmk, tmv, p, a.block_size, stream);
 }
 
 }  // namespace pkv
+
+extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                                       const int32_t *q_start, int num_seqs, int total_q, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                                       pkv_bf16 *out, int32_t *d_status, void *stream) {
+  using namespace pkv;
+  if (num_seqs < 0 || total_q < 0 || max_blocks_per_seq < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_blocks < 0 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+  const int group = num_q_heads / num_kv_heads;
+  int lg = 0;
+  while ((1 << lg) < group) ++lg;
+  if (head_dim != kD || (1 << lg) != group || group > 16) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > Layout<true>::kMaxSeqs) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start || !out) return PKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(q_start) & 3u))
+    return PKV_ERR_ARG;
+  if (num_blocks == 0) return PKV_ERR_ARG;
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
+  if (rows + block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+  // the largest item count the kernel forms: every row its own query tile
+  if (static_cast<long long>(total_q) * num_kv_heads >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+
+  const int tile_tok = kRows / group;
+  const int box_rows = block_size < kTileKeys ? block_size : kTileKeys;
+  CUtensorMap tmq, tmk, tmv;
+  // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x 128 / G tokens
+  if (!make_tensor_map_3d(&tmq, q, kD, num_q_heads, total_q, 64, group, tile_tok) ||
+      !make_tensor_map_2d(&tmk, k_cache, kD, rows, 64, box_rows) ||
+      !make_tensor_map_2d(&tmv, v_cache, kD, rows, 64, box_rows))
+    return PKV_ERR_CUDA;
+  TcParams p{};
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q_start = q_start;
+  p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+  p.status = d_status;
+  p.num_seqs = num_seqs;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.part_tokens = 0;
+  p.max_parts = 1;
+  p.oob_row = static_cast<int>(rows);
+  p.total_q = total_q;
+  p.lg_group = lg;
+  p.scale_log2 = kernel_scale_log2(scale);
+  return launch_tc<true>(tmq, tmk, tmv, p, block_size, as_stream(stream));
+}

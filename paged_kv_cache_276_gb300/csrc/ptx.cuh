@@ -105,6 +105,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
+// L2 policy for data that other CTAs read again soon (the keys and values of
+// a prompt chunk, swept once per query tile): plain LRU.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // 2-D tiled TMA load of one box into shared memory; completes `bytes` on `bar`.
 // Coordinates are in elements: x = innermost (must be a multiple of 8 for bf16),
 // y = row.  Rows outside the tensor read as zeros.
@@ -193,6 +201,12 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// min of three (one instruction).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 // The two bf16 of a packed pair widened to fp32 (exact: bf16 is fp32's top half).

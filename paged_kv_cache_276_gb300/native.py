@@ -31,6 +31,7 @@ PKV_STATUS_BAD_SLOT = 1
 PKV_STATUS_BAD_BLOCK = 2
 PKV_STATUS_BAD_LEN = 4
 PKV_STATUS_TIMEOUT = 8
+PKV_STATUS_BAD_QSTART = 16
 
 _c_int, _c_i64, _c_ptr, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_float)
@@ -55,6 +56,9 @@ SIGNATURES = {
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
+    "paged_attention_prefill": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_ptr, _c_ptr,
+                                         _c_ptr]),
     "pkv_swap_out": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
                               _c_ptr, _c_ptr]),
     "pkv_swap_in": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
@@ -197,6 +201,29 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_
         if not handle:
             raise ValueError("main_done_event: record the torch.cuda.Event once before passing it")
         _check(lib().paged_attention_decode_ex(*args, ctypes.c_void_p(handle)), "paged_attention_decode_ex")
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, d_status=None,
+                            stream=None):
+    """Chunked prefill: q, out [total_q, Hq, 128] bf16; q_start [B + 1] int32 (rows of sequence i are
+    q_start[i] .. q_start[i+1]-1, its newest tokens); caches [NB, Hkv, bs, 128]; tables [B, max_blocks]
+    int32; lens [B] int32."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (q_start, "q_start", torch.int32),
+                     (out, "out", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    total_q, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or seq_lens.shape != (B,) or q_start.shape != (B + 1,):
+        raise ValueError("shape mismatch")
+    _check(lib().paged_attention_prefill(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        _ptr(q_start), B, total_q, Hq, Hkv, d, bs, NB, float(scale), _ptr(out), _ptr(d_status),
+        _stream(stream, dev)), "paged_attention_prefill")
 
 
 def _swap_check(k_cache, v_cache, block_ids, host_k, host_v):

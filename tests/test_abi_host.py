@@ -74,6 +74,34 @@ def test_decode_rejects_bad_sizes_before_launch(native):
     assert call(B=0) == native.PKV_OK                            # nothing to do, nothing launched
 
 
+def test_prefill_rejects_bad_sizes_before_launch(native):
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails validation first
+    args = dict(q=fake, k=fake, v=fake, tbl=fake, maxb=4, lens=fake, qs=fake, B=2, T=40, Hq=64, Hkv=8,
+                d=128, bs=16, NB=8, scale=0.1, out=fake, st=None, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.paged_attention_prefill(a["q"], a["k"], a["v"], a["tbl"], a["maxb"], a["lens"], a["qs"],
+                                           a["B"], a["T"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"],
+                                           a["scale"], a["out"], a["st"], a["stream"])
+    assert call(d=64) == native.PKV_ERR_UNSUPPORTED               # tensor-core tiles are head dim 128
+    assert call(bs=8) == native.PKV_ERR_UNSUPPORTED
+    assert call(bs=256) == native.PKV_ERR_UNSUPPORTED
+    assert call(Hq=24) == native.PKV_ERR_UNSUPPORTED              # group 3: not a power of two
+    assert call(Hq=64, Hkv=2) == native.PKV_ERR_UNSUPPORTED       # group 32 > 16
+    assert call(Hq=7, Hkv=2) == native.PKV_ERR_ARG
+    assert call(B=1025) == native.PKV_ERR_UNSUPPORTED
+    assert call(T=-1) == native.PKV_ERR_ARG
+    assert call(scale=float("inf")) == native.PKV_ERR_ARG
+    assert call(qs=None) == native.PKV_ERR_ARG
+    assert call(out=ctypes.c_void_p((1 << 20) + 8)) == native.PKV_ERR_ARG  # misaligned
+    assert call(qs=ctypes.c_void_p((1 << 20) + 2)) == native.PKV_ERR_ARG
+    assert call(NB=0) == native.PKV_ERR_ARG
+    assert call(B=0) == native.PKV_OK                             # nothing to do, nothing launched
+    assert call(T=0) == native.PKV_OK
+
+
 def test_write_and_copy_reject_bad_sizes_before_launch(native):
     lib = native.lib()
     fake = ctypes.c_void_p(1 << 20)

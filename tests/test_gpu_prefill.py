@@ -1,0 +1,220 @@
+"""Parity of chunked prefill (paged_attention_prefill, through the C ABI) with the CPU oracle.
+
+Bar: |out - ref| <= 1e-2 + 1e-2 * |ref| elementwise against the fp64 oracle on
+the same bf16 inputs; rows that no sequence owns are left untouched (checked
+bit for bit against a NaN canary).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from paged_kv_cache_276_gb300 import inputs, native
+from test_gpu_parity import assert_attention_close, bits, random_case, run_decode, status_tensor
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x7FC1  # a NaN bit pattern
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_cache_276_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def prefill_case(lens, chunks, bs, Hq, Hkv, seed, d=128, spare=3):
+    rng = np.random.default_rng(seed)
+    NB = sum(inputs.entries_to_fill(n, bs) for n in lens) + spare
+    maxb = max(1, max(inputs.entries_to_fill(n, bs) for n in lens)) + 2
+    tables, _ = inputs.permuted_tables(lens, bs, NB, rng, max_blocks=maxb)
+    kc = inputs.randn_bf16((NB, Hkv, bs, d), seed * 10 + 1, "cuda")
+    vc = inputs.randn_bf16((NB, Hkv, bs, d), seed * 10 + 2, "cuda")
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = inputs.randn_bf16((int(q_start[-1]), Hq, d), seed * 10 + 3, "cuda")
+    return q, kc, vc, tables, q_start
+
+
+def run_prefill(q, kc, vc, tables, lens, q_start, scale, status=None, out=None):
+    dev = kc.device
+    if out is None:
+        out = torch.empty_like(q)
+        out.view(torch.int16).fill_(CANARY)
+    native.paged_attention_prefill(q, kc, vc, torch.as_tensor(np.asarray(tables, dtype=np.int32), device=dev),
+                                   torch.as_tensor(np.asarray(lens, dtype=np.int32), device=dev),
+                                   torch.as_tensor(np.asarray(q_start, dtype=np.int32), device=dev),
+                                   scale, out, status)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale, d=128):
+    return OA.paged_attention_varlen(bits(q), bits(kc), bits(vc), np.asarray(tables, dtype=np.int32),
+                                     np.asarray(lens, dtype=np.int32), q_start, num_q_heads=Hq,
+                                     num_kv_heads=Hkv, head_dim=d, block_size=bs, scale=scale)
+
+
+@pytest.mark.parametrize("bs,Hq,Hkv,lens,chunks", [
+    # a whole prompt, a ragged chunk behind cached context, a decode row, an empty chunk
+    (16, 64, 8, [300, 1000, 64, 77, 5], [300, 200, 1, 0, 5]),
+    (32, 32, 4, [129, 2048, 16, 700], [129, 100, 16, 33]),
+    (64, 16, 16, [513, 70, 1], [513, 70, 1]),            # G = 1: 128 tokens per tile
+    (128, 16, 8, [1000, 250, 128], [17, 250, 128]),      # G = 2, blocks of 128 in 64-key tiles
+    (16, 32, 8, [400, 9], [400, 9]),                     # G = 4
+    (16, 32, 2, [333, 40, 2000], [333, 8, 65]),          # G = 16: 8 tokens per tile
+])
+def test_prefill_matches_oracle(bs, Hq, Hkv, lens, chunks):
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=bs + Hq + len(lens))
+    scale = float(np.float32(1 / math.sqrt(128)))
+    st = status_tensor()
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale, status=st)
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, "prefill")
+
+
+def test_prefill_many_items_per_cta():
+    """More query tiles than CTAs: every CTA walks several items, the query
+    tile double buffer turns over, and the sequences of the same KV head are
+    served in the interleaved order."""
+    rng = np.random.default_rng(12)
+    lens = [int(x) for x in rng.integers(300, 1600, size=6)]
+    chunks = [min(L, 256) for L in lens]
+    Hq, Hkv, bs = 32, 4, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=12)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, "prefill, many items")
+
+
+def test_prefill_of_uniform_16_token_chunks_equals_the_decode_chunk_bit_for_bit():
+    """With one partition per sequence the decode chunk and prefill run the
+    same tiles in the same order on the same tensor-core pipeline."""
+    lens = [900, 40, 2500, 16]
+    Hq, Hkv, bs, d = 64, 8, 16, 128
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=31, q_len=16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    part = 64 * math.ceil(max(lens) / 64)
+    dec = run_decode(q, kc, vc, tables, lens, scale, part)
+    q_start = np.arange(len(lens) + 1, dtype=np.int32) * 16
+    pre = run_prefill(q.reshape(-1, Hq, d), kc, vc, tables, lens, q_start, scale)
+    assert torch.equal(dec.reshape(-1, Hq, d).view(torch.int16), pre.view(torch.int16))
+
+
+def test_prefill_rescales_running_max():
+    """Keys grow in magnitude block by block, so the running max keeps moving."""
+    lens, chunks = [1500, 700], [300, 700]
+    Hq, Hkv, bs = 16, 2, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=3)
+    growth = torch.linspace(0.5, 6.0, kc.shape[0], device="cuda").view(-1, 1, 1, 1)
+    kc = (kc.float() * growth).to(torch.bfloat16)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, "prefill rescale")
+
+
+@pytest.mark.parametrize("scale", [-0.07, 0.0])
+def test_prefill_and_decode_chunk_with_negative_or_zero_scale(scale):
+    lens, chunks = [300, 45], [300, 20]
+    Hq, Hkv, bs = 64, 8, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=8)
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, f"prefill scale {scale}")
+    # the 16-token decode chunk runs on the same tensor-core pipeline
+    q16, kc16, vc16, t16 = random_case(lens, 128, bs, Hq, Hkv, seed=9, q_len=16)
+    dec = run_decode(q16, kc16, vc16, t16, lens, scale, 128)
+    ref16 = OA.paged_attention(bits(q16), bits(kc16), bits(vc16), t16, np.asarray(lens, dtype=np.int32),
+                               num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, block_size=bs, scale=scale,
+                               q_len=16)
+    assert_attention_close(dec, ref16, f"decode chunk scale {scale}")
+
+
+def test_prefill_edge_rows():
+    """A chunk longer than its sequence (leading rows see no key: zeros), an
+    empty sequence with an empty chunk, and rows no sequence owns (untouched)."""
+    lens, chunks = [5, 0, 40], [8, 0, 40]
+    Hq, Hkv, bs = 64, 8, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=4)
+    spare = 7  # rows past q_start[-1]
+    qx = torch.cat([q, inputs.randn_bf16((spare,) + tuple(q.shape[1:]), 99, "cuda")])
+    scale = 0.08
+    st = status_tensor()
+    out = run_prefill(qx, kc, vc, tables, lens, q_start, scale, status=st)
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out[:len(q)], ref, "prefill edges")
+    assert not out[:3].float().abs().sum()
+    assert torch.all(out[len(q):].view(torch.int16) == CANARY)
+
+
+def test_prefill_unwritten_tail_slots_never_leak_nan():
+    lens, chunks = [17, 70], [17, 6]
+    Hq, Hkv, bs = 32, 4, 32
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=6)
+    for i, L in enumerate(lens):
+        last = tables[i, (L - 1) // bs]
+        off = L - ((L - 1) // bs) * bs
+        kc[last, :, off:].view(torch.int16).fill_(CANARY)
+        vc[last, :, off:].view(torch.int16).fill_(CANARY)
+    out = run_prefill(q, kc, vc, tables, lens, q_start, 0.09)
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, 0.09)
+    assert_attention_close(out, ref, "prefill nan tail")
+
+
+def test_prefill_bad_inputs_set_status_without_fault():
+    lens, chunks = [60, 90, 30], [20, 30, 10]
+    Hq, Hkv, bs = 64, 8, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=2)
+    scale = 0.1
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    # a last entry past the query rows: sequence 2 gets no rows (left untouched), the others are exact
+    bad_qs = q_start.copy()
+    bad_qs[3] = len(q) + 5
+    st = status_tensor()
+    out = run_prefill(q, kc, vc, tables, lens, bad_qs, scale, status=st)
+    assert st.item() & native.PKV_STATUS_BAD_QSTART
+    assert_attention_close(out[:q_start[2]], ref[:q_start[2]], "rows before the bad entry")
+    assert torch.all(out[q_start[2]:].view(torch.int16) == CANARY)
+    # a decreasing entry is reported too
+    bad_qs = q_start.copy()
+    bad_qs[2] = bad_qs[1] - 1
+    st.zero_()
+    run_prefill(q, kc, vc, tables, lens, bad_qs, scale, status=st)
+    assert st.item() & native.PKV_STATUS_BAD_QSTART
+    # a block id outside the pool reads as zeros and is reported
+    bad_tbl = tables.copy()
+    bad_tbl[1, 1] = kc.shape[0] + 3
+    st.zero_()
+    out = run_prefill(q, kc, vc, bad_tbl, lens, q_start, scale, status=st)
+    assert st.item() & native.PKV_STATUS_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    assert_attention_close(out[:q_start[1]], ref[:q_start[1]], "sequence 0 beside a bad block")
+    # a length past the table's capacity is clamped and reported
+    st.zero_()
+    run_prefill(q, kc, vc, tables, [60, tables.shape[1] * bs + 1, 30], q_start, scale, status=st)
+    assert st.item() & native.PKV_STATUS_BAD_LEN
+
+
+def test_mixed_step_of_decodes_and_a_prefill_chunk():
+    """One call serves a batch the way a chunked-prefill scheduler builds it:
+    many single-token decodes beside one long prompt chunk."""
+    rng = np.random.default_rng(21)
+    n_dec = 40
+    lens = [int(x) for x in rng.integers(1, 3000, size=n_dec)] + [2600]
+    chunks = [1] * n_dec + [512]
+    Hq, Hkv, bs = 64, 8, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=21)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, "mixed step")
+    # the decode rows also agree with the decode kernel itself
+    dec = run_decode(q[:n_dec].unsqueeze(1), kc, vc, tables[:n_dec], lens[:n_dec], scale)
+    assert torch.allclose(dec[:, 0].float(), out[:n_dec].float(), atol=1e-2, rtol=1e-2)
