@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = 2
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 DEFAULT_PARTITION = 768  # the library's split-K partition when the caller passes 0
 
 
@@ -50,6 +51,16 @@ def measured_hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed on its own)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured burst bf16_tflops"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def decode_kernel_source_sha():
@@ -445,6 +456,7 @@ def run_ours(args, rank, world, local):
     }
     if not args.no_workloads:
         line["workloads"] = other_workloads(args, device, rank, world, peak)
+        line["prefill"] = prefill_bench(device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_oracle_baseline(HEADLINE, budget_s=args.cpu_seconds)
@@ -571,6 +583,78 @@ def swap_bench(device):
     return res
 
 
+def prefill_bench(device, steps=10, warmup=3, only=None):
+    """Chunked prefill (paged_attention_prefill) on the prefill workloads: a
+    step is the chunk's pkv_write plus the attention call; the attention call
+    is also timed alone (the tensor-core roofline).  2 x L2 is written before
+    every step, outside the events."""
+    import torch
+    from paged_kv_cache_276_gb300 import inputs
+    from paged_kv_cache_276_gb300.workloads import PrefillCase
+    peak, peak_kind = measured_tensor_peak()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for tag, pw in inputs.PREFILL_WORKLOADS.items():
+        if only is not None and tag != only:
+            continue
+        try:
+            case = PrefillCase(pw, device)
+            status = torch.zeros(1, dtype=torch.int32, device=device)
+            pool = []
+            for _ in range(4 * (warmup + steps)):  # created and recorded once, before the timed loop
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                pool.append(e)
+            step_ev, att_ev = [], []
+            torch.cuda.synchronize()
+            with ClockSampler(gpu_id()) as clocks:
+                for i in range(warmup + steps):
+                    flush.fill_(float(i))
+                    a0, a1 = pool.pop(), pool.pop()
+                    a0.record(stream)
+                    case.step(status, stream)  # the chunk's pkv_write, then the attention
+                    a1.record(stream)
+                    flush.fill_(float(i) + 0.5)
+                    b0, b1 = pool.pop(), pool.pop()
+                    b0.record(stream)
+                    case.attend(status, stream)  # the attention call alone
+                    b1.record(stream)
+                    if i >= warmup:
+                        step_ev.append((a0, a1))
+                        att_ev.append((b0, b1))
+                torch.cuda.synchronize()
+            if status.item() != 0:
+                raise RuntimeError(f"device status {status.item()}")
+            step_ms = [x.elapsed_time(y) for x, y in step_ev]
+            att_ms = [x.elapsed_time(y) for x, y in att_ev]
+            sm, am = sum(step_ms) / steps, sum(att_ms) / steps
+            fl = case.flops()
+            tf = fl / (am * 1e-3) / 1e12
+            res[tag] = {
+                "workload": f"{pw.name}: {case.B} seqs, (L, chunk) = "
+                            + (f"({int(case.lens[0])}, {int(case.chunks[0])})" if "decodes" not in pw.extra else
+                               f"256 x (U{{1..4096}}, 1) + (8192, 1024) + (16384, 1024)")
+                            + f", block {pw.block_size}, {pw.num_q_heads}q/{pw.num_kv_heads}kv, d {pw.head_dim}, bf16",
+                "query_rows": case.total_q, "flops_per_call": fl, "kv_bytes_per_call": case.kv_bytes(),
+                "attention_ms_avg": round(am, 5), "step_ms_avg": round(sm, 5),
+                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tf / peak, 4), "peak_kind": peak_kind,
+                             "kernel": "chunk_tc_kernel<bs, prefill> (paged_attention_prefill)", "traffic": None},
+                "kv_gbs": round(case.kv_bytes() / (am * 1e-3) / 1e9, 1),
+                "query_tok_s": round(case.total_q / (sm * 1e-3), 1),
+                "step_tflops": round(fl / (sm * 1e-3) / 1e12, 1),
+                "clocks": clocks.summary(),
+            }
+            del case
+            torch.cuda.empty_cache()
+        except Exception as e:
+            res[tag] = {"error": repr(e)}
+            log(f"prefill {tag} failed: {e!r}")
+    return res
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: W untimed and K timed whole decode steps
     of the headline workload on this host's cores (rank 0 only)."""
@@ -604,6 +688,9 @@ def main():
     ap.add_argument("--workload", default=None, choices=[case_tag(*c) for c in WORKLOAD_CASES],
                     help="time only this secondary workload (for profiling runs; no headline line)")
     ap.add_argument("--swap", action="store_true", help="bandwidth of the block swap-out / swap-in copies")
+    ap.add_argument("--prefill", nargs="?", const="all", default=None,
+                    choices=["all", "prefill_long_context", "prefill_prompts", "prefill_mixed"],
+                    help="chunked prefill only (all workloads, or the one named)")
     ap.add_argument("--block-sweep", action="store_true",
                     help="block-size trade-off: decode GB/s at block 16..128 and the memory simulation")
     args = ap.parse_args()
@@ -627,6 +714,13 @@ def main():
         build.build()
         torch.cuda.set_device(local)
         line = {"swap": swap_bench(torch.device("cuda", local))}
+    elif args.prefill:
+        import torch
+        from paged_kv_cache_276_gb300 import build
+        build.build()
+        torch.cuda.set_device(local)
+        line = {"prefill": prefill_bench(torch.device("cuda", local), steps=args.steps, warmup=args.warmup,
+                                         only=None if args.prefill == "all" else args.prefill)}
     elif args.block_sweep:
         import torch
         from paged_kv_cache_276_gb300 import build

@@ -32,7 +32,9 @@
 // Warp roles: 0-7 softmax (thread = row; warps 0-3 take the even tiles of a
 // run, 4-7 the odd ones, each set with its own running max / sum and its own
 // TMEM accumulator, merged exactly at the end of the run by the even set),
-// 8 TMA producer, 9 MMA issuer (one lane) and tensor-memory owner.
+// 8 TMA producer of queries and keys, 9 score-product issuer (one lane) and
+// tensor-memory owner, 10 P V product issuer (one lane), 11 TMA producer of
+// values.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -57,10 +59,9 @@ constexpr int kTileKeys = 64;    // keys per MMA tile
 constexpr int kMaxStages = 5;    // K/V ring (at most)
 constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
 constexpr int kKVBytes = kTileKeys * kD * 2;     // 16 KiB each for K and V: [half][64 rows][128 B]
-constexpr int kStageBytes = 2 * kKVBytes;
 constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64, P: 2 x 32
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kKWarp = 8, kMmaWarp = 9, kPvWarp = 10, kVWarp = 11;
+constexpr int kThreads = 12 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 
@@ -69,20 +70,26 @@ enum : int {
   B_Q_FULL0 = 0, B_Q_FULL1, B_Q_FREE0, B_Q_FREE1, B_O_FULL, B_O_FREE,
   B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
   B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0, B_STATS_FREE1,
-  B_KV_FULL0, B_KV_EMPTY0 = B_KV_FULL0 + kMaxStages, B_COUNT = B_KV_EMPTY0 + kMaxStages
+  B_K_FULL0, B_K_EMPTY0 = B_K_FULL0 + kMaxStages, B_V_FULL0 = B_K_EMPTY0 + kMaxStages,
+  B_V_EMPTY0 = B_V_FULL0 + kMaxStages, B_COUNT = B_V_EMPTY0 + kMaxStages
 };
 
-// Shared-memory plan of each schedule.  Prefill double-buffers the query tile
-// (items are short runs, so the next tile loads while the current one is
-// still in flight) and gives up one K/V stage for it.
+// Shared-memory plan of each schedule: the query tile(s), then a ring of key
+// tiles and a ring of value tiles (kStages each).  A key stage is released as
+// soon as its score product completes, a value stage after its P V product,
+// so the keys can be fetched further ahead than the values.  Prefill
+// double-buffers the query tile (items are short runs, so the next tile
+// loads while the current one is still in flight) and gives up one stage of
+// each ring for it.
 template <bool kPrefill>
 struct Layout {
   static constexpr int kStages = kPrefill ? 4 : 5;
   static constexpr int kQBufs = kPrefill ? 2 : 1;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
   static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
-  static constexpr int kSmemRing = kQBufs * kQBytes;
-  static constexpr int kSmemStats = kSmemRing + kStages * kStageBytes;  // float2 [2][128]: odd set's (max, sum)
+  static constexpr int kSmemK = kQBufs * kQBytes;
+  static constexpr int kSmemV = kSmemK + kStages * kKVBytes;
+  static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
   static constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
   static constexpr int kSmemSeq = kSmemBars + B_COUNT * 8 + 16;  // after the TMEM slot and the abort flag
   static constexpr size_t bytes(int num_seqs) {
@@ -216,10 +223,12 @@ struct Sched {
   }
 };
 
-// Bounded wait whose outcome every lane of the warp agrees on.
+// Bounded wait whose outcome every lane of the warp agrees on; try_wait
+// parks the warp until the phase completes (or a short hardware window ends).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity));
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
+
 
 template <int BS, bool kPrefill>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) prefix[0] = 0;
   }
-  if (threadIdx.x == 32 * kProducerWarp) {
+  if (threadIdx.x == 32 * kKWarp) {
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(bar(B_Q_FULL0 + i), 1);
       mbar_init(bar(B_Q_FREE0 + i), 1);
@@ -307,8 +316,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_PV_DONE0 + i), 1);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(B_KV_FULL0 + s), 1);
-      mbar_init(bar(B_KV_EMPTY0 + s), 1);
+      mbar_init(bar(B_K_FULL0 + s), 1);
+      mbar_init(bar(B_K_EMPTY0 + s), 1);
+      mbar_init(bar(B_V_FULL0 + s), 1);
+      mbar_init(bar(B_V_EMPTY0 + s), 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -317,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
     tc::relinquish();
   }
-  if (threadIdx.x == 32 * kProducerWarp + 1) {
+  if (threadIdx.x == 32 * kKWarp + 1) {
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -327,15 +338,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
   const int I = prefix[B];
-  const uint32_t sQ = smem_u32(smem), sRing = smem_u32(smem + Lay::kSmemRing);
+  const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + Lay::kSmemK), sV = smem_u32(smem + Lay::kSmemV);
   const uint32_t tS0 = tmem + 2 * kD;        // S buffers after the two accumulators
   const uint32_t tP0 = tS0 + 2 * kTileKeys;  // P (bf16 pairs per column) after the S buffers
   const bool has_work = kPrefill ? static_cast<int>(blockIdx.x) < I
                                  : range_first(blockIdx.x, I) < range_first(blockIdx.x + 1, I);
 
   if (has_work) {
-    if (warp == kProducerWarp) {
-      // ------------------------------------------------------------ producer
+    if (warp == kKWarp || warp == kVWarp) {
+      // ------------------------------------------- producers: K (+ Q), V
+      const bool is_v = warp == kVWarp;
+      const CUtensorMap *tm = is_v ? &tmv : &tmk;
+      const uint32_t ring = is_v ? sV : sK;
+      const int full0 = is_v ? B_V_FULL0 : B_K_FULL0, empty0 = is_v ? B_V_EMPTY0 : B_K_EMPTY0;
       // decode: every key is read once; prefill: the CTAs beside this one read them too
       const uint64_t pol = kPrefill ? l2_policy_evict_normal() : l2_policy_evict_first();
       Sched<kPrefill> sc;
@@ -344,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tw_seq = -1, tw_base = 0, tw_val = -1;
       for (; sc.valid() && !*abort_flag; sc.advance(p, tab)) {
         const Item &x = sc.x;
-        if (x.run_begin && x.k_hi > x.k_lo) {  // a run with keys: load its queries
+        if (!is_v && x.run_begin && x.k_hi > x.k_lo) {  // a run with keys: load its queries
           const int qi = tpieces++, qb = qi % kQBufs, use = qi / kQBufs;
           if (use > 0 && !wait_warp(bar(B_Q_FREE0 + qb), (use - 1) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
@@ -368,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nblk_seq = ceil_div(lens[x.seq], BS);
         for (int t = 0; t < ntile; ++t, ++g) {
           const int s = g % kStages;
-          if (g >= kStages && !wait_warp(bar(B_KV_EMPTY0 + s), ((g / kStages) - 1) & 1)) {
+          if (g >= kStages && !wait_warp(bar(empty0 + s), ((g / kStages) - 1) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -384,94 +399,112 @@ __global__ void __launch_bounds__(kThreads, 1)
           int bids[kBoxes];
 #pragma unroll
           for (int j = 0; j < kBoxes; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
-          const uint32_t st = sRing + s * kStageBytes;
-          if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL0 + s), kStageBytes);
-          // one lane per (box, K/V, half): the box copies go out in parallel
-          if (lane < kBoxes * 4) {
-            const int j = lane >> 2, kv = (lane >> 1) & 1, hf = lane & 1;
+          if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), kKVBytes);
+          // one lane per (box, half): the box copies go out in parallel
+          if (lane < kBoxes * 2) {
+            const int j = lane >> 1, hf = lane & 1;
             const int b = bids[j];
             int row;
             if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
               row = (b * hkv + x.head) * BS + k0 % BS;
             } else {
-              if (blk_first + j < nblk_seq && p.status && kv == 0 && hf == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+              if (blk_first + j < nblk_seq && p.status && !is_v && hf == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
               row = p.oob_row;  // past the sequence, or a bad id: zeros
             }
-            tma_load_2d(st + kv * kKVBytes + hf * (kKVBytes / 2) + j * kBoxRows * 128, kv ? &tmv : &tmk, hf * 64,
-                        row, bar(B_KV_FULL0 + s), pol);
+            tma_load_2d(ring + s * kKVBytes + hf * (kKVBytes / 2) + j * kBoxRows * 128, tm, hf * 64, row,
+                        bar(full0 + s), pol);
           }
         }
       }
       // never leave a copy in flight into this CTA's shared memory
       if (lane == 0) {
         for (int y = g > kStages ? g - kStages : 0; y < g; ++y)
-          mbar_wait_sleep(bar(B_KV_FULL0 + (y % kStages)), (y / kStages) & 1);
-        for (int qi = tpieces > kQBufs ? tpieces - kQBufs : 0; qi < tpieces; ++qi)
-          mbar_wait_sleep(bar(B_Q_FULL0 + qi % kQBufs), (qi / kQBufs) & 1);
+          mbar_wait_sleep(bar(full0 + (y % kStages)), (y / kStages) & 1);
+        if (!is_v)
+          for (int qi = tpieces > kQBufs ? tpieces - kQBufs : 0; qi < tpieces; ++qi)
+            mbar_wait_sleep(bar(B_Q_FULL0 + qi % kQBufs), (qi / kQBufs) & 1);
       }
     } else if (warp == kMmaWarp) {
-      // ------------------------------------------------------------- MMA
+      // ------------------------------------------------- S = Q K^T issuer
+      // The score products run ahead of the P V products as far as their two
+      // buffers allow: each waits only for its key stage and for the softmax
+      // to have read the buffer's previous tile, and releases the key stage
+      // when it completes.  The waits are plain try_wait loops (woken on
+      // completion), so each issue follows its event closely.
       if (lane == 0) {
         constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
-        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
         Sched<kPrefill> sc;
         sc.begin(p, tab, I);
-        int g = 0, tpieces = 0, run_g0 = 0;
-        // the tile whose P V product is still to be issued, with its run index
-        int pend = -1, pend_run = 0;
-        bool pend_first = false, pend_last = false;
+        int g = 0, tpieces = 0;
         bool ok = true;
-        auto issue_pv = [&](int y, int run, bool first, bool last) {
-          const int pb = y & 1;  // the set (even / odd tiles): its P buffer and accumulator
-          if (!mbar_wait_sleep(bar(B_P_FULL0 + pb), (y >> 1) & 1)) return false;
-          // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
-          if (first && run > 1 && !mbar_wait_sleep(bar(B_O_FREE), (run - 2) & 1)) return false;
-          tc::fence_after();
-          const uint32_t pa = tP0 + pb * (kTileKeys / 2);
-          const uint32_t vb = sRing + (y % kStages) * kStageBytes + kKVBytes;
-#pragma unroll
-          for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
-            tc::mma_ta(tmem + pb * kD, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO,
-                       !(first && ks == 0));
-          tc::commit(bar(B_PV_DONE0 + pb));
-          tc::commit(bar(B_KV_EMPTY0 + (y % kStages)));
-          if (last) tc::commit(bar(B_O_FULL));
-          return true;
-        };
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
-          int qb = 0;
-          if (x.run_begin && ntile > 0) {
+          if (ntile == 0) continue;
+          int qb = (tpieces > 0 ? tpieces - 1 : 0) % kQBufs;
+          if (x.run_begin) {
             const int qi = tpieces++;
             qb = qi % kQBufs;
-            run_g0 = g;
-            if (!mbar_wait_sleep(bar(B_Q_FULL0 + qb), (qi / kQBufs) & 1)) { ok = false; break; }
-          } else if (tpieces > 0) {
-            qb = (tpieces - 1) % kQBufs;
+            if (!mbar_wait(bar(B_Q_FULL0 + qb), (qi / kQBufs) & 1)) { ok = false; break; }
           }
           const uint32_t sq = sQ + qb * kQBytes;
           for (int t = 0; t < ntile; ++t, ++g) {
             const int s = g % kStages, sb = g & 1;
-            if (!mbar_wait_sleep(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            if (g >= 2 && !mbar_wait_sleep(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
+            if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+            if (g >= 2 && !mbar_wait(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
             tc::fence_after();
-            const uint32_t kb = sRing + s * kStageBytes;
+            const uint32_t kb = sK + s * kKVBytes;
 #pragma unroll
             for (int ks = 0; ks < kD / 16; ++ks)
               tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * (kQBytes / 2) + (ks & 3) * 32, 16, 1024),
                       tc::desc_sw128(kb + (ks >> 2) * (kKVBytes / 2) + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
             tc::commit(bar(B_S_FULL0 + sb));
-            const bool last_of_run = x.run_end && t == ntile - 1;
-            if (last_of_run) tc::commit(bar(B_Q_FREE0 + qb));  // the queries are only read by MMAs issued so far
-            if (pend >= 0 && !issue_pv(pend, pend_run, pend_first, pend_last)) { ok = false; break; }
-            pend = g;
-            pend_run = tpieces;
-            pend_first = g - run_g0 < 2;  // the first tile of its set in this run
-            pend_last = last_of_run;
+            tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by this product only
+            if (x.run_end && t == ntile - 1) tc::commit(bar(B_Q_FREE0 + qb));  // read by MMAs issued so far only
           }
         }
-        if (ok && pend >= 0) ok = issue_pv(pend, pend_run, pend_first, pend_last);
+        if (!ok) {
+          if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+    } else if (warp == kPvWarp) {
+      // ------------------------------------------------ O += P V issuer
+      // Each product goes out, in tile order, as soon as its P is written and
+      // its values have landed; its value stage is released when it completes.
+      if (lane == 0) {
+        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
+        Sched<kPrefill> sc;
+        sc.begin(p, tab, I);
+        int g = 0, tpieces = 0, run_g0 = 0;
+        bool ok = true;
+        for (; sc.valid() && ok; sc.advance(p, tab)) {
+          const Item &x = sc.x;
+          const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
+          if (ntile == 0) continue;
+          if (x.run_begin) {
+            ++tpieces;
+            run_g0 = g;
+          }
+          for (int t = 0; t < ntile; ++t, ++g) {
+            const int pb = g & 1;  // the set (even / odd tiles): its P buffer and accumulator
+            const bool first = g - run_g0 < 2, last = x.run_end && t == ntile - 1;
+            if (!mbar_wait(bar(B_P_FULL0 + pb), (g >> 1) & 1)) { ok = false; break; }
+            if (!mbar_wait(bar(B_V_FULL0 + g % kStages), (g / kStages) & 1)) { ok = false; break; }
+            // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
+            if (first && tpieces > 1 && !mbar_wait(bar(B_O_FREE), (tpieces - 2) & 1)) { ok = false; break; }
+            tc::fence_after();
+            const uint32_t pa = tP0 + pb * (kTileKeys / 2);
+            const uint32_t vb = sV + (g % kStages) * kKVBytes;
+#pragma unroll
+            for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
+              tc::mma_ta(tmem + pb * kD, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO,
+                         !(first && ks == 0));
+            tc::commit(bar(B_PV_DONE0 + pb));
+            tc::commit(bar(B_V_EMPTY0 + (g % kStages)));
+            if (last) tc::commit(bar(B_O_FULL));
+          }
+        }
         if (!ok) {
           if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
           *abort_flag = 1;
@@ -524,66 +557,102 @@ __global__ void __launch_bounds__(kThreads, 1)
           set_has_tiles = true;
           const int sb = set;
           if (!wait_warp(bar(B_S_FULL0 + sb), (g >> 1) & 1)) { ok = false; break; }
-          tc::fence_after();
-          uint32_t sv[kTileKeys];
-          tc::ld32(tS0 + sb * kTileKeys + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tc::ld32(tS0 + sb * kTileKeys + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          tc::wait_ld();
-          tc::fence_before();
-          mbar_arrive(bar(B_S_FREE0 + sb));
-          // a negative scale turns the largest score into the smallest: take minima then
-          const bool neg = p.scale_log2 < 0.f;
-          const uint32_t masked = __float_as_uint(neg ? INFINITY : -INFINITY);
           const int k0 = x.k_lo + t * kTileKeys;
           const int vis = min(limit, x.k_hi) - k0;  // keys of this tile the row sees
-          if (!__all_sync(0xffffffffu, vis >= kTileKeys)) {
+          uint32_t pk[kTileKeys / 2];                 // P row: two bf16 per tensor-memory column
+          bool scale_o = false;
+          float alpha = 1.f;
+          if (__all_sync(0xffffffffu, vis <= 0)) {
+            // no row of this warp sees a key of the tile (rows past a short
+            // chunk's end): its weights are zero and nothing else changes
+            mbar_arrive(bar(B_S_FREE0 + sb));
 #pragma unroll
-            for (int c = 0; c < kTileKeys; ++c)
-              if (c >= vis) sv[c] = masked;
-          }
-          // the extreme raw score (its product with the scale is the largest
-          // scaled score): eight short chains of 3-input maxima (minima)
-          float rm;
-          if (!neg) {
-            float mx[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
-#pragma unroll
-            for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
-            rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            for (int c = 0; c < kTileKeys / 2; ++c) pk[c] = 0u;
           } else {
-            float mn[8];
+            tc::fence_after();
+            uint32_t sv[kTileKeys];
+            tc::ld32(tS0 + sb * kTileKeys + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tc::ld32(tS0 + sb * kTileKeys + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tc::wait_ld();
+            tc::fence_before();
+            mbar_arrive(bar(B_S_FREE0 + sb));
+            // a negative scale turns the largest score into the smallest: take minima then
+            const bool neg = p.scale_log2 < 0.f;
+            const uint32_t masked = __float_as_uint(neg ? INFINITY : -INFINITY);
+            if (!__all_sync(0xffffffffu, vis >= kTileKeys)) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mn[q] = fmin3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
+              for (int c = 0; c < kTileKeys; ++c)
+                if (c >= vis) sv[c] = masked;
+            }
+            // the extreme raw score (its product with the scale is the largest
+            // scaled score): eight short chains of 3-input maxima (minima)
+            float rm;
+            if (!neg) {
+              float mx[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
+              for (int q = 0; q < 8; ++q)
+                mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+              for (int q = 0; q < 8; ++q)
+                mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
 #pragma unroll
-            for (int q = 0; q < 8; ++q) mn[q] = fminf(mn[q], __uint_as_float(sv[q + 56]));
-            rm = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
+              for (int q = 0; q < 8; ++q)
+                mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+#pragma unroll
+              for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
+              rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            } else {
+              float mn[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                mn[q] = fmin3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
+#pragma unroll
+              for (int q = 0; q < 8; ++q) mn[q] = fminf(mn[q], __uint_as_float(sv[q + 56]));
+              rm = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
+            }
+            const float bm = rm * p.scale_log2;
+            // move the reference max only when a score passes it by more than
+            // kSlack (rare after a set's first tile); exact, since O and l share it
+            const bool move = bm > m + kSlack;
+            scale_o = move && !first_tile_of_set && m != -INFINITY;
+            alpha = scale_o ? fast_exp2(m - bm) : 1.f;
+            if (move) {
+              l = m == -INFINITY ? 0.f : l * exp2f(m - bm);
+              m = bm;
+            }
+            const float msub = m == -INFINITY ? 0.f : m;
+            const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+            const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
+            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
+#pragma unroll
+            for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys give 2^-inf
+              float x0, x1;
+              f32x2_split(ffma2(f32x2_bits(sv[2 * c], sv[2 * c + 1]), ks2, nm2), x0, x1);
+              pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+              // the running sum uses the same rounded weights as the P V product
+              ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
+            }
+            {
+              float a0, a1, b0, b1, c0, c1, d0, d1;
+              f32x2_split(ls[0], a0, a1);
+              f32x2_split(ls[1], b0, b1);
+              f32x2_split(ls[2], c0, c1);
+              f32x2_split(ls[3], d0, d1);
+              l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+            }
           }
-          const float bm = rm * p.scale_log2;
           // this set's previous tile (g - 2) must be in the accumulator before a
-          // rescale, and its P buffer free before the new P is written
+          // rescale, and its P buffer free before the new P is written; the
+          // weights above were computed while that product ran
           if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
-          // move the reference max only when a score passes it by more than
-          // kSlack (rare after a set's first tile); exact, since O and l share it
-          const bool move = bm > m + kSlack;
-          const bool scale_o = move && !first_tile_of_set && m != -INFINITY;
           if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
             tc::fence_after();
-            const float alpha = scale_o ? fast_exp2(m - bm) : 1.f;
 #pragma unroll
             for (int ch = 0; ch < kD / 32; ++ch) {
               uint32_t ov[32];
@@ -595,39 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::wait_st();
           }
-          if (move) {
-            l = m == -INFINITY ? 0.f : l * exp2f(m - bm);
-            m = bm;
-          }
-          const float msub = m == -INFINITY ? 0.f : m;
-          const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
-          const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
-          uint32_t pk[kTileKeys / 2];  // P row: two bf16 per tensor-memory column
-          uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
-#pragma unroll
-          for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys give 2^-inf
-            float x0, x1;
-            f32x2_split(ffma2(f32x2_bits(sv[2 * c], sv[2 * c + 1]), ks2, nm2), x0, x1);
-            pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-            // the running sum uses the same rounded weights as the P V product
-            ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
-          }
-          {
-            float a0, a1, b0, b1, c0, c1, d0, d1;
-            f32x2_split(ls[0], a0, a1);
-            f32x2_split(ls[1], b0, b1);
-            f32x2_split(ls[2], c0, c1);
-            f32x2_split(ls[3], d0, d1);
-            l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-          }
           tc::st32(tP0 + sb * (kTileKeys / 2) + lane_off, pk);
           tc::wait_st();
           // value rows past the sequence end were never written: zero them
           const int exist = L - k0;
           if (exist < kTileKeys) {
             const int s = g % kStages;
-            if (!wait_warp(bar(B_KV_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            const uint32_t vb = sRing + s * kStageBytes + kKVBytes;
+            if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+            const uint32_t vb = sV + s * kKVBytes;
             const int first = exist < 0 ? 0 : exist;
             for (int e = r; e < (kTileKeys - first) * 2 * 8; e += kRows) {  // 16-byte chunks
               const int row = first + e / 16, rem = e % 16, hf = rem / 8, c = rem % 8;

@@ -20,6 +20,16 @@ Workloads (seed = 1000 + workload number):
                     suffix ~ U{0..512}, block 16, 32 q / 8 KV heads, d 128
   5 long context    16 x 32768 tokens, block 16 and 32, 64 q / 8 KV heads,
                     d 128, 512-token partitions, plus a 16-token causal chunk
+
+Chunked-prefill workloads (``PREFILL_WORKLOADS``; each sequence is (context
+length L including its chunk, chunk length c)):
+  prefill_long_context  16 sequences, the last 1,024 tokens of a 32,768-token
+                        prompt (L 32768, c 1024), block 16, 64 q / 8 KV heads, d 128
+  prefill_prompts       8 prompts of 4,096 tokens prefilled whole from an empty
+                        cache (L = c = 4096), block 16, 64 q / 8 KV heads, d 128
+  prefill_mixed         one scheduler step: 256 single-token decodes with
+                        L ~ U{1..4096} and two 1,024-token prompt chunks at
+                        L 8192 and 16384, block 16, 32 q / 8 KV heads, d 128
 """
 from __future__ import annotations
 
@@ -64,6 +74,47 @@ WORKLOADS = {
     5: Workload(5, "long-context decode", 16, 16, 64, 8, 128, partition_size=512,
                 extra={"len": 32768, "chunk": 16}),
 }
+
+
+@dataclass(frozen=True)
+class PrefillWorkload:
+    tag: str
+    name: str
+    block_size: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    seed: int
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.head_dim)))
+
+
+PREFILL_WORKLOADS = {
+    "prefill_long_context": PrefillWorkload("prefill_long_context", "chunked prefill behind a 31,744-token context",
+                                            16, 64, 8, 128, 2001, extra={"seqs": 16, "len": 32768, "chunk": 1024}),
+    "prefill_prompts": PrefillWorkload("prefill_prompts", "whole 4,096-token prompts from an empty cache",
+                                       16, 64, 8, 128, 2002, extra={"seqs": 8, "len": 4096, "chunk": 4096}),
+    "prefill_mixed": PrefillWorkload("prefill_mixed", "256 decodes + two 1,024-token prompt chunks in one call",
+                                     16, 32, 8, 128, 2003,
+                                     extra={"decodes": 256, "len_max": 4096, "chunks": ((8192, 1024), (16384, 1024))}),
+}
+
+
+def prefill_shape(pw: PrefillWorkload):
+    """(lengths L, chunk lengths c) of a prefill workload's sequences, int32."""
+    e = pw.extra
+    if "decodes" in e:
+        rng = np.random.default_rng(pw.seed)
+        lens = list(rng.integers(1, e["len_max"] + 1, size=e["decodes"]))
+        chunks = [1] * e["decodes"]
+        for L, c in e["chunks"]:
+            lens.append(L)
+            chunks.append(c)
+        return np.asarray(lens, dtype=np.int32), np.asarray(chunks, dtype=np.int32)
+    return (np.full(e["seqs"], e["len"], dtype=np.int32), np.full(e["seqs"], e["chunk"], dtype=np.int32))
 
 
 def rng_for(w: Workload, salt: int = 0) -> np.random.Generator:

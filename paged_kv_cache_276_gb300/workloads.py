@@ -196,3 +196,75 @@ class DecodeSession:
     def kv_bytes(self, step: StepInputs) -> int:
         """Valid K and V bytes one step's decodes read over all layers."""
         return int(step.host_lens.astype(np.int64).sum()) * 2 * self.Hkv * self.d * 2 * self.layers
+
+
+# ------------------------------------------------------------ chunked prefill
+def causal_visible_keys(lens, chunks) -> int:
+    """Sum over every chunk row of the keys it sees: row r of a chunk of c
+    tokens in a sequence of L sees max(0, L - c + 1 + r) keys."""
+    total = 0
+    for L, c in zip(np.asarray(lens, dtype=np.int64), np.asarray(chunks, dtype=np.int64)):
+        r0 = max(0, int(c - L))               # rows before r0 see nothing
+        n = int(c) - r0
+        if n > 0:
+            first = int(L - c + 1 + r0)       # keys of row r0; the last row sees L
+            total += n * (first + int(L)) // 2
+    return total
+
+
+class PrefillCase:
+    """One chunked-prefill batch resident on the device.
+
+    The caches hold every sequence's L tokens, the chunk's own keys and values
+    included, as seeded N(0,1) bf16 in a permuted block placement (the state
+    after the chunk's ``pkv_write``).  ``step`` is one pass of the hot path: the
+    chunk's keys and values written into their slots (``chunk_k``/``chunk_v``,
+    fresh seeded values) and ``paged_attention_prefill`` over all sequences.
+    """
+
+    def __init__(self, pw: inputs.PrefillWorkload, device, pool_extra: float = 0.05):
+        self.pw = pw
+        self.device = torch.device(device)
+        self.bs, self.Hq, self.Hkv, self.d = pw.block_size, pw.num_q_heads, pw.num_kv_heads, pw.head_dim
+        self.scale = pw.scale
+        self.lens, self.chunks = inputs.prefill_shape(pw)
+        self.B = len(self.lens)
+        rng = np.random.default_rng(pw.seed)
+        NB = inputs.pool_size(self.lens, self.bs, pool_extra)
+        self.num_blocks = NB
+        self.tables, _ = inputs.permuted_tables(self.lens, self.bs, NB, rng)
+        self.k_cache = inputs.randn_bf16((NB, self.Hkv, self.bs, self.d), pw.seed * 10 + 1, self.device)
+        self.v_cache = inputs.randn_bf16((NB, self.Hkv, self.bs, self.d), pw.seed * 10 + 2, self.device)
+        self.q_start = np.concatenate([[0], np.cumsum(self.chunks)]).astype(np.int32)
+        self.total_q = int(self.q_start[-1])
+        self.q = inputs.randn_bf16((self.total_q, self.Hq, self.d), pw.seed * 10 + 3, self.device)
+        # slot of every chunk token: positions L - c .. L - 1 of its sequence
+        slots = np.empty(self.total_q, dtype=np.int64)
+        for i, (L, c) in enumerate(zip(self.lens, self.chunks)):
+            t = np.arange(L - c, L)
+            slots[self.q_start[i]:self.q_start[i + 1]] = self.tables[i, t // self.bs].astype(np.int64) * self.bs \
+                + t % self.bs
+        self.slots = torch.as_tensor(slots, device=self.device)
+        self.chunk_k = inputs.randn_bf16((self.total_q, self.Hkv, self.d), pw.seed * 10 + 4, self.device)
+        self.chunk_v = inputs.randn_bf16((self.total_q, self.Hkv, self.d), pw.seed * 10 + 5, self.device)
+        self.d_tables = torch.as_tensor(self.tables, device=self.device)
+        self.d_lens = torch.as_tensor(self.lens, device=self.device)
+        self.d_q_start = torch.as_tensor(self.q_start, device=self.device)
+        self.out = torch.empty_like(self.q)
+
+    def attend(self, d_status=None, stream=None):
+        native.paged_attention_prefill(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
+                                       self.d_q_start, self.scale, self.out, d_status, stream)
+
+    def step(self, d_status=None, stream=None):
+        native.pkv_write(self.chunk_k, self.chunk_v, self.slots, self.k_cache, self.v_cache, d_status, stream)
+        self.attend(d_status, stream)
+
+    def flops(self) -> int:
+        """Algorithmic FLOPs of the attention: per query head and visible key,
+        d multiply-adds for q.k and d for p.v."""
+        return 4 * self.d * self.Hq * causal_visible_keys(self.lens, self.chunks)
+
+    def kv_bytes(self) -> int:
+        """Distinct K and V bytes the call needs (every cached token once)."""
+        return int(self.lens.astype(np.int64).sum()) * 2 * self.Hkv * self.d * 2

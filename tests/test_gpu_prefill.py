@@ -90,6 +90,11 @@ def test_prefill_many_items_per_cta():
     out = run_prefill(q, kc, vc, tables, lens, q_start, scale)
     ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
     assert_attention_close(out, ref, "prefill, many items")
+    # the schedule is static and the arithmetic order fixed: repeated calls are
+    # bit-identical (a read that races its copy would show up here first)
+    for _ in range(3):
+        again = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+        assert torch.equal(again.view(torch.int16), out.view(torch.int16))
 
 
 def test_prefill_of_uniform_16_token_chunks_equals_the_decode_chunk_bit_for_bit():
@@ -218,3 +223,30 @@ def test_mixed_step_of_decodes_and_a_prefill_chunk():
     # the decode rows also agree with the decode kernel itself
     dec = run_decode(q[:n_dec].unsqueeze(1), kc, vc, tables[:n_dec], lens[:n_dec], scale)
     assert torch.allclose(dec[:, 0].float(), out[:n_dec].float(), atol=1e-2, rtol=1e-2)
+
+
+@pytest.mark.parametrize("tag", ["prefill_long_context", "prefill_prompts", "prefill_mixed"])
+def test_prefill_workloads_sampled(tag):
+    """The benchmark's prefill workloads at full size, in the benchmark's launch
+    configuration; sampled rows against the oracle (a chunk row equals a
+    single-token decode at the length the row sees)."""
+    from paged_kv_cache_276_gb300.workloads import PrefillCase
+    case = PrefillCase(inputs.PREFILL_WORKLOADS[tag], "cuda")
+    st = status_tensor()
+    case.attend(st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    kb, vb = bits(case.k_cache), bits(case.v_cache)
+    out = case.out
+    rng = np.random.default_rng(5)
+    seqs = sorted({0, case.B - 1, int(rng.integers(0, case.B))})
+    for i in seqs:
+        L, c = int(case.lens[i]), int(case.chunks[i])
+        rows = sorted({0, c - 1, int(rng.integers(0, c))})
+        for r in rows:
+            n = L - c + 1 + r
+            row = int(case.q_start[i]) + r
+            ref = OA.paged_attention(bits(case.q[row:row + 1].unsqueeze(0)), kb, vb, case.tables[i:i + 1],
+                                     np.array([n], dtype=np.int32), num_q_heads=case.Hq, num_kv_heads=case.Hkv,
+                                     head_dim=case.d, block_size=case.bs, scale=case.scale)
+            assert_attention_close(out[row:row + 1], ref[0], f"{tag} seq {i} row {r}")

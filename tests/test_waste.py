@@ -87,3 +87,16 @@ def test_paged_holds_more_token_state_than_contiguous_on_a_mixed_stream():
     g = waste.simulate(p, f, cap, "paged", block_size=16)
     assert g.token_state_fraction > c.token_state_fraction
     assert g.mean_running > c.mean_running and g.steps < c.steps
+
+
+def test_causal_visible_keys_matches_brute_force():
+    from paged_kv_cache_276_gb300.workloads import causal_visible_keys
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        B = int(rng.integers(1, 6))
+        lens = rng.integers(0, 300, size=B)
+        chunks = rng.integers(0, 320, size=B)
+        brute = sum(max(0, int(L) - int(c) + 1 + r) for L, c in zip(lens, chunks) for r in range(int(c)))
+        assert causal_visible_keys(lens, chunks) == brute
+    # a whole prompt from an empty cache: c (c + 1) / 2
+    assert causal_visible_keys([4096], [4096]) == 4096 * 4097 // 2
