@@ -13,7 +13,9 @@
 // section "Continuous batching is the other half of the story").
 //
 // Two schedules drive the same pipeline (persistent grid, one CTA per SM):
-//  * decode chunk (16 tokens, G = 8: one query tile per sequence and KV head).
+//  * decode chunk (the newest q_len tokens of every sequence, q_len * G <= 128:
+//    one query tile per sequence and KV head, its spare rows zero; a
+//    single-token decode is q_len 1).
 //    The (sequence, KV head, partition) items split each sequence's keys into
 //    partitions and CTA c takes a contiguous range of them.  Consecutive items
 //    of the same (sequence, KV head) accumulate into the same TMEM
@@ -53,8 +55,6 @@ namespace {
 
 constexpr int kD = 128;          // head dim
 constexpr int kRows = 128;       // query rows per tile (tokens x group heads)
-constexpr int kQLen = 16;        // decode chunk: tokens
-constexpr int kGroup = 8;        // decode chunk: query heads per KV head
 constexpr int kTileKeys = 64;    // keys per MMA tile
 constexpr int kMaxStages = 5;    // K/V ring (at most)
 constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
@@ -74,17 +74,16 @@ enum : int {
   B_V_EMPTY0 = B_V_FULL0 + kMaxStages, B_COUNT = B_V_EMPTY0 + kMaxStages
 };
 
-// Shared-memory plan of each schedule: the query tile(s), then a ring of key
+// Shared-memory plan of each schedule: two query tiles, then a ring of key
 // tiles and a ring of value tiles (kStages each).  A key stage is released as
 // soon as its score product completes, a value stage after its P V product,
-// so the keys can be fetched further ahead than the values.  Prefill
-// double-buffers the query tile (items are short runs, so the next tile
-// loads while the current one is still in flight) and gives up one stage of
-// each ring for it.
+// so the keys can be fetched further ahead than the values.  The second
+// query tile lets the producer load the next run's queries, and then its
+// keys, while the current run is still in flight.
 template <bool kPrefill>
 struct Layout {
-  static constexpr int kStages = kPrefill ? 4 : 5;
-  static constexpr int kQBufs = kPrefill ? 2 : 1;
+  static constexpr int kStages = 4;
+  static constexpr int kQBufs = 2;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
   static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
   static constexpr int kSmemK = kQBufs * kQBytes;
@@ -110,7 +109,9 @@ struct TcParams {
   int32_t *status;
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
   int part_tokens, max_parts, oob_row;
-  int total_q, lg_group;   // prefill: query rows, log2 of the group size
+  int total_q;             // prefill: query rows
+  int lg_group;            // log2 of the query heads per KV head (G)
+  int q_len;               // decode chunk: query tokens per sequence (q_len * G <= 128)
   float scale_log2;
 };
 
@@ -328,6 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
     tc::relinquish();
   }
+  if (!kPrefill && (p.q_len << p.lg_group) < kRows) {
+    // the loads fill the tile's first q_len * G rows only: the rest stay zero
+    // for the whole kernel, so their scores are finite (and masked)
+    for (int i = threadIdx.x; i < kQBufs * kQBytes / 16; i += kThreads)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(smem) + i * 16), "r"(0u) : "memory");
+    fence_proxy_async_shared();
+  }
   if (threadIdx.x == 32 * kKWarp + 1) {
     tma_prefetch_desc(&tmq);
     tma_prefetch_desc(&tmk);
@@ -368,8 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             const int gsz = 1 << p.lg_group;
-            const int qz = kPrefill ? qs[x.seq] + (kRows >> p.lg_group) * x.qt : x.seq * kQLen;
-            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kQBytes);
+            const int qz = kPrefill ? qs[x.seq] + (kRows >> p.lg_group) * x.qt : x.seq * p.q_len;
+            // decode chunk: the box holds the q_len * G rows only
+            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kPrefill ? kQBytes : (p.q_len << p.lg_group) * kD * 2);
             for (int hf = 0; hf < 2; ++hf)
               asm volatile(
                   "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -548,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           limit = row_valid ? L - c + 1 + row_tok : 0;
         } else {
           row_tok = tok;
-          row_valid = true;
-          limit = L - kQLen + 1 + tok;
+          row_valid = tok < p.q_len;
+          limit = row_valid ? L - p.q_len + 1 + tok : 0;
         }
         for (int t = 0; t < ntile; ++t, ++g) {
           if ((g & 1) != set) continue;  // the other set's tile
@@ -701,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nparts = x.nparts;
         const size_t orow =
             kPrefill ? static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + (x.head << p.lg_group) + gh
-                     : (static_cast<size_t>(x.seq) * kQLen + tok) * p.num_q_heads + x.head * kGroup + gh;
+                     : (static_cast<size_t>(x.seq) * p.q_len + tok) * p.num_q_heads + (x.head << p.lg_group) + gh;
         float fa = 0.f, fb = 0.f, M = -INFINITY, lt = 0.f;
         if (run_has_tiles) {
           if (!wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
@@ -738,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(tmp[c]);
           }
-          if (!row_valid) continue;  // a row past the chunk's end (prefill): nothing to store
+          if (!row_valid) continue;  // a spare row of the tile: nothing to store
           if (nparts == 1) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
 #pragma unroll
@@ -761,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before();
           mbar_arrive(bar(B_O_FREE));
         }
-        if (!kPrefill && nparts > 1) {
+        if (!kPrefill && nparts > 1 && row_valid) {
           p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(M, lt);
           for (int q = run_first_part + 1; q <= x.part; ++q)  // merged into the run's first slot
             p.ws_ml[orow * p.max_parts + q] = make_float2(-INFINITY, 0.f);
@@ -827,8 +836,10 @@ float kernel_scale_log2(float scale) { return (scale == 0.f ? FLT_MIN : scale) *
 
 bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                         int part_tokens) {
-  return q_len == kQLen && head_dim == kD && num_q_heads == kGroup * num_kv_heads &&
-         num_seqs <= Layout<false>::kMaxSeqs &&
+  if (num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return false;
+  const int group = num_q_heads / num_kv_heads;
+  return (q_len == 1 || q_len == 16) && (group & (group - 1)) == 0 && group <= 16 && q_len * group <= kRows &&
+         head_dim == kD && num_seqs <= Layout<false>::kMaxSeqs &&
          (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128) &&
          part_tokens % kTileKeys == 0 && part_tokens % block_size == 0;
 }
@@ -837,8 +848,11 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   const int B = a.num_seqs;
   const int box_rows = a.block_size < kTileKeys ? a.block_size : kTileKeys;
   CUtensorMap tmq, tmk, tmv;
-  // q viewed as [B*16][Hq][128]: box = 64 columns x 8 heads x 16 tokens
-  if (!make_tensor_map_3d(&tmq, a.q, kD, a.num_q_heads, static_cast<long long>(B) * kQLen, 64, kGroup, kQLen) ||
+  const int group = a.num_q_heads / a.num_kv_heads;
+  int lg = 0;
+  while ((1 << lg) < group) ++lg;
+  // q viewed as [B*q_len][Hq][128]: box = 64 columns x G heads x q_len tokens
+  if (!make_tensor_map_3d(&tmq, a.q, kD, a.num_q_heads, static_cast<long long>(B) * a.q_len, 64, group, a.q_len) ||
       !make_tensor_map_2d(&tmk, a.k_cache, kD, a.rows, 64, box_rows) ||
       !make_tensor_map_2d(&tmv, a.v_cache, kD, a.rows, 64, box_rows))
     return PKV_ERR_CUDA;
@@ -857,7 +871,8 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.part_tokens = a.part_tokens;
   p.max_parts = a.max_parts;
   p.oob_row = static_cast<int>(a.rows);
-  p.lg_group = 3;
+  p.lg_group = lg;
+  p.q_len = a.q_len;
   p.scale_log2 = kernel_scale_log2(a.scale);
   return launch_tc<false>(tmq, tmk, tmv, p, a.block_size, stream);
 }

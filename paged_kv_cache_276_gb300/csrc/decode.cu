@@ -537,6 +537,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_
 }
 
 // ------------------------------------------------------------------ host
+// Single-token decodes go to the tensor-core kernel only when the caller's
+// bound on the sequence length is at least this: its persistent CTAs pay a
+// fixed cost at the end of every (sequence, KV head) run (the accumulators
+// are read before the next run may write them), which long runs amortise and
+// short ones do not.  Measured: 16 x 32768 tokens, block 16: 0.85 -> 0.91 of
+// the copy bandwidth; 32 sequences of up to 4096: 0.72 -> 0.62.
+constexpr int kTcDecodeMinLen = 16384;
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -740,7 +747,8 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   }
 
   cudaStream_t st = as_stream(stream);
-  if (chunk_tc_supported(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, plan.part_tokens)) {
+  if (chunk_tc_supported(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, plan.part_tokens) &&
+      (q_len > 1 || max_seq_len >= kTcDecodeMinLen)) {
     ChunkTcArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -752,6 +760,7 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
     a.ws_ml = plan.ws_bytes() ? static_cast<char *>(workspace) + plan.ws_o_bytes : nullptr;
     a.status = d_status;
     a.num_seqs = num_seqs;
+    a.q_len = q_len;
     a.max_blocks = max_blocks_per_seq;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;

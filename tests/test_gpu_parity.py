@@ -322,6 +322,28 @@ def test_chunk_tensor_core_path_matches_oracle(bs, lens, partition):
     assert_attention_close(out, ref, "tcgen05 chunk")
 
 
+@pytest.mark.parametrize("bs,Hq,Hkv,lens,partition", [
+    (16, 32, 8, [3000, 1, 0, 700, 64, 65, 2049], 512),     # G = 4, empty and one-token sequences
+    (32, 64, 8, [5000, 17, 1300], 0),                      # G = 8, the default partition
+    (64, 16, 16, [900, 4100, 63], 256),                    # G = 1
+    (128, 32, 2, [2500, 129, 40], 384),                    # G = 16, blocks of 128
+])
+def test_single_token_decode_on_tensor_cores(bs, Hq, Hkv, lens, partition):
+    """A bound of 16384 on the lengths sends single-token decodes (head dim 128)
+    to the tcgen05 kernel, G valid rows of a 128-row tile; the warp-MMA kernel
+    (a smaller bound) must agree with it and both with the oracle."""
+    d = 128
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=41 + bs + Hq)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    tc = run_decode(q, kc, vc, tables, lens, scale, partition, max_len=16384, status=st)
+    assert st.item() == 0
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale)
+    assert_attention_close(tc, ref, "tcgen05 single-token decode")
+    mma = run_decode(q, kc, vc, tables, lens, scale, partition)
+    assert torch.allclose(tc.float(), mma.float(), atol=1e-2, rtol=1e-2)
+
+
 def test_chunk_tensor_core_rescales_running_max():
     """Keys grow in magnitude block by block, so the running max keeps moving (rescale path)."""
     d, bs, Hq, Hkv = 128, 16, 16, 2
