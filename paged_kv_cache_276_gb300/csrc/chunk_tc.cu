@@ -142,7 +142,9 @@ struct ItemWalker {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Decode chunk: CTA c takes items [range_first(c), range_first(c + 1)).
+// Decode chunk: CTA c takes items [range_first(c), range_first(c + 1)): equal
+// item counts.  (Equal 64-key tile counts were measured slower: the per-run
+// cost at the end of every (sequence, KV head) run weighs as much as tiles.)
 __device__ __forceinline__ int range_first(unsigned c, int total) {
   return static_cast<int>((static_cast<long long>(c) * total + gridDim.x - 1) / gridDim.x);
 }
@@ -730,23 +732,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < kD / 32; ++ch) {
           float ov[32];
-          uint32_t tmp[32];
-          if (use_a) {
-            tc::ld32(tmem + lane_off + ch * 32, tmp);
-            tc::wait_ld();
+          uint32_t ta[32], tb[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = fa != 0.f ? fa * __uint_as_float(tmp[c]) : 0.f;
-          } else {
+          for (int c = 0; c < 32; ++c) ta[c] = tb[c] = 0u;
+          // both sets' columns of this chunk in flight together, one wait
+          if (use_a) tc::ld32(tmem + lane_off + ch * 32, ta);
+          if (use_b) tc::ld32(tmem + kD + lane_off + ch * 32, tb);
+          if (use_a || use_b) tc::wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = 0.f;
-          }
-          if (use_b) {
-            tc::ld32(tmem + kD + lane_off + ch * 32, tmp);
-            tc::wait_ld();
-            if (fb != 0.f)
-#pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] += fb * __uint_as_float(tmp[c]);
-          }
+          for (int c = 0; c < 32; ++c)
+            ov[c] = (fa != 0.f ? fa * __uint_as_float(ta[c]) : 0.f) + (fb != 0.f ? fb * __uint_as_float(tb[c]) : 0.f);
           if (!row_valid) continue;  // a spare row of the tile: nothing to store
           if (nparts == 1) {
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
