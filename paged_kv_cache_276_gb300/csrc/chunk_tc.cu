@@ -2,11 +2,12 @@
 // of a decode step, and prompt chunks of any length (chunked prefill).
 //
 // For one KV head, a query tile of 128 rows holds 128 / G tokens x the G query
-// heads of the group (row r = token r / G, head r % G).  Over each 64-key tile
-// of the paged cache:
-//     S  = Q K^T                     tcgen05.mma, M 128 x N 64 x K 128 -> TMEM
-//     P  = exp2(S * scale*log2e - m)  softmax warps, one query row per thread
-//     O += P V                       tcgen05.mma, M 128 x N 128 x K 64 -> TMEM
+// heads of the group (row r = token r / G, head r % G).  Over each 128-key
+// tile of the paged cache:
+//     S  = Q K^T                     tcgen05.mma, M 128 x N 128 x K 128 -> TMEM
+//     P  = exp2(S * scale*log2e - m)  softmax warps, one query row per thread,
+//                                    bf16, stored over the scores in TMEM
+//     O += P V                       tcgen05.mma, M 128 x N 128 x K 128 -> TMEM
 // with the running max / sum of online softmax (x321.org "The serving
 // bottleneck is not just FLOPs", section "First understand what the KV cache
 // is storing"; the causal chunk and chunked prefill follow the same page's
@@ -55,11 +56,9 @@ namespace {
 
 constexpr int kD = 128;          // head dim
 constexpr int kRows = 128;       // query rows per tile (tokens x group heads)
-constexpr int kTileKeys = 64;    // keys per MMA tile
 constexpr int kMaxStages = 5;    // K/V ring (at most)
 constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
-constexpr int kKVBytes = kTileKeys * kD * 2;     // 16 KiB each for K and V: [half][64 rows][128 B]
-constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), S: 2 x 64, P: 2 x 32
+constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), then the S (and P) buffers
 constexpr int kKWarp = 8, kMmaWarp = 9, kPvWarp = 10, kVWarp = 11;
 constexpr int kThreads = 12 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -74,15 +73,25 @@ enum : int {
   B_V_EMPTY0 = B_V_FULL0 + kMaxStages, B_COUNT = B_V_EMPTY0 + kMaxStages
 };
 
-// Shared-memory plan of each schedule: two query tiles, then a ring of key
-// tiles and a ring of value tiles (kStages each).  A key stage is released as
-// soon as its score product completes, a value stage after its P V product,
-// so the keys can be fetched further ahead than the values.  The second
-// query tile lets the producer load the next run's queries, and then its
-// keys, while the current run is still in flight.
+// Tiles and shared-memory plan of each schedule.
+//  * prefill (compute-bound): 128-key tiles.  S = Q K^T is one N = 128 product
+//    per 16 head dims, and P V one K = 128 product; a set writes its weights P
+//    over its own S buffer, so a score product waits for the set's previous
+//    P V product (which reads that P).  Two key and two value stages.
+//  * decode chunk (bandwidth-bound): 64-key tiles, 4 key and 4 value stages,
+//    and P in its own buffers, so the score products run ahead of the P V
+//    products: finer, deeper rings keep more copies in flight.
+// Both keep two query tiles, then a ring of key tiles and a ring of value
+// tiles.  A key stage is released as soon as its score product completes, a
+// value stage after its P V product, so the keys can be fetched further ahead
+// than the values.  The second query tile lets the producer load the next
+// run's queries, and then its keys, while the current run is still in flight.
 template <bool kPrefill>
 struct Layout {
-  static constexpr int kStages = 4;
+  static constexpr int kTK = kPrefill ? 128 : 64;   // keys per tile
+  static constexpr bool kPOverS = kPrefill;         // P stored over its S buffer
+  static constexpr int kKVBytes = kTK * kD * 2;     // one key (or value) tile: [half][kTK rows][128 B]
+  static constexpr int kStages = kPrefill ? 2 : 4;
   static constexpr int kQBufs = 2;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
   static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
@@ -91,6 +100,12 @@ struct Layout {
   static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
   static constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
   static constexpr int kSmemSeq = kSmemBars + B_COUNT * 8 + 16;  // after the TMEM slot and the abort flag
+  // tensor memory: O accumulators at 0 and 128, S buffers at 256 (+kTK), P
+  // buffers (when not over S) after the S buffers
+  static constexpr int kTmemS = 2 * kD;
+  static constexpr int kTmemP = kPOverS ? kTmemS : kTmemS + 2 * kTK;
+  static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
+  static_assert(kTmemP + kPStride + kTK / 2 <= kTmemCols, "tensor memory");
   static constexpr size_t bytes(int num_seqs) {
     return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 1) * 4;
   }
@@ -143,7 +158,7 @@ struct ItemWalker {
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Decode chunk: CTA c takes items [range_first(c), range_first(c + 1)): equal
-// item counts.  (Equal 64-key tile counts were measured slower: the per-run
+// item counts.  (Equal key-tile counts were measured slower: the per-run
 // cost at the end of every (sequence, KV head) run weighs as much as tiles.)
 __device__ __forceinline__ int range_first(unsigned c, int total) {
   return static_cast<int>((static_cast<long long>(c) * total + gridDim.x - 1) / gridDim.x);
@@ -226,6 +241,53 @@ struct Sched {
   }
 };
 
+// The largest (smallest, for a negative scale) of 64 raw scores: eight short
+// chains of 3-input maxima.
+__device__ __forceinline__ float extreme64(const uint32_t (&v)[64], bool neg) {
+  float e[8];
+  if (!neg) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = fmax3(__uint_as_float(v[q]), __uint_as_float(v[q + 8]), __uint_as_float(v[q + 16]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = fmax3(e[q], __uint_as_float(v[q + 24]), __uint_as_float(v[q + 32]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = fmax3(e[q], __uint_as_float(v[q + 40]), __uint_as_float(v[q + 48]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) e[q] = fmaxf(e[q], __uint_as_float(v[q + 56]));
+    return fmax3(fmax3(e[0], e[1], e[2]), fmax3(e[3], e[4], e[5]), fmaxf(e[6], e[7]));
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) e[q] = fmin3(__uint_as_float(v[q]), __uint_as_float(v[q + 8]), __uint_as_float(v[q + 16]));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) e[q] = fmin3(e[q], __uint_as_float(v[q + 24]), __uint_as_float(v[q + 32]));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) e[q] = fmin3(e[q], __uint_as_float(v[q + 40]), __uint_as_float(v[q + 48]));
+#pragma unroll
+  for (int q = 0; q < 8; ++q) e[q] = fminf(e[q], __uint_as_float(v[q + 56]));
+  return fmin3(fmin3(e[0], e[1], e[2]), fmin3(e[3], e[4], e[5]), fminf(e[6], e[7]));
+}
+
+// Weights of 64 raw scores, p = 2^(s * scale * log2e - m), two at a time with a
+// packed fp32 FMA, packed to bf16 pairs; returns the sum of the rounded
+// weights (the P V product uses the same rounded values).  Masked keys hold
+// -inf (or +inf for a negative scale): their weight is 2^-inf = 0.
+__device__ __forceinline__ float weights64(const uint32_t (&v)[64], uint64_t ks2, uint64_t nm2, uint32_t (&pk)[32]) {
+  uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    float x0, x1;
+    f32x2_split(ffma2(f32x2_bits(v[2 * c], v[2 * c + 1]), ks2, nm2), x0, x1);
+    pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+    ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
+  }
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f32x2_split(ls[0], a0, a1);
+  f32x2_split(ls[1], b0, b1);
+  f32x2_split(ls[2], c0, c1);
+  f32x2_split(ls[3], d0, d1);
+  return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+}
+
 // Bounded wait whose outcome every lane of the warp agrees on; try_wait
 // parks the warp until the phase completes (or a short hardware window ends).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
@@ -238,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const TcParams p) {
   using Lay = Layout<kPrefill>;
-  constexpr int kStages = Lay::kStages, kQBufs = Lay::kQBufs;
-  // one TMA box per block of the tile (a 128-token block: the tile's half of it)
+  constexpr int kStages = Lay::kStages, kQBufs = Lay::kQBufs, kTileKeys = Lay::kTK, kKVBytes = Lay::kKVBytes;
+  // one TMA box per block of the tile (a block longer than the tile: the tile's piece of it)
   constexpr int kBoxRows = BS < kTileKeys ? BS : kTileKeys;
   constexpr int kBoxes = kTileKeys / kBoxRows;
   extern __shared__ uint8_t smem_raw[];
@@ -349,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int I = prefix[B];
   const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + Lay::kSmemK), sV = smem_u32(smem + Lay::kSmemV);
-  const uint32_t tS0 = tmem + 2 * kD;        // S buffers after the two accumulators
-  const uint32_t tP0 = tS0 + 2 * kTileKeys;  // P (bf16 pairs per column) after the S buffers
+  const uint32_t tS0 = tmem + Lay::kTmemS;  // S buffers after the two accumulators
+  const uint32_t tP0 = tmem + Lay::kTmemP;  // P buffers: over the S buffers (prefill) or after them
   const bool has_work = kPrefill ? static_cast<int>(blockIdx.x) < I
                                  : range_first(blockIdx.x, I) < range_first(blockIdx.x + 1, I);
 
@@ -437,9 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------- S = Q K^T issuer
-      // The score products run ahead of the P V products as far as their two
-      // buffers allow: each waits only for its key stage and for the softmax
-      // to have read the buffer's previous tile, and releases the key stage
+      // A score product waits for its key stage and for its S buffer: in
+      // prefill the buffer holds the set's previous P until that tile's P V
+      // product completes; in the decode chunk it is free once the softmax has
+      // read it, so the score products run ahead.  Each releases its key stage
       // when it completes.  The waits are plain try_wait loops (woken on
       // completion), so each issue follows its event closely.
       if (lane == 0) {
@@ -462,7 +525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < ntile; ++t, ++g) {
             const int s = g % kStages, sb = g & 1;
             if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            if (g >= 2 && !mbar_wait(bar(B_S_FREE0 + sb), ((g >> 1) - 1) & 1)) { ok = false; break; }
+            // prefill: the buffer holds the set's previous P until its P V product
+            // completes; decode chunk: the softmax has read the buffer's last scores
+            if (g >= 2 && !mbar_wait(bar((Lay::kPOverS ? B_PV_DONE0 : B_S_FREE0) + sb), ((g >> 1) - 1) & 1)) {
+              ok = false;
+              break;
+            }
             tc::fence_after();
             const uint32_t kb = sK + s * kKVBytes;
 #pragma unroll
@@ -505,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the first products of run j overwrite the accumulators: run j-1's epilogue must have read them
             if (first && tpieces > 1 && !mbar_wait(bar(B_O_FREE), (tpieces - 2) & 1)) { ok = false; break; }
             tc::fence_after();
-            const uint32_t pa = tP0 + pb * (kTileKeys / 2);
+            const uint32_t pa = tP0 + pb * Lay::kPStride;
             const uint32_t vb = sV + (g % kStages) * kKVBytes;
 #pragma unroll
             for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
@@ -570,66 +638,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar(B_S_FULL0 + sb), (g >> 1) & 1)) { ok = false; break; }
           const int k0 = x.k_lo + t * kTileKeys;
           const int vis = min(limit, x.k_hi) - k0;  // keys of this tile the row sees
-          uint32_t pk[kTileKeys / 2];                 // P row: two bf16 per tensor-memory column
+          const uint32_t tSb = tS0 + sb * kTileKeys + lane_off;      // this row's scores
+          const uint32_t tPb = tP0 + sb * Lay::kPStride + lane_off;  // this row's weights
+          // no row of this warp sees a key of the tile (rows past a short
+          // chunk's end): its weights are zero and nothing else changes
+          const bool skip = __all_sync(0xffffffffu, vis <= 0);
+          const bool partial = !__all_sync(0xffffffffu, vis >= kTileKeys);
+          // a negative scale turns the largest score into the smallest: take minima then
+          const bool neg = p.scale_log2 < 0.f;
+          const uint32_t masked = __float_as_uint(neg ? INFINITY : -INFINITY);
           bool scale_o = false;
           float alpha = 1.f;
-          if (__all_sync(0xffffffffu, vis <= 0)) {
-            // no row of this warp sees a key of the tile (rows past a short
-            // chunk's end): its weights are zero and nothing else changes
-            mbar_arrive(bar(B_S_FREE0 + sb));
-#pragma unroll
-            for (int c = 0; c < kTileKeys / 2; ++c) pk[c] = 0u;
-          } else {
-            tc::fence_after();
-            uint32_t sv[kTileKeys];
-            tc::ld32(tS0 + sb * kTileKeys + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tc::ld32(tS0 + sb * kTileKeys + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            tc::wait_ld();
-            tc::fence_before();
-            mbar_arrive(bar(B_S_FREE0 + sb));
-            // a negative scale turns the largest score into the smallest: take minima then
-            const bool neg = p.scale_log2 < 0.f;
-            const uint32_t masked = __float_as_uint(neg ? INFINITY : -INFINITY);
-            if (!__all_sync(0xffffffffu, vis >= kTileKeys)) {
-#pragma unroll
-              for (int c = 0; c < kTileKeys; ++c)
-                if (c >= vis) sv[c] = masked;
-            }
-            // the extreme raw score (its product with the scale is the largest
-            // scaled score): eight short chains of 3-input maxima (minima)
-            float rm;
-            if (!neg) {
-              float mx[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mx[q] = fmax3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mx[q] = fmax3(mx[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], __uint_as_float(sv[q + 56]));
-              rm = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            } else {
-              float mn[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mn[q] = fmin3(__uint_as_float(sv[q]), __uint_as_float(sv[q + 8]), __uint_as_float(sv[q + 16]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 24]), __uint_as_float(sv[q + 32]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                mn[q] = fmin3(mn[q], __uint_as_float(sv[q + 40]), __uint_as_float(sv[q + 48]));
-#pragma unroll
-              for (int q = 0; q < 8; ++q) mn[q] = fminf(mn[q], __uint_as_float(sv[q + 56]));
-              rm = fmin3(fmin3(mn[0], mn[1], mn[2]), fmin3(mn[3], mn[4], mn[5]), fminf(mn[6], mn[7]));
-            }
+          // move the reference max only when a score passes it by more than
+          // kSlack (rare after a set's first tile); exact, since O and l share
+          // it.  rm is the extreme raw score (times the scale: the largest scaled
+          // score).  Returns the reference to subtract.
+          auto new_reference = [&](float rm) {
             const float bm = rm * p.scale_log2;
-            // move the reference max only when a score passes it by more than
-            // kSlack (rare after a set's first tile); exact, since O and l share it
             const bool move = bm > m + kSlack;
             scale_o = move && !first_tile_of_set && m != -INFINITY;
             alpha = scale_o ? fast_exp2(m - bm) : 1.f;
@@ -637,45 +662,98 @@ __global__ void __launch_bounds__(kThreads, 1)
               l = m == -INFINITY ? 0.f : l * exp2f(m - bm);
               m = bm;
             }
-            const float msub = m == -INFINITY ? 0.f : m;
-            const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
-            const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
-            uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
+            return m == -INFINITY ? 0.f : m;
+          };
+          auto mask = [&](uint32_t(&sv)[64], int c0) {
+            if (partial) {
 #pragma unroll
-            for (int c = 0; c < kTileKeys / 2; ++c) {  // p = 2^(s * scale * log2e - m); masked keys give 2^-inf
-              float x0, x1;
-              f32x2_split(ffma2(f32x2_bits(sv[2 * c], sv[2 * c + 1]), ks2, nm2), x0, x1);
-              pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-              // the running sum uses the same rounded weights as the P V product
-              ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
+              for (int c = 0; c < 64; ++c)
+                if (c0 + c >= vis) sv[c] = masked;
             }
-            {
-              float a0, a1, b0, b1, c0, c1, d0, d1;
-              f32x2_split(ls[0], a0, a1);
-              f32x2_split(ls[1], b0, b1);
-              f32x2_split(ls[2], c0, c1);
-              f32x2_split(ls[3], d0, d1);
-              l += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
-            }
-          }
-          // this set's previous tile (g - 2) must be in the accumulator before a
-          // rescale, and its P buffer free before the new P is written; the
-          // weights above were computed while that product ran
-          if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
-          if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
-            tc::fence_after();
+          };
+          auto rescale_o = [&]() {
+            if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
 #pragma unroll
-            for (int ch = 0; ch < kD / 32; ++ch) {
-              uint32_t ov[32];
-              tc::ld32(tO + lane_off + ch * 32, ov);
+              for (int ch = 0; ch < kD / 32; ++ch) {
+                uint32_t ov[32];
+                tc::ld32(tO + lane_off + ch * 32, ov);
+                tc::wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                tc::st32(tO + lane_off + ch * 32, ov);
+              }
+            }
+          };
+          tc::fence_after();
+          if constexpr (Lay::kPOverS) {
+            if (skip) {
+              uint32_t z[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) z[c] = 0u;
+#pragma unroll
+              for (int hh = 0; hh < kTileKeys / 64; ++hh) tc::st32(tPb + hh * 32, z);
+            } else {
+              uint32_t sv[64];
+              // pass 1: the row's extreme raw score, 64 columns at a time
+              float rm = neg ? INFINITY : -INFINITY;
+#pragma unroll
+              for (int hh = 0; hh < kTileKeys / 64; ++hh) {
+                tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tc::wait_ld();
+                mask(sv, hh * 64);
+                const float e = extreme64(sv, neg);
+                rm = neg ? fminf(rm, e) : fmaxf(rm, e);
+              }
+              const float msub = new_reference(rm);
+              const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+              const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
+              // pass 2: the weights, 64 keys at a time, stored over score columns
+              // already read (keys 0-63 -> columns 0-31, keys 64-127 -> 32-63)
+              float lsum = 0.f;
+#pragma unroll
+              for (int hh = 0; hh < kTileKeys / 64; ++hh) {
+                tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tc::wait_ld();
+                mask(sv, hh * 64);
+                uint32_t pk[32];
+                lsum += weights64(sv, ks2, nm2, pk);
+                tc::st32(tPb + hh * 32, pk);
+              }
+              l += lsum;
+            }
+            // the set's previous P V product completed before this tile's score
+            // product was issued (the score product waited for it): the
+            // accumulator can be rescaled now
+            rescale_o();
+          } else {
+            uint32_t pk[32];
+            if (skip) {
+              mbar_arrive(bar(B_S_FREE0 + sb));
+#pragma unroll
+              for (int c = 0; c < 32; ++c) pk[c] = 0u;
+            } else {
+              uint32_t sv[64];
+              tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+              tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
               tc::wait_ld();
-#pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-              tc::st32(tO + lane_off + ch * 32, ov);
+              tc::fence_before();
+              mbar_arrive(bar(B_S_FREE0 + sb));  // the next score product may overwrite the buffer
+              mask(sv, 0);
+              const float msub = new_reference(extreme64(sv, neg));
+              const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+              const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
+              l += weights64(sv, ks2, nm2, pk);
             }
-            tc::wait_st();
+            // this set's previous tile (g - 2) must be in the accumulator before a
+            // rescale, and its P buffer free before the new P is written; the
+            // weights above were computed while that product ran
+            if (g >= 2 && !wait_warp(bar(B_PV_DONE0 + sb), ((g - 2) >> 1) & 1)) { ok = false; break; }
+            tc::fence_after();
+            rescale_o();
+            tc::st32(tPb, pk);
           }
-          tc::st32(tP0 + sb * (kTileKeys / 2) + lane_off, pk);
           tc::wait_st();
           // value rows past the sequence end were never written: zero them
           const int exist = L - k0;
@@ -836,12 +914,12 @@ bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_hea
   return (q_len == 1 || q_len == 16) && (group & (group - 1)) == 0 && group <= 16 && q_len * group <= kRows &&
          head_dim == kD && num_seqs <= Layout<false>::kMaxSeqs &&
          (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128) &&
-         part_tokens % kTileKeys == 0 && part_tokens % block_size == 0;
+         part_tokens % Layout<false>::kTK == 0 && part_tokens % block_size == 0;
 }
 
 int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   const int B = a.num_seqs;
-  const int box_rows = a.block_size < kTileKeys ? a.block_size : kTileKeys;
+  const int box_rows = a.block_size < Layout<false>::kTK ? a.block_size : Layout<false>::kTK;
   CUtensorMap tmq, tmk, tmv;
   const int group = a.num_q_heads / a.num_kv_heads;
   int lg = 0;
@@ -904,7 +982,7 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
 
   const int tile_tok = kRows / group;
-  const int box_rows = block_size < kTileKeys ? block_size : kTileKeys;
+  const int box_rows = block_size < Layout<true>::kTK ? block_size : Layout<true>::kTK;
   CUtensorMap tmq, tmk, tmv;
   // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x 128 / G tokens
   if (!make_tensor_map_3d(&tmq, q, kD, num_q_heads, total_q, 64, group, tile_tok) ||

@@ -306,9 +306,11 @@ def test_chunked_causal_query_matches_oracle(d, bs, Hq, Hkv, lens, partition):
 @pytest.mark.parametrize("bs,lens,partition", [
     (16, [16, 17, 40, 600, 64, 65, 1000], 512),
     (32, [1000, 31, 2048, 3], 128),
-    (16, [0, 5, 15, 16, 200, 0, 130], 64),         # empty and shorter-than-chunk sequences
+    (16, [0, 5, 15, 16, 200, 0, 130], 128),        # empty and shorter-than-chunk sequences
     (16, [int(x) for x in np.random.default_rng(4).integers(1, 3000, size=40)], 256),  # many runs per CTA
-    (32, [4096, 4096, 100, 7], 64),
+    (32, [4096, 4096, 100, 7], 128),
+    (64, [3000, 129, 1], 384),
+    (128, [2500, 700, 128, 127], 256),
 ])
 def test_chunk_tensor_core_path_matches_oracle(bs, lens, partition):
     """16-token causal chunk with 8 query heads per KV head and head dim 128: the tcgen05 kernel."""
@@ -363,7 +365,7 @@ def test_chunk_tensor_core_and_warp_mma_paths_agree():
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=5, q_len=16)
     scale = float(np.float32(1 / math.sqrt(d)))
     a = run_decode(q, kc, vc, tables, lens, scale, 512).float()   # tcgen05
-    b = run_decode(q, kc, vc, tables, lens, scale, 496).float()   # not a multiple of 64: warp MMA
+    b = run_decode(q, kc, vc, tables, lens, scale, 496).float()   # not a multiple of 128: warp MMA
     assert torch.allclose(a, b, atol=1e-2, rtol=1e-2)
 
 

@@ -97,18 +97,22 @@ def test_prefill_many_items_per_cta():
         assert torch.equal(again.view(torch.int16), out.view(torch.int16))
 
 
-def test_prefill_of_uniform_16_token_chunks_equals_the_decode_chunk_bit_for_bit():
-    """With one partition per sequence the decode chunk and prefill run the
-    same tiles in the same order on the same tensor-core pipeline."""
+def test_prefill_of_uniform_16_token_chunks_matches_the_decode_chunk():
+    """The same 16-token causal chunks through both tensor-core schedules (the
+    decode chunk on 64-key tiles with one partition per sequence, prefill on
+    128-key tiles) agree within the attention tolerance, and with the oracle."""
     lens = [900, 40, 2500, 16]
     Hq, Hkv, bs, d = 64, 8, 16, 128
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=31, q_len=16)
     scale = float(np.float32(1 / math.sqrt(d)))
-    part = 64 * math.ceil(max(lens) / 64)
+    part = 128 * math.ceil(max(lens) / 128)
     dec = run_decode(q, kc, vc, tables, lens, scale, part)
     q_start = np.arange(len(lens) + 1, dtype=np.int32) * 16
     pre = run_prefill(q.reshape(-1, Hq, d), kc, vc, tables, lens, q_start, scale)
-    assert torch.equal(dec.reshape(-1, Hq, d).view(torch.int16), pre.view(torch.int16))
+    ref = oracle_prefill(q.reshape(-1, Hq, d), kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(pre, ref, "prefill")
+    assert_attention_close(dec.reshape(-1, Hq, d), ref, "decode chunk")
+    assert torch.allclose(dec.reshape(-1, Hq, d).float(), pre.float(), atol=1e-2, rtol=1e-2)
 
 
 def test_prefill_rescales_running_max():
