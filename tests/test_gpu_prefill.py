@@ -254,3 +254,37 @@ def test_prefill_workloads_sampled(tag):
                                      np.array([n], dtype=np.int32), num_q_heads=case.Hq, num_kv_heads=case.Hkv,
                                      head_dim=case.d, block_size=case.bs, scale=case.scale)
             assert_attention_close(out[row:row + 1], ref[0], f"{tag} seq {i} row {r}")
+
+
+def test_prefill_at_the_sequence_limit():
+    """1024 sequences (the most one prefill call takes): the per-sequence
+    tables fill the kernel's shared memory and every lane of the setup warp
+    scans 32 sequences."""
+    rng = np.random.default_rng(44)
+    B = 1024
+    lens = [int(x) for x in rng.integers(1, 90, size=B)]
+    chunks = [int(min(L, c)) for L, c in zip(lens, rng.integers(0, 40, size=B))]
+    Hq, Hkv, bs = 16, 2, 16
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=44)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    st = status_tensor()
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale, status=st)
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, "prefill, 1024 sequences")
+
+
+def test_tensor_core_decode_chunk_at_the_sequence_limit():
+    """2048 sequences (the most the tensor-core decode chunk takes) of short
+    16-token chunks, 8 query heads per KV head."""
+    rng = np.random.default_rng(45)
+    lens = [int(x) for x in rng.integers(0, 200, size=2048)]
+    Hq, Hkv, bs, d = 8, 1, 16, 128
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=45, q_len=16)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_decode(q, kc, vc, tables, lens, scale, 128, status=st)
+    assert st.item() == 0
+    ref = OA.paged_attention(bits(q), bits(kc), bits(vc), tables, np.asarray(lens, dtype=np.int32), num_q_heads=Hq,
+                             num_kv_heads=Hkv, head_dim=d, block_size=bs, scale=scale, q_len=16)
+    assert_attention_close(out, ref, "decode chunk, 2048 sequences")
