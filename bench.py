@@ -301,47 +301,59 @@ class Runner:
 
     def time_e2e(self, steps):
         """Same metric through the public API with host buffers: allocator work,
-        pinned host -> device copies of the step inputs, the kernels, and the
-        device -> host read of the outputs, all inside the timed region."""
+        the host -> device copy of the step inputs, the kernels, and the
+        device -> host read of the outputs, all inside the timed region.
+
+        The step's inputs (queries, new keys and values, slots, block tables,
+        lengths) live in one page-locked staging buffer that the allocator
+        fills in place and that goes to the device in one copy; the kernels
+        read views of its device twin."""
         torch = self.torch
         from paged_kv_cache_276_gb300 import native
         sess = self.sess
         toks = sess.new_token_tensors(1, seed=self.w.seed + 5)
-        q_h = toks[0][0].cpu().pin_memory()
-        k_h = [t.cpu().pin_memory() for t in toks[0][1]]
-        v_h = [t.cpu().pin_memory() for t in toks[0][2]]
-        q_d = torch.empty_like(toks[0][0])
-        k_d = [torch.empty_like(t) for t in toks[0][1]]
-        v_d = [torch.empty_like(t) for t in toks[0][2]]
-        out_d = torch.empty_like(q_d)
+        parts = [("q", toks[0][0].shape, torch.bfloat16)]
+        parts += [(f"k{l}", t.shape, torch.bfloat16) for l, t in enumerate(toks[0][1])]
+        parts += [(f"v{l}", t.shape, torch.bfloat16) for l, t in enumerate(toks[0][2])]
+        parts += [("slots", (sess.B * sess.q_len,), torch.int64), ("tables", (sess.B, sess.max_blocks), torch.int32),
+                  ("lens", (sess.B,), torch.int32)]
+        offs, total = {}, 0
+        for name, shape, dt in parts:  # 256-byte aligned segments
+            offs[name] = total
+            total += -(-int(np.prod(shape)) * torch.empty((), dtype=dt).element_size() // 256) * 256
+        stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+        stage_d = torch.empty(total, dtype=torch.uint8, device=self.device)
+
+        def view(buf, name):
+            shape, dt = next((sh, d) for n, sh, d in parts if n == name)
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+            return buf[offs[name]:offs[name] + nbytes].view(dt).view(shape)
+
+        view(stage_h, "q").copy_(toks[0][0].cpu())
+        for l in range(sess.layers):
+            view(stage_h, f"k{l}").copy_(toks[0][1][l].cpu())
+            view(stage_h, f"v{l}").copy_(toks[0][2][l].cpu())
+        q_d = view(stage_d, "q")
+        k_d = [view(stage_d, f"k{l}") for l in range(sess.layers)]
+        v_d = [view(stage_d, f"v{l}") for l in range(sess.layers)]
+        slots_d, tables_d, lens_d = view(stage_d, "slots"), view(stage_d, "tables"), view(stage_d, "lens")
+        slots_np = view(stage_h, "slots").numpy()
+        tables_np = view(stage_h, "tables").numpy()
+        lens_np = view(stage_h, "lens").numpy()
+        out_d = torch.empty_like(toks[0][0])
         out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
         ws = sess.workspace(int(sess.alloc.block_table(range(sess.B), sess.max_blocks)[1].max()) + steps + 8)
         stream = torch.cuda.current_stream()
-        # page-locked staging that the allocator fills in place every step
         seq_ids = np.arange(sess.B, dtype=np.int64)
-        slots_h = torch.empty(sess.B * sess.q_len, dtype=torch.int64).pin_memory()
-        tables_h = torch.empty((sess.B, sess.max_blocks), dtype=torch.int32).pin_memory()
-        lens_h = torch.empty(sess.B, dtype=torch.int32).pin_memory()
-        slots_d = torch.empty(sess.B * sess.q_len, dtype=torch.int64, device=self.device)
-        tables_d = torch.empty((sess.B, sess.max_blocks), dtype=torch.int32, device=self.device)
-        lens_d = torch.empty(sess.B, dtype=torch.int32, device=self.device)
-        slots_np, tables_np, lens_np = slots_h.numpy(), tables_h.numpy(), lens_h.numpy()
-        times, kv, h2d = [], [], 0
+        times, kv = [], []
         for i in range(steps + 1):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-            # host allocator work of the step (public API, one call each), then the uploads
+            # host allocator work of the step (public API, one call each) into the staging buffer
             sess.alloc.seq_append_batch(seq_ids, sess.q_len, out=slots_np)
             sess.alloc.block_table(seq_ids, sess.max_blocks, table_out=tables_np, lens_out=lens_np)
-            slots_d.copy_(slots_h, non_blocking=True)
-            tables_d.copy_(tables_h, non_blocking=True)
-            lens_d.copy_(lens_h, non_blocking=True)
-            lens = lens_np
-            q_d.copy_(q_h, non_blocking=True)
-            for l in range(sess.layers):
-                k_d[l].copy_(k_h[l], non_blocking=True)
-                v_d[l].copy_(v_h[l], non_blocking=True)
-            max_len = int(lens.max())
+            stage_d.copy_(stage_h, non_blocking=True)
+            max_len = int(lens_np.max())
             for l in range(sess.layers):
                 native.pkv_write(k_d[l], v_d[l], slots_d, sess.k_caches[l], sess.v_caches[l], None, stream)
                 native.paged_attention_decode(q_d, sess.k_caches[l], sess.v_caches[l], tables_d, lens_d, max_len,
@@ -351,11 +363,9 @@ class Runner:
             t1 = time.perf_counter()
             if i:  # the first pass warms the pinned-memory paths
                 times.append((t1 - t0) * 1e3)
-                kv.append(int(lens.astype(np.int64).sum()) * 2 * sess.Hkv * sess.d * 2 * sess.layers)
-                h2d = (slots_h.numel() * 8 + tables_h.numel() * 4 + lens_h.numel() * 4 + q_h.numel() * 2
-                       + sum(t.numel() * 2 for t in k_h) + sum(t.numel() * 2 for t in v_h))
+                kv.append(int(lens_np.astype(np.int64).sum()) * 2 * sess.Hkv * sess.d * 2 * sess.layers)
         ms = sum(times) / len(times)
-        return {"ms_per_step": ms, "kv_bytes_per_step": sum(kv) / len(kv), "h2d": h2d,
+        return {"ms_per_step": ms, "kv_bytes_per_step": sum(kv) / len(kv), "h2d": int(total),
                 "d2h": out_h.numel() * 2}
 
 
