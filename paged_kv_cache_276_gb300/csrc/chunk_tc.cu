@@ -2,12 +2,12 @@
 // of a decode step, and prompt chunks of any length (chunked prefill).
 //
 // For one KV head, a query tile of 128 rows holds 128 / G tokens x the G query
-// heads of the group (row r = token r / G, head r % G).  Over each 128-key
-// tile of the paged cache:
-//     S  = Q K^T                     tcgen05.mma, M 128 x N 128 x K 128 -> TMEM
+// heads of the group (row r = token r / G, head r % G).  Over each tile of T
+// keys of the paged cache (T = 128 in prefill, 64 in the decode chunk):
+//     S  = Q K^T                     tcgen05.mma, M 128 x N T x K 128 -> TMEM
 //     P  = exp2(S * scale*log2e - m)  softmax warps, one query row per thread,
-//                                    bf16, stored over the scores in TMEM
-//     O += P V                       tcgen05.mma, M 128 x N 128 x K 128 -> TMEM
+//                                    bf16 in TMEM (prefill: over the scores)
+//     O += P V                       tcgen05.mma, M 128 x N 128 x K T -> TMEM
 // with the running max / sum of online softmax (x321.org "The serving
 // bottleneck is not just FLOPs", section "First understand what the KV cache
 // is storing"; the causal chunk and chunked prefill follow the same page's
@@ -118,9 +118,9 @@ struct TcParams {
   const int32_t *block_tables;
   const int32_t *seq_lens;
   const int32_t *q_start;  // prefill: [B + 1] first query row of each sequence
-  __nv_bfloat16 *out;      // decode chunk: [B][16][Hq][128]; prefill: [total_q][Hq][128]
-  float *ws_o;             // decode chunk: [B * 16 * Hq][P][128]
-  float2 *ws_ml;           // decode chunk: [B * 16 * Hq][P]
+  __nv_bfloat16 *out;      // decode chunk: [B][q_len][Hq][128]; prefill: [total_q][Hq][128]
+  float *ws_o;             // decode chunk: [B * q_len * Hq][P][128]
+  float2 *ws_ml;           // decode chunk: [B * q_len * Hq][P]
   int32_t *status;
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
   int part_tokens, max_parts, oob_row;
@@ -293,7 +293,6 @@ __device__ __forceinline__ float weights64(const uint32_t (&v)[64], uint64_t ks2
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
-
 
 template <int BS, bool kPrefill>
 __global__ void __launch_bounds__(kThreads, 1)
