@@ -466,7 +466,7 @@ def run_ours(args, rank, world, local):
     }
     if not args.no_workloads:
         line["workloads"] = other_workloads(args, device, rank, world, peak)
-        line["prefill"] = prefill_bench(device)
+        line["prefill"] = prefill_bench(device, cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_oracle_baseline(HEADLINE, budget_s=args.cpu_seconds)
@@ -593,7 +593,33 @@ def swap_bench(device):
     return res
 
 
-def prefill_bench(device, steps=10, warmup=3, only=None):
+def prefill_cpu_baseline(case, rows=16, max_seqs=8):
+    """The fp64 oracle as it stands on this host's cores, on a bounded sample of a
+    prefill workload: the last ``rows`` query rows of the chunks of up to
+    ``max_seqs`` sequences (those rows see the most keys), in TFLOP/s of the
+    same algorithmic count as the kernel's."""
+    from oracle import attention as OA
+    seqs = [i for i in range(case.B) if int(case.chunks[i]) >= rows][:max_seqs]
+    if not seqs:
+        return {"error": "no chunk of that many rows"}
+    kb, vb = OA.as_bf16_bits(case.k_cache), OA.as_bf16_bits(case.v_cache)
+    qall = OA.as_bf16_bits(case.q)
+    q = np.stack([qall[int(case.q_start[i]) + int(case.chunks[i]) - rows:int(case.q_start[i]) + int(case.chunks[i])]
+                  for i in seqs])
+    lens = case.lens[seqs]
+    cores = OA.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    OA.paged_attention(q, kb, vb, case.tables[seqs], lens, num_q_heads=case.Hq, num_kv_heads=case.Hkv,
+                       head_dim=case.d, block_size=case.bs, scale=case.scale, q_len=rows)
+    el = time.perf_counter() - t0
+    keys = sum(rows * int(L) - rows * (rows - 1) // 2 for L in lens)
+    fl = 4 * case.d * case.Hq * keys
+    return {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"the last {rows} query rows of {len(seqs)} sequences' chunks ({fl / 1e9:.1f} GFLOP) in "
+                      f"{el:.2f} s, fp64, OpenMP over (sequence, KV head)", "seconds": el}
+
+
+def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False):
     """Chunked prefill (paged_attention_prefill) on the prefill workloads: a
     step is the chunk's pkv_write plus the attention call; the attention call
     is also timed alone (the tensor-core roofline).  2 x L2 is written before
@@ -657,6 +683,14 @@ def prefill_bench(device, steps=10, warmup=3, only=None):
                 "step_tflops": round(fl / (sm * 1e-3) / 1e12, 1),
                 "clocks": clocks.summary(),
             }
+            if cpu:
+                try:
+                    cb = prefill_cpu_baseline(case)
+                    if "value" in cb:
+                        cb["value"] = round(cb["value"], 6)
+                    res[tag]["cpu_baseline"] = cb
+                except Exception as e:  # reported, never fatal
+                    res[tag]["cpu_baseline"] = {"error": repr(e)}
             del case
             torch.cuda.empty_cache()
         except Exception as e:
@@ -730,7 +764,8 @@ def main():
         build.build()
         torch.cuda.set_device(local)
         line = {"prefill": prefill_bench(torch.device("cuda", local), steps=args.steps, warmup=args.warmup,
-                                         only=None if args.prefill == "all" else args.prefill)}
+                                         only=None if args.prefill == "all" else args.prefill,
+                                         cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)}
     elif args.block_sweep:
         import torch
         from paged_kv_cache_276_gb300 import build
