@@ -208,7 +208,7 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
  * q_start[i] + r (r < c) and query head g see keys t < n = L - c + 1 + r of KV
  * head g / (num_q_heads/num_kv_heads); out = sum_t softmax_t(scale * q.k_t) v_t
  * rounded to bf16; n <= 0 gives zeros.
- *   q, out        device, [total_q][num_q_heads][128] bf16
+ *   q, out        device, [total_q][num_q_heads][head_dim] bf16
  *   q_start       device, [num_seqs + 1] int32, never decreasing, within
  *                 [0, total_q] (normally q_start[0] = 0 and q_start[num_seqs] =
  *                 total_q).  A sequence whose pair of entries breaks this sets
@@ -220,8 +220,8 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
  * No workspace: every query tile of 128 / G tokens x G heads
  * (G = num_q_heads / num_kv_heads) is one unit of work over all the keys it
  * sees, on the tensor cores.
- * Supported: head_dim 128; G in {1, 2, 4, 8, 16}; block_size in {16, 32, 64,
- * 128}; num_seqs <= 1024.  Other sizes return PKV_ERR_UNSUPPORTED.
+ * Supported: head_dim in {64, 128}; G in {1, 2, 4, 8, 16}; block_size in {16,
+ * 32, 64, 128}; num_seqs <= 1024.  Other sizes return PKV_ERR_UNSUPPORTED.
  * total_q == 0 or num_seqs == 0 is a no-op.
  */
 int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,

@@ -54,10 +54,8 @@
 namespace pkv {
 namespace {
 
-constexpr int kD = 128;          // head dim
 constexpr int kRows = 128;       // query rows per tile (tokens x group heads)
 constexpr int kMaxStages = 5;    // K/V ring (at most)
-constexpr int kQBytes = kRows * kD * 2;          // 32 KiB: [half][128 rows][128 B]
 constexpr int kTmemCols = 512;   // O: 2 x 128 columns (even / odd tiles), then the S (and P) buffers
 constexpr int kKWarp = 8, kMmaWarp = 9, kPvWarp = 10, kVWarp = 11;
 constexpr int kThreads = 12 * 32;
@@ -86,11 +84,16 @@ enum : int {
 // value stage after its P V product, so the keys can be fetched further ahead
 // than the values.  The second query tile lets the producer load the next
 // run's queries, and then its keys, while the current run is still in flight.
-template <bool kPrefill>
+template <bool kPrefill, int D>
 struct Layout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kHalves = D / 64;           // 64-column (128-byte) halves of a row
+  static constexpr int kQHalf = kRows * 128;       // one half of the query tile
+  static constexpr int kQBytes = kHalves * kQHalf;  // query tile: [half][128 rows][128 B]
   static constexpr int kTK = kPrefill ? 128 : 64;   // keys per tile
   static constexpr bool kPOverS = kPrefill;         // P stored over its S buffer
-  static constexpr int kKVBytes = kTK * kD * 2;     // one key (or value) tile: [half][kTK rows][128 B]
+  static constexpr int kKVHalf = kTK * 128;         // one half of a key (or value) tile
+  static constexpr int kKVBytes = kHalves * kKVHalf;  // key (or value) tile: [half][kTK rows][128 B]
   static constexpr int kStages = kPrefill ? 2 : 4;
   static constexpr int kQBufs = 2;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
@@ -100,9 +103,9 @@ struct Layout {
   static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
   static constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
   static constexpr int kSmemSeq = kSmemBars + B_COUNT * 8 + 16;  // after the TMEM slot and the abort flag
-  // tensor memory: O accumulators at 0 and 128, S buffers at 256 (+kTK), P
+  // tensor memory: O accumulators at 0 and D, S buffers at 2 D (+kTK), P
   // buffers (when not over S) after the S buffers
-  static constexpr int kTmemS = 2 * kD;
+  static constexpr int kTmemS = 2 * D;
   static constexpr int kTmemP = kPOverS ? kTmemS : kTmemS + 2 * kTK;
   static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
   static_assert(kTmemP + kPStride + kTK / 2 <= kTmemCols, "tensor memory");
@@ -110,16 +113,16 @@ struct Layout {
     return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 1) * 4;
   }
 };
-static_assert(Layout<false>::bytes(Layout<false>::kMaxSeqs) <= 227 * 1024, "shared memory");
-static_assert(Layout<true>::bytes(Layout<true>::kMaxSeqs) <= 227 * 1024, "shared memory");
-static_assert(Layout<false>::kStages <= kMaxStages && Layout<true>::kStages <= kMaxStages, "stages");
+static_assert(Layout<false, 128>::bytes(Layout<false, 128>::kMaxSeqs) <= 227 * 1024, "shared memory");
+static_assert(Layout<true, 128>::bytes(Layout<true, 128>::kMaxSeqs) <= 227 * 1024, "shared memory");
+static_assert(Layout<false, 128>::kStages <= kMaxStages && Layout<true, 128>::kStages <= kMaxStages, "stages");
 
 struct TcParams {
   const int32_t *block_tables;
   const int32_t *seq_lens;
   const int32_t *q_start;  // prefill: [B + 1] first query row of each sequence
-  __nv_bfloat16 *out;      // decode chunk: [B][q_len][Hq][128]; prefill: [total_q][Hq][128]
-  float *ws_o;             // decode chunk: [B * q_len * Hq][P][128]
+  __nv_bfloat16 *out;      // decode chunk: [B][q_len][Hq][D]; prefill: [total_q][Hq][D]
+  float *ws_o;             // decode chunk: [B * q_len * Hq][P][D]
   float2 *ws_ml;           // decode chunk: [B * q_len * Hq][P]
   int32_t *status;
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
@@ -294,12 +297,13 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-template <int BS, bool kPrefill>
+template <int BS, bool kPrefill, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const TcParams p) {
-  using Lay = Layout<kPrefill>;
+  using Lay = Layout<kPrefill, D>;
   constexpr int kStages = Lay::kStages, kQBufs = Lay::kQBufs, kTileKeys = Lay::kTK, kKVBytes = Lay::kKVBytes;
+  constexpr int kHalves = Lay::kHalves, kQBytes = Lay::kQBytes;
   // one TMA box per block of the tile (a block longer than the tile: the tile's piece of it)
   constexpr int kBoxRows = BS < kTileKeys ? BS : kTileKeys;
   constexpr int kBoxes = kTileKeys / kBoxRows;
@@ -441,11 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int gsz = 1 << p.lg_group;
             const int qz = kPrefill ? qs[x.seq] + (kRows >> p.lg_group) * x.qt : x.seq * p.q_len;
             // decode chunk: the box holds the q_len * G rows only
-            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kPrefill ? kQBytes : (p.q_len << p.lg_group) * kD * 2);
-            for (int hf = 0; hf < 2; ++hf)
+            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kPrefill ? kQBytes : (p.q_len << p.lg_group) * D * 2);
+            for (int hf = 0; hf < kHalves; ++hf)
               asm volatile(
                   "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + qb * kQBytes + hf * (kQBytes / 2)),
+                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + qb * kQBytes + hf * Lay::kQHalf),
                   "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(hf * 64), "r"(x.head * gsz), "r"(qz),
                   "r"(bar(B_Q_FULL0 + qb))
                   : "memory");
@@ -473,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kBoxes; ++j) bids[j] = __shfl_sync(0xffffffffu, tw_val, blk_first + j - tw_base);
           if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), kKVBytes);
           // one lane per (box, half): the box copies go out in parallel
-          if (lane < kBoxes * 2) {
-            const int j = lane >> 1, hf = lane & 1;
+          if (lane < kBoxes * kHalves) {
+            const int j = lane / kHalves, hf = lane % kHalves;
             const int b = bids[j];
             int row;
             if (blk_first + j < nblk_seq && b >= 0 && b < p.num_blocks) {
@@ -483,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (blk_first + j < nblk_seq && p.status && !is_v && hf == 0) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
               row = p.oob_row;  // past the sequence, or a bad id: zeros
             }
-            tma_load_2d(ring + s * kKVBytes + hf * (kKVBytes / 2) + j * kBoxRows * 128, tm, hf * 64, row,
+            tma_load_2d(ring + s * kKVBytes + hf * Lay::kKVHalf + j * kBoxRows * 128, tm, hf * 64, row,
                         bar(full0 + s), pol);
           }
         }
@@ -533,9 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after();
             const uint32_t kb = sK + s * kKVBytes;
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)
-              tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * (kQBytes / 2) + (ks & 3) * 32, 16, 1024),
-                      tc::desc_sw128(kb + (ks >> 2) * (kKVBytes / 2) + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+              tc::mma(tS0 + sb * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
+                      tc::desc_sw128(kb + (ks >> 2) * Lay::kKVHalf + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
             tc::commit(bar(B_S_FULL0 + sb));
             tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by this product only
             if (x.run_end && t == ntile - 1) tc::commit(bar(B_Q_FREE0 + qb));  // read by MMAs issued so far only
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Each product goes out, in tile order, as soon as its P is written and
       // its values have landed; its value stage is released when it completes.
       if (lane == 0) {
-        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, kD, false, true);
+        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, D, false, true);
         Sched<kPrefill> sc;
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0, run_g0 = 0;
@@ -576,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t vb = sV + (g % kStages) * kKVBytes;
 #pragma unroll
             for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
-              tc::mma_ta(tmem + pb * kD, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, kKVBytes / 2, 1024), kIdO,
+              tc::mma_ta(tmem + pb * D, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
                          !(first && ks == 0));
             tc::commit(bar(B_PV_DONE0 + pb));
             tc::commit(bar(B_V_EMPTY0 + (g % kStages)));
@@ -595,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tok = r >> p.lg_group, gh = r & ((1 << p.lg_group) - 1);
       const int tile_tok = kRows >> p.lg_group;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const uint32_t tO = tmem + set * kD;        // this set's accumulator
+      const uint32_t tO = tmem + set * D;         // this set's accumulator
       float2 *stats = reinterpret_cast<float2 *>(smem + Lay::kSmemStats);
       Sched<kPrefill> sc;
       sc.begin(p, tab, I);
@@ -673,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto rescale_o = [&]() {
             if (__any_sync(0xffffffffu, scale_o)) {  // warp-uniform: tcgen05.ld/st are warp-wide
 #pragma unroll
-              for (int ch = 0; ch < kD / 32; ++ch) {
+              for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t ov[32];
                 tc::ld32(tO + lane_off + ch * 32, ov);
                 tc::wait_ld();
@@ -761,9 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
             const uint32_t vb = sV + s * kKVBytes;
             const int first = exist < 0 ? 0 : exist;
-            for (int e = r; e < (kTileKeys - first) * 2 * 8; e += kRows) {  // 16-byte chunks
-              const int row = first + e / 16, rem = e % 16, hf = rem / 8, c = rem % 8;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + hf * (kKVBytes / 2) + row * 128 + c * 16),
+            for (int e = r; e < (kTileKeys - first) * kHalves * 8; e += kRows) {  // 16-byte chunks
+              const int row = first + e / (kHalves * 8), rem = e % (kHalves * 8), hf = rem / 8, c = rem % 8;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + hf * Lay::kKVHalf + row * 128 + c * 16),
                            "r"(0u)
                            : "memory");
             }
@@ -807,21 +811,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool use_a = __any_sync(0xffffffffu, fa != 0.f), use_b = __any_sync(0xffffffffu, fb != 0.f);
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
-        for (int ch = 0; ch < kD / 32; ++ch) {
+        for (int ch = 0; ch < D / 32; ++ch) {
           float ov[32];
           uint32_t ta[32], tb[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) ta[c] = tb[c] = 0u;
           // both sets' columns of this chunk in flight together, one wait
           if (use_a) tc::ld32(tmem + lane_off + ch * 32, ta);
-          if (use_b) tc::ld32(tmem + kD + lane_off + ch * 32, tb);
+          if (use_b) tc::ld32(tmem + D + lane_off + ch * 32, tb);
           if (use_a || use_b) tc::wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             ov[c] = (fa != 0.f ? fa * __uint_as_float(ta[c]) : 0.f) + (fb != 0.f ? fb * __uint_as_float(tb[c]) : 0.f);
           if (!row_valid) continue;  // a spare row of the tile: nothing to store
           if (nparts == 1) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kD + ch * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + ch * 32);
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
               uint4 v;
@@ -832,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[c8] = v;
             }
           } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + run_first_part) * kD + ch * 32);
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + run_first_part) * D + ch * 32);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
               dst[c4] = make_float4(ov[c4 * 4], ov[c4 * 4 + 1], ov[c4 * 4 + 2], ov[c4 * 4 + 3]);
@@ -862,24 +866,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kPrefill>
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
 
-template <bool kPrefill>
-KernelFn<kPrefill> pick_kernel(int block_size) {
+template <bool kPrefill, int D>
+KernelFn pick_kernel(int block_size) {
   switch (block_size) {
-    case 16: return chunk_tc_kernel<16, kPrefill>;
-    case 32: return chunk_tc_kernel<32, kPrefill>;
-    case 64: return chunk_tc_kernel<64, kPrefill>;
-    default: return chunk_tc_kernel<128, kPrefill>;
+    case 16: return chunk_tc_kernel<16, kPrefill, D>;
+    case 32: return chunk_tc_kernel<32, kPrefill, D>;
+    case 64: return chunk_tc_kernel<64, kPrefill, D>;
+    default: return chunk_tc_kernel<128, kPrefill, D>;
   }
 }
 
-template <bool kPrefill>
-int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
-              int block_size, cudaStream_t stream) {
-  using Lay = Layout<kPrefill>;
-  const KernelFn<kPrefill> kernel = pick_kernel<kPrefill>(block_size);
+template <bool kPrefill, int D>
+int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
+                int block_size, cudaStream_t stream) {
+  using Lay = Layout<kPrefill, D>;
+  const KernelFn kernel = pick_kernel<kPrefill, D>(block_size);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(Lay::bytes(Lay::kMaxSeqs)))) != cudaSuccess)
@@ -899,6 +902,13 @@ int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap 
   return PKV_OK;
 }
 
+template <bool kPrefill>
+int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
+              int block_size, int head_dim, cudaStream_t stream) {
+  return head_dim == 64 ? launch_tc_d<kPrefill, 64>(tmq, tmk, tmv, p, block_size, stream)
+                        : launch_tc_d<kPrefill, 128>(tmq, tmk, tmv, p, block_size, stream);
+}
+
 // The kernels compare raw scores before scaling them; a zero scale would turn
 // the masked -inf scores into NaN, so it runs as the smallest normal float,
 // whose products with finite scores round to the same weights (all 1).
@@ -911,22 +921,23 @@ bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_hea
   if (num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return false;
   const int group = num_q_heads / num_kv_heads;
   return (q_len == 1 || q_len == 16) && (group & (group - 1)) == 0 && group <= 16 && q_len * group <= kRows &&
-         head_dim == kD && num_seqs <= Layout<false>::kMaxSeqs &&
+         (head_dim == 64 || head_dim == 128) && num_seqs <= Layout<false, 128>::kMaxSeqs &&
          (block_size == 16 || block_size == 32 || block_size == 64 || block_size == 128) &&
-         part_tokens % Layout<false>::kTK == 0 && part_tokens % block_size == 0;
+         part_tokens % Layout<false, 128>::kTK == 0 && part_tokens % block_size == 0;
 }
 
 int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   const int B = a.num_seqs;
-  const int box_rows = a.block_size < Layout<false>::kTK ? a.block_size : Layout<false>::kTK;
+  const int box_rows = a.block_size < Layout<false, 128>::kTK ? a.block_size : Layout<false, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
   const int group = a.num_q_heads / a.num_kv_heads;
   int lg = 0;
   while ((1 << lg) < group) ++lg;
   // q viewed as [B*q_len][Hq][128]: box = 64 columns x G heads x q_len tokens
-  if (!make_tensor_map_3d(&tmq, a.q, kD, a.num_q_heads, static_cast<long long>(B) * a.q_len, 64, group, a.q_len) ||
-      !make_tensor_map_2d(&tmk, a.k_cache, kD, a.rows, 64, box_rows) ||
-      !make_tensor_map_2d(&tmv, a.v_cache, kD, a.rows, 64, box_rows))
+  if (!make_tensor_map_3d(&tmq, a.q, a.head_dim, a.num_q_heads, static_cast<long long>(B) * a.q_len, 64, group,
+                          a.q_len) ||
+      !make_tensor_map_2d(&tmk, a.k_cache, a.head_dim, a.rows, 64, box_rows) ||
+      !make_tensor_map_2d(&tmv, a.v_cache, a.head_dim, a.rows, 64, box_rows))
     return PKV_ERR_CUDA;
   TcParams p{};
   p.block_tables = a.block_tables;
@@ -946,7 +957,7 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.lg_group = lg;
   p.q_len = a.q_len;
   p.scale_log2 = kernel_scale_log2(a.scale);
-  return launch_tc<false>(tmq, tmk, tmv, p, a.block_size, stream);
+  return launch_tc<false>(tmq, tmk, tmv, p, a.block_size, a.head_dim, stream);
 }
 
 }  // namespace pkv
@@ -964,9 +975,9 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   const int group = num_q_heads / num_kv_heads;
   int lg = 0;
   while ((1 << lg) < group) ++lg;
-  if (head_dim != kD || (1 << lg) != group || group > 16) return PKV_ERR_UNSUPPORTED;
+  if ((head_dim != 64 && head_dim != 128) || (1 << lg) != group || group > 16) return PKV_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs > Layout<true>::kMaxSeqs) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > Layout<true, 128>::kMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start || !out) return PKV_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
@@ -981,12 +992,12 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
 
   const int tile_tok = kRows / group;
-  const int box_rows = block_size < Layout<true>::kTK ? block_size : Layout<true>::kTK;
+  const int box_rows = block_size < Layout<true, 128>::kTK ? block_size : Layout<true, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
   // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x 128 / G tokens
-  if (!make_tensor_map_3d(&tmq, q, kD, num_q_heads, total_q, 64, group, tile_tok) ||
-      !make_tensor_map_2d(&tmk, k_cache, kD, rows, 64, box_rows) ||
-      !make_tensor_map_2d(&tmv, v_cache, kD, rows, 64, box_rows))
+  if (!make_tensor_map_3d(&tmq, q, head_dim, num_q_heads, total_q, 64, group, tile_tok) ||
+      !make_tensor_map_2d(&tmk, k_cache, head_dim, rows, 64, box_rows) ||
+      !make_tensor_map_2d(&tmv, v_cache, head_dim, rows, 64, box_rows))
     return PKV_ERR_CUDA;
   TcParams p{};
   p.block_tables = block_tables;
@@ -1005,5 +1016,5 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   p.total_q = total_q;
   p.lg_group = lg;
   p.scale_log2 = kernel_scale_log2(scale);
-  return launch_tc<true>(tmq, tmk, tmv, p, block_size, as_stream(stream));
+  return launch_tc<true>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
 }

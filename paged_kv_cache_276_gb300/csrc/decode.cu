@@ -761,6 +761,7 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
     a.status = d_status;
     a.num_seqs = num_seqs;
     a.q_len = q_len;
+    a.head_dim = head_dim;
     a.max_blocks = max_blocks_per_seq;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
@@ -789,7 +790,8 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
     cudaError_t e = head_dim == 128
                         ? launch_pdl(combine_kernel<128>, dim3((total + 3) / 4), dim3(128), 0, st, pc, block_size,
                                      total, crows)
-                        : cudaErrorInvalidValue;
+                        : launch_pdl(combine_kernel<64>, dim3((total + 3) / 4), dim3(128), 0, st, pc, block_size,
+                                     total, crows);
     if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
     return PKV_OK;
   }

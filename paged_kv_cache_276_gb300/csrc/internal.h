@@ -26,7 +26,7 @@ struct ChunkTcArgs {
   float *ws_o;
   void *ws_ml;
   int32_t *status;
-  int num_seqs, q_len, max_blocks, num_q_heads, num_kv_heads, num_blocks, block_size;
+  int num_seqs, q_len, max_blocks, num_q_heads, num_kv_heads, num_blocks, block_size, head_dim;
   int part_tokens, max_parts;
   long long rows;  // num_blocks * num_kv_heads * block_size
   float scale;

@@ -85,7 +85,7 @@ def test_prefill_rejects_bad_sizes_before_launch(native):
         return lib.paged_attention_prefill(a["q"], a["k"], a["v"], a["tbl"], a["maxb"], a["lens"], a["qs"],
                                            a["B"], a["T"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"],
                                            a["scale"], a["out"], a["st"], a["stream"])
-    assert call(d=64) == native.PKV_ERR_UNSUPPORTED               # tensor-core tiles are head dim 128
+    assert call(d=96) == native.PKV_ERR_UNSUPPORTED               # tensor-core tiles: head dim 64 or 128
     assert call(bs=8) == native.PKV_ERR_UNSUPPORTED
     assert call(bs=256) == native.PKV_ERR_UNSUPPORTED
     assert call(Hq=24) == native.PKV_ERR_UNSUPPORTED              # group 3: not a power of two

@@ -346,6 +346,22 @@ def test_single_token_decode_on_tensor_cores(bs, Hq, Hkv, lens, partition):
     assert torch.allclose(tc.float(), mma.float(), atol=1e-2, rtol=1e-2)
 
 
+@pytest.mark.parametrize("q_len,G,lens,max_len", [
+    (16, 8, [900, 17, 2500], None),          # 16-token chunk, head dim 64, on the tcgen05 kernel
+    (1, 4, [3000, 1, 700], 16384),           # a single-token decode routed to it by the length bound
+])
+def test_tensor_core_kernel_head_dim_64(q_len, G, lens, max_len):
+    d, bs, Hkv = 64, 32, 2
+    Hq = G * Hkv
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=51 + q_len, q_len=q_len)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_decode(q, kc, vc, tables, lens, scale, 256, max_len=max_len, status=st)
+    assert st.item() == 0
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), scale, q_len=q_len)
+    assert_attention_close(out, ref, f"tcgen05, head dim 64, q_len {q_len}")
+
+
 def test_chunk_tensor_core_rescales_running_max():
     """Keys grow in magnitude block by block, so the running max keeps moving (rescale path)."""
     d, bs, Hq, Hkv = 128, 16, 16, 2

@@ -58,6 +58,20 @@ def oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale, d=128):
                                      num_kv_heads=Hkv, head_dim=d, block_size=bs, scale=scale)
 
 
+@pytest.mark.parametrize("d,bs,Hq,Hkv,lens,chunks", [
+    (64, 16, 32, 4, [700, 129, 40], [300, 129, 1]),      # head dim 64: one 128-byte half per row
+    (64, 128, 16, 16, [1000, 64], [256, 64]),            # head dim 64, G = 1, blocks of 128
+])
+def test_prefill_head_dim_64_matches_oracle(d, bs, Hq, Hkv, lens, chunks):
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=d + bs, d=d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_prefill(q, kc, vc, tables, lens, q_start, scale, status=st)
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale, d=d)
+    assert_attention_close(out, ref, "prefill, head dim 64")
+
+
 @pytest.mark.parametrize("bs,Hq,Hkv,lens,chunks", [
     # a whole prompt, a ragged chunk behind cached context, a decode row, an empty chunk
     (16, 64, 8, [300, 1000, 64, 77, 5], [300, 200, 1, 0, 5]),
