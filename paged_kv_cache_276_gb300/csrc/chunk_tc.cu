@@ -103,10 +103,12 @@ struct Layout {
   static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
   static constexpr int kSmemBars = kSmemStats + 2 * kRows * 8;
   static constexpr int kSmemSeq = kSmemBars + B_COUNT * 8 + 16;  // after the TMEM slot and the abort flag
-  // tensor memory: O accumulators at 0 and D, S buffers at 2 D (+kTK), P
-  // buffers (when not over S) after the S buffers
+  // tensor memory: O accumulators at 0 and D, S buffers at 2 D (+kTK); P in
+  // the upper half of its S buffer (prefill: keys 0..63 over S columns 64..95,
+  // keys 64..127 over 96..127, written after those scores are read) or after
+  // the S buffers
   static constexpr int kTmemS = 2 * D;
-  static constexpr int kTmemP = kPOverS ? kTmemS : kTmemS + 2 * kTK;
+  static constexpr int kTmemP = kPOverS ? kTmemS + kTK / 2 : kTmemS + 2 * kTK;
   static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
   static_assert(kTmemP + kPStride + kTK / 2 <= kTmemCols, "tensor memory");
   static constexpr size_t bytes(int num_seqs) {
@@ -711,15 +713,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float msub = new_reference(rm);
               const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
               const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
-              // pass 2: the weights, 64 keys at a time, stored over score columns
-              // already read (keys 0-63 -> columns 0-31, keys 64-127 -> 32-63)
+              // pass 2: the weights, 64 keys at a time, last half first (its
+              // scores are still in registers); each half's weights land on
+              // score columns already read (keys 64..127 -> columns 96..127, then
+              // keys 0..63 -> columns 64..95)
               float lsum = 0.f;
 #pragma unroll
-              for (int hh = 0; hh < kTileKeys / 64; ++hh) {
-                tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tc::wait_ld();
-                mask(sv, hh * 64);
+              for (int hh = kTileKeys / 64 - 1; hh >= 0; --hh) {
+                if (hh != kTileKeys / 64 - 1) {
+                  tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                  tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                  tc::wait_ld();
+                  mask(sv, hh * 64);
+                }
                 uint32_t pk[32];
                 lsum += weights64(sv, ks2, nm2, pk);
                 tc::st32(tPb + hh * 32, pk);
