@@ -388,6 +388,112 @@ int pkv_num_free(const pkv_alloc *a);
 /* Refcount of a block, or PKV_ERR_RANGE. */
 int pkv_refcount(const pkv_alloc *a, int block);
 
+/* ------------------------------------------------------------------------
+ * Decode step runner: one decode step of a batch through every layer of a
+ * model, issued by one host call.
+ *
+ * Pages: each decode step grows every running sequence by one token, taking a
+ * new block when its last one is full, stores the token's keys and values in
+ * its slot, and runs attention over the sequence's blocks through its table
+ * (x321.org "The serving bottleneck is not just FLOPs", "PagedAttention
+ * borrows an operating-system trick").  The runner chains exactly those calls
+ * of this library: pkv_seq_append_batch, pkv_block_table, then per layer
+ * pkv_write and paged_attention_decode.  The pages have no counterpart to the
+ * runner itself; it exists so that a serving loop pays one host call per step
+ * instead of one per operation and per layer.
+ *
+ * Buffers (all owned by the caller, sized by pkv_step_layout_of):
+ *   host_stage / dev_stage  page-locked host memory and device memory of
+ *       layout.stage_bytes each, 16-byte aligned.  The caller writes each
+ *       step's inputs into host_stage; the runner writes the slots, tables and
+ *       lengths into it and copies all of it to dev_stage in one copy.
+ *       Segments (byte offsets; every segment starts on a 256-byte boundary):
+ *         queries of layer l  q_offset + l * q_layer_bytes,
+ *                             [max_seqs][q_len][num_q_heads][head_dim] bf16
+ *         new keys of layer l k_offset + l * kv_layer_bytes,
+ *         new values          v_offset + l * kv_layer_bytes,
+ *                             [max_seqs * q_len][num_kv_heads][head_dim] bf16
+ *         slots               slots_offset, [max_seqs * q_len] int64
+ *         block tables        tables_offset, [max_seqs][max_blocks_per_seq] int32
+ *         lengths             lens_offset, [max_seqs] int32
+ *       A run over n sequences uses the first n rows of each segment.
+ *   dev_out / host_out      device and page-locked host memory of
+ *       layout.out_bytes; layer l's output [max_seqs][q_len][num_q_heads]
+ *       [head_dim] bf16 at l * out_layer_bytes.  Each run copies all of
+ *       dev_out to host_out.
+ *   workspace               device, layout.workspace_bytes (split-K scratch
+ *       for the longest sequence the tables can hold; may be NULL when 0).
+ *   k_caches / v_caches     host arrays of num_layers device pointers, one
+ *       pool per layer, each [num_blocks][num_kv_heads][block_size][head_dim].
+ *
+ * With use_graph != 0 the device part of a run (copy in, the layers' writes
+ * and decodes, copy out) is captured once into a CUDA graph for each pair
+ * (n, number of partitions of the longest sequence) and replayed; the decode's
+ * max_seq_len is then that number of partitions times partition_size, an upper
+ * bound of the lengths (at most 32 graphs are kept; capture happens on a
+ * private stream).  With use_graph == 0 the same copies and kernels are
+ * enqueued one by one on every run, with the exact maximum length.  Graphs
+ * save host time when a step has many short kernels (many layers); a step of
+ * a few long kernels gains nothing from them.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int num_layers;          /* >= 1 */
+  int max_seqs;            /* largest batch of a run, >= 1 */
+  int q_len;               /* new tokens per sequence and step (1 or 16) */
+  int num_q_heads, num_kv_heads, head_dim;
+  int block_size, num_blocks, max_blocks_per_seq;
+  int partition_size;      /* as paged_attention_decode; 0 = its default */
+  float scale;
+  int use_graph;           /* 0: enqueue calls one by one; else CUDA graphs */
+} pkv_step_config;
+
+typedef struct {
+  size_t q_offset, q_layer_bytes;
+  size_t k_offset, v_offset, kv_layer_bytes;
+  size_t slots_offset, tables_offset, lens_offset;
+  size_t stage_bytes;      /* host_stage and dev_stage */
+  size_t out_layer_bytes, out_bytes;
+  size_t workspace_bytes;
+} pkv_step_layout;
+
+typedef struct pkv_step pkv_step;
+
+/* Buffer layout of a configuration (host only).  PKV_ERR_ARG for sizes below
+ * 1 (partition_size below 0) or byte counts that overflow. */
+int pkv_step_layout_of(const pkv_step_config *cfg, pkv_step_layout *layout);
+
+/* Create a runner over an allocator and caller-owned buffers (see above).
+ * PKV_ERR_ARG for a null, misaligned or too small buffer, or a host buffer
+ * that is not page-locked; PKV_ERR_CUDA if the runner's event or stream cannot
+ * be made.  The allocator, caches and buffers must outlive the runner. */
+int pkv_step_create(const pkv_step_config *cfg, pkv_alloc *alloc, pkv_bf16 *const *k_caches,
+                    pkv_bf16 *const *v_caches, void *host_stage, void *dev_stage, pkv_bf16 *dev_out,
+                    pkv_bf16 *host_out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                    pkv_step **out);
+
+/* Waits for the runner's last run, then releases its graphs, event and stream. */
+void pkv_step_destroy(pkv_step *s);
+
+/* One step for the n <= max_seqs distinct sequences seq_ids (host array):
+ *   1. wait until the runner's previous run has finished on the GPU;
+ *   2. check that every sequence has room for q_len more tokens in
+ *      max_blocks_per_seq blocks (PKV_ERR_RANGE, nothing changed, if not);
+ *   3. pkv_seq_append_batch of q_len tokens each (its errors are returned and
+ *      change nothing), slots into host_stage; pkv_block_table of the n
+ *      sequences into host_stage;
+ *   4. enqueue on `stream`: host_stage -> dev_stage, for each layer l the
+ *      pkv_write of its n * q_len new keys and values and the
+ *      paged_attention_decode of its n query rows, dev_out -> host_out.
+ * Returns after the enqueue.  The caller writes the step's queries, keys and
+ * values for rows 0..n-1 into host_stage before the call, and may touch
+ * host_stage and host_out again only after pkv_step_wait (or a synchronisation
+ * of `stream`).  A CUDA error after step 3 returns PKV_ERR_CUDA with the
+ * tokens appended.  n == 0 only waits. */
+int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream);
+
+/* Block until the runner's last run has finished; PKV_ERR_CUDA on failure. */
+int pkv_step_wait(pkv_step *s);
+
 #ifdef __cplusplus
 }
 #endif

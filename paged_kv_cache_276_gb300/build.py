@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["decode.cu", "chunk_tc.cu", "cache_ops.cu", "alloc.cpp"]
+SOURCES = ["decode.cu", "chunk_tc.cu", "cache_ops.cu", "alloc.cpp", "step.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

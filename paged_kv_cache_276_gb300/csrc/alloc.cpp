@@ -307,11 +307,16 @@ int pkv_seq_append_batch(pkv_alloc *a, const int64_t *seq_ids, int n, int n_toke
   // validate all, and count the blocks all of them need, before changing anything
   const int64_t bs = a->block_size;
   int64_t need = 0;
+  if (n > 32) {  // each sequence once: sorted copy for large batches, pairwise below
+    std::vector<int64_t> ids(seq_ids, seq_ids + n);
+    std::sort(ids.begin(), ids.end());
+    if (std::adjacent_find(ids.begin(), ids.end()) != ids.end()) return PKV_ERR_ARG;
+  }
   for (int i = 0; i < n; ++i) {
     const Sequence *s = a->find(seq_ids[i]);
     if (!s || s->swapped) return PKV_ERR_ARG;
-    for (int j = 0; j < i; ++j)
-      if (seq_ids[j] == seq_ids[i]) return PKV_ERR_ARG;  // each sequence once
+    for (int j = 0; n <= 32 && j < i; ++j)
+      if (seq_ids[j] == seq_ids[i]) return PKV_ERR_ARG;
     if (s->len % bs != 0 && a->refcount[s->blocks.back()] > 1) return PKV_ERR_SHARED;
     need += a->blocks_for(s->len + n_tokens) - static_cast<int64_t>(s->blocks.size());
   }

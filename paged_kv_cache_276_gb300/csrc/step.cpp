@@ -1,0 +1,253 @@
+// Decode step runner (pkv_step_*): the host side of one decode step of a batch
+// through every layer, issued by one call.
+//
+// A step is the allocator's append and table fill (host), one copy of the
+// step's inputs to the device, per layer the slot write and the paged decode,
+// and one copy of the outputs back.  Issued one by one from a scripting
+// language those are a dozen calls whose argument handling costs more than
+// the copies; here they are one C call, and with graphs the device part is a
+// single graph launch captured once per (batch size, partition count).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <map>
+#include <new>
+#include <utility>
+#include <vector>
+
+#include "internal.h"
+#include "pkv.h"
+
+namespace {
+
+constexpr int kMaxGraphs = 32;
+constexpr int kDefaultPartition = 768;  // paged_attention_decode's default
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool pinned_host(const void *p) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
+struct pkv_step {
+  pkv_step_config cfg{};
+  pkv_step_layout lay{};
+  pkv_alloc *alloc = nullptr;
+  std::vector<pkv_bf16 *> k, v;
+  char *hs = nullptr, *ds = nullptr;
+  char *dout = nullptr, *hout = nullptr;
+  void *ws = nullptr;
+  size_t ws_bytes = 0;
+  int32_t *status = nullptr;
+  int part = kDefaultPartition;
+  cudaStream_t cap = nullptr;
+  cudaEvent_t done = nullptr;
+  bool pending = false;
+  std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
+};
+
+namespace {
+
+void drop_graphs(pkv_step *s) {
+  for (auto &g : s->graphs) cudaGraphExecDestroy(g.second);
+  s->graphs.clear();
+}
+
+// Copy in, every layer's write and decode, copy out, on `st`.
+int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len) {
+  const pkv_step_config &c = s->cfg;
+  const pkv_step_layout &L = s->lay;
+  cudaError_t e = cudaMemcpyAsync(s->ds, s->hs, L.stage_bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  const auto *slots = reinterpret_cast<const int64_t *>(s->ds + L.slots_offset);
+  const auto *tables = reinterpret_cast<const int32_t *>(s->ds + L.tables_offset);
+  const auto *lens = reinterpret_cast<const int32_t *>(s->ds + L.lens_offset);
+  for (int l = 0; l < c.num_layers; ++l) {
+    const auto *q = reinterpret_cast<const pkv_bf16 *>(s->ds + L.q_offset + l * L.q_layer_bytes);
+    const auto *kn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.k_offset + l * L.kv_layer_bytes);
+    const auto *vn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.v_offset + l * L.kv_layer_bytes);
+    auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
+    int rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
+                       c.head_dim, s->status, st);
+    if (rc != PKV_OK) return rc;
+    rc = paged_attention_decode(q, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n, max_seq_len, c.q_len,
+                                c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.scale,
+                                c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
+    if (rc != PKV_OK) return rc;
+  }
+  e = cudaMemcpyAsync(s->hout, s->dout, L.out_bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+int capture(pkv_step *s, int n, int max_seq_len, cudaGraphExec_t *exec) {
+  cudaError_t e;
+  if (!s->cap && (e = cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking)) != cudaSuccess)
+    return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  // Relaxed: the launch helpers may set kernel attributes or look up driver
+  // entry points while the stream is being captured.
+  if ((e = cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeRelaxed)) != cudaSuccess)
+    return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  const int rc = enqueue(s, s->cap, n, max_seq_len);
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(s->cap, &g);
+  if (rc != PKV_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    if (rc != PKV_OK) return rc;
+    return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  }
+  e = cudaGraphInstantiate(exec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_step_layout_of(const pkv_step_config *c, pkv_step_layout *o) {
+  if (!c || !o) return PKV_ERR_ARG;
+  if (c->num_layers < 1 || c->max_seqs < 1 || c->q_len < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1 ||
+      c->head_dim < 1 || c->block_size < 1 || c->num_blocks < 1 || c->max_blocks_per_seq < 1 ||
+      c->partition_size < 0)
+    return PKV_ERR_ARG;
+  const long long cap = static_cast<long long>(c->max_blocks_per_seq) * c->block_size;
+  if (cap >= (1ll << 31)) return PKV_ERR_ARG;
+  // Every count below is a product of ints; bound them so no size_t product overflows.
+  const double rows = static_cast<double>(c->max_seqs) * c->q_len;
+  const double worst = rows * (c->num_q_heads + 2.0 * c->num_kv_heads) * c->head_dim * 2.0 * c->num_layers +
+                       static_cast<double>(c->max_seqs) * c->max_blocks_per_seq * 4.0;
+  if (worst > 9.0e15) return PKV_ERR_ARG;
+  const size_t r = static_cast<size_t>(c->max_seqs) * c->q_len;
+  const size_t qb = up256(r * c->num_q_heads * c->head_dim * 2);
+  const size_t kvb = up256(r * c->num_kv_heads * c->head_dim * 2);
+  std::memset(o, 0, sizeof(*o));
+  o->q_offset = 0;
+  o->q_layer_bytes = qb;
+  o->kv_layer_bytes = kvb;
+  o->k_offset = o->q_offset + c->num_layers * qb;
+  o->v_offset = o->k_offset + c->num_layers * kvb;
+  o->slots_offset = o->v_offset + c->num_layers * kvb;
+  o->tables_offset = o->slots_offset + up256(r * sizeof(int64_t));
+  o->lens_offset = o->tables_offset + up256(static_cast<size_t>(c->max_seqs) * c->max_blocks_per_seq * 4);
+  o->stage_bytes = o->lens_offset + up256(static_cast<size_t>(c->max_seqs) * 4);
+  o->out_layer_bytes = qb;
+  o->out_bytes = c->num_layers * qb;
+  o->workspace_bytes = paged_attention_workspace_size(c->max_seqs, c->q_len, c->num_q_heads, c->head_dim,
+                                                      static_cast<int>(cap), c->partition_size);
+  return PKV_OK;
+}
+
+int pkv_step_create(const pkv_step_config *cfg, pkv_alloc *alloc, pkv_bf16 *const *k_caches,
+                    pkv_bf16 *const *v_caches, void *host_stage, void *dev_stage, pkv_bf16 *dev_out,
+                    pkv_bf16 *host_out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                    pkv_step **out) {
+  if (!out) return PKV_ERR_ARG;
+  *out = nullptr;
+  pkv_step_layout lay;
+  int rc = pkv_step_layout_of(cfg, &lay);
+  if (rc != PKV_OK) return rc;
+  if (!alloc || !k_caches || !v_caches || !host_stage || !dev_stage || !dev_out || !host_out) return PKV_ERR_ARG;
+  if (!pkv::aligned16(host_stage) || !pkv::aligned16(dev_stage) || !pkv::aligned16(dev_out) ||
+      !pkv::aligned16(host_out))
+    return PKV_ERR_ARG;
+  if (lay.workspace_bytes > 0 && (!workspace || workspace_bytes < lay.workspace_bytes)) return PKV_ERR_WORKSPACE;
+  for (int l = 0; l < cfg->num_layers; ++l)
+    if (!k_caches[l] || !v_caches[l]) return PKV_ERR_ARG;
+  if (!pinned_host(host_stage) || !pinned_host(host_out)) return PKV_ERR_ARG;
+
+  auto *s = new (std::nothrow) pkv_step;
+  if (!s) return PKV_ERR_OOM;
+  s->cfg = *cfg;
+  s->lay = lay;
+  s->alloc = alloc;
+  s->k.assign(k_caches, k_caches + cfg->num_layers);
+  s->v.assign(v_caches, v_caches + cfg->num_layers);
+  s->hs = static_cast<char *>(host_stage);
+  s->ds = static_cast<char *>(dev_stage);
+  s->dout = reinterpret_cast<char *>(dev_out);
+  s->hout = reinterpret_cast<char *>(host_out);
+  s->ws = workspace;
+  s->ws_bytes = workspace_bytes;
+  s->status = d_status;
+  s->part = cfg->partition_size > 0 ? cfg->partition_size : kDefaultPartition;
+  const cudaError_t e = cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    delete s;
+    return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  }
+  *out = s;
+  return PKV_OK;
+}
+
+int pkv_step_wait(pkv_step *s) {
+  if (!s) return PKV_ERR_ARG;
+  if (!s->pending) return PKV_OK;
+  const cudaError_t e = cudaEventSynchronize(s->done);
+  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  s->pending = false;
+  return PKV_OK;
+}
+
+void pkv_step_destroy(pkv_step *s) {
+  if (!s) return;
+  pkv_step_wait(s);
+  drop_graphs(s);
+  if (s->cap) cudaStreamDestroy(s->cap);
+  if (s->done) cudaEventDestroy(s->done);
+  delete s;
+}
+
+int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
+  if (!s || n < 0 || n > s->cfg.max_seqs || (n > 0 && !seq_ids)) return PKV_ERR_ARG;
+  int rc = pkv_step_wait(s);
+  if (rc != PKV_OK || n == 0) return rc;
+  const pkv_step_config &c = s->cfg;
+  const long long cap = static_cast<long long>(c.max_blocks_per_seq) * c.block_size;
+  for (int i = 0; i < n; ++i) {
+    const int64_t len = pkv_seq_len(s->alloc, seq_ids[i]);
+    if (len < 0) return static_cast<int>(len);
+    if (len + c.q_len > cap) return PKV_ERR_RANGE;
+  }
+  auto *slots = reinterpret_cast<int64_t *>(s->hs + s->lay.slots_offset);
+  auto *tables = reinterpret_cast<int32_t *>(s->hs + s->lay.tables_offset);
+  auto *lens = reinterpret_cast<int32_t *>(s->hs + s->lay.lens_offset);
+  if ((rc = pkv_seq_append_batch(s->alloc, seq_ids, n, c.q_len, slots)) != PKV_OK) return rc;
+  if ((rc = pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, lens)) != PKV_OK) return rc;
+  int max_len = 0;
+  for (int i = 0; i < n; ++i) max_len = lens[i] > max_len ? lens[i] : max_len;
+
+  cudaStream_t st = pkv::as_stream(stream);
+  if (!c.use_graph) {
+    rc = enqueue(s, st, n, max_len);
+  } else {
+    const int parts = max_len > 0 ? (max_len + s->part - 1) / s->part : 1;
+    const auto key = std::make_pair(n, parts);
+    auto it = s->graphs.find(key);
+    if (it == s->graphs.end()) {
+      if (static_cast<int>(s->graphs.size()) >= kMaxGraphs) drop_graphs(s);
+      cudaGraphExec_t exec = nullptr;
+      const long long bound = static_cast<long long>(parts) * s->part;
+      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), &exec);
+      if (rc != PKV_OK) return rc;
+      it = s->graphs.emplace(key, exec).first;
+    }
+    const cudaError_t e = cudaGraphLaunch(it->second, st);
+    if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  }
+  if (rc != PKV_OK) return rc;
+  const cudaError_t e = cudaEventRecord(s->done, st);
+  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  s->pending = true;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -36,8 +36,29 @@ PKV_STATUS_BAD_QSTART = 16
 _c_int, _c_i64, _c_ptr, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_float)
 
+class StepConfig(ctypes.Structure):
+    """pkv_step_config."""
+    _fields_ = [("num_layers", _c_int), ("max_seqs", _c_int), ("q_len", _c_int), ("num_q_heads", _c_int),
+                ("num_kv_heads", _c_int), ("head_dim", _c_int), ("block_size", _c_int), ("num_blocks", _c_int),
+                ("max_blocks_per_seq", _c_int), ("partition_size", _c_int), ("scale", _c_float),
+                ("use_graph", _c_int)]
+
+
+class StepLayout(ctypes.Structure):
+    """pkv_step_layout (byte offsets and sizes)."""
+    _fields_ = [(n, _c_size) for n in ("q_offset", "q_layer_bytes", "k_offset", "v_offset", "kv_layer_bytes",
+                                       "slots_offset", "tables_offset", "lens_offset", "stage_bytes",
+                                       "out_layer_bytes", "out_bytes", "workspace_bytes")]
+
+
 # name -> (restype, argtypes); mirrors include/pkv.h
 SIGNATURES = {
+    "pkv_step_layout_of": (_c_int, [ctypes.POINTER(StepConfig), ctypes.POINTER(StepLayout)]),
+    "pkv_step_create": (_c_int, [ctypes.POINTER(StepConfig), _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                 _c_ptr, _c_ptr, _c_size, _c_ptr, ctypes.POINTER(_c_ptr)]),
+    "pkv_step_destroy": (None, [_c_ptr]),
+    "pkv_step_run": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_ptr]),
+    "pkv_step_wait": (_c_int, [_c_ptr]),
     "pkv_error_string": (ctypes.c_char_p, [_c_int]),
     "pkv_last_cuda_error": (ctypes.c_char_p, []),
     "pkv_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int,
@@ -126,8 +147,11 @@ def _ptr(t):
 
 
 def _stream(stream, device):
+    """A torch.cuda.Stream, a raw cudaStream_t handle (int), or None for the current stream."""
     if stream is None:
         stream = torch.cuda.current_stream(device)
+    elif isinstance(stream, int):
+        return ctypes.c_void_p(stream)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -395,3 +419,103 @@ class BlockAllocator:
         if rc < 0:
             raise PkvError(rc, "pkv_refcount")
         return int(rc)
+
+
+# --------------------------------------------------------------- step runner
+class DecodeStep:
+    """pkv_step_*: one decode step of a batch through every layer, one C call.
+
+    Owns the runner's buffers (page-locked staging and output buffers, their
+    device twins, the split-K workspace), laid out by ``pkv_step_layout_of``.
+    Per step: write the step's queries and new keys / values of rows
+    0..n-1 into ``q(l)``, ``k(l)``, ``v(l)`` (host views), call ``run(seq_ids)``,
+    then ``wait()``; the outputs are in ``out(l)`` (host views).  The runner
+    appends the tokens to the allocator and fills the slots, tables and lengths
+    itself; ``slots``, ``tables`` and ``lens`` show them.
+    """
+
+    def __init__(self, alloc, k_caches, v_caches, max_seqs, q_len, num_q_heads, max_blocks_per_seq, scale,
+                 partition_size=0, use_graph=False, d_status=None):
+        k_caches, v_caches = list(k_caches), list(v_caches)
+        if not k_caches or len(k_caches) != len(v_caches):
+            raise ValueError("one key and one value cache per layer expected")
+        dev = k_caches[0].device
+        for i, (kc, vc) in enumerate(zip(k_caches, v_caches)):
+            _need(kc, torch.bfloat16, f"k_caches[{i}]", dev)
+            _need(vc, torch.bfloat16, f"v_caches[{i}]", dev)
+            if kc.shape != k_caches[0].shape or vc.shape != kc.shape:
+                raise ValueError("every layer's caches must have the same shape")
+        NB, Hkv, bs, d = k_caches[0].shape
+        self.cfg = StepConfig(len(k_caches), int(max_seqs), int(q_len), int(num_q_heads), Hkv, d, bs, NB,
+                              int(max_blocks_per_seq), int(partition_size), float(scale), 1 if use_graph else 0)
+        lay = StepLayout()
+        _check(lib().pkv_step_layout_of(ctypes.byref(self.cfg), ctypes.byref(lay)), "pkv_step_layout_of")
+        self.layout = lay
+        self.device = dev
+        u8 = torch.uint8
+        self.host_stage = torch.empty(lay.stage_bytes, dtype=u8).pin_memory()
+        self.dev_stage = torch.empty(lay.stage_bytes, dtype=u8, device=dev)
+        self.host_out = torch.empty(lay.out_bytes, dtype=u8).pin_memory()
+        self.dev_out = torch.empty(lay.out_bytes, dtype=u8, device=dev)
+        self.workspace = torch.empty(max(lay.workspace_bytes, 16), dtype=u8, device=dev)
+        self._caches = (k_caches, v_caches)  # kept alive with the runner
+        kp = (_c_ptr * len(k_caches))(*[t.data_ptr() for t in k_caches])
+        vp = (_c_ptr * len(v_caches))(*[t.data_ptr() for t in v_caches])
+        self._alloc = alloc
+        h = _c_ptr()
+        _check(lib().pkv_step_create(ctypes.byref(self.cfg), alloc._h, kp, vp, _ptr(self.host_stage),
+                                     _ptr(self.dev_stage), _ptr(self.dev_out), _ptr(self.host_out),
+                                     _ptr(self.workspace), lay.workspace_bytes, _ptr(d_status), ctypes.byref(h)),
+               "pkv_step_create")
+        self._h = h
+        self._run = lib().pkv_step_run
+        B, H, ql = int(max_seqs), int(num_q_heads), int(q_len)
+        self._q_shape, self._kv_shape = (B, ql, H, d), (B * ql, Hkv, d)
+        self.slots = self._view(self.host_stage, lay.slots_offset, torch.int64, (B * ql,))
+        self.tables = self._view(self.host_stage, lay.tables_offset, torch.int32, (B, int(max_blocks_per_seq)))
+        self.lens = self._view(self.host_stage, lay.lens_offset, torch.int32, (B,))
+
+    @staticmethod
+    def _view(buf, off, dtype, shape):
+        n = 1
+        for x in shape:
+            n *= x
+        return buf[off:off + n * torch.empty((), dtype=dtype).element_size()].view(dtype).view(shape)
+
+    def q(self, layer):
+        return self._view(self.host_stage, self.layout.q_offset + layer * self.layout.q_layer_bytes,
+                          torch.bfloat16, self._q_shape)
+
+    def k(self, layer):
+        return self._view(self.host_stage, self.layout.k_offset + layer * self.layout.kv_layer_bytes,
+                          torch.bfloat16, self._kv_shape)
+
+    def v(self, layer):
+        return self._view(self.host_stage, self.layout.v_offset + layer * self.layout.kv_layer_bytes,
+                          torch.bfloat16, self._kv_shape)
+
+    def out(self, layer):
+        return self._view(self.host_out, layer * self.layout.out_layer_bytes, torch.bfloat16, self._q_shape)
+
+    def run(self, seq_ids, stream=None):
+        """Enqueue one step for ``seq_ids`` (int64 numpy array or sequence); returns at once."""
+        import numpy as np
+        ids = seq_ids if (isinstance(seq_ids, np.ndarray) and seq_ids.dtype == np.int64
+                          and seq_ids.flags.c_contiguous) else np.ascontiguousarray(seq_ids, dtype=np.int64)
+        rc = self._run(self._h, ids.ctypes.data, len(ids), _stream(stream, self.device))
+        if rc != PKV_OK:
+            raise PkvError(rc, "pkv_step_run")
+
+    def wait(self):
+        _check(lib().pkv_step_wait(self._h), "pkv_step_wait")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pkv_step_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

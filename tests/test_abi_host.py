@@ -326,3 +326,67 @@ def test_batched_append_equals_single_appends_and_is_all_or_nothing(native):
     assert np.array_equal(a.block_table(range(6), 8)[0], before[0]) and a.num_free() == before[1]
     a.close()
     b.close()
+
+
+def test_large_batched_append_rejects_duplicates(native):
+    a = native.BlockAllocator(400, 16)
+    for i in range(40):
+        a.seq_add(i)
+    ids = list(range(40))
+    with pytest.raises(native.PkvError) as e:
+        a.seq_append_batch(ids + [17], 1)  # 41 ids: the sorted check of large batches
+    assert e.value.code == native.PKV_ERR_ARG
+    assert all(a.seq_len(i) == 0 for i in ids)
+    slots = a.seq_append_batch(ids[::-1], 3)
+    assert len(set(slots.tolist())) == 120 and all(a.seq_len(i) == 3 for i in ids)
+    a.close()
+
+
+def test_step_layout_host_only(native):
+    import ctypes
+    B, ql, Hq, Hkv, d, L, mb = 32, 1, 32, 8, 128, 3, 260
+    cfg = native.StepConfig(L, B, ql, Hq, Hkv, d, 16, 9000, mb, 768, 0.088, 1)
+    lay = native.StepLayout()
+    assert native.lib().pkv_step_layout_of(ctypes.byref(cfg), ctypes.byref(lay)) == native.PKV_OK
+    up = lambda x: -(-x // 256) * 256  # noqa: E731
+    assert lay.q_layer_bytes == up(B * ql * Hq * d * 2) and lay.kv_layer_bytes == up(B * ql * Hkv * d * 2)
+    segs = [(lay.q_offset, L * lay.q_layer_bytes), (lay.k_offset, L * lay.kv_layer_bytes),
+            (lay.v_offset, L * lay.kv_layer_bytes), (lay.slots_offset, B * ql * 8),
+            (lay.tables_offset, B * mb * 4), (lay.lens_offset, B * 4)]
+    end = 0
+    for off, size in segs:  # in order, 256-byte aligned, not overlapping
+        assert off % 256 == 0 and off >= end
+        end = off + size
+    assert lay.stage_bytes >= end and lay.stage_bytes % 256 == 0
+    assert lay.out_layer_bytes == lay.q_layer_bytes and lay.out_bytes == L * lay.q_layer_bytes
+    assert lay.workspace_bytes == native.paged_attention_workspace_size(B, ql, Hq, d, mb * 16, 768)
+    for field, bad in (("num_layers", 0), ("max_seqs", 0), ("q_len", 0), ("block_size", 0),
+                       ("max_blocks_per_seq", 0), ("partition_size", -1), ("max_blocks_per_seq", 1 << 28)):
+        c = native.StepConfig(L, B, ql, Hq, Hkv, d, 16, 9000, mb, 768, 0.088, 1)
+        setattr(c, field, bad)
+        assert native.lib().pkv_step_layout_of(ctypes.byref(c), ctypes.byref(lay)) == native.PKV_ERR_ARG
+    assert native.lib().pkv_step_layout_of(None, ctypes.byref(lay)) == native.PKV_ERR_ARG
+
+
+def test_step_create_and_run_reject_bad_arguments_before_any_launch(native):
+    import ctypes
+    cfg = native.StepConfig(1, 2, 1, 8, 2, 64, 16, 64, 8, 0, 0.1, 1)
+    h = ctypes.c_void_p()
+    a = native.BlockAllocator(64, 16)
+    lib = native.lib()
+    arr = (ctypes.c_void_p * 1)(16)
+    # null buffers, then a missing workspace (the layout needs one: 128-token tables, 768-token partitions -> 0)
+    assert lib.pkv_step_create(ctypes.byref(cfg), a._h, arr, arr, None, None, None, None, None, 0, None,
+                               ctypes.byref(h)) == native.PKV_ERR_ARG
+    assert lib.pkv_step_create(ctypes.byref(cfg), None, arr, arr, 16, 16, 16, 16, None, 0, None,
+                               ctypes.byref(h)) == native.PKV_ERR_ARG
+    assert lib.pkv_step_create(ctypes.byref(cfg), a._h, arr, arr, 24, 16, 16, 16, None, 0, None,
+                               ctypes.byref(h)) == native.PKV_ERR_ARG   # misaligned
+    cfg.partition_size = 16  # 8 partitions: a workspace is needed
+    assert lib.pkv_step_create(ctypes.byref(cfg), a._h, arr, arr, 16, 16, 16, 16, None, 0, None,
+                               ctypes.byref(h)) == native.PKV_ERR_WORKSPACE
+    assert not h.value
+    assert lib.pkv_step_run(None, None, 0, None) == native.PKV_ERR_ARG
+    assert lib.pkv_step_wait(None) == native.PKV_ERR_ARG
+    lib.pkv_step_destroy(None)
+    a.close()
