@@ -66,7 +66,8 @@ constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 enum : int {
   B_Q_FULL0 = 0, B_Q_FULL1, B_Q_FREE0, B_Q_FREE1, B_O_FULL, B_O_FREE,
   B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
-  B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0, B_STATS_FREE1,
+  B_P_FULL0, B_P_FULL1, B_P_LO0, B_P_LO1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0,
+  B_STATS_FREE1,
   B_K_FULL0, B_K_EMPTY0 = B_K_FULL0 + kMaxStages, B_V_FULL0 = B_K_EMPTY0 + kMaxStages,
   B_V_EMPTY0 = B_V_FULL0 + kMaxStages, B_COUNT = B_V_EMPTY0 + kMaxStages
 };
@@ -383,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_S_FULL0 + i), 1);
       mbar_init(bar(B_S_FREE0 + i), kRows);
       mbar_init(bar(B_P_FULL0 + i), kRows);
+      mbar_init(bar(B_P_LO0 + i), kRows);
       mbar_init(bar(B_PV_DONE0 + i), 1);
     }
     for (int s = 0; s < kStages; ++s) {
@@ -580,10 +582,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after();
             const uint32_t pa = tP0 + pb * Lay::kPStride;
             const uint32_t vb = sV + (g % kStages) * kKVBytes;
+            constexpr int kSteps = kTileKeys / 16;  // 16 keys = 8 packed columns of P
+            if constexpr (Lay::kPOverS) {
+              // the weights of keys kTK/2.. come first (P_FULL); those of keys
+              // 0.. follow while this half's product runs (P_LO)
 #pragma unroll
-            for (int ks = 0; ks < kTileKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
-              tc::mma_ta(tmem + pb * D, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
-                         !(first && ks == 0));
+              for (int ks = kSteps / 2; ks < kSteps; ++ks)
+                tc::mma_ta(tmem + pb * D, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
+                           !(first && ks == kSteps / 2));
+              if (!mbar_wait(bar(B_P_LO0 + pb), (g >> 1) & 1)) { ok = false; break; }
+              tc::fence_after();
+#pragma unroll
+              for (int ks = 0; ks < kSteps / 2; ++ks)
+                tc::mma_ta(tmem + pb * D, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
+                           true);
+            } else {
+#pragma unroll
+              for (int ks = 0; ks < kSteps; ++ks)
+                tc::mma_ta(tmem + pb * D, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
+                           !(first && ks == 0));
+            }
             tc::commit(bar(B_PV_DONE0 + pb));
             tc::commit(bar(B_V_EMPTY0 + (g % kStages)));
             if (last) tc::commit(bar(B_O_FULL));
@@ -689,20 +707,49 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           };
+          // value rows past the sequence end were never written: zero them
+          // before any P V product of this tile reads the stage
+          auto zero_tail_values = [&]() {
+            const int exist = L - k0;
+            if (exist >= kTileKeys) return true;
+            const int s = g % kStages;
+            if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) return false;
+            const uint32_t vb = sV + s * kKVBytes;
+            const int first = exist < 0 ? 0 : exist;
+            for (int e = r; e < (kTileKeys - first) * kHalves * 8; e += kRows) {  // 16-byte chunks
+              const int row = first + e / (kHalves * 8), rem = e % (kHalves * 8), hf = rem / 8, c = rem % 8;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + hf * Lay::kKVHalf + row * 128 + c * 16),
+                           "r"(0u)
+                           : "memory");
+            }
+            return true;
+          };
+          // make this thread's P (tensor memory) and zeroed values (shared
+          // memory) visible to the P V issuer, then count in at barrier bi
+          auto publish = [&](int bi) {
+            tc::wait_st();
+            fence_proxy_async_shared();
+            tc::fence_before();
+            mbar_arrive(bar(bi));
+          };
           tc::fence_after();
           if constexpr (Lay::kPOverS) {
+            static_assert(kTileKeys == 128, "two 64-key halves");
             if (skip) {
               uint32_t z[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) z[c] = 0u;
-#pragma unroll
-              for (int hh = 0; hh < kTileKeys / 64; ++hh) tc::st32(tPb + hh * 32, z);
+              tc::st32(tPb, z);
+              tc::st32(tPb + 32, z);
+              if (!zero_tail_values()) { ok = false; break; }
+              publish(B_P_FULL0 + sb);
+              mbar_arrive(bar(B_P_LO0 + sb));
             } else {
               uint32_t sv[64];
               // pass 1: the row's extreme raw score, 64 columns at a time
               float rm = neg ? INFINITY : -INFINITY;
 #pragma unroll
-              for (int hh = 0; hh < kTileKeys / 64; ++hh) {
+              for (int hh = 0; hh < 2; ++hh) {
                 tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tc::wait_ld();
@@ -713,29 +760,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float msub = new_reference(rm);
               const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
               const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
-              // pass 2: the weights, 64 keys at a time, last half first (its
-              // scores are still in registers); each half's weights land on
-              // score columns already read (keys 64..127 -> columns 96..127, then
-              // keys 0..63 -> columns 64..95)
-              float lsum = 0.f;
-#pragma unroll
-              for (int hh = kTileKeys / 64 - 1; hh >= 0; --hh) {
-                if (hh != kTileKeys / 64 - 1) {
-                  tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                  tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                  tc::wait_ld();
-                  mask(sv, hh * 64);
-                }
-                uint32_t pk[32];
-                lsum += weights64(sv, ks2, nm2, pk);
-                tc::st32(tPb + hh * 32, pk);
-              }
+              // pass 2, keys 64..127 first (their scores are still in
+              // registers): weights over score columns 96..127, already read;
+              // their P V product starts while keys 0..63 are weighted
+              uint32_t pk[32];
+              float lsum = weights64(sv, ks2, nm2, pk);
+              tc::st32(tPb + 32, pk);
+              // the set's previous P V product completed before this tile's
+              // score product was issued (the score product waited for it), and
+              // none of this tile's is issued before P_FULL: the accumulator is still
+              rescale_o();
+              if (!zero_tail_values()) { ok = false; break; }
+              publish(B_P_FULL0 + sb);
+              // keys 0..63: weights over score columns 64..95
+              tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+              tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+              tc::wait_ld();
+              mask(sv, 0);
+              lsum += weights64(sv, ks2, nm2, pk);
+              tc::st32(tPb, pk);
+              tc::wait_st();
+              tc::fence_before();
+              mbar_arrive(bar(B_P_LO0 + sb));
               l += lsum;
             }
-            // the set's previous P V product completed before this tile's score
-            // product was issued (the score product waited for it): the
-            // accumulator can be rescaled now
-            rescale_o();
           } else {
             uint32_t pk[32];
             if (skip) {
@@ -762,25 +810,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after();
             rescale_o();
             tc::st32(tPb, pk);
+            if (!zero_tail_values()) { ok = false; break; }
+            publish(B_P_FULL0 + sb);
           }
-          tc::wait_st();
-          // value rows past the sequence end were never written: zero them
-          const int exist = L - k0;
-          if (exist < kTileKeys) {
-            const int s = g % kStages;
-            if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            const uint32_t vb = sV + s * kKVBytes;
-            const int first = exist < 0 ? 0 : exist;
-            for (int e = r; e < (kTileKeys - first) * kHalves * 8; e += kRows) {  // 16-byte chunks
-              const int row = first + e / (kHalves * 8), rem = e % (kHalves * 8), hf = rem / 8, c = rem % 8;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(vb + hf * Lay::kKVHalf + row * 128 + c * 16),
-                           "r"(0u)
-                           : "memory");
-            }
-          }
-          fence_proxy_async_shared();
-          tc::fence_before();
-          mbar_arrive(bar(B_P_FULL0 + sb));
         }
         if (!ok) break;
         // ---- end of a run
