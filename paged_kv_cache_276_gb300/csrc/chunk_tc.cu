@@ -25,19 +25,24 @@
 //    the run's other partitions empty, and the split-K combine kernel merges
 //    the slots.  A sequence with a single partition gets its bf16 output
 //    directly.
-//  * prefill (a chunk of its own length per sequence).  One item per
-//    (sequence, KV head, query tile), covering every key the tile's last token
-//    sees; items of one (sequence, KV head) are numbered together, longest
-//    first, and CTA c takes items c, c + grid, c + 2 grid, ...  The CTAs that
-//    run at the same time then sweep the same keys, so the re-reads hit L2.
-//    Every item writes its bf16 output directly; no workspace.
+//  * prefill (a chunk of its own length per sequence).  Batches of long
+//    chunks: one item per (sequence, KV head, pair of query tiles), covering
+//    every key the pair's last token sees; both query tiles are multiplied
+//    against each key and value tile, so the key / value traffic per product
+//    halves.  Batches of mostly short chunks (decode rows): one item per
+//    (sequence, KV head, query tile).  Items of one (sequence, KV head) are
+//    numbered together, longest first, and CTA c takes items c, c + grid,
+//    c + 2 grid, ...  The CTAs that run at the same time then sweep the same
+//    keys, so the re-reads hit L2.  Every item writes its bf16 output
+//    directly; no workspace.
 //
-// Warp roles: 0-7 softmax (thread = row; warps 0-3 take the even tiles of a
-// run, 4-7 the odd ones, each set with its own running max / sum and its own
-// TMEM accumulator, merged exactly at the end of the run by the even set),
-// 8 TMA producer of queries and keys, 9 score-product issuer (one lane) and
-// tensor-memory owner, 10 P V product issuer (one lane), 11 TMA producer of
-// values.
+// Warp roles: 0-7 softmax (thread = row).  Warps 0-3 and 4-7 are two sets,
+// each with its own running max / sum and its own TMEM accumulator: over a
+// pair of query tiles set q takes query tile q against every key tile;
+// otherwise set 0 takes the even key tiles of a run and set 1 the odd ones,
+// merged exactly at the end of the run by set 0.  8 TMA producer of queries
+// and keys, 9 score-product issuer (one lane) and tensor-memory owner, 10 P V
+// product issuer (one lane), 11 TMA producer of values.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -64,7 +69,7 @@ constexpr float kSlack = 8.f;    // lazy rescale threshold (log2 units)
 
 // barrier indices (8 bytes each)
 enum : int {
-  B_Q_FULL0 = 0, B_Q_FULL1, B_Q_FREE0, B_Q_FREE1, B_O_FULL, B_O_FREE,
+  B_Q_FULL0 = 0, B_Q_FULL1, B_Q_FREE0, B_Q_FREE1, B_O_FULL, B_O_FULL1, B_O_FREE, B_O_FREE1,
   B_S_FULL0, B_S_FULL1, B_S_FREE0, B_S_FREE1,
   B_P_FULL0, B_P_FULL1, B_P_LO0, B_P_LO1, B_PV_DONE0, B_PV_DONE1, B_STATS0, B_STATS1, B_STATS_FREE0,
   B_STATS_FREE1,
@@ -178,15 +183,18 @@ struct SeqTab {
   const int *qc;      // prefill: [B] chunk length (0 for a bad q_start entry)
 };
 
-// One work item: a query tile against the keys [k_lo, k_hi) of one sequence
-// and KV head.  A run is a maximal sequence of items sharing one accumulator.
+// One work item: a query tile (prefill: a pair of query tiles 2 qt and
+// 2 qt + 1, the second one present when has_b) against the keys [k_lo, k_hi)
+// of one sequence and KV head.  A run is a maximal sequence of items sharing
+// one accumulator.
 struct Item {
   int seq, head, qt, part, nparts, k_lo, k_hi;
-  bool run_begin, run_end;
+  bool run_begin, run_end, has_b;
 };
 
 // The items of this CTA in order (every role walks the same sequence).
-template <bool kPrefill>
+// kPairs: prefill items are pairs of query tiles.
+template <bool kPrefill, bool kPairs = false>
 struct Sched {
   int it, end, step;
   ItemWalker w;
@@ -232,10 +240,13 @@ struct Sched {
       x.part = 0;
       x.nparts = 1;
       x.k_lo = 0;
-      x.k_hi = min(L, max(0, L - c + min(c, tile_tok * (x.qt + 1))));
+      const int span = kPairs ? 2 * tile_tok : tile_tok;  // query tokens per item
+      x.k_hi = min(L, max(0, L - c + min(c, span * (x.qt + 1))));  // keys the item's last row sees
+      x.has_b = kPairs && (2 * x.qt + 1) * tile_tok < c;
       x.run_end = true;
     } else {
       x.qt = 0;
+      x.has_b = false;
       x.part = w.part;
       x.nparts = w.nparts;
       x.k_lo = w.part * p.part_tokens;
@@ -300,11 +311,12 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-template <int BS, bool kPrefill, int D>
+template <int BS, bool kPrefill, int D, bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const TcParams p) {
   using Lay = Layout<kPrefill, D>;
+  constexpr bool kP2 = kPrefill && kPairs;  // prefill over pairs of query tiles
   constexpr int kStages = Lay::kStages, kQBufs = Lay::kQBufs, kTileKeys = Lay::kTK, kKVBytes = Lay::kKVBytes;
   constexpr int kHalves = Lay::kHalves, kQBytes = Lay::kQBytes;
   // one TMA box per block of the tile (a block longer than the tile: the tile's piece of it)
@@ -351,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         qs[i] = a;
         qc[i] = c;
-        n = ceil_div(c, tile_tok) * hkv;
+        n = ceil_div(c, (kP2 ? 2 : 1) * tile_tok) * hkv;  // query tiles, or pairs of them
       } else {
         n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
       }
@@ -376,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_Q_FULL0 + i), 1);
       mbar_init(bar(B_Q_FREE0 + i), 1);
     }
-    mbar_init(bar(B_O_FULL), 1);
-    mbar_init(bar(B_O_FREE), kRows);
+    for (int i = 0; i < 2; ++i) {  // decode chunk: index 0 only; prefill: one per query tile of the pair
+      mbar_init(bar(B_O_FULL + i), 1);
+      mbar_init(bar(B_O_FREE + i), kRows);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_STATS0 + i), kRows);
       mbar_init(bar(B_STATS_FREE0 + i), kRows);
@@ -432,13 +446,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int full0 = is_v ? B_V_FULL0 : B_K_FULL0, empty0 = is_v ? B_V_EMPTY0 : B_K_EMPTY0;
       // decode: every key is read once; prefill: the CTAs beside this one read them too
       const uint64_t pol = kPrefill ? l2_policy_evict_normal() : l2_policy_evict_first();
-      Sched<kPrefill> sc;
+      Sched<kPrefill, kP2> sc;
       sc.begin(p, tab, I);
       int g = 0, tpieces = 0;
       int tw_seq = -1, tw_base = 0, tw_val = -1;
       for (; sc.valid() && !*abort_flag; sc.advance(p, tab)) {
         const Item &x = sc.x;
-        if (!is_v && x.run_begin && x.k_hi > x.k_lo) {  // a run with keys: load its queries
+        if (kP2 && !is_v && x.k_hi > x.k_lo) {  // the pair's query tiles, both into buffers 0 and 1
+          const int qi = tpieces++;
+          if (qi > 0 && !wait_warp(bar(B_Q_FREE0), (qi - 1) & 1)) {
+            if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          if (lane == 0) {
+            const int gsz = 1 << p.lg_group, tile_tok = kRows >> p.lg_group;
+            const int ntq = x.has_b ? 2 : 1;
+            mbar_arrive_expect_tx(bar(B_Q_FULL0), ntq * kQBytes);
+            for (int q = 0; q < ntq; ++q)
+              for (int hf = 0; hf < kHalves; ++hf)
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + q * kQBytes + hf * Lay::kQHalf),
+                    "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(hf * 64), "r"(x.head * gsz),
+                    "r"(qs[x.seq] + tile_tok * (2 * x.qt + q)), "r"(bar(B_Q_FULL0))
+                    : "memory");
+          }
+        }
+        if (!kP2 && !is_v && x.run_begin && x.k_hi > x.k_lo) {  // a run with keys: load its queries
           const int qi = tpieces++, qb = qi % kQBufs, use = qi / kQBufs;
           if (use > 0 && !wait_warp(bar(B_Q_FREE0 + qb), (use - 1) & 1)) {
             if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
@@ -500,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         for (int y = g > kStages ? g - kStages : 0; y < g; ++y)
           mbar_wait_sleep(bar(full0 + (y % kStages)), (y / kStages) & 1);
-        if (!is_v)
+        if (!is_v && kP2 && tpieces > 0) mbar_wait_sleep(bar(B_Q_FULL0), (tpieces - 1) & 1);
+        if (!is_v && !kP2)
           for (int qi = tpieces > kQBufs ? tpieces - kQBufs : 0; qi < tpieces; ++qi)
             mbar_wait_sleep(bar(B_Q_FULL0 + qi % kQBufs), (qi / kQBufs) & 1);
       }
@@ -514,14 +550,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       // completion), so each issue follows its event closely.
       if (lane == 0) {
         constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
-        Sched<kPrefill> sc;
+        Sched<kPrefill, kP2> sc;
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0;
         bool ok = true;
+        int na = 0, nb = 0;  // prefill: score products of each query tile of the pair so far
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
           if (ntile == 0) continue;
+          if constexpr (kP2) {
+            // both query tiles of the pair against each key tile: tile A into
+            // S buffer 0, tile B into buffer 1; each buffer holds its tile's
+            // previous P until that P V product completes
+            const int qi = tpieces++;
+            if (!mbar_wait(bar(B_Q_FULL0), qi & 1)) { ok = false; break; }
+            for (int t = 0; t < ntile && ok; ++t, ++g) {
+              const int s = g % kStages;
+              if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+              const uint32_t kb = sK + s * kKVBytes;
+              for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
+                int &n = q ? nb : na;
+                if (n > 0 && !mbar_wait(bar(B_PV_DONE0 + q), (n - 1) & 1)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t sq = sQ + q * kQBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                  tc::mma(tS0 + q * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
+                          tc::desc_sw128(kb + (ks >> 2) * Lay::kKVHalf + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
+                tc::commit(bar(B_S_FULL0 + q));
+                ++n;
+              }
+              if (!ok) break;
+              tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by these products only
+              if (t == ntile - 1) tc::commit(bar(B_Q_FREE0));
+            }
+            continue;
+          }
           int qb = (tpieces > 0 ? tpieces - 1 : 0) % kQBufs;
           if (x.run_begin) {
             const int qi = tpieces++;
@@ -560,14 +625,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // its values have landed; its value stage is released when it completes.
       if (lane == 0) {
         constexpr uint32_t kIdO = tc::idesc_bf16(kRows, D, false, true);
-        Sched<kPrefill> sc;
+        Sched<kPrefill, kP2> sc;
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0, run_g0 = 0;
+        int na = 0, nb = 0, ia = 0, ib = 0;  // prefill: P V products and items of each query tile of the pair
         bool ok = true;
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
           if (ntile == 0) continue;
+          if constexpr (kP2) {
+            // per key tile: tile A's product, then tile B's (so that B's
+            // product follows A's zeroing of the value rows past the end)
+            ++ia;
+            if (x.has_b) ++ib;
+            for (int t = 0; t < ntile && ok; ++t, ++g) {
+              const int vs = g % kStages;
+              if (!mbar_wait(bar(B_V_FULL0 + vs), (g / kStages) & 1)) { ok = false; break; }
+              const uint32_t vb = sV + vs * kKVBytes;
+              constexpr int kSteps = kTileKeys / 16;  // 16 keys = 8 packed columns of P
+              for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
+                int &n = q ? nb : na;
+                const int items = q ? ib : ia;
+                if (!mbar_wait(bar(B_P_FULL0 + q), n & 1)) { ok = false; break; }
+                // the item's first product overwrites the accumulator: the previous epilogue must have read it
+                if (t == 0 && items > 1 && !mbar_wait(bar(B_O_FREE + q), (items - 2) & 1)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t pa = tP0 + q * Lay::kPStride, acc = tmem + q * D;
+                // keys kTK/2.. first (P_FULL), keys 0.. once weighted (P_LO)
+#pragma unroll
+                for (int ks = kSteps / 2; ks < kSteps; ++ks)
+                  tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
+                             !(t == 0 && ks == kSteps / 2));
+                if (!mbar_wait(bar(B_P_LO0 + q), n & 1)) { ok = false; break; }
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kSteps / 2; ++ks)
+                  tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO, true);
+                tc::commit(bar(B_PV_DONE0 + q));
+                if (t == ntile - 1) tc::commit(bar(B_O_FULL + q));
+                ++n;
+              }
+              if (!ok) break;
+              tc::commit(bar(B_V_EMPTY0 + vs));
+            }
+            continue;
+          }
           if (x.run_begin) {
             ++tpieces;
             run_g0 = g;
@@ -614,16 +717,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------------ softmax warps
-      const int set = warp >> 2;                  // 0: even tiles of a run, 1: odd tiles
+      // decode chunk: set 0 takes the even tiles of a run, set 1 the odd ones;
+      // prefill: set q takes every tile of query tile q of the pair
+      const int set = warp >> 2;
       const int r = threadIdx.x & (kRows - 1);    // query row = TMEM lane
       const int tok = r >> p.lg_group, gh = r & ((1 << p.lg_group) - 1);
       const int tile_tok = kRows >> p.lg_group;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tO = tmem + set * D;         // this set's accumulator
       float2 *stats = reinterpret_cast<float2 *>(smem + Lay::kSmemStats);
-      Sched<kPrefill> sc;
+      Sched<kPrefill, kP2> sc;
       sc.begin(p, tab, I);
       int g = 0, tpieces = 0;
+      int n_set = 0, items_set = 0;  // prefill: this set's tiles and items so far
       float m = -INFINITY, l = 0.f;
       int run_first_part = 0;
       bool run_has_tiles = false, set_has_tiles = false;
@@ -632,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item &x = sc.x;
         const int L = lens[x.seq];
         const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
+        if (kP2 && set == 1 && !x.has_b) continue;  // the pair has no second query tile
         if (x.run_begin) {
           m = -INFINITY;
           l = 0.f;
@@ -645,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool row_valid;
         if (kPrefill) {
           const int c = qc[x.seq];
-          row_tok = tile_tok * x.qt + tok;
+          row_tok = tile_tok * (kP2 ? 2 * x.qt + set : x.qt) + tok;
           row_valid = row_tok < c;
           limit = row_valid ? L - c + 1 + row_tok : 0;
         } else {
@@ -654,11 +761,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           limit = row_valid ? L - p.q_len + 1 + tok : 0;
         }
         for (int t = 0; t < ntile; ++t, ++g) {
-          if ((g & 1) != set) continue;  // the other set's tile
+          if (!kP2 && (g & 1) != set) continue;  // the other set's tile
           const bool first_tile_of_set = !set_has_tiles;
           set_has_tiles = true;
           const int sb = set;
-          if (!wait_warp(bar(B_S_FULL0 + sb), (g >> 1) & 1)) { ok = false; break; }
+          const uint32_t sphase = kP2 ? (n_set++ & 1) : ((g >> 1) & 1);
+          if (!wait_warp(bar(B_S_FULL0 + sb), sphase)) { ok = false; break; }
           const int k0 = x.k_lo + t * kTileKeys;
           const int vis = min(limit, x.k_hi) - k0;  // keys of this tile the row sees
           const uint32_t tSb = tS0 + sb * kTileKeys + lane_off;      // this row's scores
@@ -711,7 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // before any P V product of this tile reads the stage
           auto zero_tail_values = [&]() {
             const int exist = L - k0;
-            if (exist >= kTileKeys) return true;
+            // prefill: query tile A's set zeroes; B's P V product is issued after A's
+            if (exist >= kTileKeys || (kP2 && set == 1)) return true;
             const int s = g % kStages;
             if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) return false;
             const uint32_t vb = sV + s * kKVBytes;
@@ -817,6 +926,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // ---- end of a run
         if (!x.run_end) continue;
+        if constexpr (kP2) {
+          // this set's query tile: normalise its accumulator and store its rows
+          float inv = 0.f;
+          if (run_has_tiles) {
+            ++items_set;
+            if (!wait_warp(bar(B_O_FULL + set), (items_set - 1) & 1)) { ok = false; break; }
+            tc::fence_after();
+            inv = l > 0.f ? 1.f / l : 0.f;
+          }
+          const size_t orow = static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + (x.head << p.lg_group) + gh;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t ov[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = 0u;
+            if (run_has_tiles) {
+              tc::ld32(tO + lane_off + ch * 32, ov);
+              tc::wait_ld();
+            }
+            if (!row_valid) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + ch * 32);
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 0]) * inv, __uint_as_float(ov[c8 * 8 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 2]) * inv, __uint_as_float(ov[c8 * 8 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 4]) * inv, __uint_as_float(ov[c8 * 8 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 6]) * inv, __uint_as_float(ov[c8 * 8 + 7]) * inv);
+              dst[c8] = v;
+            }
+          }
+          if (run_has_tiles) {
+            tc::fence_before();
+            mbar_arrive(bar(B_O_FREE + set));
+          }
+          continue;
+        }
         const int rp = tpieces & 1;
         if (set == 1) {  // the odd set hands its (max, sum) to the even set
           if (run_has_tiles) {
@@ -906,21 +1052,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
 
-template <bool kPrefill, int D>
+template <bool kPrefill, int D, bool kPairs>
 KernelFn pick_kernel(int block_size) {
   switch (block_size) {
-    case 16: return chunk_tc_kernel<16, kPrefill, D>;
-    case 32: return chunk_tc_kernel<32, kPrefill, D>;
-    case 64: return chunk_tc_kernel<64, kPrefill, D>;
-    default: return chunk_tc_kernel<128, kPrefill, D>;
+    case 16: return chunk_tc_kernel<16, kPrefill, D, kPairs>;
+    case 32: return chunk_tc_kernel<32, kPrefill, D, kPairs>;
+    case 64: return chunk_tc_kernel<64, kPrefill, D, kPairs>;
+    default: return chunk_tc_kernel<128, kPrefill, D, kPairs>;
   }
 }
 
-template <bool kPrefill, int D>
+template <bool kPrefill, int D, bool kPairs>
 int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
                 int block_size, cudaStream_t stream) {
   using Lay = Layout<kPrefill, D>;
-  const KernelFn kernel = pick_kernel<kPrefill, D>(block_size);
+  const KernelFn kernel = pick_kernel<kPrefill, D, kPairs>(block_size);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(Lay::bytes(Lay::kMaxSeqs)))) != cudaSuccess)
@@ -940,11 +1086,11 @@ int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMa
   return PKV_OK;
 }
 
-template <bool kPrefill>
+template <bool kPrefill, bool kPairs>
 int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
               int block_size, int head_dim, cudaStream_t stream) {
-  return head_dim == 64 ? launch_tc_d<kPrefill, 64>(tmq, tmk, tmv, p, block_size, stream)
-                        : launch_tc_d<kPrefill, 128>(tmq, tmk, tmv, p, block_size, stream);
+  return head_dim == 64 ? launch_tc_d<kPrefill, 64, kPairs>(tmq, tmk, tmv, p, block_size, stream)
+                        : launch_tc_d<kPrefill, 128, kPairs>(tmq, tmk, tmv, p, block_size, stream);
 }
 
 // The kernels compare raw scores before scaling them; a zero scale would turn
@@ -995,7 +1141,7 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.lg_group = lg;
   p.q_len = a.q_len;
   p.scale_log2 = kernel_scale_log2(a.scale);
-  return launch_tc<false>(tmq, tmk, tmv, p, a.block_size, a.head_dim, stream);
+  return launch_tc<false, false>(tmq, tmk, tmv, p, a.block_size, a.head_dim, stream);
 }
 
 }  // namespace pkv
@@ -1054,5 +1200,11 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   p.total_q = total_q;
   p.lg_group = lg;
   p.scale_log2 = kernel_scale_log2(scale);
-  return launch_tc<true>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
+  // Batches of long chunks run over pairs of query tiles, which share every
+  // key and value tile (half the key / value traffic per product); batches
+  // of mostly short chunks (decodes) split each query tile's keys between the
+  // two softmax sets instead, so that both sets work on every item.
+  if (static_cast<long long>(total_q) >= 2ll * (kRows >> lg) * num_seqs)
+    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
+  return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
 }

@@ -302,3 +302,27 @@ def test_tensor_core_decode_chunk_at_the_sequence_limit():
     ref = OA.paged_attention(bits(q), bits(kc), bits(vc), tables, np.asarray(lens, dtype=np.int32), num_q_heads=Hq,
                              num_kv_heads=Hkv, head_dim=d, block_size=bs, scale=scale, q_len=16)
     assert_attention_close(out, ref, "decode chunk, 2048 sequences")
+
+
+@pytest.mark.parametrize("d,bs,Hq,Hkv", [(128, 16, 64, 8), (64, 32, 32, 4), (128, 32, 16, 4)])
+def test_both_prefill_schedules_match_the_oracle(d, bs, Hq, Hkv):
+    """A batch of long chunks runs over pairs of query tiles; padding the
+    batch with empty sequences (chunk 0: no rows) lowers the mean chunk below
+    two query tiles, and the call then splits each query tile's keys between
+    the two softmax sets instead.  Every real row matches the oracle both ways."""
+    lens = [700, 129, 40, 1000, 3]
+    chunks = [300, 129, 1, 257, 3]
+    G = Hq // Hkv
+    tile_tok = 128 // G
+    n_pad = int(sum(chunks) // (2 * tile_tok)) + 1 - len(lens)  # mean chunk < 2 query tiles
+    assert sum(chunks) >= 2 * tile_tok * len(lens)
+    pad_lens, pad_chunks = lens + [17] * n_pad, chunks + [0] * n_pad
+    assert sum(pad_chunks) < 2 * tile_tok * len(pad_lens)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    for L_, C_ in ((lens, chunks), (pad_lens, pad_chunks)):
+        q, kc, vc, tables, q_start = prefill_case(L_, C_, bs, Hq, Hkv, seed=40 + d, d=d)
+        st = status_tensor()
+        out = run_prefill(q, kc, vc, tables, L_, q_start, scale, status=st)
+        assert st.item() == 0
+        ref = oracle_prefill(q, kc, vc, tables, L_, q_start, Hq, Hkv, bs, scale, d=d)
+        assert_attention_close(out, ref, f"prefill schedule for {len(L_)} sequences")
