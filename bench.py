@@ -230,6 +230,7 @@ class Runner:
         ev = pool.pop
         step_ms, dec_ms, main_ms = [], [], []
         launches = 0
+        fused = sess.q_len == 1  # single-token decode: the new token's store folded into the decode
         barrier(world)
         torch.cuda.synchronize()
         with ClockSampler(gpu_id()) as clocks:
@@ -244,16 +245,23 @@ class Runner:
                     if p.cow_pairs is not None:
                         native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
                         launches += i >= warmup
-                    native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
                     d0, d1 = ev(), ev()
-                    d0.record(stream)
-                    native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
-                                                  p.max_len, sess.scale, out, ws, sess.partition_size, status,
-                                                  stream)
+                    if fused:  # the new token's store runs inside the decode's grid
+                        d0.record(stream)
+                        native.paged_attention_decode_write(q, ks[l], vs[l], p.slots, sess.k_caches[l],
+                                                            sess.v_caches[l], p.tables, p.lens, p.max_len,
+                                                            sess.scale, out, ws, sess.partition_size, status, stream)
+                    else:
+                        native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
+                        d0.record(stream)
+                        native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
+                                                      p.max_len, sess.scale, out, ws, sess.partition_size, status,
+                                                      stream)
                     d1.record(stream)
                     dec.append((d0, d1))
                     nparts = math.ceil(p.max_len / (sess.partition_size or DEFAULT_PARTITION)) if p.max_len else 1
-                    launches += (i >= warmup) * (2 + (nparts > 1))  # write, decode, cross-partition combine
+                    # (write,) decode, cross-partition combine
+                    launches += (i >= warmup) * ((1 if fused else 2) + (nparts > 1))
                 s1.record(stream)
                 if i >= warmup:
                     step_ms.append((s0, s1))
@@ -271,12 +279,19 @@ class Runner:
                 for l in range(sess.layers):
                     if p.cow_pairs is not None:
                         native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
-                    native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
                     d0, dm = ev(), ev()
-                    d0.record(stream)
-                    native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
-                                                  p.max_len, sess.scale, out, ws, sess.partition_size, status,
-                                                  stream, main_done_event=dm)
+                    if fused:
+                        d0.record(stream)
+                        native.paged_attention_decode_write(q, ks[l], vs[l], p.slots, sess.k_caches[l],
+                                                            sess.v_caches[l], p.tables, p.lens, p.max_len,
+                                                            sess.scale, out, ws, sess.partition_size, status, stream,
+                                                            main_done_event=dm)
+                    else:
+                        native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
+                        d0.record(stream)
+                        native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
+                                                      p.max_len, sess.scale, out, ws, sess.partition_size, status,
+                                                      stream, main_done_event=dm)
                     main_ms.append((d0, dm))
             torch.cuda.synchronize()
         barrier(world)
@@ -488,7 +503,8 @@ def run_ours(args, rank, world, local):
                    "l2": "flushed before every step (write of 2x L2), outside the per-step CUDA events",
                    "kv_bytes_per_step": int(dev_res["kv_bytes_per_step"]),
                    "query_tokens_per_step": dev_res["query_tokens_per_step"],
-                   "step": "host allocator (precomputed) + pkv_write + paged_attention_decode (+combine)"},
+                   "step": "host allocator (precomputed) + paged_attention_decode_write (the new tokens' store "
+                           "and the decode in one grid) + cross-partition combine"},
         "query_tok_s": round(dev_res["query_tokens_per_step"] * world / (ms * 1e-3), 1),
         "step_ms_p10": round(dev_res["step_ms_p10"], 5), "step_ms_p90": round(dev_res["step_ms_p90"], 5),
         "roofline": {"bound": "hbm", "achieved": round(main_gbs, 1), "peak": peak, "unit": "GB/s",

@@ -192,6 +192,40 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                               void *main_done_event);
 
 /*
+ * paged_attention_decode_write -- the decode step of single-token sequences
+ * with the new token's store folded in: pkv_write of num_seqs tokens followed
+ * by paged_attention_decode with q_len = 1, as one call.
+ *
+ * Pages: each decode step stores the new token's keys and values in their
+ * slot and then attends over the sequence's blocks (x321.org "The serving
+ * bottleneck is not just FLOPs", "First understand what the KV cache is
+ * storing" and "PagedAttention borrows an operating-system trick").
+ *   k_new, v_new   device, [num_seqs][num_kv_heads][head_dim] bf16: the newest
+ *                  token of each sequence
+ *   slot_mapping   device, [num_seqs] int64: slot of sequence i's newest token,
+ *                  which must be its table position, i.e. block_tables[i][(L-1)
+ *                  / block_size] * block_size + (L-1) % block_size with L =
+ *                  seq_lens[i] (the slot the allocator's append returns), or
+ *                  negative for no store
+ *   everything else as paged_attention_decode (q, out [num_seqs][1][Hq][d]).
+ * The CTA that reads the newest token's block stores the token's rows itself
+ * before its first copy, so no separate write grid runs.  A non-negative slot
+ * other than the newest token's table position is undefined: where the check
+ * runs it sets PKV_STATUS_BAD_SLOT and the token is not stored.  Where the
+ * decode runs on the tensor cores (max_seq_len >= 16384) the store is a
+ * separate pkv_write launch before it.  main_done_event as in
+ * paged_attention_decode_ex (may be NULL).
+ */
+int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                 const int64_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, float scale, int partition_size, pkv_bf16 *out,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                 void *stream, void *main_done_event);
+
+/*
  * paged_attention_prefill -- attention of a chunk of new tokens per sequence,
  * each sequence with its own chunk length (chunked prefill).
  *
@@ -398,7 +432,8 @@ int pkv_refcount(const pkv_alloc *a, int block);
  * (x321.org "The serving bottleneck is not just FLOPs", "PagedAttention
  * borrows an operating-system trick").  The runner chains exactly those calls
  * of this library: pkv_seq_append_batch, pkv_block_table, then per layer
- * pkv_write and paged_attention_decode.  The pages have no counterpart to the
+ * pkv_write and paged_attention_decode (for single-token steps the pair as
+ * paged_attention_decode_write).  The pages have no counterpart to the
  * runner itself; it exists so that a serving loop pays one host call per step
  * instead of one per operation and per layer.
  *
@@ -483,7 +518,8 @@ void pkv_step_destroy(pkv_step *s);
  *      sequences into host_stage;
  *   4. enqueue on `stream`: host_stage -> dev_stage, for each layer l the
  *      pkv_write of its n * q_len new keys and values and the
- *      paged_attention_decode of its n query rows, dev_out -> host_out.
+ *      paged_attention_decode of its n query rows (q_len = 1: both as one
+ *      paged_attention_decode_write), dev_out -> host_out.
  * Returns after the enqueue.  The caller writes the step's queries, keys and
  * values for rows 0..n-1 into host_stage before the call, and may touch
  * host_stage and host_out again only after pkv_step_wait (or a synchronisation

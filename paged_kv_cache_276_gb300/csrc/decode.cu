@@ -67,6 +67,11 @@ struct Params {
   int oob_row;       // a TMA row coordinate wholly outside the cache (reads zeros)
   int active_warps;  // chunk kernel: consumer warps that own at least one real row
   float scale_log2;  // scale * log2(e)
+  // single-token decode with the new token's write folded in (k_new == nullptr: none):
+  // sequence i's key / value rows [Hkv][D] go to slot slots[i] before the reads
+  const uint4 *k_new, *v_new;
+  const int64_t *slots;
+  uint4 *k_cache, *v_cache;
 };
 
 // A block is staged as one or more "units" of consecutive token rows: the
@@ -114,6 +119,34 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 __device__ __forceinline__ int first_window(const Params &p, int seq, int part, int lane) {
   const int e = part * p.part_blocks + lane;
   return e < p.max_blocks ? p.block_tables[static_cast<size_t>(seq) * p.max_blocks + e] : -1;
+}
+
+// The new token's key and value rows of (seq, KV head h), stored by the
+// producer warp of the CTA whose partition holds the token (the last one)
+// before it issues any copy: one 16-byte chunk per lane, then a proxy fence so
+// that the tensor copies that follow read the new rows.  Only this CTA reads
+// the token's slot, which is the table position of token L - 1; a different
+// slot is reported (PKV_STATUS_BAD_SLOT) and not written.
+template <int D, int BS>
+__device__ __forceinline__ void store_new_token(const Params &p, int seq, int h, int L, int lane) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+  const int64_t slot = p.slots[seq];
+  if (slot < 0) return;
+  const int last = L - 1, e = last / BS;
+  const int entry = last >= 0 && e < p.max_blocks ? p.block_tables[static_cast<size_t>(seq) * p.max_blocks + e] : -1;
+  if (entry < 0 || entry >= p.num_blocks || slot != static_cast<int64_t>(entry) * BS + last % BS) {
+    if (lane == 0 && h == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_SLOT);
+    return;
+  }
+  const size_t src = (static_cast<size_t>(seq) * p.num_kv_heads + h) * kChunks;
+  const size_t dst = ((static_cast<size_t>(entry) * p.num_kv_heads + h) * BS + last % BS) * kChunks;
+  if (lane < kChunks) {
+    p.k_cache[dst + lane] = p.k_new[src + lane];
+  } else if (lane < 2 * kChunks) {
+    p.v_cache[dst + lane - kChunks] = p.v_new[src + lane - kChunks];
+  }
+  fence_proxy_async_global();
+  __syncwarp();
 }
 
 // Producer (one whole warp): walk this partition's block-table entries and
@@ -226,6 +259,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   WarpAcc<D, NT> acc;
   if (warp == kDecodeWarps) {
+    if (p.k_new && part == nparts - 1) store_new_token<D, BS>(p, seq, h, L, lane);
     produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
@@ -685,6 +719,20 @@ bool make_tensor_map_3d(void *map, const void *base, int dim0, int dim1, long lo
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The new token of every sequence, written by the decode itself
+// (paged_attention_decode_write): rows [num_seqs][Hkv][D] and their slots.
+struct NewTokens {
+  const void *k, *v;
+  const int64_t *slots;
+  pkv_bf16 *k_cache, *v_cache;
+};
+
+int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
+                 int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                 int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                 void *stream, void *main_done_event, const NewTokens *nt);
+
 }  // namespace pkv
 
 extern "C" {
@@ -713,7 +761,37 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
                               int head_dim, int block_size, int num_blocks, float scale, int partition_size,
                               pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
                               void *stream, void *main_done_event) {
-  using namespace pkv;
+  return pkv::decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                           q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                           partition_size, out, workspace, workspace_bytes, d_status, stream, main_done_event,
+                           nullptr);
+}
+
+int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                 const int64_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                                 int num_seqs, int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, float scale, int partition_size, pkv_bf16 *out,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status, void *stream,
+                                 void *main_done_event) {
+  if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping)) return PKV_ERR_ARG;
+  if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_ERR_ARG;
+  const pkv::NewTokens nt{k_new, v_new, slot_mapping, k_cache, v_cache};
+  return pkv::decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                           1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                           out, workspace, workspace_bytes, d_status, stream, main_done_event, &nt);
+}
+
+}  // extern "C"
+
+namespace pkv {
+
+int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
+                 int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                 int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                 void *stream, void *main_done_event, const NewTokens *nt) {
   cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   if (num_seqs < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
@@ -749,6 +827,12 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   cudaStream_t st = as_stream(stream);
   if (chunk_tc_supported(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size, plan.part_tokens) &&
       (q_len > 1 || max_seq_len >= kTcDecodeMinLen)) {
+    if (nt) {  // the tensor-core kernel takes the new tokens from the cache: write them first
+      const int rc = pkv_write(static_cast<const pkv_bf16 *>(nt->k), static_cast<const pkv_bf16 *>(nt->v), nt->slots,
+                               num_seqs, nt->k_cache, nt->v_cache, num_blocks, block_size, num_kv_heads, head_dim,
+                               d_status, stream);
+      if (rc != PKV_OK) return rc;
+    }
     ChunkTcArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -821,6 +905,13 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   p.oob_row = static_cast<int>(rows);
   p.active_warps = (group * kChunkLen + 15) / 16;
   p.scale_log2 = scale * kLog2e;
+  if (nt) {
+    p.k_new = static_cast<const uint4 *>(nt->k);
+    p.v_new = static_cast<const uint4 *>(nt->v);
+    p.slots = nt->slots;
+    p.k_cache = reinterpret_cast<uint4 *>(nt->k_cache);
+    p.v_cache = reinterpret_cast<uint4 *>(nt->v_cache);
+  }
 
   switch (head_dim * 1000 + block_size) {
     case 128016: return launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done);
@@ -834,7 +925,7 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
   }
 }
 
-}  // extern "C"
+}  // namespace pkv
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of paged_attention_decode.

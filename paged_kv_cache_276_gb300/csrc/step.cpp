@@ -74,12 +74,20 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len) {
     const auto *kn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.k_offset + l * L.kv_layer_bytes);
     const auto *vn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.v_offset + l * L.kv_layer_bytes);
     auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
-    int rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
-                       c.head_dim, s->status, st);
-    if (rc != PKV_OK) return rc;
-    rc = paged_attention_decode(q, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n, max_seq_len, c.q_len,
-                                c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks, c.scale,
-                                c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
+    int rc;
+    if (c.q_len == 1) {  // the allocator's slots are the newest tokens' table positions: one grid
+      rc = paged_attention_decode_write(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
+                                        max_seq_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                                        c.num_blocks, c.scale, c.partition_size, out, s->ws, s->ws_bytes,
+                                        s->status, st, nullptr);
+    } else {
+      rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
+                     c.head_dim, s->status, st);
+      if (rc != PKV_OK) return rc;
+      rc = paged_attention_decode(q, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n, max_seq_len,
+                                  c.q_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks,
+                                  c.scale, c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
+    }
     if (rc != PKV_OK) return rc;
   }
   e = cudaMemcpyAsync(s->hout, s->dout, L.out_bytes, cudaMemcpyDeviceToHost, st);

@@ -74,6 +74,9 @@ SIGNATURES = {
                                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                            _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
                                            _c_ptr, _c_ptr]),
+    "paged_attention_decode_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
+                                              _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                              _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr, _c_ptr]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -225,6 +228,38 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, seq_lens, max_seq_
         if not handle:
             raise ValueError("main_done_event: record the torch.cuda.Event once before passing it")
         _check(lib().paged_attention_decode_ex(*args, ctypes.c_void_p(handle)), "paged_attention_decode_ex")
+
+
+def paged_attention_decode_write(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens,
+                                 max_seq_len, scale, out, workspace=None, partition_size=0, d_status=None,
+                                 stream=None, main_done_event=None):
+    """pkv_write of each sequence's newest token + single-token decode, one call.
+
+    q, out: [B, 1, Hq, d] bf16; k_new, v_new: [B, Hkv, d] bf16; slot_mapping: [B] int64 (the newest
+    token's slot, or negative); caches [NB, Hkv, bs, d]; tables [B, max_blocks] int32; lens [B] int32."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_new, "k_new", torch.bfloat16), (v_new, "v_new", torch.bfloat16),
+                     (slot_mapping, "slot_mapping", torch.int64), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (out, "out", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    B, q_len, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if q_len != 1 or d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape \
+            or k_new.shape != (B, Hkv, d) or v_new.shape != (B, Hkv, d) or slot_mapping.shape != (B,) \
+            or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ev = None
+    if main_done_event is not None:
+        ev = main_done_event.cuda_event
+        if not ev:
+            raise ValueError("main_done_event: record the torch.cuda.Event once before passing it")
+    _check(lib().paged_attention_decode_write(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), B, int(max_seq_len), Hq, Hkv, d, bs, NB, float(scale),
+        int(partition_size), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev),
+        None if ev is None else ctypes.c_void_p(ev)), "paged_attention_decode_write")
 
 
 def paged_attention_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, d_status=None,

@@ -390,3 +390,19 @@ def test_step_create_and_run_reject_bad_arguments_before_any_launch(native):
     assert lib.pkv_step_wait(None) == native.PKV_ERR_ARG
     lib.pkv_step_destroy(None)
     a.close()
+
+
+def test_decode_write_rejects_bad_arguments_before_launch(native):
+    lib = native.lib()
+    args = dict(q=16, kn=16, vn=16, slots=16, kc=16, vc=16, tb=16, lens=16)
+
+    def call(**over):
+        a = {**args, **over}
+        return lib.paged_attention_decode_write(a["q"], a["kn"], a["vn"], a["slots"], a["kc"], a["vc"], a["tb"], 4,
+                                                a["lens"], 2, 64, 32, 8, 128, 16, 10, 0.1, 0, 16, None, 0, None, None,
+                                                None)
+    assert call(kn=None) == native.PKV_ERR_ARG       # no new keys
+    assert call(slots=None) == native.PKV_ERR_ARG
+    assert call(vn=24) == native.PKV_ERR_ARG         # misaligned
+    assert call(slots=12) == native.PKV_ERR_ARG      # int64 slots must be 8-byte aligned
+    assert call(q=24) == native.PKV_ERR_ARG

@@ -637,3 +637,99 @@ def test_shared_prefix_layout_equals_private_copies_bit_exact():
         T2[i, j] = n
     out2 = run_decode(q, kc2, vc2, T2, step.host_lens, sess.scale, sess.partition_size, step.max_len)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+# ------------------------------------------------------------------ decode with the new token's store
+def _newest_slots(tables, lens, bs):
+    return np.array([int(tables[i][(n - 1) // bs]) * bs + (n - 1) % bs if n > 0 else -1
+                     for i, n in enumerate(lens)], dtype=np.int64)
+
+
+@pytest.mark.parametrize("d,bs,Hq,Hkv,part", [(128, 16, 32, 8, 256), (64, 32, 16, 4, 0), (128, 128, 32, 2, 512),
+                                             (128, 64, 8, 8, 128), (64, 16, 64, 4, 0)])
+def test_decode_write_equals_write_then_decode(d, bs, Hq, Hkv, part):
+    """paged_attention_decode_write = pkv_write of the newest tokens + single-token
+    decode: the same output and cache bits, and the oracle on the written cache."""
+    lens = [1, 17, 300, 1025, 64, 2000, 33]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=d + bs + Hq)
+    B = len(lens)
+    slots = _newest_slots(tables, lens, bs)
+    slots[4] = -1  # no store for one sequence
+    k_new = inputs.randn_bf16((B, Hkv, d), 901, "cuda")
+    v_new = inputs.randn_bf16((B, Hkv, d), 902, "cuda")
+    slots_d = torch.as_tensor(slots, device="cuda")
+    tables_d = torch.as_tensor(np.asarray(tables, dtype=np.int32), device="cuda")
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    max_len = max(lens)
+    n = native.paged_attention_workspace_size(B, 1, Hq, d, max_len, part)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    kc2, vc2 = kc.clone(), vc.clone()
+    st = status_tensor()
+    native.pkv_write(k_new, v_new, slots_d, kc, vc, st)
+    ref_out = torch.empty_like(q)
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max_len, 0.09, ref_out, ws, part, st)
+    out = torch.empty_like(q)
+    native.paged_attention_decode_write(q, k_new, v_new, slots_d, kc2, vc2, tables_d, lens_d, max_len, 0.09, out,
+                                        ws, part, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(vc2.view(torch.int16), vc.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    ref = oracle_decode(q, kc2, vc2, tables, lens, (Hq, Hkv, d, bs), 0.09)
+    assert_attention_close(out, ref, "decode with the new token's store")
+
+
+def test_decode_write_reports_a_slot_other_than_the_newest_position():
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    lens = [40, 100, 7]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=77, spare=8)
+    slots = _newest_slots(tables, lens, bs)
+    foreign = int(slots[1]) - 3  # a slot of sequence 1 that is not its newest token's
+    slots[1] = foreign
+    k_new = inputs.randn_bf16((3, Hkv, d), 903, "cuda")
+    v_new = inputs.randn_bf16((3, Hkv, d), 904, "cuda")
+    before_k = bits(kc)
+    st = status_tensor()
+    out = torch.empty_like(q)
+    native.paged_attention_decode_write(q, k_new, v_new, torch.as_tensor(slots, device="cuda"), kc, vc,
+                                        torch.as_tensor(np.asarray(tables, dtype=np.int32), device="cuda"),
+                                        torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda"), max(lens),
+                                        0.09, out, None, 0, st)
+    torch.cuda.synchronize()
+    assert st.item() & native.PKV_STATUS_BAD_SLOT
+    after_k = bits(kc)
+    blk, off = divmod(foreign, bs)
+    assert np.array_equal(after_k[blk, :, off], before_k[blk, :, off])  # not stored
+    for i in (0, 2):  # the other sequences' tokens are stored
+        b, o = divmod(int(slots[i]), bs)
+        assert np.array_equal(after_k[b, :, o], bits(k_new)[i])
+
+
+def test_decode_write_on_the_tensor_core_route_equals_write_then_decode():
+    """max_seq_len >= 16384 routes single-token decodes to the tensor cores; the
+    store then runs as its own launch first, with the same result."""
+    d, bs, Hq, Hkv = 128, 32, 64, 8
+    lens = [16400, 300, 17000]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=88)
+    B = len(lens)
+    slots = _newest_slots(tables, lens, bs)
+    k_new = inputs.randn_bf16((B, Hkv, d), 905, "cuda")
+    v_new = inputs.randn_bf16((B, Hkv, d), 906, "cuda")
+    slots_d = torch.as_tensor(slots, device="cuda")
+    tables_d = torch.as_tensor(np.asarray(tables, dtype=np.int32), device="cuda")
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    n = native.paged_attention_workspace_size(B, 1, Hq, d, max(lens), 512)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    kc2, vc2 = kc.clone(), vc.clone()
+    st = status_tensor()
+    native.pkv_write(k_new, v_new, slots_d, kc, vc, st)
+    ref_out = torch.empty_like(q)
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max(lens), 0.09, ref_out, ws, 512, st)
+    out = torch.empty_like(q)
+    native.paged_attention_decode_write(q, k_new, v_new, slots_d, kc2, vc2, tables_d, lens_d, max(lens), 0.09, out,
+                                        ws, 512, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
