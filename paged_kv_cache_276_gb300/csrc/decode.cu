@@ -121,32 +121,32 @@ __device__ __forceinline__ int first_window(const Params &p, int seq, int part, 
   return e < p.max_blocks ? p.block_tables[static_cast<size_t>(seq) * p.max_blocks + e] : -1;
 }
 
-// The new token's key and value rows of (seq, KV head h), stored by the
-// producer warp of the CTA whose partition holds the token (the last one)
-// before it issues any copy: one 16-byte chunk per lane, then a proxy fence so
-// that the tensor copies that follow read the new rows.  Only this CTA reads
-// the token's slot, which is the table position of token L - 1; a different
-// slot is reported (PKV_STATUS_BAD_SLOT) and not written.
-template <int D, int BS>
-__device__ __forceinline__ void store_new_token(const Params &p, int seq, int h, int L, int lane) {
-  constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+// The new token of (seq, KV head h) when the decode stores it itself
+// (paged_attention_decode_write).  Its slot must be the table position of
+// token L - 1: returns that block (or -1: no store; a non-negative slot
+// elsewhere is reported as PKV_STATUS_BAD_SLOT when report is set).
+template <int BS>
+__device__ __forceinline__ int new_token_block(const Params &p, int seq, int L, bool report) {
   const int64_t slot = p.slots[seq];
-  if (slot < 0) return;
+  if (slot < 0) return -1;
   const int last = L - 1, e = last / BS;
   const int entry = last >= 0 && e < p.max_blocks ? p.block_tables[static_cast<size_t>(seq) * p.max_blocks + e] : -1;
   if (entry < 0 || entry >= p.num_blocks || slot != static_cast<int64_t>(entry) * BS + last % BS) {
-    if (lane == 0 && h == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_SLOT);
-    return;
+    if (report && p.status) atomicOr(p.status, PKV_STATUS_BAD_SLOT);
+    return -1;
   }
+  return entry;
+}
+
+// Lane l's 16-byte chunk of the new token's key row (l < D/8) or value row
+// (D/8 <= l < D/4) for KV head h.
+template <int D>
+__device__ __forceinline__ uint4 new_token_chunk(const Params &p, int seq, int h, int lane) {
+  constexpr int kChunks = D / 8;
   const size_t src = (static_cast<size_t>(seq) * p.num_kv_heads + h) * kChunks;
-  const size_t dst = ((static_cast<size_t>(entry) * p.num_kv_heads + h) * BS + last % BS) * kChunks;
-  if (lane < kChunks) {
-    p.k_cache[dst + lane] = p.k_new[src + lane];
-  } else if (lane < 2 * kChunks) {
-    p.v_cache[dst + lane - kChunks] = p.v_new[src + lane - kChunks];
-  }
-  fence_proxy_async_global();
-  __syncwarp();
+  if (lane < kChunks) return p.k_new[src + lane];
+  if (lane < 2 * kChunks) return p.v_new[src + lane - kChunks];
+  return make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Producer (one whole warp): walk this partition's block-table entries and
@@ -259,7 +259,19 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
 
   WarpAcc<D, NT> acc;
   if (warp == kDecodeWarps) {
-    if (p.k_new && part == nparts - 1) store_new_token<D, BS>(p, seq, h, L, lane);
+    // The new token (paged_attention_decode_write): the CTA of the partition
+    // holding it stores its rows to the cache.  No copy of this grid waits for
+    // that store: the consumer warp of the token's unit puts the same rows into
+    // its staged tile itself (below).
+    if (p.k_new && part == nparts - 1) {
+      const int entry = new_token_block<BS>(p, seq, L, h == 0 && lane == 0);
+      if (entry >= 0 && lane < D / 4) {
+        const size_t dst = (static_cast<size_t>(entry) * p.num_kv_heads + h) * BS + (L - 1) % BS;
+        const uint4 c = new_token_chunk<D>(p, seq, h, lane);
+        if (lane < D / 8) p.k_cache[dst * (D / 8) + lane] = c;
+        else p.v_cache[dst * (D / 8) + lane - D / 8] = c;
+      }
+    }
     produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
@@ -276,6 +288,16 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
         qf[nt][ks][1] = real ? qrow[ks * 8 + 4 + c4] : 0u;
       }
     }
+    // the new token's unit: its rows come from the inputs (registers), not
+    // from the copy, which may have read the slot before this grid's store
+    int patch_unit = -1, patch_row = 0;
+    uint4 patch = make_uint4(0u, 0u, 0u, 0u);
+    if (p.k_new && part == nparts - 1 && nunit > 0 && warp == (nunit - 1) % kDecodeWarps &&
+        new_token_block<BS>(p, seq, L, false) >= 0) {
+      patch_unit = nunit - 1;
+      patch_row = (L - 1) - (tok0 + patch_unit * U::kRows);
+      patch = new_token_chunk<D>(p, seq, h, lane);
+    }
     acc.init();
     for (int j = warp; j < nunit; j += kDecodeWarps) {
       const int s = j % S;
@@ -283,6 +305,17 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
         if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
         *abort_flag = 1;
         break;
+      }
+      if (j == patch_unit) {  // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r % 8)
+        if (lane < D / 4) {
+          const int v = lane >= D / 8, c = v ? lane - D / 8 : lane;
+          const uint32_t dst = ring + s * T::kStageBytes + v * T::kTileBytes + (c >> 3) * T::kBoxBytes +
+                               patch_row * 128 + (((c & 7) ^ (patch_row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(patch.x), "r"(patch.y),
+                       "r"(patch.z), "r"(patch.w)
+                       : "memory");
+        }
+        __syncwarp();
       }
       const int valid = min(U::kRows, L - (tok0 + j * U::kRows));
       int vis[NT][2];
