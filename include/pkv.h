@@ -208,10 +208,11 @@ int paged_attention_decode_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache,
  *                  seq_lens[i] (the slot the allocator's append returns), or
  *                  negative for no store
  *   everything else as paged_attention_decode (q, out [num_seqs][1][Hq][d]).
- * The CTA that reads the newest token's block stores the token's rows itself
- * before its first copy, so no separate write grid runs.  A non-negative slot
- * other than the newest token's table position is undefined: where the check
- * runs it sets PKV_STATUS_BAD_SLOT and the token is not stored.  Where the
+ * The CTA that reads the newest token's block stores the token's rows and
+ * also places them into its staged copy of that block, so no separate write
+ * grid runs and no copy has to wait for the store.  A non-negative slot other
+ * than the newest token's table position is undefined: where the check runs
+ * it sets PKV_STATUS_BAD_SLOT and the token is not stored.  Where the
  * decode runs on the tensor cores (max_seq_len >= 16384) the store is a
  * separate pkv_write launch before it.  main_done_event as in
  * paged_attention_decode_ex (may be NULL).
@@ -498,6 +499,7 @@ typedef struct pkv_step pkv_step;
 int pkv_step_layout_of(const pkv_step_config *cfg, pkv_step_layout *layout);
 
 /* Create a runner over an allocator and caller-owned buffers (see above).
+ * Like the allocator, a runner has one owner and is not thread-safe.
  * PKV_ERR_ARG for a null, misaligned or too small buffer, or a host buffer
  * that is not page-locked; PKV_ERR_CUDA if the runner's event or stream cannot
  * be made.  The allocator, caches and buffers must outlive the runner. */
