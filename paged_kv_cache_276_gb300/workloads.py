@@ -182,13 +182,20 @@ class DecodeSession:
 
     # ------------------------------------------------------------ one step
     def run_step(self, step: StepInputs, q, ks, vs, out, workspace, d_status=None, stream=None,
-                 per_layer_out=None):
-        """One pass of the hot path over every layer."""
+                 per_layer_out=None, fused=False):
+        """One pass of the hot path over every layer.  fused (single-token steps):
+        the new tokens' store runs inside the decode grid (paged_attention_decode_write)."""
+        fused = fused and self.q_len == 1
         for l in range(self.layers):
             if step.cow_pairs is not None:
                 native.pkv_block_copy(self.k_caches[l], self.v_caches[l], step.cow_pairs, d_status, stream)
-            native.pkv_write(ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l], d_status, stream)
             o = out if per_layer_out is None else per_layer_out[l]
+            if fused:
+                native.paged_attention_decode_write(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
+                                                    step.tables, step.lens, step.max_len, self.scale, o, workspace,
+                                                    self.partition_size, d_status, stream)
+                continue
+            native.pkv_write(ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l], d_status, stream)
             native.paged_attention_decode(q, self.k_caches[l], self.v_caches[l], step.tables, step.lens,
                                           step.max_len, self.scale, o, workspace, self.partition_size,
                                           d_status, stream)

@@ -553,9 +553,11 @@ def test_unwritten_tail_slots_never_leak_nan():
 
 # ------------------------------------------------------------------ workloads
 def session_step_parity(w, n_check, block_size=None, q_len=None, layers=None, check_layers=(0,),
-                        prefix_len=None, seed=0):
+                        prefix_len=None, seed=0, fused=False):
     """One full step of a workload on the GPU (in the launch configuration the
-    benchmark times), the oracle on sampled sequences and layers."""
+    benchmark times; fused: the new tokens' store inside the decode grid, as the
+    benchmark's single-token step runs it), the oracle on sampled sequences and
+    layers."""
     sess = DecodeSession(w, "cuda", allocator_factory=OracleAllocator, block_size=block_size, q_len=q_len,
                          layers=layers, extra_steps=1, prefix_len=prefix_len)
     pre = {l: (bits(sess.k_caches[l]), bits(sess.v_caches[l])) for l in check_layers}
@@ -567,7 +569,7 @@ def session_step_parity(w, n_check, block_size=None, q_len=None, layers=None, ch
     (q, ks, vs), = sess.new_token_tensors(1, seed=w.seed + seed)
     outs = [torch.empty_like(q) for _ in range(sess.layers)]
     ws = sess.workspace(step.max_len)
-    sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs)
+    sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs, fused=fused)
     torch.cuda.synchronize()
     assert st.item() == 0
     rng = np.random.default_rng(w.seed)
@@ -590,16 +592,19 @@ def test_workload_tiny_full():
     session_step_parity(inputs.WORKLOADS[1], n_check=2)
 
 
-def test_workload_batched_gqa_sampled():
-    session_step_parity(inputs.WORKLOADS[2], n_check=6)
+@pytest.mark.parametrize("fused", [False, True])
+def test_workload_batched_gqa_sampled(fused):
+    session_step_parity(inputs.WORKLOADS[2], n_check=6, fused=fused)
 
 
-def test_workload_continuous_batching_sampled():
-    session_step_parity(inputs.WORKLOADS[3], n_check=4, check_layers=(0, 31))
+@pytest.mark.parametrize("fused", [False, True])
+def test_workload_continuous_batching_sampled(fused):
+    session_step_parity(inputs.WORKLOADS[3], n_check=4, check_layers=(0, 31), fused=fused)
 
 
-def test_workload_shared_prefix_sampled():
-    sess, _ = session_step_parity(inputs.WORKLOADS[4], n_check=4)
+@pytest.mark.parametrize("fused", [False, True])
+def test_workload_shared_prefix_sampled(fused):
+    sess, _ = session_step_parity(inputs.WORKLOADS[4], n_check=4, fused=fused)
     assert len(sess.setup_cow_pairs) == 64 * 7
 
 
@@ -611,7 +616,8 @@ def test_workload_shared_prefix_partial_block_cow():
 
 @pytest.mark.parametrize("bs,q_len", [(16, 1), (32, 1), (16, 16), (32, 16)])
 def test_workload_long_context_sampled(bs, q_len):
-    session_step_parity(inputs.WORKLOADS[5], n_check=1 if q_len == 16 else 2, block_size=bs, q_len=q_len)
+    session_step_parity(inputs.WORKLOADS[5], n_check=1 if q_len == 16 else 2, block_size=bs, q_len=q_len,
+                        fused=q_len == 1)
 
 
 def test_shared_prefix_layout_equals_private_copies_bit_exact():
