@@ -515,6 +515,8 @@ void pkv_step_destroy(pkv_step *s);
  *   1. wait until the runner's previous run has finished on the GPU;
  *   2. check that every sequence has room for q_len more tokens in
  *      max_blocks_per_seq blocks (PKV_ERR_RANGE, nothing changed, if not);
+ *      with use_graph, capture the step's graph if this (n, partition count)
+ *      has none yet (a failed capture returns its error, nothing changed);
  *   3. pkv_seq_append_batch of q_len tokens each (its errors are returned and
  *      change nothing), slots into host_stage; pkv_block_table of the n
  *      sequences into host_stage;
@@ -525,8 +527,11 @@ void pkv_step_destroy(pkv_step *s);
  * Returns after the enqueue.  The caller writes the step's queries, keys and
  * values for rows 0..n-1 into host_stage before the call, and may touch
  * host_stage and host_out again only after pkv_step_wait (or a synchronisation
- * of `stream`).  A CUDA error after step 3 returns PKV_ERR_CUDA with the
- * tokens appended.  n == 0 only waits. */
+ * of `stream`).  Every failure except a CUDA error from the enqueue itself
+ * leaves the allocator unchanged.  A CUDA error in step 4 returns PKV_ERR_CUDA
+ * with the tokens appended but their keys and values not stored: the caller
+ * must free those sequences (or store the tokens itself) before decoding them
+ * again.  n == 0 only waits. */
 int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream);
 
 /* Block until the runner's last run has finished; PKV_ERR_CUDA on failure. */

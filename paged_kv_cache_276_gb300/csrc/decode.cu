@@ -820,12 +820,13 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
 
 namespace pkv {
 
-int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+// Every check of a decode call's arguments that does not involve the
+// workspace, in the order the entry points apply them; on PKV_OK *plan holds
+// the split-K partitioning (and *plan is set only then).
+int decode_check(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                 int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                 void *stream, void *main_done_event, const NewTokens *nt) {
-  cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
+                 int partition_size, const pkv_bf16 *out, Plan *plan) {
   if (num_seqs < 0 || max_blocks_per_seq < 0 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -850,9 +851,26 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
   if (rows + block_size >= (1ll << 31) || num_blocks == 0) return num_blocks == 0 ? PKV_ERR_ARG : PKV_ERR_UNSUPPORTED;
 
+  Plan pl;
+  if (!make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &pl)) return PKV_ERR_ARG;
+  if (pl.max_parts > 65535) return PKV_ERR_UNSUPPORTED;
+  *plan = pl;
+  return PKV_OK;
+}
+
+int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
+                 int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                 int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                 void *stream, void *main_done_event, const NewTokens *nt) {
+  cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   Plan plan;
-  if (!make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &plan)) return PKV_ERR_ARG;
-  if (plan.max_parts > 65535) return PKV_ERR_UNSUPPORTED;
+  const int checked = decode_check(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                   max_seq_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                   scale, partition_size, out, &plan);
+  if (checked != PKV_OK || num_seqs == 0) return checked;
+  const int group = num_q_heads / num_kv_heads;
+  const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
   if (plan.ws_bytes() > 0) {
     if (!workspace || workspace_bytes < plan.ws_bytes() || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   }
@@ -1010,9 +1028,13 @@ extern "C" int paged_attention_decode_static_scratch(
     int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
     int partition_size, pkv_bf16 *out, int32_t *d_status, void *stream) {
+  // The same argument checks as paged_attention_decode first, so an unsupported
+  // or malformed call gets the same error code here as there.
   pkv::Plan plan;
-  if (!pkv::make_plan(num_seqs, q_len, num_q_heads, head_dim, max_seq_len, partition_size, &plan))
-    return PKV_ERR_ARG;
+  const int checked = pkv::decode_check(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                        max_seq_len, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                        num_blocks, scale, partition_size, out, &plan);
+  if (checked != PKV_OK || num_seqs == 0) return checked;
   if (plan.ws_bytes() > kStaticScratchBytes) return PKV_ERR_WORKSPACE;
   void *scratch = nullptr;
   if (plan.ws_bytes() > 0) {

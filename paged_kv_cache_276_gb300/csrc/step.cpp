@@ -220,38 +220,43 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
   if (rc != PKV_OK || n == 0) return rc;
   const pkv_step_config &c = s->cfg;
   const long long cap = static_cast<long long>(c.max_blocks_per_seq) * c.block_size;
+  int max_len = 0;  // every length after this step's append
   for (int i = 0; i < n; ++i) {
     const int64_t len = pkv_seq_len(s->alloc, seq_ids[i]);
     if (len < 0) return static_cast<int>(len);
     if (len + c.q_len > cap) return PKV_ERR_RANGE;
+    max_len = len + c.q_len > max_len ? static_cast<int>(len + c.q_len) : max_len;
   }
-  auto *slots = reinterpret_cast<int64_t *>(s->hs + s->lay.slots_offset);
-  auto *tables = reinterpret_cast<int32_t *>(s->hs + s->lay.tables_offset);
-  auto *lens = reinterpret_cast<int32_t *>(s->hs + s->lay.lens_offset);
-  if ((rc = pkv_seq_append_batch(s->alloc, seq_ids, n, c.q_len, slots)) != PKV_OK) return rc;
-  if ((rc = pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, lens)) != PKV_OK) return rc;
-  int max_len = 0;
-  for (int i = 0; i < n; ++i) max_len = lens[i] > max_len ? lens[i] : max_len;
-
+  // Everything that can fail without a CUDA fault (a graph capture included)
+  // happens before the allocator changes; the append is the last host step.
   cudaStream_t st = pkv::as_stream(stream);
-  if (!c.use_graph) {
-    rc = enqueue(s, st, n, max_len);
-  } else {
+  cudaGraphExec_t exec = nullptr;
+  if (c.use_graph) {
     const int parts = max_len > 0 ? (max_len + s->part - 1) / s->part : 1;
     const auto key = std::make_pair(n, parts);
     auto it = s->graphs.find(key);
     if (it == s->graphs.end()) {
       if (static_cast<int>(s->graphs.size()) >= kMaxGraphs) drop_graphs(s);
-      cudaGraphExec_t exec = nullptr;
       const long long bound = static_cast<long long>(parts) * s->part;
       rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), &exec);
       if (rc != PKV_OK) return rc;
       it = s->graphs.emplace(key, exec).first;
     }
-    const cudaError_t e = cudaGraphLaunch(it->second, st);
-    if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+    exec = it->second;
   }
-  if (rc != PKV_OK) return rc;
+  auto *slots = reinterpret_cast<int64_t *>(s->hs + s->lay.slots_offset);
+  auto *tables = reinterpret_cast<int32_t *>(s->hs + s->lay.tables_offset);
+  auto *lens = reinterpret_cast<int32_t *>(s->hs + s->lay.lens_offset);
+  if ((rc = pkv_seq_append_batch(s->alloc, seq_ids, n, c.q_len, slots)) != PKV_OK) return rc;
+  // cannot fail: every id is resident (the append took it) and its table has room (checked above)
+  if ((rc = pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, lens)) != PKV_OK) return rc;
+
+  if (exec) {
+    const cudaError_t e = cudaGraphLaunch(exec, st);
+    if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  } else if ((rc = enqueue(s, st, n, max_len)) != PKV_OK) {
+    return rc;
+  }
   const cudaError_t e = cudaEventRecord(s->done, st);
   if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
   s->pending = true;

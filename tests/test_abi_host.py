@@ -74,6 +74,40 @@ def test_decode_rejects_bad_sizes_before_launch(native):
     assert call(B=0) == native.PKV_OK                            # nothing to do, nothing launched
 
 
+def test_static_scratch_decode_gives_the_regular_error_codes(native):
+    """The allocation-free decode checks its arguments the way paged_attention_decode
+    does before it compares the scratch need with its fixed array."""
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails validation first
+    args = dict(q=fake, k=fake, v=fake, tbl=fake, maxb=4, lens=fake, B=2, maxlen=64, qlen=1, Hq=8, Hkv=2,
+                d=128, bs=16, NB=8, scale=0.1, part=0, out=fake)
+
+    def regular(**kw):
+        a = dict(args, **kw)
+        return lib.paged_attention_decode(a["q"], a["k"], a["v"], a["tbl"], a["maxb"], a["lens"], a["B"],
+                                          a["maxlen"], a["qlen"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["NB"],
+                                          a["scale"], a["part"], a["out"], None, 0, None, None)
+
+    def static(**kw):
+        a = dict(args, **kw)
+        return lib.paged_attention_decode_static_scratch(a["q"], a["k"], a["v"], a["tbl"], a["maxb"], a["lens"],
+                                                         a["B"], a["maxlen"], a["qlen"], a["Hq"], a["Hkv"], a["d"],
+                                                         a["bs"], a["NB"], a["scale"], a["part"], a["out"], None,
+                                                         None)
+    # each of these also asks for far more scratch than the array holds
+    big = dict(maxlen=1 << 19, part=16)
+    cases = [dict(d=96), dict(bs=8), dict(qlen=3), dict(qlen=0), dict(Hq=7), dict(Hq=40, Hkv=2),
+             dict(qlen=16, Hq=32, Hkv=2), dict(part=24), dict(scale=float("nan")), dict(NB=0),
+             dict(q=ctypes.c_void_p((1 << 20) + 2)), dict(tbl=None)]
+    for kw in cases:
+        want = regular(**kw)
+        assert want not in (native.PKV_OK, native.PKV_ERR_WORKSPACE), kw
+        assert static(**kw) == want, kw
+        assert static(**{**big, **kw}) == want, kw
+    assert static(**big) == native.PKV_ERR_WORKSPACE
+    assert static(B=0, **big) == native.PKV_OK  # nothing to do, nothing launched
+
+
 def test_prefill_rejects_bad_sizes_before_launch(native):
     lib = native.lib()
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: every case fails validation first
