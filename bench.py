@@ -2,18 +2,21 @@
 """Benchmark of the paged KV-cache decode hot path on one GB300 (or N replicas).
 
 A step is one pass of the whole hot path over one batch: host allocator work
-(block tables, slots, copy-on-write decisions), the ``pkv_write`` of the new
-tokens' keys and values, any ``pkv_block_copy``, and ``paged_attention_decode``
-(with its cross-partition combine), for every layer of the workload.
+(block tables, slots, copy-on-write decisions), the store of the new tokens'
+keys and values, any ``pkv_block_copy``, and the paged decode (with its
+cross-partition combine), for every layer of the workload.
 
-Headline: the batched GQA decode workload (32 sequences, L ~ U{1..4096}, block
-16, 32 query / 8 KV heads, head dim 128, bf16).  Metric: KV-cache GB/s read
-(valid K and V rows) per step; query tokens/s alongside.  The other workloads
-are reported under "workloads".
+Headline: the continuous-batching mix (256 sequences, log-normal lengths with
+median 512, block 16, 32 query / 8 KV heads, head dim 128, bf16, 32 layers with
+a block pool each: 128 KiB of cache per token), timed as whole 32-layer steps.
+Metric: KV-cache GB/s read (valid K and V rows) per step; query tokens/s
+alongside.  The other decode workloads and the chunked-prefill workloads are
+reported compactly under "workloads" and "prefill".
 
-``--impl reference`` times the fp64 CPU oracle on the same workload instead.
-Multi-GPU (torchrun): every rank runs its own independent replica (weak
-scaling, no data-path collective); the step time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload instead.  Multi-GPU (torchrun): every rank runs its own independent
+replica (weak scaling, no data-path collective); the step time is the max over
+ranks.
 """
 from __future__ import annotations
 
@@ -32,7 +35,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = 2
+HEADLINE = 3
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 DEFAULT_PARTITION = 768  # the library's split-K partition when the caller passes 0
@@ -63,22 +66,31 @@ def measured_tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def decode_kernel_source_sha():
-    """sha256 of the device code the decode kernel is built from: decode.cu up to
-    its host section, then attend.cuh and ptx.cuh."""
+def _source_sha(parts):
+    """sha256 over (file, cut marker or None) parts of csrc: each file up to its
+    marker (its host section), whole if the marker is None."""
     csrc = os.path.join(ROOT, "paged_kv_cache_276_gb300", "csrc")
-    text = open(os.path.join(csrc, "decode.cu"), "rb").read()
-    cut = text.find(b"// ------------------------------------------------------------------ host")
-    h = hashlib.sha256(text[:cut] if cut >= 0 else text)
-    for name in ("attend.cuh", "ptx.cuh"):
-        h.update(open(os.path.join(csrc, name), "rb").read())
+    h = hashlib.sha256()
+    for name, marker in parts:
+        text = open(os.path.join(csrc, name), "rb").read()
+        cut = text.find(marker) if marker else -1
+        h.update(text[:cut] if cut >= 0 else text)
     return h.hexdigest()
 
 
-def kernel_traffic(workload_tag):
-    """DRAM bytes per decode launch from the committed ncu summary, only if the
-    kernel's device code is unchanged since that capture (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+HOST_MARK = b"// ------------------------------------------------------------------ host"
+# the device code each traffic record covers
+TRAFFIC_SOURCES = {
+    "decode_kernel_traffic.txt": [("decode.cu", HOST_MARK), ("attend.cuh", None), ("ptx.cuh", None)],
+    "chunk_tc_kernel_traffic.txt": [("chunk_tc.cu", HOST_MARK), ("tc.cuh", None), ("ptx.cuh", None)],
+}
+
+
+def kernel_traffic(record, workload_tag):
+    """DRAM bytes per launch of a kernel from its committed ncu summary under
+    profiles/, only while the kernel's device code still hashes to the value the
+    capture was taken at (else None)."""
+    path = os.path.join(ROOT, "profiles", record)
     try:
         rec = {}
         with open(path) as f:
@@ -86,8 +98,7 @@ def kernel_traffic(workload_tag):
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     rec[k.strip()] = v.strip()
-        sha = decode_kernel_source_sha()
-        if rec.get("source_sha256") != sha:
+        if rec.get("source_sha256") != _source_sha(TRAFFIC_SOURCES[record]):
             return None
         key = f"dram_bytes_per_launch[{workload_tag}]"
         return float(rec[key]) if key in rec else None
@@ -348,83 +359,17 @@ class Runner:
         finally:
             step.close()
 
-    def time_e2e(self, steps):
-        """Same metric through the public API with host buffers: allocator work,
-        the host -> device copy of the step inputs, the kernels, and the
-        device -> host read of the outputs, all inside the timed region.
 
-        The step's inputs (queries, new keys and values, slots, block tables,
-        lengths) live in one page-locked staging buffer that the allocator
-        fills in place and that goes to the device in one copy; the kernels
-        read views of its device twin."""
-        torch = self.torch
-        from paged_kv_cache_276_gb300 import native
-        sess = self.sess
-        toks = sess.new_token_tensors(1, seed=self.w.seed + 5)
-        parts = [("q", toks[0][0].shape, torch.bfloat16)]
-        parts += [(f"k{l}", t.shape, torch.bfloat16) for l, t in enumerate(toks[0][1])]
-        parts += [(f"v{l}", t.shape, torch.bfloat16) for l, t in enumerate(toks[0][2])]
-        parts += [("slots", (sess.B * sess.q_len,), torch.int64), ("tables", (sess.B, sess.max_blocks), torch.int32),
-                  ("lens", (sess.B,), torch.int32)]
-        offs, total = {}, 0
-        for name, shape, dt in parts:  # 256-byte aligned segments
-            offs[name] = total
-            total += -(-int(np.prod(shape)) * torch.empty((), dtype=dt).element_size() // 256) * 256
-        stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
-        stage_d = torch.empty(total, dtype=torch.uint8, device=self.device)
-
-        def view(buf, name):
-            shape, dt = next((sh, d) for n, sh, d in parts if n == name)
-            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
-            return buf[offs[name]:offs[name] + nbytes].view(dt).view(shape)
-
-        view(stage_h, "q").copy_(toks[0][0].cpu())
-        for l in range(sess.layers):
-            view(stage_h, f"k{l}").copy_(toks[0][1][l].cpu())
-            view(stage_h, f"v{l}").copy_(toks[0][2][l].cpu())
-        q_d = view(stage_d, "q")
-        k_d = [view(stage_d, f"k{l}") for l in range(sess.layers)]
-        v_d = [view(stage_d, f"v{l}") for l in range(sess.layers)]
-        slots_d, tables_d, lens_d = view(stage_d, "slots"), view(stage_d, "tables"), view(stage_d, "lens")
-        slots_np = view(stage_h, "slots").numpy()
-        tables_np = view(stage_h, "tables").numpy()
-        lens_np = view(stage_h, "lens").numpy()
-        out_d = torch.empty_like(toks[0][0])
-        out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
-        ws = sess.workspace(int(sess.alloc.block_table(range(sess.B), sess.max_blocks)[1].max()) + steps + 8)
-        stream = torch.cuda.current_stream()
-        seq_ids = np.arange(sess.B, dtype=np.int64)
-        times, kv = [], []
-        for i in range(steps + 1):
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            # host allocator work of the step (public API, one call each) into the staging buffer
-            sess.alloc.seq_append_batch(seq_ids, sess.q_len, out=slots_np)
-            sess.alloc.block_table(seq_ids, sess.max_blocks, table_out=tables_np, lens_out=lens_np)
-            stage_d.copy_(stage_h, non_blocking=True)
-            max_len = int(lens_np.max())
-            for l in range(sess.layers):
-                native.pkv_write(k_d[l], v_d[l], slots_d, sess.k_caches[l], sess.v_caches[l], None, stream)
-                native.paged_attention_decode(q_d, sess.k_caches[l], sess.v_caches[l], tables_d, lens_d, max_len,
-                                              sess.scale, out_d, ws, sess.partition_size, None, stream)
-            out_h.copy_(out_d, non_blocking=True)
-            torch.cuda.synchronize()
-            t1 = time.perf_counter()
-            if i:  # the first pass warms the pinned-memory paths
-                times.append((t1 - t0) * 1e3)
-                kv.append(int(lens_np.astype(np.int64).sum()) * 2 * sess.Hkv * sess.d * 2 * sess.layers)
-        ms = sum(times) / len(times)
-        return {"ms_per_step": ms, "kv_bytes_per_step": sum(kv) / len(kv), "h2d": int(total),
-                "d2h": out_h.numel() * 2}
-
-
-def cpu_oracle_baseline(wnum, budget_s=12.0, reps=None, warmup=0):
-    """The fp64 oracle as it stands, on this host's cores: whole decode steps of
-    the workload (all sequences), repeated ``reps`` times or until ~budget_s
-    seconds have passed."""
+def cpu_oracle_baseline(wnum, budget_s=12.0, reps=None, warmup=0, layers_per_rep=None):
+    """The fp64 oracle as it stands, on this host's cores.  A rep decodes the
+    whole batch of the workload (every sequence) over ``layers_per_rep`` layers
+    (default: all of the workload's layers); the layers of a workload share the
+    sequence lengths, so the host keeps one layer's pool and decodes it once per
+    layer.  Repeated ``reps`` times, or until ~budget_s seconds have passed."""
     from oracle import attention as OA
     from paged_kv_cache_276_gb300 import inputs
     w = inputs.WORKLOADS[wnum]
+    layers = layers_per_rep or w.layers
     rng = inputs.rng_for(w)
     lens = inputs.lengths(w, rng)
     NB = inputs.pool_size(lens, w.block_size, 0.10)
@@ -436,8 +381,9 @@ def cpu_oracle_baseline(wnum, budget_s=12.0, reps=None, warmup=0):
     cores = OA.set_threads(os.cpu_count() or 1)
 
     def one():
-        OA.paged_attention(qb, kb, vb, tables, lens, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
-                           head_dim=w.head_dim, block_size=w.block_size, scale=w.scale)
+        for _ in range(layers):
+            OA.paged_attention(qb, kb, vb, tables, lens, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                               head_dim=w.head_dim, block_size=w.block_size, scale=w.scale)
 
     for _ in range(warmup):
         one()
@@ -448,22 +394,26 @@ def cpu_oracle_baseline(wnum, budget_s=12.0, reps=None, warmup=0):
         el = time.perf_counter() - t0
         if (reps is not None and n >= reps) or (reps is None and el >= budget_s):
             break
-    kv = int(lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * 2
+    kv = int(lens.astype(np.int64).sum()) * 2 * w.num_kv_heads * w.head_dim * 2 * layers
+    what = "whole decode steps" if layers == w.layers else f"samples of {layers} of the {w.layers} layer decodes"
     return {"value": kv * n / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} whole decode steps of the workload ({len(lens)} sequences, {int(lens.sum())} tokens) "
-                      f"in {el:.1f} s, fp64, OpenMP over (sequence, KV head)",
-            "seconds": el, "reps": n, "query_tok_s": len(lens) * n / el}
+            "sample": f"{n} {what} of all {len(lens)} sequences ({int(lens.sum())} tokens) in {el:.1f} s, fp64",
+            "seconds": el, "reps": n, "query_tok_s": len(lens) * n * layers / w.layers / el}
 
 
-def workload_desc(wnum, bs=None, q_len=None):
+def workload_desc(wnum, bs=None, q_len=None, layers=None):
     from paged_kv_cache_276_gb300 import inputs
     w = inputs.WORKLOADS[wnum]
     bs = bs or w.block_size
     q_len = q_len or w.q_len
+    layers = layers or w.layers
     lens = {1: "L=[17,33,64]", 2: "L~U{1..4096}", 3: "L=lognormal(median 512, sigma 1) clip [1,8192]",
             4: "2048 shared prefix + U{0..512} suffix", 5: "L=32768"}[wnum]
     return (f"{w.name}: {w.num_seqs} seqs, {lens}, block {bs}, {w.num_q_heads}q/{w.num_kv_heads}kv heads, "
-            f"d {w.head_dim}, {w.layers} layer(s), q_len {q_len}, bf16")
+            f"d {w.head_dim}, {layers} layer(s), q_len {q_len}, bf16")
+
+
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def run_ours(args, rank, world, local):
@@ -475,7 +425,8 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_hbm_peak()
 
     e2e_steps = max(3, min(args.steps, 10))
-    r = Runner(HEADLINE, device, rank, steps_needed=args.warmup + args.steps + 3 * (e2e_steps + 1) + 8)
+    r = Runner(HEADLINE, device, rank, steps_needed=args.warmup + args.steps + 2 * (e2e_steps + 1) + 8,
+               layers=args.layers)
     dev_res = r.time_device(args.warmup, args.steps, world)
     ms = max_over_ranks(dev_res["ms_per_step"], world)
     total_bytes = dev_res["kv_bytes_per_step"] * world
@@ -488,60 +439,53 @@ def run_ours(args, rank, world, local):
     e2e = r.time_e2e_step(e2e_steps, use_graph=False)
     e2e_value, e2e_ms = e2e_gbs(e2e)
     e2e_graph, e2e_graph_ms = e2e_gbs(r.time_e2e_step(e2e_steps, use_graph=True))
-    e2e_calls, e2e_calls_ms = e2e_gbs(r.time_e2e(e2e_steps))
-    # the dominant kernel: paged_attention_decode's main kernel, timed from an
-    # event before the call to the event the library records right after it
+    # the dominant kernel: the decode's main kernel, timed from an event before
+    # the call to the event the library records right after it
     main_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["main_ms_avg"] * 1e-3) / 1e9
     op_gbs = dev_res["kv_bytes_per_decode"] / (dev_res["decode_ms_avg"] * 1e-3) / 1e9
-    traffic = kernel_traffic("batched_gqa")
+    layers = r.sess.layers
+    del r
+    torch.cuda.empty_cache()
     line = {
         "metric": "paged decode attention KV-cache read bandwidth (valid K+V bytes / step time)",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V/Q, seeded lengths and block placement)",
-        "config": {"workload": workload_desc(HEADLINE), "parallelism": f"replicas x{world} (independent batches)",
-                   "l2": "flushed before every step (write of 2x L2), outside the per-step CUDA events",
+        "config": {"workload": workload_desc(HEADLINE, layers=layers),
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "flushed before every step (write of 2x L2), outside the events",
                    "kv_bytes_per_step": int(dev_res["kv_bytes_per_step"]),
-                   "query_tokens_per_step": dev_res["query_tokens_per_step"],
-                   "step": "host allocator (precomputed) + paged_attention_decode_write (the new tokens' store "
-                           "and the decode in one grid) + cross-partition combine"},
+                   "query_tokens_per_step": dev_res["query_tokens_per_step"]},
         "query_tok_s": round(dev_res["query_tokens_per_step"] * world / (ms * 1e-3), 1),
-        "step_ms_p10": round(dev_res["step_ms_p10"], 5), "step_ms_p90": round(dev_res["step_ms_p90"], 5),
         "roofline": {"bound": "hbm", "achieved": round(main_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(main_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-                     "kernel": "decode_kernel (main kernel of paged_attention_decode)",
-                     "kernel_ms_avg": round(dev_res["main_ms_avg"], 5),
-                     "algorithmic_bytes_per_launch": int(dev_res["kv_bytes_per_decode"]),
-                     "traffic": traffic,
-                     "whole_call": {"kernels": "decode_kernel + cross-partition combine_kernel",
-                                    "ms_avg": round(dev_res["decode_ms_avg"], 5), "achieved": round(op_gbs, 1),
-                                    "frac": round(op_gbs / peak, 4)}},
+                     "traffic": kernel_traffic("decode_kernel_traffic.txt", "continuous_batching"),
+                     "kernel": "decode_kernel", "bytes_per_launch": int(dev_res["kv_bytes_per_decode"]),
+                     "ms_per_launch": round(dev_res["main_ms_avg"], 5),
+                     "frac_of_nominal": round(main_gbs / NOMINAL_HBM_GBS, 4),
+                     "call_frac": round(op_gbs / peak, 4)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
                 "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4),
-                "api": "native.DecodeStep.run + wait (pkv_step_run: allocator append, table fill, one copy in, "
-                       "write + decode per layer, one copy out, enqueued by one C call)",
-                "with_graph": {"value": round(e2e_graph, 2), "ms_per_step": round(e2e_graph_ms, 4),
-                               "api": "the same runner, its device part replayed from a CUDA graph"},
-                "separate_calls": {"value": round(e2e_calls, 2), "ms_per_step": round(e2e_calls_ms, 4),
-                                   "api": "seq_append_batch, block_table, one copy in, pkv_write, "
-                                          "paged_attention_decode, one copy out, each from Python"}},
+                "graph_value": round(e2e_graph, 2), "graph_ms_per_step": round(e2e_graph_ms, 4)},
         "gpu_launches": dev_res["launches"],
         "clocks": dev_res["clocks"],
     }
     if not args.no_workloads:
         line["workloads"] = other_workloads(args, device, rank, world, peak)
-        line["prefill"] = prefill_bench(device, cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)
+        line["prefill"] = prefill_bench(device, cpu=rank == 0 and world == 1 and not args.no_cpu_baseline,
+                                        compact=True)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            line["cpu_baseline"] = cpu_oracle_baseline(HEADLINE, budget_s=args.cpu_seconds)
-            line["cpu_baseline"]["value"] = round(line["cpu_baseline"]["value"], 4)
+            cb = cpu_oracle_baseline(HEADLINE, budget_s=args.cpu_seconds, layers_per_rep=1)
+            line["cpu_baseline"] = {k: (round(v, 4) if k == "value" else v) for k, v in cb.items()
+                                    if k in ("value", "unit", "cores", "kind", "sample")}
         except Exception as e:  # reported, never fatal
             line["cpu_baseline"] = {"error": repr(e)}
     return line
 
 
-WORKLOAD_CASES = [(1, None, None), (3, None, None), (4, None, None), (5, 16, None), (5, 32, None), (5, 16, 16),
-                  (5, 32, 16)]
+WORKLOAD_CASES = [(1, None, None), (2, None, None), (4, None, None), (5, 16, None), (5, 32, None), (5, 16, 16),
+                  (5, 32, 16), (3, None, None)]
 
 
 def case_tag(wnum, bs, q_len):
@@ -549,28 +493,29 @@ def case_tag(wnum, bs, q_len):
 
 
 def other_workloads(args, device, rank, world, peak, only=None):
+    """The other decode workloads, a few numbers each: step time and KV GB/s,
+    the decode kernel's and the whole decode call's fraction of the HBM peak,
+    and query tokens/s.  The headline workload is timed again only when named."""
     res = {}
     for wnum, bs, q_len in WORKLOAD_CASES:
         tag = case_tag(wnum, bs, q_len)
-        if only is not None and tag != only:
+        if (only is None and wnum == HEADLINE) or (only is not None and tag != only):
             continue
         try:
             steps = 5 if wnum == 3 else 10
-            r = Runner(wnum, device, rank, block_size=bs, q_len=q_len, steps_needed=steps + 3)
+            layers = args.layers if wnum == 3 else None
+            r = Runner(wnum, device, rank, block_size=bs, q_len=q_len, steps_needed=steps + 3, layers=layers)
             d = r.time_device(3, steps, world)
             ms = max_over_ranks(d["ms_per_step"], world)
             dec = d["kv_bytes_per_decode"] / (d["main_ms_avg"] * 1e-3) / 1e9
             op = d["kv_bytes_per_decode"] / (d["decode_ms_avg"] * 1e-3) / 1e9
-            res[tag] = {"workload": workload_desc(wnum, bs, q_len), "ms_per_step": round(ms, 5),
-                        "kv_gbs_step": round(d["kv_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1),
-                        "decode_kernel_gbs": round(dec, 1), "decode_frac_of_peak": round(dec / peak, 4),
-                        "decode_kernel_ms_avg": round(d["main_ms_avg"], 5),
-                        "decode_call_gbs": round(op, 1), "decode_call_frac_of_peak": round(op / peak, 4),
-                        "decode_ms_avg": round(d["decode_ms_avg"], 5),
-                        "query_tok_s": round(d["query_tokens_per_step"] * world / (ms * 1e-3), 1),
-                        "clocks_sm_mhz": d["clocks"]["sm_mhz"]}
-            if wnum == 4:
-                res[tag]["setup_cow_pairs"] = int(len(r.sess.setup_cow_pairs))
+            res[tag] = {"ms": round(ms, 5), "gbs": round(d["kv_bytes_per_step"] * world / (ms * 1e-3) / 1e9, 1),
+                        "kernel_frac": round(dec / peak, 4), "call_frac": round(op / peak, 4),
+                        "tok_s": round(d["query_tokens_per_step"] * world / (ms * 1e-3), 1)}
+            if only is not None:  # a profiling run: the long form
+                res[tag].update(workload=workload_desc(wnum, bs, q_len, layers), kernel_gbs=round(dec, 1),
+                                kernel_ms=round(d["main_ms_avg"], 5), call_ms=round(d["decode_ms_avg"], 5),
+                                clocks=d["clocks"])
             del r
             import torch
             torch.cuda.empty_cache()
@@ -683,7 +628,7 @@ def prefill_cpu_baseline(case, rows=16, max_seqs=8):
                       f"{el:.2f} s, fp64, OpenMP over (sequence, KV head)", "seconds": el}
 
 
-def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False):
+def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=False):
     """Chunked prefill (paged_attention_prefill) on the prefill workloads: a
     step is the chunk's pkv_write plus the attention call; the attention call
     is also timed alone (the tensor-core roofline).  2 x L2 is written before
@@ -732,27 +677,27 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False):
             sm, am = sum(step_ms) / steps, sum(att_ms) / steps
             fl = case.flops()
             tf = fl / (am * 1e-3) / 1e12
-            res[tag] = {
-                "workload": f"{pw.name}: {case.B} seqs, (L, chunk) = "
-                            + (f"({int(case.lens[0])}, {int(case.chunks[0])})" if "decodes" not in pw.extra else
-                               f"256 x (U{{1..4096}}, 1) + (8192, 1024) + (16384, 1024)")
-                            + f", block {pw.block_size}, {pw.num_q_heads}q/{pw.num_kv_heads}kv, d {pw.head_dim}, bf16",
-                "query_rows": case.total_q, "flops_per_call": fl, "kv_bytes_per_call": case.kv_bytes(),
-                "attention_ms_avg": round(am, 5), "step_ms_avg": round(sm, 5),
-                "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                             "frac": round(tf / peak, 4), "peak_kind": peak_kind,
-                             "kernel": "chunk_tc_kernel<bs, prefill> (paged_attention_prefill)", "traffic": None},
-                "kv_gbs": round(case.kv_bytes() / (am * 1e-3) / 1e9, 1),
-                "query_tok_s": round(case.total_q / (sm * 1e-3), 1),
-                "step_tflops": round(fl / (sm * 1e-3) / 1e12, 1),
-                "clocks": clocks.summary(),
-            }
+            roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(tf / peak, 4), "peak_kind": peak_kind,
+                    "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag)}
+            res[tag] = {"ms": round(am, 5), "roofline": roof, "kv_gbs": round(case.kv_bytes() / (am * 1e-3) / 1e9, 1),
+                        "rows_s": round(case.total_q / (sm * 1e-3), 1), "step_ms": round(sm, 5)}
+            if not compact:
+                res[tag].update(
+                    workload=f"{pw.name}: {case.B} seqs, (L, chunk) = "
+                    + (f"({int(case.lens[0])}, {int(case.chunks[0])})" if "decodes" not in pw.extra else
+                       "256 x (U{1..4096}, 1) + (8192, 1024) + (16384, 1024)")
+                    + f", block {pw.block_size}, {pw.num_q_heads}q/{pw.num_kv_heads}kv, d {pw.head_dim}, bf16",
+                    query_rows=case.total_q, flops_per_call=fl, kv_bytes_per_call=case.kv_bytes(),
+                    step_tflops=round(fl / (sm * 1e-3) / 1e12, 1), clocks=clocks.summary())
             if cpu:
                 try:
                     cb = prefill_cpu_baseline(case)
-                    if "value" in cb:
-                        cb["value"] = round(cb["value"], 6)
-                    res[tag]["cpu_baseline"] = cb
+                    if compact:
+                        res[tag]["cpu_tflops"] = round(cb["value"], 5) if "value" in cb else None
+                    else:
+                        cb["value"] = round(cb["value"], 6) if "value" in cb else None
+                        res[tag]["cpu_baseline"] = cb
                 except Exception as e:  # reported, never fatal
                     res[tag]["cpu_baseline"] = {"error": repr(e)}
             del case
@@ -764,11 +709,12 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False):
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: W untimed and K timed whole decode steps
-    of the headline workload on this host's cores (rank 0 only)."""
+    """The oracle as the reference arm, on this host's cores (rank 0 only): W
+    untimed and K timed steps, each a bounded sample of the headline workload's
+    step (every sequence, 4 of its 32 layer decodes)."""
     if rank != 0:
         return None
-    cb = cpu_oracle_baseline(HEADLINE, reps=args.steps, warmup=args.warmup)
+    cb = cpu_oracle_baseline(HEADLINE, reps=args.steps, warmup=args.warmup, layers_per_rep=4)
     ms = cb["seconds"] * 1e3 / cb["reps"]
     return {
         "impl": "reference", "metric": "paged decode attention KV-cache read bandwidth (valid K+V bytes / step time)",
@@ -791,6 +737,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-workloads", action="store_true", help="headline only")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode only this many layers of the multi-layer workload (profiling runs only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--workload", default=None, choices=[case_tag(*c) for c in WORKLOAD_CASES],

@@ -1050,6 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ host
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
 
 template <bool kPrefill, int D, bool kPairs>

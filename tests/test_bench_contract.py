@@ -1,6 +1,6 @@
 """The benchmark's reference arm on CPU: the JSON line keeps the contract's keys
-(the oracle timed on this host's cores, one whole decode step of the headline
-workload)."""
+(the oracle timed on this host's cores, one bounded sample of the headline
+workload's step: every sequence, 4 of its layer decodes)."""
 import json
 import sys
 

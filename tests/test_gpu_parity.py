@@ -552,78 +552,120 @@ def test_unwritten_tail_slots_never_leak_nan():
 
 
 # ------------------------------------------------------------------ workloads
-def session_step_parity(w, n_check, block_size=None, q_len=None, layers=None, check_layers=(0,),
-                        prefix_len=None, seed=0, fused=False):
-    """One full step of a workload on the GPU (in the launch configuration the
-    benchmark times; fused: the new tokens' store inside the decode grid, as the
-    benchmark's single-token step runs it), the oracle on sampled sequences and
-    layers."""
-    sess = DecodeSession(w, "cuda", allocator_factory=OracleAllocator, block_size=block_size, q_len=q_len,
+class RecordingAllocator:
+    """The native allocator, logging every call and its result so that the same
+    calls can be replayed on the oracle allocator afterwards (the oracle never
+    enters a product object)."""
+
+    def __init__(self, num_blocks, block_size):
+        self.inner = native.BlockAllocator(num_blocks, block_size)
+        self.num_blocks, self.block_size = num_blocks, block_size
+        self.log = []
+
+    def __getattr__(self, name):
+        fn = getattr(self.inner, name)
+
+        def call(*args):
+            res = fn(*args)
+            self.log.append((name, tuple(list(a) if isinstance(a, range) else a for a in args), res))
+            return res
+        return call
+
+
+def _plain(x):
+    if x is None:
+        return None
+    if isinstance(x, tuple):
+        return tuple(_plain(v) for v in x)
+    return np.asarray(x).astype(np.int64).tolist()
+
+
+def replay_on_oracle(rec):
+    """Every call the native allocator served, again on the oracle allocator:
+    each result (slots, copy-on-write pairs, tables, lengths) bit for bit, then
+    every refcount and the free count."""
+    oa = OracleAllocator(rec.num_blocks, rec.block_size)
+    for name, args, res in rec.log:
+        want = getattr(oa, name)(*args)
+        assert _plain(res) == _plain(want), f"native {name}{args[:2]} differs from the oracle allocator"
+    assert rec.inner.num_free() == oa.num_free()
+    assert [rec.inner.refcount(b) for b in range(rec.num_blocks)] == oa.refcount
+    return oa
+
+
+def session_step_parity(w, block_size=None, q_len=None, layers=None, check_layers=(0,), prefix_len=None, seed=0,
+                        fused=False):
+    """One full step of a workload on the GPU, on the native allocator and in the
+    launch configuration the benchmark times (fused: the new tokens' store inside
+    the decode grid, as the benchmark's single-token step runs it).  The
+    allocator's calls are replayed on the oracle allocator, the oracle's write
+    and copy run on host copies of the checked layers' caches, and every
+    sequence's output on those layers is compared with the fp64 oracle."""
+    sess = DecodeSession(w, "cuda", allocator_factory=RecordingAllocator, block_size=block_size, q_len=q_len,
                          layers=layers, extra_steps=1, prefix_len=prefix_len)
+    assert isinstance(sess.alloc.inner, native.BlockAllocator)
     pre = {l: (bits(sess.k_caches[l]), bits(sess.v_caches[l])) for l in check_layers}
     st = status_tensor()
     sess.apply_setup_copies(st)
     for l in check_layers:
         cache_ops.block_copy(pre[l][0], pre[l][1], sess.setup_cow_pairs)
     step = sess.plan_step()
+    replay_on_oracle(sess.alloc)
     (q, ks, vs), = sess.new_token_tensors(1, seed=w.seed + seed)
     outs = [torch.empty_like(q) for _ in range(sess.layers)]
     ws = sess.workspace(step.max_len)
     sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs, fused=fused)
     torch.cuda.synchronize()
     assert st.item() == 0
-    rng = np.random.default_rng(w.seed)
-    order = np.argsort(step.host_lens)
-    pick = sorted(set([int(order[0]), int(order[-1])] + list(rng.choice(sess.B, n_check, replace=False))))
     slots = step.slots.cpu().numpy()
     for l in check_layers:
-        kh, vh = pre[l]
+        kh, vh = pre.pop(l)
         cache_ops.write(bits(ks[l]), bits(vs[l]), slots, kh, vh, sess.bs)
         assert np.array_equal(bits(sess.k_caches[l]), kh), "pkv_write / block copy not bit-exact"
         assert np.array_equal(bits(sess.v_caches[l]), vh)
-        ref = OA.paged_attention(bits(q[pick]), kh, vh, step.host_tables[pick], step.host_lens[pick],
-                                 num_q_heads=sess.Hq, num_kv_heads=sess.Hkv, head_dim=sess.d,
-                                 block_size=sess.bs, scale=sess.scale, q_len=sess.q_len)
-        assert_attention_close(outs[l][pick], ref, f"workload {w.number} layer {l}")
+        ref = OA.paged_attention(bits(q), kh, vh, step.host_tables, step.host_lens, num_q_heads=sess.Hq,
+                                 num_kv_heads=sess.Hkv, head_dim=sess.d, block_size=sess.bs, scale=sess.scale,
+                                 q_len=sess.q_len)
+        assert_attention_close(outs[l], ref, f"workload {w.number} layer {l}")
+        del kh, vh, ref
     return sess, step
 
 
 def test_workload_tiny_full():
-    session_step_parity(inputs.WORKLOADS[1], n_check=2)
+    session_step_parity(inputs.WORKLOADS[1])
 
 
 @pytest.mark.parametrize("fused", [False, True])
-def test_workload_batched_gqa_sampled(fused):
-    session_step_parity(inputs.WORKLOADS[2], n_check=6, fused=fused)
+def test_workload_batched_gqa_whole_batch(fused):
+    session_step_parity(inputs.WORKLOADS[2], fused=fused)
 
 
 @pytest.mark.parametrize("fused", [False, True])
-def test_workload_continuous_batching_sampled(fused):
-    session_step_parity(inputs.WORKLOADS[3], n_check=4, check_layers=(0, 31), fused=fused)
+def test_workload_continuous_batching_whole_batch(fused):
+    session_step_parity(inputs.WORKLOADS[3], check_layers=(0, 15, 31), fused=fused)
 
 
 @pytest.mark.parametrize("fused", [False, True])
-def test_workload_shared_prefix_sampled(fused):
-    sess, _ = session_step_parity(inputs.WORKLOADS[4], n_check=4, fused=fused)
+def test_workload_shared_prefix_whole_batch(fused):
+    sess, _ = session_step_parity(inputs.WORKLOADS[4], fused=fused)
     assert len(sess.setup_cow_pairs) == 64 * 7
 
 
 def test_workload_shared_prefix_partial_block_cow():
     w = inputs.WORKLOADS[4]
-    sess, _ = session_step_parity(w, n_check=3, prefix_len=2043, seed=1)
+    sess, _ = session_step_parity(w, prefix_len=2043, seed=1)
     assert len(sess.setup_cow_pairs) == 64 * 7
 
 
 @pytest.mark.parametrize("bs,q_len", [(16, 1), (32, 1), (16, 16), (32, 16)])
-def test_workload_long_context_sampled(bs, q_len):
-    session_step_parity(inputs.WORKLOADS[5], n_check=1 if q_len == 16 else 2, block_size=bs, q_len=q_len,
-                        fused=q_len == 1)
+def test_workload_long_context_whole_batch(bs, q_len):
+    session_step_parity(inputs.WORKLOADS[5], block_size=bs, q_len=q_len, fused=q_len == 1)
 
 
 def test_shared_prefix_layout_equals_private_copies_bit_exact():
     """Refcounted shared blocks and fully private copies give identical bits."""
     w = inputs.WORKLOADS[4]
-    sess = DecodeSession(w, "cuda", allocator_factory=OracleAllocator, extra_steps=1)
+    sess = DecodeSession(w, "cuda", extra_steps=1)
     sess.apply_setup_copies()
     step = sess.plan_step()
     (q, ks, vs), = sess.new_token_tensors(1, seed=3)

@@ -244,10 +244,12 @@ def test_mixed_step_of_decodes_and_a_prefill_chunk():
 
 
 @pytest.mark.parametrize("tag", ["prefill_long_context", "prefill_prompts", "prefill_mixed"])
-def test_prefill_workloads_sampled(tag):
+def test_prefill_workloads_every_sequence(tag):
     """The benchmark's prefill workloads at full size, in the benchmark's launch
-    configuration; sampled rows against the oracle (a chunk row equals a
-    single-token decode at the length the row sees)."""
+    configuration.  Every sequence is compared with the oracle on whole query
+    tiles (128 / G tokens x the G heads of each KV head, the unit the kernel
+    computes): its first and last tile and one tile in between, and the single
+    row of every decode."""
     from paged_kv_cache_276_gb300.workloads import PrefillCase
     case = PrefillCase(inputs.PREFILL_WORKLOADS[tag], "cuda")
     st = status_tensor()
@@ -255,19 +257,35 @@ def test_prefill_workloads_sampled(tag):
     torch.cuda.synchronize()
     assert st.item() == 0
     kb, vb = bits(case.k_cache), bits(case.v_cache)
-    out = case.out
+    qb = bits(case.q)
+    out = case.out.float().cpu().double().numpy()
+    tile = 128 // (case.Hq // case.Hkv)
     rng = np.random.default_rng(5)
-    seqs = sorted({0, case.B - 1, int(rng.integers(0, case.B))})
-    for i in seqs:
+    # (first row, row count, sequence, keys the last row sees) of every checked tile;
+    # a decode is a one-row tile.  Rows lo..hi-1 of a chunk of c tokens in a sequence
+    # of L see L - c + 1 + r keys: the causal rule of an (hi - lo)-row chunk whose
+    # last row sees L - c + hi keys.
+    groups = {}
+    for i in range(case.B):
         L, c = int(case.lens[i]), int(case.chunks[i])
-        rows = sorted({0, c - 1, int(rng.integers(0, c))})
-        for r in rows:
-            n = L - c + 1 + r
-            row = int(case.q_start[i]) + r
-            ref = OA.paged_attention(bits(case.q[row:row + 1].unsqueeze(0)), kb, vb, case.tables[i:i + 1],
-                                     np.array([n], dtype=np.int32), num_q_heads=case.Hq, num_kv_heads=case.Hkv,
-                                     head_dim=case.d, block_size=case.bs, scale=case.scale)
-            assert_attention_close(out[row:row + 1], ref[0], f"{tag} seq {i} row {r}")
+        if c == 0:
+            continue
+        ntiles = -(-c // tile)
+        for t in sorted({0, ntiles - 1, int(rng.integers(0, ntiles))}):
+            lo, hi = t * tile, min(c, (t + 1) * tile)
+            groups.setdefault(hi - lo, []).append((int(case.q_start[i]) + lo, i, L - c + hi))
+    checked = set()
+    for n, tiles in groups.items():  # one oracle call per tile height
+        first = np.array([t[0] for t in tiles])
+        seqs = [t[1] for t in tiles]
+        q = np.stack([qb[r:r + n] for r in first])
+        ref = OA.paged_attention(q, kb, vb, case.tables[seqs], np.array([t[2] for t in tiles], dtype=np.int32),
+                                 num_q_heads=case.Hq, num_kv_heads=case.Hkv, head_dim=case.d, block_size=case.bs,
+                                 scale=case.scale, q_len=n)
+        got = np.stack([out[r:r + n] for r in first])
+        assert_attention_close(torch.as_tensor(got), ref, f"{tag}: {len(tiles)} tiles of {n} rows")
+        checked.update(seqs)
+    assert checked == {i for i in range(case.B) if case.chunks[i] > 0}
 
 
 def test_prefill_at_the_sequence_limit():
