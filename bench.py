@@ -257,11 +257,13 @@ class Runner:
                         native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
                         launches += i >= warmup
                     d0, d1 = ev(), ev()
-                    if fused:  # the new token's store runs inside the decode's grid
+                    if fused:  # the new token's store inside the decode's grid, over the host-built work list
                         d0.record(stream)
-                        native.paged_attention_decode_write(q, ks[l], vs[l], p.slots, sess.k_caches[l],
+                        native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
                                                             sess.v_caches[l], p.tables, p.lens, p.max_len,
-                                                            sess.scale, out, ws, sess.partition_size, status, stream)
+                                                            sess.scale, out, p.items, workspace=ws,
+                                                            partition_size=sess.partition_size, d_status=status,
+                                                            stream=stream)
                     else:
                         native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
                         d0.record(stream)
@@ -293,10 +295,11 @@ class Runner:
                     d0, dm = ev(), ev()
                     if fused:
                         d0.record(stream)
-                        native.paged_attention_decode_write(q, ks[l], vs[l], p.slots, sess.k_caches[l],
+                        native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
                                                             sess.v_caches[l], p.tables, p.lens, p.max_len,
-                                                            sess.scale, out, ws, sess.partition_size, status, stream,
-                                                            main_done_event=dm)
+                                                            sess.scale, out, p.items, workspace=ws,
+                                                            partition_size=sess.partition_size, d_status=status,
+                                                            stream=stream, main_done_event=dm)
                     else:
                         native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
                         d0.record(stream)

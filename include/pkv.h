@@ -65,6 +65,7 @@ typedef uint16_t pkv_bf16;
 #define PKV_STATUS_BAD_LEN    4  /* seq_len < 0 or above the table's capacity    */
 #define PKV_STATUS_TIMEOUT    8  /* a bounded on-chip wait gave up               */
 #define PKV_STATUS_BAD_QSTART 16 /* prefill: q_start entry out of order or range */
+#define PKV_STATUS_BAD_ITEM   32 /* decode work list: item out of range, or built for other lengths / tables */
 
 /* Human-readable name of a return code (static storage). */
 const char *pkv_error_string(int code);
@@ -223,6 +224,62 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                                  const int32_t *seq_lens, int num_seqs, int max_seq_len,
                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                  int num_blocks, float scale, int partition_size, pkv_bf16 *out,
+                                 void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                 void *stream, void *main_done_event);
+
+/*
+ * pkv_decode_items -- host: the work list of a single-token decode batch, for
+ * paged_attention_decode_items.
+ *
+ * The pages have no counterpart to this call; it moves the decode's schedule
+ * to the host, which knows every length when it builds the step (the
+ * allocator's append and table fill).  Each sequence's keys are split into
+ * partitions of partition_size tokens (0: 768) as paged_attention_decode
+ * splits them, and every (partition, KV head) becomes one item:
+ *   {sequence, KV head | partition << 16, length, physical block of the
+ *    partition's first logical block (-1 if block_tables is NULL or the
+ *    partition is empty)}
+ * The items are ordered longest partition first (ties in sequence, partition
+ * and head order), so the CTAs that start first carry the most keys and the
+ * shortest partitions fill the end of the grid.  A sequence of length 0 gets
+ * one empty item per KV head (its output rows are zeros).
+ *   seq_lens      host, [num_seqs] int32, each in [0, max_blocks_per_seq *
+ *                 block_size] (else PKV_ERR_RANGE)
+ *   block_tables  host, [num_seqs][max_blocks_per_seq] int32, or NULL
+ *   items_out     host, [1 + max_items][4] int32: row 0 = {count, 0, 0, 0},
+ *                 rows 1..count the items
+ * *num_items receives the count (also when it exceeds max_items, which
+ * returns PKV_ERR_RANGE and writes no item).  partition_size must be a
+ * multiple of block_size (PKV_ERR_ARG).
+ */
+int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int max_blocks_per_seq,
+                     int num_seqs, int num_kv_heads, int block_size, int partition_size,
+                     int32_t *items_out, int max_items, int *num_items);
+
+/*
+ * paged_attention_decode_items -- the single-token decode over a work list:
+ * paged_attention_decode_write (or, with k_new, v_new and slot_mapping all
+ * NULL, paged_attention_decode with q_len = 1), one CTA per item.
+ *   items       device, 16-byte aligned, [1 + grid_items][4] int32: the rows
+ *               pkv_decode_items wrote for these seq_lens, block_tables and
+ *               partition_size (row 0 holds the count)
+ *   grid_items  CTAs to launch, >= the count in row 0 (CTAs past the count do
+ *               nothing), so a CUDA graph can be captured for a bound
+ * Every other argument and the result are those of paged_attention_decode_write.
+ * An item naming a sequence, head or partition out of range, a length other
+ * than seq_lens[sequence], or a first block other than the table's sets
+ * PKV_STATUS_BAD_ITEM (the item is skipped, or computed with the table's
+ * blocks); a list built for other arguments gives undefined output but never
+ * reads or writes out of bounds.  Where the decode runs on the tensor cores
+ * (max_seq_len >= 16384) the list is not used.
+ */
+int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                 const int64_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq,
+                                 const int32_t *seq_lens, int num_seqs, int max_seq_len,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, float scale, int partition_size,
+                                 const int32_t *items, int grid_items, pkv_bf16 *out,
                                  void *workspace, size_t workspace_bytes, int32_t *d_status,
                                  void *stream, void *main_done_event);
 
@@ -434,7 +491,8 @@ int pkv_refcount(const pkv_alloc *a, int block);
  * borrows an operating-system trick").  The runner chains exactly those calls
  * of this library: pkv_seq_append_batch, pkv_block_table, then per layer
  * pkv_write and paged_attention_decode (for single-token steps the pair as
- * paged_attention_decode_write).  The pages have no counterpart to the
+ * paged_attention_decode_items over the pkv_decode_items work list the runner
+ * builds from the step's lengths).  The pages have no counterpart to the
  * runner itself; it exists so that a serving loop pays one host call per step
  * instead of one per operation and per layer.
  *
@@ -452,7 +510,9 @@ int pkv_refcount(const pkv_alloc *a, int block);
  *         slots               slots_offset, [max_seqs * q_len] int64
  *         block tables        tables_offset, [max_seqs][max_blocks_per_seq] int32
  *         lengths             lens_offset, [max_seqs] int32
- *       A run over n sequences uses the first n rows of each segment.
+ *         work list (q_len 1) items_offset, [1 + max_items][4] int32
+ *       A run over n sequences uses the first n rows of each segment; the
+ *       runner writes the work list itself.
  *   dev_out / host_out      device and page-locked host memory of
  *       layout.out_bytes; layer l's output [max_seqs][q_len][num_q_heads]
  *       [head_dim] bf16 at l * out_layer_bytes.  Each run copies all of
@@ -490,6 +550,8 @@ typedef struct {
   size_t stage_bytes;      /* host_stage and dev_stage */
   size_t out_layer_bytes, out_bytes;
   size_t workspace_bytes;
+  size_t items_offset;     /* q_len 1: the decode's work list (pkv_decode_items), 0 otherwise */
+  int max_items;           /* rows of that list after its header */
 } pkv_step_layout;
 
 typedef struct pkv_step pkv_step;

@@ -28,10 +28,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "pkv.h"
@@ -72,6 +74,11 @@ struct Params {
   const uint4 *k_new, *v_new;
   const int64_t *slots;
   uint4 *k_cache, *v_cache;
+  // single-token decode over a host-built work list (nullptr: the grid is
+  // (partition, KV head, sequence)): items[0].x = item count, then one item per
+  // CTA, {sequence, KV head | partition << 16, length, first physical block}
+  const int4 *items;
+  int num_seqs;
 };
 
 // A block is staged as one or more "units" of consecutive token rows: the
@@ -99,6 +106,20 @@ struct Tile {
 
 __device__ __forceinline__ int clamp_len(const Params &p, int seq, int block_size, bool report) {
   int L = p.seq_lens[seq];
+  const long long cap_tbl = static_cast<long long>(p.max_blocks) * block_size;
+  const long long cap_grid = static_cast<long long>(p.max_parts) * p.part_blocks * block_size;
+  const long long cap = cap_tbl < cap_grid ? cap_tbl : cap_grid;
+  if (L < 0 || L > cap) {
+    if (report && p.status) atomicOr(p.status, PKV_STATUS_BAD_LEN);
+    L = L < 0 ? 0 : static_cast<int>(cap);
+  }
+  return L;
+}
+
+// A work item's length: clamped like clamp_len, and checked against seq_lens
+// (a list built for other lengths is reported, PKV_STATUS_BAD_ITEM).
+__device__ __forceinline__ int clamp_item_len(const Params &p, int seq, int L, int block_size, bool report) {
+  if (report && p.status && p.seq_lens[seq] != L) atomicOr(p.status, PKV_STATUS_BAD_ITEM);
   const long long cap_tbl = static_cast<long long>(p.max_blocks) * block_size;
   const long long cap_grid = static_cast<long long>(p.max_parts) * p.part_blocks * block_size;
   const long long cap = cap_tbl < cap_grid ? cap_tbl : cap_grid;
@@ -153,9 +174,12 @@ __device__ __forceinline__ uint4 new_token_chunk(const Params &p, int seq, int h
 // stream K/V tiles into the ring.  The warp reads 32 table entries with one
 // coalesced load and lane 0 issues the copies.  Stages are released by the
 // consumers through the empty barriers (count given at init).
+// b0 >= 0: the partition's first block id, known from the work item, so the
+// first copies go out before the table window has arrived; the window's first
+// entry is checked against it afterwards (PKV_STATUS_BAD_ITEM if they differ).
 template <int D, int BS>
 __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq, int h,
-                        int blk0, int nunit, int window0, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        int blk0, int nunit, int window0, int b0, uint32_t ring, uint32_t full0, uint32_t empty0,
                         volatile int *abort_flag, int lane) {
   using U = Unit<BS>;
   using T = Tile<D, U::kRows>;
@@ -163,11 +187,12 @@ __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Pa
   const uint64_t pol = l2_policy_evict_first();
   const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
   const int nblk = (nunit + U::kPerBlock - 1) / U::kPerBlock;
-  int issued = 0, window = 0;
+  int issued = 0;
+  int window = lane < nblk ? window0 : -1;
   for (int j = 0; j < nunit; ++j) {
     const int e = j / U::kPerBlock, piece = j - e * U::kPerBlock;  // table entry, unit within the block
-    if (piece == 0 && (e & 31) == 0) window = e + lane < nblk ? (e == 0 ? window0 : tbl[e + lane]) : -1;
-    const int b = __shfl_sync(0xffffffffu, window, e & 31);
+    if (piece == 0 && (e & 31) == 0 && e > 0) window = e + lane < nblk ? tbl[e + lane] : -1;
+    const int b = e == 0 && b0 >= 0 ? b0 : __shfl_sync(0xffffffffu, window, e & 31);
     const int s = j % S;
     bool ok = true;
     if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) ok = false;
@@ -198,6 +223,10 @@ __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Pa
     }
     ++issued;
   }
+  if (b0 >= 0 && nunit > 0) {
+    const int first = __shfl_sync(0xffffffffu, lane < nblk ? window0 : -1, 0);
+    if (lane == 0 && first != b0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_ITEM);
+  }
   // never leave a copy in flight into this CTA's shared memory
   if (lane == 0)
     for (int j = issued > S ? issued - S : 0; j < issued; ++j) mbar_wait(full0 + 8 * (j % S), (j / S) & 1);
@@ -224,15 +253,35 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kRingBytes);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * S);
 
-  const int part = blockIdx.x, h = blockIdx.y, seq = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Let the merge grid queued behind this one become resident now; it still
   // waits for this whole grid's results before it reads anything.
   grid_launch_dependents();
   grid_dependency_wait();  // inputs may come from the kernel launched just before
-  // the producer's first 32 block-table entries load while the length does
-  const int window0 = warp == kDecodeWarps ? first_window(p, seq, part, lane) : -1;
-  const int L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
+  int part, h, seq, L, window0, b0 = -1;
+  if (p.items) {
+    // a host-built work list: one 16-byte load names this CTA's partition, its
+    // length and its first block, so the first copy needs no other load
+    const int4 it = p.items[1 + blockIdx.x];
+    if (static_cast<int>(blockIdx.x) >= p.items[0].x) return;  // past the list (a grid sized for a bound)
+    seq = it.x;
+    h = it.y & 0xffff;
+    part = static_cast<int>(static_cast<unsigned>(it.y) >> 16);
+    if (seq < 0 || seq >= p.num_seqs || h >= p.num_kv_heads || part >= p.max_parts) {
+      if (threadIdx.x == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_ITEM);
+      return;
+    }
+    window0 = warp == kDecodeWarps ? first_window(p, seq, part, lane) : -1;
+    L = clamp_item_len(p, seq, it.z, BS, threadIdx.x == 0);
+    b0 = it.w;
+  } else {
+    part = blockIdx.x;
+    h = blockIdx.y;
+    seq = blockIdx.z;
+    // the producer's first 32 block-table entries load while the length does
+    window0 = warp == kDecodeWarps ? first_window(p, seq, part, lane) : -1;
+    L = clamp_len(p, seq, BS, part == 0 && threadIdx.x == 0);
+  }
   const int part_tokens = p.part_blocks * BS;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
   if (part >= nparts) return;
@@ -272,7 +321,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
         else p.v_cache[dst * (D / 8) + lane - D / 8] = c;
       }
     }
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, b0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
     uint32_t qf[NT][D / 16][2];
@@ -434,7 +483,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   __syncthreads();
 
   if (warp == kChunkWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, -1, ring, full0, empty0, abort_flag, lane);
     return;
   }
   if (warp >= p.active_warps) return;
@@ -695,8 +744,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 template <int D, int BS>
 int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int num_seqs, int q_len,
-           cudaStream_t stream, cudaEvent_t main_done) {
-  const dim3 grid(p.max_parts, p.num_kv_heads, num_seqs);
+           int grid_items, cudaStream_t stream, cudaEvent_t main_done) {
+  const dim3 grid = p.items ? dim3(grid_items) : dim3(p.max_parts, p.num_kv_heads, num_seqs);
   constexpr size_t smem = smem_bytes<D, BS>();
   cudaError_t e;
   if (q_len == 1) {
@@ -764,7 +813,8 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                 void *stream, void *main_done_event, const NewTokens *nt);
+                 void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items = nullptr,
+                 int grid_items = 0);
 
 }  // namespace pkv
 
@@ -816,6 +866,86 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                            out, workspace, workspace_bytes, d_status, stream, main_done_event, &nt);
 }
 
+// Host: the work list of a single-token decode batch (see pkv.h).
+int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
+                     int num_kv_heads, int block_size, int partition_size, int32_t *items_out, int max_items,
+                     int *num_items) {
+  if (!num_items) return PKV_ERR_ARG;
+  *num_items = 0;
+  if (num_seqs < 0 || num_kv_heads < 1 || num_kv_heads > 65535 || block_size < 1 || max_blocks_per_seq < 0 ||
+      max_items < 0 || partition_size < 0 || (num_seqs > 0 && !seq_lens) || !items_out)
+    return PKV_ERR_ARG;
+  const int part = partition_size == 0 ? pkv::kDefaultPartition : partition_size;
+  if (part % block_size != 0) return PKV_ERR_ARG;
+  const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+  long long count = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    const int L = seq_lens[i];
+    if (L < 0 || L > cap) return PKV_ERR_RANGE;
+    const long long np = L > 0 ? (static_cast<long long>(L) + part - 1) / part : 1;
+    if (np > 65535) return PKV_ERR_UNSUPPORTED;
+    count += np * num_kv_heads;
+  }
+  if (count > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
+  *num_items = static_cast<int>(count);
+  if (count > max_items) return PKV_ERR_RANGE;
+  struct Piece {
+    int ntok, seq, part, len;
+  };
+  std::vector<Piece> pieces;
+  pieces.reserve(static_cast<size_t>(count / num_kv_heads));
+  for (int i = 0; i < num_seqs; ++i) {
+    const int L = seq_lens[i];
+    const int np = L > 0 ? (L + part - 1) / part : 1;
+    for (int j = 0; j < np; ++j) {
+      const long long lo = static_cast<long long>(j) * part;
+      const long long hi = std::min<long long>(L, lo + part);
+      pieces.push_back({static_cast<int>(std::max<long long>(0, hi - lo)), i, j, L});
+    }
+  }
+  // longest first: the CTAs launched first carry the most keys, the shortest fill the tail
+  std::stable_sort(pieces.begin(), pieces.end(), [](const Piece &a, const Piece &b) { return a.ntok > b.ntok; });
+  int32_t *o = items_out;
+  o[0] = static_cast<int32_t>(count);
+  o[1] = o[2] = o[3] = 0;
+  o += 4;
+  const long long part_blocks = part / block_size;
+  for (const Piece &pc : pieces) {
+    const long long e = pc.part * part_blocks;
+    const int b0 = block_tables && pc.ntok > 0 && e < max_blocks_per_seq
+                       ? block_tables[static_cast<size_t>(pc.seq) * max_blocks_per_seq + e]
+                       : -1;
+    for (int h = 0; h < num_kv_heads; ++h, o += 4) {
+      o[0] = pc.seq;
+      o[1] = static_cast<int32_t>(static_cast<uint32_t>(h) | (static_cast<uint32_t>(pc.part) << 16));
+      o[2] = pc.len;
+      o[3] = b0;
+    }
+  }
+  return PKV_OK;
+}
+
+int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                                 const int64_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                                 const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                                 int num_seqs, int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, float scale, int partition_size,
+                                 const int32_t *items, int grid_items, pkv_bf16 *out, void *workspace,
+                                 size_t workspace_bytes, int32_t *d_status, void *stream, void *main_done_event) {
+  if (num_seqs > 0 && (!items || grid_items < 1 || (reinterpret_cast<uintptr_t>(items) & 15u))) return PKV_ERR_ARG;
+  const bool store = k_new || v_new || slot_mapping;
+  if (store) {
+    if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping)) return PKV_ERR_ARG;
+    if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+      return PKV_ERR_ARG;
+  }
+  const pkv::NewTokens nt{k_new, v_new, slot_mapping, k_cache, v_cache};
+  return pkv::decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                           1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                           out, workspace, workspace_bytes, d_status, stream, main_done_event,
+                           store ? &nt : nullptr, items, grid_items);
+}
+
 }  // extern "C"
 
 namespace pkv {
@@ -862,7 +992,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                 void *stream, void *main_done_event, const NewTokens *nt) {
+                 void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items, int grid_items) {
   cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   Plan plan;
   const int checked = decode_check(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -956,6 +1086,8 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   p.oob_row = static_cast<int>(rows);
   p.active_warps = (group * kChunkLen + 15) / 16;
   p.scale_log2 = scale * kLog2e;
+  p.num_seqs = num_seqs;
+  if (items) p.items = reinterpret_cast<const int4 *>(items);  // q_len == 1, grid_items >= 1 (entry checks)
   if (nt) {
     p.k_new = static_cast<const uint4 *>(nt->k);
     p.v_new = static_cast<const uint4 *>(nt->v);
@@ -965,14 +1097,14 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   }
 
   switch (head_dim * 1000 + block_size) {
-    case 128016: return launch<128, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 128032: return launch<128, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 128064: return launch<128, 64>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 128128: return launch<128, 128>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 64016: return launch<64, 16>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 64032: return launch<64, 32>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    case 64064: return launch<64, 64>(tmk, tmv, p, num_seqs, q_len, st, main_done);
-    default: return launch<64, 128>(tmk, tmv, p, num_seqs, q_len, st, main_done);
+    case 128016: return launch<128, 16>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 128032: return launch<128, 32>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 128064: return launch<128, 64>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 128128: return launch<128, 128>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 64016: return launch<64, 16>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 64032: return launch<64, 32>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    case 64064: return launch<64, 64>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
+    default: return launch<64, 128>(tmk, tmv, p, num_seqs, q_len, grid_items, st, main_done);
   }
 }
 

@@ -60,8 +60,9 @@ void drop_graphs(pkv_step *s) {
   s->graphs.clear();
 }
 
-// Copy in, every layer's write and decode, copy out, on `st`.
-int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len) {
+// Copy in, every layer's write and decode, copy out, on `st`.  q_len 1: the
+// decode runs grid_items CTAs over the work list in the staging buffer.
+int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items) {
   const pkv_step_config &c = s->cfg;
   const pkv_step_layout &L = s->lay;
   cudaError_t e = cudaMemcpyAsync(s->ds, s->hs, L.stage_bytes, cudaMemcpyHostToDevice, st);
@@ -76,10 +77,11 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len) {
     auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
     int rc;
     if (c.q_len == 1) {  // the allocator's slots are the newest tokens' table positions: one grid
-      rc = paged_attention_decode_write(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
+      const auto *items = reinterpret_cast<const int32_t *>(s->ds + L.items_offset);
+      rc = paged_attention_decode_items(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
                                         max_seq_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
-                                        c.num_blocks, c.scale, c.partition_size, out, s->ws, s->ws_bytes,
-                                        s->status, st, nullptr);
+                                        c.num_blocks, c.scale, c.partition_size, items, grid_items, out, s->ws,
+                                        s->ws_bytes, s->status, st, nullptr);
     } else {
       rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
                      c.head_dim, s->status, st);
@@ -95,7 +97,7 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len) {
   return PKV_OK;
 }
 
-int capture(pkv_step *s, int n, int max_seq_len, cudaGraphExec_t *exec) {
+int capture(pkv_step *s, int n, int max_seq_len, int grid_items, cudaGraphExec_t *exec) {
   cudaError_t e;
   if (!s->cap && (e = cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking)) != cudaSuccess)
     return pkv::set_cuda_error(e), PKV_ERR_CUDA;
@@ -103,7 +105,7 @@ int capture(pkv_step *s, int n, int max_seq_len, cudaGraphExec_t *exec) {
   // entry points while the stream is being captured.
   if ((e = cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeRelaxed)) != cudaSuccess)
     return pkv::set_cuda_error(e), PKV_ERR_CUDA;
-  const int rc = enqueue(s, s->cap, n, max_seq_len);
+  const int rc = enqueue(s, s->cap, n, max_seq_len, grid_items);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(s->cap, &g);
   if (rc != PKV_OK || e != cudaSuccess) {
@@ -146,7 +148,16 @@ int pkv_step_layout_of(const pkv_step_config *c, pkv_step_layout *o) {
   o->slots_offset = o->v_offset + c->num_layers * kvb;
   o->tables_offset = o->slots_offset + up256(r * sizeof(int64_t));
   o->lens_offset = o->tables_offset + up256(static_cast<size_t>(c->max_seqs) * c->max_blocks_per_seq * 4);
-  o->stage_bytes = o->lens_offset + up256(static_cast<size_t>(c->max_seqs) * 4);
+  const size_t after_lens = o->lens_offset + up256(static_cast<size_t>(c->max_seqs) * 4);
+  o->stage_bytes = after_lens;
+  if (c->q_len == 1) {  // the decode's work list: at most every sequence's partitions x KV heads
+    const int part = c->partition_size > 0 ? c->partition_size : kDefaultPartition;
+    const long long items = static_cast<long long>(c->max_seqs) * c->num_kv_heads * ((cap + part - 1) / part);
+    if (items > 0x7ffffffell) return PKV_ERR_ARG;
+    o->items_offset = after_lens;
+    o->max_items = static_cast<int>(items);
+    o->stage_bytes = after_lens + up256(static_cast<size_t>(items + 1) * 16);
+  }
   o->out_layer_bytes = qb;
   o->out_bytes = c->num_layers * qb;
   o->workspace_bytes = paged_attention_workspace_size(c->max_seqs, c->q_len, c->num_q_heads, c->head_dim,
@@ -238,7 +249,9 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
     if (it == s->graphs.end()) {
       if (static_cast<int>(s->graphs.size()) >= kMaxGraphs) drop_graphs(s);
       const long long bound = static_cast<long long>(parts) * s->part;
-      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), &exec);
+      // the work list of any step with this key has at most n x KV heads x parts items
+      const int grid_items = c.q_len == 1 ? n * c.num_kv_heads * parts : 0;
+      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), grid_items, &exec);
       if (rc != PKV_OK) return rc;
       it = s->graphs.emplace(key, exec).first;
     }
@@ -250,11 +263,18 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
   if ((rc = pkv_seq_append_batch(s->alloc, seq_ids, n, c.q_len, slots)) != PKV_OK) return rc;
   // cannot fail: every id is resident (the append took it) and its table has room (checked above)
   if ((rc = pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, lens)) != PKV_OK) return rc;
+  int count = 0;
+  if (c.q_len == 1) {  // cannot fail either: the lengths fit the tables and the list its segment
+    auto *items = reinterpret_cast<int32_t *>(s->hs + s->lay.items_offset);
+    if ((rc = pkv_decode_items(lens, tables, c.max_blocks_per_seq, n, c.num_kv_heads, c.block_size,
+                               c.partition_size, items, s->lay.max_items, &count)) != PKV_OK)
+      return rc;
+  }
 
   if (exec) {
     const cudaError_t e = cudaGraphLaunch(exec, st);
     if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
-  } else if ((rc = enqueue(s, st, n, max_len)) != PKV_OK) {
+  } else if ((rc = enqueue(s, st, n, max_len, count)) != PKV_OK) {
     return rc;
   }
   const cudaError_t e = cudaEventRecord(s->done, st);

@@ -32,6 +32,7 @@ PKV_STATUS_BAD_BLOCK = 2
 PKV_STATUS_BAD_LEN = 4
 PKV_STATUS_TIMEOUT = 8
 PKV_STATUS_BAD_QSTART = 16
+PKV_STATUS_BAD_ITEM = 32
 
 _c_int, _c_i64, _c_ptr, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_float)
@@ -48,7 +49,8 @@ class StepLayout(ctypes.Structure):
     """pkv_step_layout (byte offsets and sizes)."""
     _fields_ = [(n, _c_size) for n in ("q_offset", "q_layer_bytes", "k_offset", "v_offset", "kv_layer_bytes",
                                        "slots_offset", "tables_offset", "lens_offset", "stage_bytes",
-                                       "out_layer_bytes", "out_bytes", "workspace_bytes")]
+                                       "out_layer_bytes", "out_bytes", "workspace_bytes", "items_offset")] \
+        + [("max_items", _c_int)]
 
 
 # name -> (restype, argtypes); mirrors include/pkv.h
@@ -77,6 +79,12 @@ SIGNATURES = {
     "paged_attention_decode_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
                                               _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr, _c_ptr]),
+    "pkv_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int,
+                                  ctypes.POINTER(_c_int)]),
+    "paged_attention_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
+                                              _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                              _c_float, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
+                                              _c_ptr, _c_ptr]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -260,6 +268,71 @@ def paged_attention_decode_write(q, k_new, v_new, slot_mapping, k_cache, v_cache
         block_tables.shape[1], _ptr(seq_lens), B, int(max_seq_len), Hq, Hkv, d, bs, NB, float(scale),
         int(partition_size), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev),
         None if ev is None else ctypes.c_void_p(ev)), "paged_attention_decode_write")
+
+
+def pkv_decode_items(seq_lens, block_tables, num_kv_heads, block_size, partition_size=0, out=None):
+    """Host work list of a single-token decode batch (numpy int32 lengths [B] and
+    tables [B, max_blocks], or None): returns int32 [1 + count, 4], row 0 = {count, 0, 0, 0}.
+    ``out`` (int32 [1 + n, 4], C-contiguous) is filled in place when it has room."""
+    import numpy as np
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    tbl = None if block_tables is None else np.ascontiguousarray(block_tables, dtype=np.int32)
+    B = lens.shape[0]
+    maxb = 0 if tbl is None else tbl.shape[1]
+    if tbl is None:
+        maxb = int(-(-int(lens.max(initial=0)) // block_size))
+    elif tbl.shape[0] != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    n = ctypes.c_int(0)
+    buf = out if out is not None else np.empty((1, 4), dtype=np.int32)
+    for _ in range(2):
+        rc = lib().pkv_decode_items(lens.ctypes.data, None if tbl is None else tbl.ctypes.data, maxb, B,
+                                    int(num_kv_heads), int(block_size), int(partition_size), buf.ctypes.data,
+                                    buf.shape[0] - 1, ctypes.byref(n))
+        if rc == PKV_ERR_RANGE and n.value > buf.shape[0] - 1 and out is None:
+            buf = np.empty((1 + n.value, 4), dtype=np.int32)
+            continue
+        _check(rc, "pkv_decode_items")
+        return buf[:1 + n.value]
+    raise PkvError(PKV_ERR_RANGE, "pkv_decode_items")
+
+
+def paged_attention_decode_items(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens,
+                                 max_seq_len, scale, out, items, grid_items=None, workspace=None, partition_size=0,
+                                 d_status=None, stream=None, main_done_event=None):
+    """Single-token decode over a work list (device int32 [1 + n, 4] from
+    ``pkv_decode_items``); k_new / v_new / slot_mapping all None: no store."""
+    dev = k_cache.device
+    store = k_new is not None or v_new is not None or slot_mapping is not None
+    checks = [(q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
+              (block_tables, "block_tables", torch.int32), (seq_lens, "seq_lens", torch.int32),
+              (out, "out", torch.bfloat16), (items, "items", torch.int32)]
+    if store:
+        checks += [(k_new, "k_new", torch.bfloat16), (v_new, "v_new", torch.bfloat16),
+                   (slot_mapping, "slot_mapping", torch.int64)]
+    for t, n, dt in checks:
+        _need(t, dt, n, dev)
+    B, q_len, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    if q_len != 1 or d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape \
+            or block_tables.shape[0] != B or seq_lens.shape != (B,) or items.dim() != 2 or items.shape[1] != 4:
+        raise ValueError("shape mismatch")
+    if store and (k_new.shape != (B, Hkv, d) or v_new.shape != (B, Hkv, d) or slot_mapping.shape != (B,)):
+        raise ValueError("shape mismatch")
+    grid = items.shape[0] - 1 if grid_items is None else int(grid_items)
+    if grid > items.shape[0] - 1:
+        raise ValueError("grid_items exceeds the rows of items")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ev = None
+    if main_done_event is not None:
+        ev = main_done_event.cuda_event
+        if not ev:
+            raise ValueError("main_done_event: record the torch.cuda.Event once before passing it")
+    _check(lib().paged_attention_decode_items(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), B, int(max_seq_len), Hq, Hkv, d, bs, NB, float(scale),
+        int(partition_size), _ptr(items), grid, _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status),
+        _stream(stream, dev), None if ev is None else ctypes.c_void_p(ev)), "paged_attention_decode_items")
 
 
 def paged_attention_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, d_status=None,

@@ -48,6 +48,7 @@ class StepInputs:
     cow_pairs: torch.Tensor | None  # [n, 2] int32, device, or None
     host_tables: np.ndarray
     host_lens: np.ndarray
+    items: torch.Tensor | None = None  # single-token steps: the decode's work list [1 + n, 4] int32, device
 
 
 class DecodeSession:
@@ -149,9 +150,13 @@ class DecodeSession:
         lens = np.asarray(lens, dtype=np.int32)
         dev = self.device
         cow = torch.as_tensor(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), device=dev) if pairs else None
+        items = None
+        if self.q_len == 1:  # the host knows every length: the decode's longest-first work list
+            items = torch.as_tensor(native.pkv_decode_items(lens, tables, self.Hkv, self.bs, self.partition_size),
+                                    device=dev)
         return StepInputs(torch.as_tensor(slots, device=dev), torch.as_tensor(tables, device=dev),
                           torch.as_tensor(lens, device=dev), int(lens.max()) if len(lens) else 0, cow,
-                          tables, lens)
+                          tables, lens, items)
 
     def plan_steps(self, n: int):
         return [self.plan_step() for _ in range(n)]
@@ -182,14 +187,21 @@ class DecodeSession:
 
     # ------------------------------------------------------------ one step
     def run_step(self, step: StepInputs, q, ks, vs, out, workspace, d_status=None, stream=None,
-                 per_layer_out=None, fused=False):
+                 per_layer_out=None, fused=False, planned=False):
         """One pass of the hot path over every layer.  fused (single-token steps):
-        the new tokens' store runs inside the decode grid (paged_attention_decode_write)."""
+        the new tokens' store runs inside the decode grid (paged_attention_decode_write);
+        planned: that grid runs the host-built work list (paged_attention_decode_items)."""
         fused = fused and self.q_len == 1
         for l in range(self.layers):
             if step.cow_pairs is not None:
                 native.pkv_block_copy(self.k_caches[l], self.v_caches[l], step.cow_pairs, d_status, stream)
             o = out if per_layer_out is None else per_layer_out[l]
+            if fused and planned:
+                native.paged_attention_decode_items(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
+                                                    step.tables, step.lens, step.max_len, self.scale, o, step.items,
+                                                    workspace=workspace, partition_size=self.partition_size,
+                                                    d_status=d_status, stream=stream)
+                continue
             if fused:
                 native.paged_attention_decode_write(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
                                                     step.tables, step.lens, step.max_len, self.scale, o, workspace,

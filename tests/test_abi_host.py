@@ -440,3 +440,56 @@ def test_decode_write_rejects_bad_arguments_before_launch(native):
     assert call(vn=24) == native.PKV_ERR_ARG         # misaligned
     assert call(slots=12) == native.PKV_ERR_ARG      # int64 slots must be 8-byte aligned
     assert call(q=24) == native.PKV_ERR_ARG
+
+
+def test_decode_work_list_is_longest_first_and_complete(native):
+    """pkv_decode_items: one item per (partition, KV head), longest partition
+    first, ties in sequence / partition / head order, with each item's length
+    and first physical block; a length-0 sequence gets empty items."""
+    lens = np.array([0, 5, 1000, 768], dtype=np.int32)
+    tables = np.full((4, 70), -1, dtype=np.int32)
+    tables[1, 0] = 7
+    tables[2, :63] = np.arange(100, 163)
+    tables[3, :48] = np.arange(200, 248)
+    items = native.pkv_decode_items(lens, tables, num_kv_heads=2, block_size=16, partition_size=768)
+    assert items[0].tolist() == [10, 0, 0, 0]
+
+    def it(seq, part, h, L, b0):
+        return [seq, h | (part << 16), L, b0]
+    want = [it(2, 0, 0, 1000, 100), it(2, 0, 1, 1000, 100),   # 768 tokens
+            it(3, 0, 0, 768, 200), it(3, 0, 1, 768, 200),     # 768 tokens
+            it(2, 1, 0, 1000, 148), it(2, 1, 1, 1000, 148),   # 232 tokens, from logical block 48
+            it(1, 0, 0, 5, 7), it(1, 0, 1, 5, 7),             # 5 tokens
+            it(0, 0, 0, 0, -1), it(0, 0, 1, 0, -1)]           # empty: zeros
+    assert items[1:].tolist() == want
+    # without tables the first block is unknown (-1); the default partition is 768
+    assert native.pkv_decode_items(lens, None, 2, 16)[1:, 3].tolist() == [-1] * 10
+    # a length past the table, a partition that is not a multiple of the block, no room
+    lib = native.lib()
+    n = ctypes.c_int(0)
+    buf = np.zeros((11, 4), dtype=np.int32)
+    bad = np.array([16 * 70 + 1], dtype=np.int32)
+    assert lib.pkv_decode_items(bad.ctypes.data, None, 70, 1, 2, 16, 0, buf.ctypes.data, 10,
+                                ctypes.byref(n)) == native.PKV_ERR_RANGE
+    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 16, 24, buf.ctypes.data, 10,
+                                ctypes.byref(n)) == native.PKV_ERR_ARG
+    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 16, 768, buf.ctypes.data, 9,
+                                ctypes.byref(n)) == native.PKV_ERR_RANGE and n.value == 10
+
+
+def test_decode_items_rejects_bad_arguments_before_launch(native):
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    base = [fake, None, None, None, fake, fake, fake, 4, fake, 2, 64, 8, 2, 128, 16, 8, 0.1, 0]
+
+    def call(items=fake, grid=3, **kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[{"k_new": 1, "slots": 3, "Hq": 11, "d": 13}[k]] = v
+        return lib.paged_attention_decode_items(*a, items, grid, fake, None, 0, None, None, None)
+    assert call(items=None) == native.PKV_ERR_ARG
+    assert call(grid=0) == native.PKV_ERR_ARG
+    assert call(items=ctypes.c_void_p((1 << 20) + 4)) == native.PKV_ERR_ARG   # items must be 16-byte aligned
+    assert call(k_new=fake) == native.PKV_ERR_ARG                             # a store needs k, v and slots
+    assert call(d=96) == native.PKV_ERR_UNSUPPORTED
+    assert call(Hq=7) == native.PKV_ERR_ARG

@@ -594,10 +594,11 @@ def replay_on_oracle(rec):
 
 
 def session_step_parity(w, block_size=None, q_len=None, layers=None, check_layers=(0,), prefix_len=None, seed=0,
-                        fused=False):
+                        fused=False, planned=False):
     """One full step of a workload on the GPU, on the native allocator and in the
     launch configuration the benchmark times (fused: the new tokens' store inside
-    the decode grid, as the benchmark's single-token step runs it).  The
+    the decode grid; planned: over the host-built work list, as the benchmark's
+    single-token step runs it).  The
     allocator's calls are replayed on the oracle allocator, the oracle's write
     and copy run on host copies of the checked layers' caches, and every
     sequence's output on those layers is compared with the fp64 oracle."""
@@ -614,7 +615,7 @@ def session_step_parity(w, block_size=None, q_len=None, layers=None, check_layer
     (q, ks, vs), = sess.new_token_tensors(1, seed=w.seed + seed)
     outs = [torch.empty_like(q) for _ in range(sess.layers)]
     ws = sess.workspace(step.max_len)
-    sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs, fused=fused)
+    sess.run_step(step, q, ks, vs, None, ws, st, per_layer_out=outs, fused=fused, planned=planned)
     torch.cuda.synchronize()
     assert st.item() == 0
     slots = step.slots.cpu().numpy()
@@ -635,19 +636,19 @@ def test_workload_tiny_full():
     session_step_parity(inputs.WORKLOADS[1])
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_workload_batched_gqa_whole_batch(fused):
-    session_step_parity(inputs.WORKLOADS[2], fused=fused)
+@pytest.mark.parametrize("fused,planned", [(False, False), (True, False), (True, True)])
+def test_workload_batched_gqa_whole_batch(fused, planned):
+    session_step_parity(inputs.WORKLOADS[2], fused=fused, planned=planned)
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_workload_continuous_batching_whole_batch(fused):
-    session_step_parity(inputs.WORKLOADS[3], check_layers=(0, 15, 31), fused=fused)
+@pytest.mark.parametrize("fused,planned", [(False, False), (True, True)])
+def test_workload_continuous_batching_whole_batch(fused, planned):
+    session_step_parity(inputs.WORKLOADS[3], check_layers=(0, 15, 31), fused=fused, planned=planned)
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_workload_shared_prefix_whole_batch(fused):
-    sess, _ = session_step_parity(inputs.WORKLOADS[4], fused=fused)
+@pytest.mark.parametrize("fused,planned", [(False, False), (True, True)])
+def test_workload_shared_prefix_whole_batch(fused, planned):
+    sess, _ = session_step_parity(inputs.WORKLOADS[4], fused=fused, planned=planned)
     assert len(sess.setup_cow_pairs) == 64 * 7
 
 
@@ -659,7 +660,7 @@ def test_workload_shared_prefix_partial_block_cow():
 
 @pytest.mark.parametrize("bs,q_len", [(16, 1), (32, 1), (16, 16), (32, 16)])
 def test_workload_long_context_whole_batch(bs, q_len):
-    session_step_parity(inputs.WORKLOADS[5], block_size=bs, q_len=q_len, fused=q_len == 1)
+    session_step_parity(inputs.WORKLOADS[5], block_size=bs, q_len=q_len, fused=q_len == 1, planned=q_len == 1)
 
 
 def test_shared_prefix_layout_equals_private_copies_bit_exact():
@@ -781,3 +782,73 @@ def test_decode_write_on_the_tensor_core_route_equals_write_then_decode():
     assert st.item() == 0
     assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16))
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+
+
+# ------------------------------------------------------------------ host-built work list
+@pytest.mark.parametrize("d,bs,Hq,Hkv,part", [(128, 16, 32, 8, 768), (64, 32, 16, 4, 256), (128, 128, 32, 2, 512),
+                                             (128, 64, 8, 8, 128), (64, 16, 64, 4, 0)])
+def test_decode_items_equals_the_grid_decode_bit_exact(d, bs, Hq, Hkv, part):
+    """paged_attention_decode_items (the host-built, longest-first list) gives the
+    same bits as paged_attention_decode_write / paged_attention_decode, with and
+    without the new tokens' store, and with a grid larger than the list."""
+    lens = [1, 17, 300, 1025, 64, 2000, 33, 0, 4000]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=d + bs + Hq + 5)
+    B = len(lens)
+    slots = _newest_slots(tables, lens, bs)
+    k_new = inputs.randn_bf16((B, Hkv, d), 911, "cuda")
+    v_new = inputs.randn_bf16((B, Hkv, d), 912, "cuda")
+    slots_d = torch.as_tensor(slots, device="cuda")
+    tables_d = torch.as_tensor(np.asarray(tables, dtype=np.int32), device="cuda")
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    max_len = max(lens)
+    n = native.paged_attention_workspace_size(B, 1, Hq, d, max_len, part)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    items = native.pkv_decode_items(np.asarray(lens, dtype=np.int32), tables, Hkv, bs, part)
+    count = int(items[0, 0])
+    padded = np.zeros((1 + count + 37, 4), dtype=np.int32)  # a grid of count + 37 CTAs
+    padded[:1 + count] = items
+    items_d = torch.as_tensor(padded, device="cuda")
+    st = status_tensor()
+    kc2, vc2 = kc.clone(), vc.clone()
+    ref = torch.empty_like(q)
+    native.paged_attention_decode_write(q, k_new, v_new, slots_d, kc, vc, tables_d, lens_d, max_len, 0.09, ref, ws,
+                                        part, st)
+    got = torch.full_like(q, float("nan"))
+    native.paged_attention_decode_items(q, k_new, v_new, slots_d, kc2, vc2, tables_d, lens_d, max_len, 0.09, got,
+                                        items_d, grid_items=count, workspace=ws, partition_size=part, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16)) and torch.equal(vc2.view(torch.int16),
+                                                                                    vc.view(torch.int16))
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    # no store, and a grid of more CTAs than items
+    ref2 = torch.empty_like(q)
+    native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max_len, 0.09, ref2, ws, part, st)
+    got2 = torch.full_like(q, float("nan"))
+    native.paged_attention_decode_items(q, None, None, None, kc, vc, tables_d, lens_d, max_len, 0.09, got2, items_d,
+                                        grid_items=count + 37, workspace=ws, partition_size=part, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(got2.view(torch.int16), ref2.view(torch.int16))
+    oracle = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.09)
+    assert_attention_close(got2, oracle, "decode over the work list")
+
+
+def test_decode_items_built_for_other_lengths_is_reported():
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    lens = [900, 40, 2000]
+    q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=97)
+    items = native.pkv_decode_items(np.asarray([900, 40, 1990], dtype=np.int32), tables, Hkv, bs, 512)
+    st = status_tensor()
+    out = torch.empty_like(q)
+    n = native.paged_attention_workspace_size(3, 1, Hq, d, 2000, 512)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    native.paged_attention_decode_items(q, None, None, None, kc, vc, torch.as_tensor(tables, device="cuda"),
+                                        torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda"), 2000, 0.09,
+                                        out, torch.as_tensor(items, device="cuda"), workspace=ws, partition_size=512,
+                                        d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & native.PKV_STATUS_BAD_ITEM
+    # the sequences the list describes correctly are still right
+    ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.09)
+    assert_attention_close(out[:2], ref[:2], "sequences the list matches")
