@@ -309,11 +309,13 @@ int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const
  *   block_tables, seq_lens, k_cache, v_cache, num_blocks, block_size, scale:
  *                 as paged_attention_decode (L <= max_blocks_per_seq *
  *                 block_size, else PKV_STATUS_BAD_LEN and L is clamped)
- * No workspace: every query tile of 128 / G tokens x G heads
+ * No workspace: every query tile of floor(128 / G) tokens x G heads
  * (G = num_q_heads / num_kv_heads) is one unit of work over all the keys it
  * sees, on the tensor cores.
- * Supported: head_dim in {64, 128}; G in {1, 2, 4, 8, 16}; block_size in {16,
- * 32, 64, 128}; num_seqs <= 1024.  Other sizes return PKV_ERR_UNSUPPORTED.
+ * Supported: head_dim in {64, 128}; G from 1 to 16 (a G that does not divide
+ * 128 makes tiles of floor(128 / G) tokens, whose last 128 mod G rows are
+ * spare); block_size in {16, 32, 64, 128}; num_seqs <= 1024.  Other sizes
+ * return PKV_ERR_UNSUPPORTED.
  * total_q == 0 or num_seqs == 0 is a no-op.
  */
 int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,

@@ -136,7 +136,8 @@ struct TcParams {
   int num_seqs, max_blocks, num_q_heads, num_kv_heads, num_blocks;
   int part_tokens, max_parts, oob_row;
   int total_q;             // prefill: query rows
-  int lg_group;            // log2 of the query heads per KV head (G)
+  int group;               // query heads per KV head (G, 1..16)
+  int tile_tok;            // query tokens per tile: floor(128 / G); rows tile_tok * G .. 127 are spare
   int q_len;               // decode chunk: query tokens per sequence (q_len * G <= 128)
   float scale_log2;
 };
@@ -235,7 +236,7 @@ struct Sched {
     x.run_begin = begins;
     if (kPrefill) {
       const int c = t.qc[w.seq];
-      const int tile_tok = kRows >> p.lg_group;
+      const int tile_tok = p.tile_tok;
       x.qt = w.nparts - 1 - w.part;  // longest first
       x.part = 0;
       x.nparts = 1;
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lo = min(B, lane * per), hi = min(B, lo + per);
     const int cap_tbl = p.max_blocks * BS, cap_grid = p.max_parts * p.part_tokens;
     const int cap = kPrefill || cap_tbl < cap_grid ? cap_tbl : cap_grid;
-    const int tile_tok = kRows >> p.lg_group;
+    const int tile_tok = p.tile_tok;
     int sum = 0;
     for (int i = lo; i < hi; ++i) {
       int L = p.seq_lens[i];
@@ -414,9 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
     tc::relinquish();
   }
-  if (!kPrefill && (p.q_len << p.lg_group) < kRows) {
-    // the loads fill the tile's first q_len * G rows only: the rest stay zero
-    // for the whole kernel, so their scores are finite (and masked)
+  if (kPrefill ? p.tile_tok * p.group < kRows : p.q_len * p.group < kRows) {
+    // the loads fill the tile's first q_len * G (prefill: tile_tok * G) rows
+    // only: the rest stay zero for the whole kernel, so their scores are
+    // finite (and masked)
     for (int i = threadIdx.x; i < kQBufs * kQBytes / 16; i += kThreads)
       asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(smem) + i * 16), "r"(0u) : "memory");
     fence_proxy_async_shared();
@@ -460,9 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (lane == 0) {
-            const int gsz = 1 << p.lg_group, tile_tok = kRows >> p.lg_group;
+            const int gsz = p.group, tile_tok = p.tile_tok;
             const int ntq = x.has_b ? 2 : 1;
-            mbar_arrive_expect_tx(bar(B_Q_FULL0), ntq * kQBytes);
+            mbar_arrive_expect_tx(bar(B_Q_FULL0), ntq * tile_tok * gsz * D * 2);  // the boxes' bytes
             for (int q = 0; q < ntq; ++q)
               for (int hf = 0; hf < kHalves; ++hf)
                 asm volatile(
@@ -481,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (lane == 0) {
-            const int gsz = 1 << p.lg_group;
-            const int qz = kPrefill ? qs[x.seq] + (kRows >> p.lg_group) * x.qt : x.seq * p.q_len;
-            // decode chunk: the box holds the q_len * G rows only
-            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), kPrefill ? kQBytes : (p.q_len << p.lg_group) * D * 2);
+            const int gsz = p.group;
+            const int qz = kPrefill ? qs[x.seq] + p.tile_tok * x.qt : x.seq * p.q_len;
+            // the box holds tile_tok * G (decode chunk: q_len * G) rows
+            mbar_arrive_expect_tx(bar(B_Q_FULL0 + qb), (kPrefill ? p.tile_tok : p.q_len) * gsz * D * 2);
             for (int hf = 0; hf < kHalves; ++hf)
               asm volatile(
                   "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -721,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // prefill: set q takes every tile of query tile q of the pair
       const int set = warp >> 2;
       const int r = threadIdx.x & (kRows - 1);    // query row = TMEM lane
-      const int tok = r >> p.lg_group, gh = r & ((1 << p.lg_group) - 1);
-      const int tile_tok = kRows >> p.lg_group;
+      const int tok = r / p.group, gh = r - tok * p.group;
+      const int tile_tok = p.tile_tok;
       const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const uint32_t tO = tmem + set * D;         // this set's accumulator
       float2 *stats = reinterpret_cast<float2 *>(smem + Lay::kSmemStats);
@@ -753,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kPrefill) {
           const int c = qc[x.seq];
           row_tok = tile_tok * (kP2 ? 2 * x.qt + set : x.qt) + tok;
-          row_valid = row_tok < c;
+          row_valid = tok < tile_tok && row_tok < c;  // a spare row of the tile is never valid
           limit = row_valid ? L - c + 1 + row_tok : 0;
         } else {
           row_tok = tok;
@@ -935,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after();
             inv = l > 0.f ? 1.f / l : 0.f;
           }
-          const size_t orow = static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + (x.head << p.lg_group) + gh;
+          const size_t orow = static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + x.head * p.group + gh;
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t ov[32];
@@ -976,8 +978,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int nparts = x.nparts;
         const size_t orow =
-            kPrefill ? static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + (x.head << p.lg_group) + gh
-                     : (static_cast<size_t>(x.seq) * p.q_len + tok) * p.num_q_heads + (x.head << p.lg_group) + gh;
+            kPrefill ? static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + x.head * p.group + gh
+                     : (static_cast<size_t>(x.seq) * p.q_len + tok) * p.num_q_heads + x.head * p.group + gh;
         float fa = 0.f, fb = 0.f, M = -INFINITY, lt = 0.f;
         if (run_has_tiles) {
           if (!wait_warp(bar(B_O_FULL), (tpieces - 1) & 1)) { ok = false; break; }
@@ -1116,8 +1118,6 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   const int box_rows = a.block_size < Layout<false, 128>::kTK ? a.block_size : Layout<false, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
   const int group = a.num_q_heads / a.num_kv_heads;
-  int lg = 0;
-  while ((1 << lg) < group) ++lg;
   // q viewed as [B*q_len][Hq][128]: box = 64 columns x G heads x q_len tokens
   if (!make_tensor_map_3d(&tmq, a.q, a.head_dim, a.num_q_heads, static_cast<long long>(B) * a.q_len, 64, group,
                           a.q_len) ||
@@ -1139,7 +1139,8 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
   p.part_tokens = a.part_tokens;
   p.max_parts = a.max_parts;
   p.oob_row = static_cast<int>(a.rows);
-  p.lg_group = lg;
+  p.group = group;
+  p.tile_tok = kRows / group;
   p.q_len = a.q_len;
   p.scale_log2 = kernel_scale_log2(a.scale);
   return launch_tc<false, false>(tmq, tmk, tmv, p, a.block_size, a.head_dim, stream);
@@ -1158,9 +1159,7 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
     return PKV_ERR_ARG;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
   const int group = num_q_heads / num_kv_heads;
-  int lg = 0;
-  while ((1 << lg) < group) ++lg;
-  if ((head_dim != 64 && head_dim != 128) || (1 << lg) != group || group > 16) return PKV_ERR_UNSUPPORTED;
+  if ((head_dim != 64 && head_dim != 128) || group > 16) return PKV_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > Layout<true, 128>::kMaxSeqs) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
@@ -1179,7 +1178,8 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   const int tile_tok = kRows / group;
   const int box_rows = block_size < Layout<true, 128>::kTK ? block_size : Layout<true, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
-  // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x 128 / G tokens
+  // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x floor(128 / G)
+  // tokens (G not a power of two: the tile's last 128 mod G rows are spare)
   if (!make_tensor_map_3d(&tmq, q, head_dim, num_q_heads, total_q, 64, group, tile_tok) ||
       !make_tensor_map_2d(&tmk, k_cache, head_dim, rows, 64, box_rows) ||
       !make_tensor_map_2d(&tmv, v_cache, head_dim, rows, 64, box_rows))
@@ -1199,13 +1199,14 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   p.max_parts = 1;
   p.oob_row = static_cast<int>(rows);
   p.total_q = total_q;
-  p.lg_group = lg;
+  p.group = group;
+  p.tile_tok = tile_tok;
   p.scale_log2 = kernel_scale_log2(scale);
   // Batches of long chunks run over pairs of query tiles, which share every
   // key and value tile (half the key / value traffic per product); batches
   // of mostly short chunks (decodes) split each query tile's keys between the
   // two softmax sets instead, so that both sets work on every item.
-  if (static_cast<long long>(total_q) >= 2ll * (kRows >> lg) * num_seqs)
+  if (static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs)
     return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
   return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
 }

@@ -122,7 +122,7 @@ def test_prefill_rejects_bad_sizes_before_launch(native):
     assert call(d=96) == native.PKV_ERR_UNSUPPORTED               # tensor-core tiles: head dim 64 or 128
     assert call(bs=8) == native.PKV_ERR_UNSUPPORTED
     assert call(bs=256) == native.PKV_ERR_UNSUPPORTED
-    assert call(Hq=24) == native.PKV_ERR_UNSUPPORTED              # group 3: not a power of two
+    assert call(Hq=24, NB=0) == native.PKV_ERR_ARG                # group 3 passes the shape checks
     assert call(Hq=64, Hkv=2) == native.PKV_ERR_UNSUPPORTED       # group 32 > 16
     assert call(Hq=7, Hkv=2) == native.PKV_ERR_ARG
     assert call(B=1025) == native.PKV_ERR_UNSUPPORTED

@@ -344,3 +344,31 @@ def test_both_prefill_schedules_match_the_oracle(d, bs, Hq, Hkv):
         assert st.item() == 0
         ref = oracle_prefill(q, kc, vc, tables, L_, q_start, Hq, Hkv, bs, scale, d=d)
         assert_attention_close(out, ref, f"prefill schedule for {len(L_)} sequences")
+
+
+@pytest.mark.parametrize("d,bs,Hq,Hkv", [(128, 16, 24, 8), (128, 32, 48, 8), (64, 16, 12, 1), (128, 64, 40, 8),
+                                         (128, 16, 6, 2)])
+def test_prefill_groups_that_do_not_divide_the_tile(d, bs, Hq, Hkv):
+    """G = 3, 6, 12, 5: query tiles of floor(128 / G) tokens x G heads with
+    128 mod G spare rows.  Both schedules (pairs of query tiles for long
+    chunks; the even / odd key split when most chunks are short) match the
+    oracle, chunk ends fall inside tiles, and no row outside the chunks is
+    written (the NaN canary survives)."""
+    G = Hq // Hkv
+    tile_tok = 128 // G
+    lens = [700, 129, 40, 1000, 3, 2 * tile_tok + 1]
+    chunks = [300, 129, 1, 257, 3, 2 * tile_tok + 1]
+    n_pad = int(sum(chunks) // (2 * tile_tok)) + 1 - len(lens)
+    pad_lens, pad_chunks = lens + [17] * max(n_pad, 0), chunks + [0] * max(n_pad, 0)
+    assert sum(chunks) >= 2 * tile_tok * len(lens) and sum(pad_chunks) < 2 * tile_tok * len(pad_lens)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    for L_, C_ in ((lens, chunks), (pad_lens, pad_chunks)):
+        q, kc, vc, tables, q_start = prefill_case(L_, C_, bs, Hq, Hkv, seed=60 + G, d=d)
+        out = torch.empty((int(q_start[-1]) + 5,) + tuple(q.shape[1:]), dtype=q.dtype, device=q.device)
+        out.view(torch.int16).fill_(CANARY)
+        st = status_tensor()
+        run_prefill(q, kc, vc, tables, L_, q_start, scale, status=st, out=out[:q.shape[0]])
+        assert st.item() == 0
+        ref = oracle_prefill(q, kc, vc, tables, L_, q_start, Hq, Hkv, bs, scale, d=d)
+        assert_attention_close(out[:q.shape[0]], ref, f"prefill, group {G}, {len(L_)} sequences")
+        assert (bits(out[q.shape[0]:]) == CANARY).all()  # rows past the batch untouched
