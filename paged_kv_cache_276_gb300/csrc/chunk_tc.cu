@@ -103,7 +103,7 @@ struct Layout {
   static constexpr int kStages = kPrefill ? 2 : 4;
   static constexpr int kQBufs = 2;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
-  static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
+  static constexpr int kSeqInts = kPrefill ? 5 : 2;  // per-sequence ints after the item prefix
   static constexpr int kSmemK = kQBufs * kQBytes;
   static constexpr int kSmemV = kSmemK + kStages * kKVBytes;
   static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
@@ -118,7 +118,7 @@ struct Layout {
   static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
   static_assert(kTmemP + kPStride + kTK / 2 <= kTmemCols, "tensor memory");
   static constexpr size_t bytes(int num_seqs) {
-    return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 1) * 4;
+    return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 2) * 4;
   }
 };
 static_assert(Layout<false, 128>::bytes(Layout<false, 128>::kMaxSeqs) <= 227 * 1024, "shared memory");
@@ -178,10 +178,11 @@ __device__ __forceinline__ int range_first(unsigned c, int total) {
 
 // Per-sequence values kept in shared memory.
 struct SeqTab {
-  const int *prefix;  // [B + 1] items before each sequence
+  const int *prefix;  // [B + 1] items before each sequence (prefill: the heavy class's items)
   const int *lens;    // [B] clamped lengths
   const int *qs;      // prefill: [B] first query row
   const int *qc;      // prefill: [B] chunk length (0 for a bad q_start entry)
+  const int *prefix_light;  // prefill: [B + 1] the light class's items before each sequence
 };
 
 // One work item: a query tile (prefill: a pair of query tiles 2 qt and
@@ -212,16 +213,31 @@ struct Sched {
       step = 1;
     }
     if (it < end) {
-      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+      locate(p, t);
       fill(p, t, true);
     }
+  }
+  // Prefill: item `it` of the whole order.  The heavy items (chunks of more
+  // than one query tile) and the light ones (decodes, short chunks) are merged
+  // in proportion, so that at any time some CTAs run compute-bound chunk tiles
+  // while the others stream the decodes' keys; within a class, items of one
+  // (sequence, KV head) stay together, longest first.
+  __device__ void locate(const TcParams &p, const SeqTab &t) {
+    if (!kPrefill) {
+      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+      return;
+    }
+    const long long na = t.prefix[p.num_seqs], n = na + t.prefix_light[p.num_seqs];
+    const int a0 = static_cast<int>(it * na / n), a1 = static_cast<int>((it + 1ll) * na / n);
+    if (a1 > a0) w.seek(t.prefix, p.num_seqs, p.num_kv_heads, a0);
+    else w.seek(t.prefix_light, p.num_seqs, p.num_kv_heads, it - a0);
   }
   __device__ bool valid() const { return it < end; }
   __device__ void advance(const TcParams &p, const SeqTab &t) {
     it += step;
     if (it >= end) return;
     if (kPrefill) {
-      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+      locate(p, t);
       fill(p, t, true);
     } else {
       const int s0 = w.seq, h0 = w.head;
@@ -332,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *lens = prefix + p.num_seqs + 1;                          // [B]
   int *qs = lens + p.num_seqs;                                  // prefill: [B]
   int *qc = qs + p.num_seqs;                                    // prefill: [B]
-  const SeqTab tab{prefix, lens, qs, qc};
+  int *prefix_light = qc + p.num_seqs;                          // prefill: [B + 1]
+  const SeqTab tab{prefix, lens, qs, qc, prefix_light};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs, hkv = p.num_kv_heads;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cap_tbl = p.max_blocks * BS, cap_grid = p.max_parts * p.part_tokens;
     const int cap = kPrefill || cap_tbl < cap_grid ? cap_tbl : cap_grid;
     const int tile_tok = p.tile_tok;
-    int sum = 0;
+    int sum = 0, sum_light = 0;
     for (int i = lo; i < hi; ++i) {
       int L = p.seq_lens[i];
       if (L < 0 || L > cap) {
@@ -365,24 +382,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         qs[i] = a;
         qc[i] = c;
         n = ceil_div(c, (kP2 ? 2 : 1) * tile_tok) * hkv;  // query tiles, or pairs of them
+        // light: a chunk of at most one query tile (a decode row, a short chunk)
+        const bool light = !kP2 && c <= tile_tok;
+        prefix_light[i + 1] = light ? n : 0;
+        sum_light += light ? n : 0;
+        if (light) n = 0;
       } else {
         n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
       }
       prefix[i + 1] = n;
       sum += n;
     }
-    int incl = sum;
+    // exclusive prefixes over the lanes' ranges (the light class only in prefill)
+    auto scan = [&](int *pre, int total) {
+      int incl = total;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      run += prefix[i + 1];
-      prefix[i + 1] = run;
-    }
-    if (lane == 0) prefix[0] = 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - total;
+      for (int i = lo; i < hi; ++i) {
+        run += pre[i + 1];
+        pre[i + 1] = run;
+      }
+      if (lane == 0) pre[0] = 0;
+    };
+    scan(prefix, sum);
+    if (kPrefill) scan(prefix_light, sum_light);
   }
   if (threadIdx.x == 32 * kKWarp) {
     for (int i = 0; i < kQBufs; ++i) {
@@ -432,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int I = prefix[B];
+  const int I = prefix[B] + (kPrefill ? prefix_light[B] : 0);
   const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + Lay::kSmemK), sV = smem_u32(smem + Lay::kSmemV);
   const uint32_t tS0 = tmem + Lay::kTmemS;  // S buffers after the two accumulators
   const uint32_t tP0 = tmem + Lay::kTmemP;  // P buffers: over the S buffers (prefill) or after them
