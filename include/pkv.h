@@ -326,6 +326,35 @@ int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pk
                             int32_t *d_status, void *stream);
 
 /*
+ * paged_attention_prefill_ex -- paged_attention_prefill with its keys split
+ * into partitions (split-K), for batches with fewer query tiles than the GPU
+ * has SMs (a short chunk behind a long context).
+ *
+ * The pages have no counterpart to the split; the result is the same
+ * attention (it changes only the fp32 summation order).  With partition_size
+ * > 0 (a multiple of 128 tokens), every query tile's keys are cut into
+ * partitions of partition_size keys, each computed by its own unit of work
+ * into the workspace as (running max, sum, unnormalised output), and a second
+ * kernel merges each row's partitions exactly (log-sum-exp).  max_seq_len
+ * bounds every seq_lens entry (a larger one sets PKV_STATUS_BAD_LEN and is
+ * clamped).  partition_size == 0 is paged_attention_prefill (no workspace).
+ *   workspace      device, 16-byte aligned, at least
+ *                  paged_attention_prefill_workspace_size(...) bytes
+ *                  (PKV_ERR_WORKSPACE otherwise); nothing in it needs clearing
+ * Everything else as paged_attention_prefill.
+ */
+size_t paged_attention_prefill_workspace_size(int total_q, int num_q_heads, int head_dim, int max_seq_len,
+                                              int partition_size);
+
+int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *seq_lens, const int32_t *q_start, int num_seqs,
+                               int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, float scale, int max_seq_len,
+                               int partition_size, pkv_bf16 *out, void *workspace,
+                               size_t workspace_bytes, int32_t *d_status, void *stream);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace and without allocating anything.
  *

@@ -52,6 +52,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "pkv.h"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -103,7 +104,7 @@ struct Layout {
   static constexpr int kStages = kPrefill ? 2 : 4;
   static constexpr int kQBufs = 2;
   static constexpr int kMaxSeqs = kPrefill ? 1024 : 2048;
-  static constexpr int kSeqInts = kPrefill ? 5 : 2;  // per-sequence ints after the item prefix
+  static constexpr int kSeqInts = kPrefill ? 4 : 2;  // per-sequence ints after the item prefix
   static constexpr int kSmemK = kQBufs * kQBytes;
   static constexpr int kSmemV = kSmemK + kStages * kKVBytes;
   static constexpr int kSmemStats = kSmemV + kStages * kKVBytes;  // float2 [2][128]: odd set's (max, sum)
@@ -118,7 +119,7 @@ struct Layout {
   static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
   static_assert(kTmemP + kPStride + kTK / 2 <= kTmemCols, "tensor memory");
   static constexpr size_t bytes(int num_seqs) {
-    return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 2) * 4;
+    return 1024 + kSmemSeq + (static_cast<size_t>(kSeqInts) * num_seqs + 1) * 4;
   }
 };
 static_assert(Layout<false, 128>::bytes(Layout<false, 128>::kMaxSeqs) <= 227 * 1024, "shared memory");
@@ -178,11 +179,10 @@ __device__ __forceinline__ int range_first(unsigned c, int total) {
 
 // Per-sequence values kept in shared memory.
 struct SeqTab {
-  const int *prefix;  // [B + 1] items before each sequence (prefill: the heavy class's items)
+  const int *prefix;  // [B + 1] items before each sequence
   const int *lens;    // [B] clamped lengths
   const int *qs;      // prefill: [B] first query row
   const int *qc;      // prefill: [B] chunk length (0 for a bad q_start entry)
-  const int *prefix_light;  // prefill: [B + 1] the light class's items before each sequence
 };
 
 // One work item: a query tile (prefill: a pair of query tiles 2 qt and
@@ -192,7 +192,14 @@ struct SeqTab {
 struct Item {
   int seq, head, qt, part, nparts, k_lo, k_hi;
   bool run_begin, run_end, has_b;
+  bool skip;  // prefill split over keys: a partition past this query tile's keys (no work, no output)
 };
+
+// Prefill split over keys (part_tokens > 0): partitions per query tile of a
+// sequence of L keys; 1 without the split.
+__device__ __forceinline__ int split_parts(const TcParams &p, int L) {
+  return p.part_tokens > 0 && L > 0 ? ceil_div(L, p.part_tokens) : 1;
+}
 
 // The items of this CTA in order (every role walks the same sequence).
 // kPairs: prefill items are pairs of query tiles.
@@ -213,31 +220,16 @@ struct Sched {
       step = 1;
     }
     if (it < end) {
-      locate(p, t);
+      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
       fill(p, t, true);
     }
-  }
-  // Prefill: item `it` of the whole order.  The heavy items (chunks of more
-  // than one query tile) and the light ones (decodes, short chunks) are merged
-  // in proportion, so that at any time some CTAs run compute-bound chunk tiles
-  // while the others stream the decodes' keys; within a class, items of one
-  // (sequence, KV head) stay together, longest first.
-  __device__ void locate(const TcParams &p, const SeqTab &t) {
-    if (!kPrefill) {
-      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
-      return;
-    }
-    const long long na = t.prefix[p.num_seqs], n = na + t.prefix_light[p.num_seqs];
-    const int a0 = static_cast<int>(it * na / n), a1 = static_cast<int>((it + 1ll) * na / n);
-    if (a1 > a0) w.seek(t.prefix, p.num_seqs, p.num_kv_heads, a0);
-    else w.seek(t.prefix_light, p.num_seqs, p.num_kv_heads, it - a0);
   }
   __device__ bool valid() const { return it < end; }
   __device__ void advance(const TcParams &p, const SeqTab &t) {
     it += step;
     if (it >= end) return;
     if (kPrefill) {
-      locate(p, t);
+      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
       fill(p, t, true);
     } else {
       const int s0 = w.seq, h0 = w.head;
@@ -253,15 +245,29 @@ struct Sched {
     if (kPrefill) {
       const int c = t.qc[w.seq];
       const int tile_tok = p.tile_tok;
-      x.qt = w.nparts - 1 - w.part;  // longest first
-      x.part = 0;
-      x.nparts = 1;
-      x.k_lo = 0;
+      // split over keys: every query tile of the sequence has ps partitions of
+      // part_tokens keys (the last tile's count); items past a tile's keys are empty
+      const int ps = split_parts(p, L);
+      x.qt = w.nparts / ps - 1 - w.part / ps;  // longest first
       const int span = kPairs ? 2 * tile_tok : tile_tok;  // query tokens per item
-      x.k_hi = min(L, max(0, L - c + min(c, span * (x.qt + 1))));  // keys the item's last row sees
+      const int k_hi = min(L, max(0, L - c + min(c, span * (x.qt + 1))));  // keys the tile's last row sees
+      x.skip = false;
+      if (ps == 1) {
+        x.part = 0;
+        x.nparts = 1;
+        x.k_lo = 0;
+        x.k_hi = k_hi;
+      } else {
+        x.part = w.part % ps;
+        x.nparts = max(1, ceil_div(k_hi, p.part_tokens));  // this tile's partitions
+        x.skip = x.part >= x.nparts;
+        x.k_lo = x.skip ? 0 : x.part * p.part_tokens;
+        x.k_hi = x.skip ? 0 : min(k_hi, x.k_lo + p.part_tokens);
+      }
       x.has_b = kPairs && (2 * x.qt + 1) * tile_tok < c;
       x.run_end = true;
     } else {
+      x.skip = false;
       x.qt = 0;
       x.has_b = false;
       x.part = w.part;
@@ -348,8 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *lens = prefix + p.num_seqs + 1;                          // [B]
   int *qs = lens + p.num_seqs;                                  // prefill: [B]
   int *qc = qs + p.num_seqs;                                    // prefill: [B]
-  int *prefix_light = qc + p.num_seqs;                          // prefill: [B + 1]
-  const SeqTab tab{prefix, lens, qs, qc, prefix_light};
+  const SeqTab tab{prefix, lens, qs, qc};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int B = p.num_seqs, hkv = p.num_kv_heads;
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -361,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per = (B + 31) / 32;
     const int lo = min(B, lane * per), hi = min(B, lo + per);
     const int cap_tbl = p.max_blocks * BS, cap_grid = p.max_parts * p.part_tokens;
-    const int cap = kPrefill || cap_tbl < cap_grid ? cap_tbl : cap_grid;
+    // prefill without the key split has no partition grid
+    const int cap = (kPrefill && p.part_tokens == 0) || cap_tbl < cap_grid ? cap_tbl : cap_grid;
     const int tile_tok = p.tile_tok;
-    int sum = 0, sum_light = 0;
+    int sum = 0;
     for (int i = lo; i < hi; ++i) {
       int L = p.seq_lens[i];
       if (L < 0 || L > cap) {
@@ -381,35 +387,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         qs[i] = a;
         qc[i] = c;
-        n = ceil_div(c, (kP2 ? 2 : 1) * tile_tok) * hkv;  // query tiles, or pairs of them
-        // light: a chunk of at most one query tile (a decode row, a short chunk)
-        const bool light = !kP2 && c <= tile_tok;
-        prefix_light[i + 1] = light ? n : 0;
-        sum_light += light ? n : 0;
-        if (light) n = 0;
+        n = ceil_div(c, (kP2 ? 2 : 1) * tile_tok) * split_parts(p, L) * hkv;  // query tiles, pairs, or partitions
       } else {
         n = (L > 0 ? ceil_div(L, p.part_tokens) : 1) * hkv;
       }
       prefix[i + 1] = n;
       sum += n;
     }
-    // exclusive prefixes over the lanes' ranges (the light class only in prefill)
-    auto scan = [&](int *pre, int total) {
-      int incl = total;
+    int incl = sum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int run = incl - total;
-      for (int i = lo; i < hi; ++i) {
-        run += pre[i + 1];
-        pre[i + 1] = run;
-      }
-      if (lane == 0) pre[0] = 0;
-    };
-    scan(prefix, sum);
-    if (kPrefill) scan(prefix_light, sum_light);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      run += prefix[i + 1];
+      prefix[i + 1] = run;
+    }
+    if (lane == 0) prefix[0] = 0;
   }
   if (threadIdx.x == 32 * kKWarp) {
     for (int i = 0; i < kQBufs; ++i) {
@@ -459,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int I = prefix[B] + (kPrefill ? prefix_light[B] : 0);
+  const int I = prefix[B];
   const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + Lay::kSmemK), sV = smem_u32(smem + Lay::kSmemV);
   const uint32_t tS0 = tmem + Lay::kTmemS;  // S buffers after the two accumulators
   const uint32_t tP0 = tmem + Lay::kTmemP;  // P buffers: over the S buffers (prefill) or after them
@@ -768,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int L = lens[x.seq];
         const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
         if (kP2 && set == 1 && !x.has_b) continue;  // the pair has no second query tile
+        if (x.skip) continue;                        // an empty partition: nothing to compute or store
         if (x.run_begin) {
           m = -INFINITY;
           l = 0.f;
@@ -1059,7 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before();
           mbar_arrive(bar(B_O_FREE));
         }
-        if (!kPrefill && nparts > 1 && row_valid) {
+        if (nparts > 1 && row_valid) {
           p.ws_ml[orow * p.max_parts + run_first_part] = make_float2(M, lt);
           for (int q = run_first_part + 1; q <= x.part; ++q)  // merged into the run's first slot
             p.ws_ml[orow * p.max_parts + q] = make_float2(-INFINITY, 0.f);
@@ -1077,6 +1074,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }
+}
+
+// Prefill split over keys: one warp per (query row, query head) merges the
+// partitions of the row's query tile.  The row's sequence is found by a binary
+// search of q_start (copied to shared memory); rows of no valid sequence, and
+// rows whose tile has one partition (written directly), are left alone.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const TcParams p, int block_size) {
+  extern __shared__ int sq[];  // q_start [B + 1]
+  grid_launch_dependents();
+  grid_dependency_wait();  // the partials come from the grid launched just before
+  for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) sq[i] = p.q_start[i];
+  __syncthreads();
+  const long long wg = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= static_cast<long long>(p.total_q) * p.num_q_heads) return;
+  const int row = static_cast<int>(wg / p.num_q_heads);
+  int lo = 0, hi = p.num_seqs;  // the last sequence whose first row is at most `row`
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sq[mid] <= row) lo = mid; else hi = mid;
+  }
+  const int a = sq[lo], b = sq[lo + 1];
+  if (a < 0 || b < a || b > p.total_q || row < a || row >= b) return;
+  const int cap = min(p.max_blocks * block_size, p.max_parts * p.part_tokens);  // as the main kernel clamps
+  int L = p.seq_lens[lo];
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int c = b - a, qt = (row - a) / p.tile_tok;
+  const int k_hi = min(L, max(0, L - c + min(c, p.tile_tok * (qt + 1))));
+  const int nparts = max(1, ceil_div(k_hi, p.part_tokens));
+  if (nparts <= 1) return;
+  merge_partials<D>(p.ws_ml + wg * p.max_parts, p.ws_o + wg * p.max_parts * D, nparts, p.out + wg * D, lane);
 }
 
 // ------------------------------------------------------------------ host
@@ -1175,12 +1204,35 @@ int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream) {
 
 }  // namespace pkv
 
-extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
-                                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
-                                       const int32_t *q_start, int num_seqs, int total_q, int num_q_heads,
-                                       int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                                       pkv_bf16 *out, int32_t *d_status, void *stream) {
-  using namespace pkv;
+namespace pkv {
+namespace {
+
+struct PrefillPlan {
+  int part_tokens = 0, max_parts = 1;
+  size_t ws_o_bytes = 0, ws_ml_bytes = 0;
+  size_t ws_bytes() const { return part_tokens > 0 ? ws_o_bytes + ws_ml_bytes : 0; }
+};
+
+bool make_prefill_plan(int total_q, int num_q_heads, int head_dim, int max_seq_len, int partition_size,
+                       PrefillPlan *plan) {
+  if (total_q < 0 || num_q_heads < 1 || head_dim < 1 || max_seq_len < 0 || partition_size < 0) return false;
+  if (partition_size == 0) return *plan = PrefillPlan{}, true;
+  if (partition_size % Layout<true, 128>::kTK != 0) return false;  // whole key tiles
+  const long long parts = max_seq_len > 0 ? (static_cast<long long>(max_seq_len) + partition_size - 1) / partition_size : 1;
+  if (parts > 65535) return false;
+  plan->part_tokens = partition_size;
+  plan->max_parts = static_cast<int>(parts);
+  const size_t rows = static_cast<size_t>(total_q) * num_q_heads;
+  plan->ws_o_bytes = (rows * plan->max_parts * head_dim * sizeof(float) + 255) & ~size_t(255);
+  plan->ws_ml_bytes = rows * plan->max_parts * sizeof(float2);
+  return true;
+}
+
+int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
+                  int max_blocks_per_seq, const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
+                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                  int max_seq_len, int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes,
+                  int32_t *d_status, void *stream) {
   if (num_seqs < 0 || total_q < 0 || max_blocks_per_seq < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -1189,6 +1241,8 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   if ((head_dim != 64 && head_dim != 128) || group > 16) return PKV_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > Layout<true, 128>::kMaxSeqs) return PKV_ERR_UNSUPPORTED;
+  PrefillPlan plan;
+  if (!make_prefill_plan(total_q, num_q_heads, head_dim, max_seq_len, partition_size, &plan)) return PKV_ERR_ARG;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start || !out) return PKV_ERR_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
@@ -1198,11 +1252,13 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   if (num_blocks == 0) return PKV_ERR_ARG;
   const long long rows = static_cast<long long>(num_blocks) * num_kv_heads * block_size;
   if (rows + block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
-  // the largest item count the kernel forms: every row its own query tile
-  if (static_cast<long long>(total_q) * num_kv_heads >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
-  if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
-
   const int tile_tok = kRows / group;
+  // the largest item count the kernel forms: every row its own query tile, split
+  if (static_cast<long long>(total_q) * num_kv_heads * plan.max_parts >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+  if (plan.ws_bytes() > 0 && (!workspace || workspace_bytes < plan.ws_bytes() || !aligned16(workspace)))
+    return PKV_ERR_WORKSPACE;
+
   const int box_rows = block_size < Layout<true, 128>::kTK ? block_size : Layout<true, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
   // q viewed as [total_q][Hq][128]: box = 64 columns x G heads x floor(128 / G)
@@ -1222,18 +1278,76 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;
   p.num_blocks = num_blocks;
-  p.part_tokens = 0;
-  p.max_parts = 1;
+  p.part_tokens = plan.part_tokens;
+  p.max_parts = plan.max_parts;
   p.oob_row = static_cast<int>(rows);
   p.total_q = total_q;
   p.group = group;
   p.tile_tok = tile_tok;
   p.scale_log2 = kernel_scale_log2(scale);
+  cudaStream_t st = as_stream(stream);
+  if (plan.part_tokens > 0) {
+    // split over keys: single query tiles (every partition item has both softmax
+    // sets), then the merge of each row's partitions
+    p.ws_o = static_cast<float *>(workspace);
+    p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.ws_o_bytes);
+    const int rc = launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st);
+    if (rc != PKV_OK) return rc;
+    const long long warps = static_cast<long long>(total_q) * num_q_heads;
+    const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
+    const size_t smem = (static_cast<size_t>(num_seqs) + 1) * sizeof(int);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, prefill_combine_kernel<128>, p, block_size)
+                                          : cudaLaunchKernelEx(&cfg, prefill_combine_kernel<64>, p, block_size);
+    if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
+    return PKV_OK;
+  }
   // Batches of long chunks run over pairs of query tiles, which share every
   // key and value tile (half the key / value traffic per product); batches
   // of mostly short chunks (decodes) split each query tile's keys between the
   // two softmax sets instead, so that both sets work on every item.
   if (static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs)
-    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
-  return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, as_stream(stream));
+    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st);
+  return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" size_t paged_attention_prefill_workspace_size(int total_q, int num_q_heads, int head_dim, int max_seq_len,
+                                                         int partition_size) {
+  pkv::PrefillPlan plan;
+  if (!pkv::make_prefill_plan(total_q, num_q_heads, head_dim, max_seq_len, partition_size, &plan)) return 0;
+  return plan.ws_bytes();
+}
+
+extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                                       const int32_t *q_start, int num_seqs, int total_q, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                                       pkv_bf16 *out, int32_t *d_status, void *stream) {
+  return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
+                            total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0, 0, out,
+                            nullptr, 0, d_status, stream);
+}
+
+extern "C" int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, int max_seq_len, int partition_size,
+                                          pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                                          void *stream) {
+  return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
+                            total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, max_seq_len,
+                            partition_size, out, workspace, workspace_bytes, d_status, stream);
 }

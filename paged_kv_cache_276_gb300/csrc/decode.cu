@@ -38,6 +38,7 @@
 #include "internal.h"
 #include "pkv.h"
 #include "attend.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -581,14 +582,10 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
 }
 
 // ---------------------------------------------- cross-partition combine
-// One warp per (sequence, query row): out = sum_p O_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
-// The partitions' (max, sum) pairs are read by the lanes in parallel and each
-// lane then issues every partition's slice of O at once, so the merge costs a
-// few memory round trips instead of two per partition.
+// One warp per (sequence, query row): the exact merge of its partitions.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
                                                       int rows) {
-  constexpr int PER = D / 32;
   grid_launch_dependents();
   grid_dependency_wait();  // the partials come from the grid launched just before
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -599,57 +596,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_
   const int part_tokens = p.part_blocks * block_size;
   const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
   if (nparts <= 1) return;
-  const float2 *ml = p.ws_ml + static_cast<size_t>(wg) * p.max_parts;
-  const float *o = p.ws_o + static_cast<size_t>(wg) * p.max_parts * D + lane * PER;
-  float M = -INFINITY;
-  for (int i = lane; i < nparts; i += 32) M = fmaxf(M, ml[i].x);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float den = 0.f, accv[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) accv[k] = 0.f;
-  for (int base = 0; base < nparts; base += 32) {
-    // lane i holds the weight of partition base + i (0 for an empty slot)
-    const int i = base + lane;
-    float f = 0.f;
-    if (i < nparts) {
-      const float2 v = ml[i];
-      f = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
-      den += v.y * f;
-    }
-    const int cnt = min(32, nparts - base);
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float w[8];
-      float x[8][PER];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {  // eight independent loads in flight
-        w[j] = __shfl_sync(0xffffffffu, f, (j0 + j) & 31);
-        const bool use = j0 + j < cnt && w[j] != 0.f;  // an empty slot's O is never read
-#pragma unroll
-        for (int k = 0; k < PER; ++k) x[j][k] = 0.f;
-        if (use) {
-          const float *src = o + static_cast<size_t>(base + j0 + j) * D;
-          if constexpr (PER == 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(src);
-            x[j][0] = t.x; x[j][1] = t.y; x[j][2] = t.z; x[j][3] = t.w;
-          } else {
-            const float2 t = *reinterpret_cast<const float2 *>(src);
-            x[j][0] = t.x; x[j][1] = t.y;
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int k = 0; k < PER; ++k) accv[k] += w[j] * x[j][k];
-    }
-  }
-#pragma unroll
-  for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  __nv_bfloat16 *dst = p.out + static_cast<size_t>(wg) * D + lane * PER;
-#pragma unroll
-  for (int k = 0; k < PER; ++k) dst[k] = __float2bfloat16_rn(accv[k] * inv);
+  merge_partials<D>(p.ws_ml + static_cast<size_t>(wg) * p.max_parts, p.ws_o + static_cast<size_t>(wg) * p.max_parts * D,
+                    nparts, p.out + static_cast<size_t>(wg) * D, lane);
 }
 
 // ------------------------------------------------------------------ host

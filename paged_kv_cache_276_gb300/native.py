@@ -85,6 +85,10 @@ SIGNATURES = {
                                               _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_float, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
                                               _c_ptr, _c_ptr]),
+    "paged_attention_prefill_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "paged_attention_prefill_ex": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
+                                            _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                            _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -356,6 +360,34 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_start
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
         _ptr(q_start), B, total_q, Hq, Hkv, d, bs, NB, float(scale), _ptr(out), _ptr(d_status),
         _stream(stream, dev)), "paged_attention_prefill")
+
+
+def paged_attention_prefill_workspace_size(total_q, num_q_heads, head_dim, max_seq_len, partition_size):
+    return int(lib().paged_attention_prefill_workspace_size(int(total_q), int(num_q_heads), int(head_dim),
+                                                            int(max_seq_len), int(partition_size)))
+
+
+def paged_attention_prefill_ex(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, max_seq_len,
+                               partition_size, workspace=None, d_status=None, stream=None):
+    """paged_attention_prefill with the keys split into partitions of
+    ``partition_size`` tokens (0: no split), merged through ``workspace``."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (q_start, "q_start", torch.int32),
+                     (out, "out", torch.bfloat16)):
+        _need(t, dt, n, dev)
+    total_q, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or seq_lens.shape != (B,) or q_start.shape != (B + 1,):
+        raise ValueError("shape mismatch")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().paged_attention_prefill_ex(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        _ptr(q_start), B, total_q, Hq, Hkv, d, bs, NB, float(scale), int(max_seq_len), int(partition_size),
+        _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_prefill_ex")
 
 
 def _swap_check(k_cache, v_cache, block_ids, host_k, host_v):

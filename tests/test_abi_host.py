@@ -493,3 +493,22 @@ def test_decode_items_rejects_bad_arguments_before_launch(native):
     assert call(k_new=fake) == native.PKV_ERR_ARG                             # a store needs k, v and slots
     assert call(d=96) == native.PKV_ERR_UNSUPPORTED
     assert call(Hq=7) == native.PKV_ERR_ARG
+
+
+def test_split_prefill_sizes_and_argument_checks(native):
+    f = native.paged_attention_prefill_workspace_size
+    assert f(128, 64, 128, 32768, 0) == 0                     # no split: no workspace
+    n = f(128, 64, 128, 32768, 4096)                          # 8 partitions per row
+    assert n >= 128 * 64 * 8 * (128 * 4 + 8)
+    assert f(128, 64, 128, 32768, 100) == 0                   # not whole 128-key tiles: invalid
+    lib = native.lib()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(part=4096, ws=None, wsb=0, maxlen=32768):
+        return lib.paged_attention_prefill_ex(fake, fake, fake, fake, 4, fake, fake, 1, 128, 64, 8, 128, 16, 8, 0.1,
+                                              maxlen, part, fake, ws, wsb, None, None)
+    assert call(part=100) == native.PKV_ERR_ARG
+    assert call(part=-128) == native.PKV_ERR_ARG
+    assert call() == native.PKV_ERR_WORKSPACE                  # the split needs its workspace
+    assert call(ws=fake, wsb=n - 1) == native.PKV_ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p((1 << 20) + 8), wsb=n) == native.PKV_ERR_WORKSPACE  # misaligned

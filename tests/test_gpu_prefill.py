@@ -372,3 +372,55 @@ def test_prefill_groups_that_do_not_divide_the_tile(d, bs, Hq, Hkv):
         ref = oracle_prefill(q, kc, vc, tables, L_, q_start, Hq, Hkv, bs, scale, d=d)
         assert_attention_close(out[:q.shape[0]], ref, f"prefill, group {G}, {len(L_)} sequences")
         assert (bits(out[q.shape[0]:]) == CANARY).all()  # rows past the batch untouched
+
+
+def run_prefill_split(q, kc, vc, tables, lens, q_start, scale, max_len, part, status=None):
+    dev = kc.device
+    out = torch.empty_like(q)
+    out.view(torch.int16).fill_(CANARY)
+    n = native.paged_attention_prefill_workspace_size(q.shape[0], q.shape[1], q.shape[2], max_len, part)
+    ws = torch.randint(0, 256, (max(n, 16),), dtype=torch.uint8, device=dev)  # stale bytes: nothing needs clearing
+    native.paged_attention_prefill_ex(q, kc, vc, torch.as_tensor(np.asarray(tables, dtype=np.int32), device=dev),
+                                      torch.as_tensor(np.asarray(lens, dtype=np.int32), device=dev),
+                                      torch.as_tensor(np.asarray(q_start, dtype=np.int32), device=dev), scale, out,
+                                      max_len, part, ws, status)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("d,bs,Hq,Hkv,part", [(128, 16, 64, 8, 1024), (128, 32, 32, 8, 256), (64, 16, 24, 8, 128),
+                                              (128, 128, 16, 16, 512)])
+def test_prefill_split_over_keys_matches_the_oracle(d, bs, Hq, Hkv, part):
+    """Split-K prefill: chunks behind long contexts, a decode row, a chunk whose
+    early tiles fit one partition while its last ones need several, an empty
+    chunk and a chunk shorter than a partition; the merged rows match the oracle
+    and the unsplit call."""
+    lens = [5000, 3000, 77, 2000, 300, 40]
+    chunks = [128, 1, 77, 0, 300, 33]
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=90 + Hq + part, d=d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_prefill_split(q, kc, vc, tables, lens, q_start, scale, max(lens), part, status=st)
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale, d=d)
+    assert_attention_close(out, ref, f"split prefill, partitions of {part}")
+    whole = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    assert torch.allclose(out.float(), whole.float(), atol=1e-2, rtol=1e-2)
+
+
+def test_prefill_split_of_a_short_chunk_behind_a_long_context():
+    """One 128-token chunk behind 32k cached tokens (64 query / 8 KV heads):
+    8 query tiles x 8 KV heads = 64 units of work unsplit; split into 2048-key
+    partitions it is 1024 units over every SM.  Sampled tiles match the oracle."""
+    L, c = 32768, 128
+    Hq, Hkv, bs, d = 64, 8, 16, 128
+    q, kc, vc, tables, q_start = prefill_case([L], [c], bs, Hq, Hkv, seed=97, d=d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    st = status_tensor()
+    out = run_prefill_split(q, kc, vc, tables, [L], q_start, scale, L, 2048, status=st)
+    assert st.item() == 0
+    for lo in (0, 64, 112):  # whole query tiles of 16 tokens
+        ref = OA.paged_attention(bits(q[lo:lo + 16])[None], bits(kc), bits(vc), tables,
+                                 np.array([L - c + lo + 16], dtype=np.int32), num_q_heads=Hq, num_kv_heads=Hkv,
+                                 head_dim=d, block_size=bs, scale=scale, q_len=16)
+        assert_attention_close(out[lo:lo + 16], ref[0], f"tile at row {lo}")
