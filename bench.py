@@ -649,6 +649,12 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
             continue
         try:
             case = PrefillCase(pw, device)
+            # a batch led by single-token decodes runs as one mixed step: the
+            # decodes over their work list beside the chunks on the tensor cores
+            mixed = 0 < case.num_decodes < case.B
+            if mixed:
+                case.prepare_mixed()
+            attend = case.attend_mixed if mixed else case.attend
             status = torch.zeros(1, dtype=torch.int32, device=device)
             pool = []
             for _ in range(4 * (warmup + steps)):  # created and recorded once, before the timed loop
@@ -662,12 +668,13 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
                     flush.fill_(float(i))
                     a0, a1 = pool.pop(), pool.pop()
                     a0.record(stream)
-                    case.step(status, stream)  # the chunk's pkv_write, then the attention
+                    case.write(status, stream)  # the chunk's pkv_write, then the attention
+                    attend(status, stream)
                     a1.record(stream)
                     flush.fill_(float(i) + 0.5)
                     b0, b1 = pool.pop(), pool.pop()
                     b0.record(stream)
-                    case.attend(status, stream)  # the attention call alone
+                    attend(status, stream)  # the attention call alone
                     b1.record(stream)
                     if i >= warmup:
                         step_ev.append((a0, a1))
@@ -680,11 +687,22 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
             sm, am = sum(step_ms) / steps, sum(att_ms) / steps
             fl = case.flops()
             tf = fl / (am * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(tf / peak, 4), "peak_kind": peak_kind,
-                    "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag)}
-            res[tag] = {"ms": round(am, 5), "roofline": roof, "kv_gbs": round(case.kv_bytes() / (am * 1e-3) / 1e9, 1),
+            kv_gbs = case.kv_bytes() / (am * 1e-3) / 1e9
+            hbm_peak, hbm_kind = measured_hbm_peak()
+            if case.kv_bytes() / (hbm_peak * 1e9) > fl / (peak * 1e12):
+                # more time in moving K/V than in the products at the peaks: bandwidth-bound
+                roof = {"bound": "hbm", "achieved": round(kv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                        "frac": round(kv_gbs / hbm_peak, 4), "peak_kind": f"{hbm_kind} hbm_gbs",
+                        "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag),
+                        "tflops": round(tf, 1)}
+            else:
+                roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                        "frac": round(tf / peak, 4), "peak_kind": peak_kind,
+                        "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag)}
+            res[tag] = {"ms": round(am, 5), "roofline": roof, "kv_gbs": round(kv_gbs, 1),
                         "rows_s": round(case.total_q / (sm * 1e-3), 1), "step_ms": round(sm, 5)}
+            if mixed:
+                res[tag]["call"] = f"paged_attention_mixed ({case.mixed_nd} decodes, chunks on {case.mixed_ctas} CTAs)"
             if not compact:
                 res[tag].update(
                     workload=f"{pw.name}: {case.B} seqs, (L, chunk) = "

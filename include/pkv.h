@@ -355,6 +355,44 @@ int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const
                                size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
+ * paged_attention_mixed -- one continuous-batching step: single-token decodes
+ * and prompt chunks in one call, the decodes streamed by the decode kernel
+ * while the chunks run on the tensor cores.
+ *
+ * Pages: the scheduler runs chunks of long prompts in the same step as the
+ * decodes of other requests; the prompt side is compute-heavy, the decode side
+ * memory-bound (x321.org "The serving bottleneck is not just FLOPs", section
+ * "Continuous batching is the other half of the story").  The result is that
+ * of paged_attention_prefill over the whole batch.
+ *   The first num_decodes sequences are single-token decodes whose query rows
+ *   are rows 0 .. num_decodes-1 of q (q_start[i] = i for i <= num_decodes);
+ *   sequences num_decodes .. num_seqs-1 are chunks (any length, rows from
+ *   q_start[num_decodes] on).
+ *   decode_items  device, the pkv_decode_items list of the decodes' lengths
+ *                 seq_lens[0 .. num_decodes-1] and tables, for
+ *                 decode_partition_size; decode_grid as grid_items of
+ *                 paged_attention_decode_items
+ *   max_decode_len, decode_partition_size, workspace: as max_seq_len,
+ *                 partition_size and workspace of paged_attention_decode for
+ *                 the num_decodes decodes (paged_attention_workspace_size)
+ *   prefill_ctas  the chunks' persistent grid: at most this many CTAs, one per
+ *                 SM (0: every SM); the decodes' CTAs take the other SMs from
+ *                 the start and every SM the chunks free later.  Size it to the
+ *                 chunks' share of the step's work.
+ * Everything else as paged_attention_prefill.  Rows of decodes and chunks must
+ * not overlap.  Where the decodes' bound reaches the tensor-core route
+ * (max_decode_len >= 16384) the two parts run one after the other.
+ */
+int paged_attention_mixed(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                          const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                          const int32_t *q_start, int num_seqs, int total_q, int num_decodes,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, float scale, int max_decode_len, int decode_partition_size,
+                          const int32_t *decode_items, int decode_grid, int prefill_ctas,
+                          pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                          void *stream);
+
+/*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a
  * caller-provided workspace and without allocating anything.
  *

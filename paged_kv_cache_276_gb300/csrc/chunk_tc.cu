@@ -359,8 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int B = p.num_seqs, hkv = p.num_kv_heads;
   auto bar = [&](int i) { return smem_u32(bars + i); };
 
-  grid_launch_dependents();  // the merge grid may become resident; it waits for our results
+  // Wait for the kernel before this one, then let the grid queued behind this
+  // one become resident (a merge grid still waits for our results).  In this
+  // order a dependent grid that reads nothing of ours, such as the decode rows
+  // of a mixed step, can skip its own wait: our inputs, which are its inputs
+  // too, are complete once every CTA of this grid has passed this point.
   grid_dependency_wait();
+  grid_launch_dependents();
 
   if (warp == 0) {  // items per sequence -> exclusive prefix
     const int per = (B + 31) / 32;
@@ -1123,7 +1128,7 @@ KernelFn pick_kernel(int block_size) {
 
 template <bool kPrefill, int D, bool kPairs>
 int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
-                int block_size, cudaStream_t stream) {
+                int block_size, cudaStream_t stream, int max_ctas) {
   using Lay = Layout<kPrefill, D>;
   const KernelFn kernel = pick_kernel<kPrefill, D, kPairs>(block_size);
   cudaError_t e;
@@ -1131,7 +1136,8 @@ int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMa
                                 static_cast<int>(Lay::bytes(Lay::kMaxSeqs)))) != cudaSuccess)
     return set_cuda_error(e), PKV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
+  // one persistent CTA per SM, or fewer when the caller leaves SMs to a concurrent grid
+  cfg.gridDim = dim3(max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms());
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Lay::bytes(p.num_seqs);
   cfg.stream = stream;
@@ -1147,9 +1153,9 @@ int launch_tc_d(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMa
 
 template <bool kPrefill, bool kPairs>
 int launch_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv, const TcParams &p,
-              int block_size, int head_dim, cudaStream_t stream) {
-  return head_dim == 64 ? launch_tc_d<kPrefill, 64, kPairs>(tmq, tmk, tmv, p, block_size, stream)
-                        : launch_tc_d<kPrefill, 128, kPairs>(tmq, tmk, tmv, p, block_size, stream);
+              int block_size, int head_dim, cudaStream_t stream, int max_ctas = 0) {
+  return head_dim == 64 ? launch_tc_d<kPrefill, 64, kPairs>(tmq, tmk, tmv, p, block_size, stream, max_ctas)
+                        : launch_tc_d<kPrefill, 128, kPairs>(tmq, tmk, tmv, p, block_size, stream, max_ctas);
 }
 
 // The kernels compare raw scores before scaling them; a zero scale would turn
@@ -1228,11 +1234,13 @@ bool make_prefill_plan(int total_q, int num_q_heads, int head_dim, int max_seq_l
   return true;
 }
 
+}  // namespace
+
 int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                   int max_seq_len, int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes,
-                  int32_t *d_status, void *stream) {
+                  int32_t *d_status, void *stream, int max_ctas) {
   if (num_seqs < 0 || total_q < 0 || max_blocks_per_seq < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -1291,7 +1299,7 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
     // sets), then the merge of each row's partitions
     p.ws_o = static_cast<float *>(workspace);
     p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.ws_o_bytes);
-    const int rc = launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st);
+    const int rc = launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
     if (rc != PKV_OK) return rc;
     const long long warps = static_cast<long long>(total_q) * num_q_heads;
     const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
@@ -1316,11 +1324,10 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
   // of mostly short chunks (decodes) split each query tile's keys between the
   // two softmax sets instead, so that both sets work on every item.
   if (static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs)
-    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st);
-  return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st);
+    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
+  return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
 }
 
-}  // namespace
 }  // namespace pkv
 
 extern "C" size_t paged_attention_prefill_workspace_size(int total_q, int num_q_heads, int head_dim, int max_seq_len,
@@ -1337,7 +1344,7 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
                                        pkv_bf16 *out, int32_t *d_status, void *stream) {
   return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
                             total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0, 0, out,
-                            nullptr, 0, d_status, stream);
+                            nullptr, 0, d_status, stream, 0);
 }
 
 extern "C" int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
@@ -1349,5 +1356,5 @@ extern "C" int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_c
                                           void *stream) {
   return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
                             total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, max_seq_len,
-                            partition_size, out, workspace, workspace_bytes, d_status, stream);
+                            partition_size, out, workspace, workspace_bytes, d_status, stream, 0);
 }

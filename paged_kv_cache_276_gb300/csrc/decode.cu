@@ -80,6 +80,10 @@ struct Params {
   // CTA, {sequence, KV head | partition << 16, length, first physical block}
   const int4 *items;
   int num_seqs;
+  // launched right behind a grid whose results this one does not read (the
+  // chunk kernel of a mixed step), which waited for our inputs before it let
+  // this grid start: no wait here, so the two grids run side by side
+  int skip_dependency_wait;
 };
 
 // A block is staged as one or more "units" of consecutive token rows: the
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   // Let the merge grid queued behind this one become resident now; it still
   // waits for this whole grid's results before it reads anything.
   grid_launch_dependents();
-  grid_dependency_wait();  // inputs may come from the kernel launched just before
+  if (!p.skip_dependency_wait) grid_dependency_wait();  // inputs may come from the kernel launched just before
   int part, h, seq, L, window0, b0 = -1;
   if (p.items) {
     // a host-built work list: one 16-byte load names this CTA's partition, its
@@ -762,7 +766,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
                  void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items = nullptr,
-                 int grid_items = 0);
+                 int grid_items = 0, bool skip_dependency_wait = false);
 
 }  // namespace pkv
 
@@ -894,6 +898,38 @@ int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                            store ? &nt : nullptr, items, grid_items);
 }
 
+// One continuous-batching step (see pkv.h): the chunks on the tensor cores with
+// a capped grid, the decode rows over their work list right behind it.
+int paged_attention_mixed(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                          const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+                          const int32_t *q_start, int num_seqs, int total_q, int num_decodes, int num_q_heads,
+                          int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                          int max_decode_len, int decode_partition_size, const int32_t *decode_items,
+                          int decode_grid, int prefill_ctas, pkv_bf16 *out, void *workspace,
+                          size_t workspace_bytes, int32_t *d_status, void *stream) {
+  if (num_decodes < 0 || num_decodes > num_seqs || num_decodes > total_q || prefill_ctas < 0 || max_blocks_per_seq < 0)
+    return PKV_ERR_ARG;
+  const int chunks = num_seqs - num_decodes;
+  if (chunks > 0) {
+    // the chunk sequences: rows q_start[num_decodes] ...; the decode rows are not theirs
+    const int rc = pkv::prefill_entry(q, k_cache, v_cache,
+                                      block_tables ? block_tables + static_cast<size_t>(num_decodes) * max_blocks_per_seq
+                                                   : nullptr,
+                                      max_blocks_per_seq, seq_lens ? seq_lens + num_decodes : nullptr,
+                                      q_start ? q_start + num_decodes : nullptr, chunks, total_q, num_q_heads,
+                                      num_kv_heads, head_dim, block_size, num_blocks, scale, 0, 0, out, nullptr, 0,
+                                      d_status, stream, num_decodes > 0 ? prefill_ctas : 0);
+    if (rc != PKV_OK) return rc;
+  }
+  if (num_decodes == 0) return PKV_OK;
+  if (!decode_items || decode_grid < 1 || (reinterpret_cast<uintptr_t>(decode_items) & 15u)) return PKV_ERR_ARG;
+  // rows 0 .. num_decodes-1 of q and out are [num_decodes][1][Hq][d]
+  return pkv::decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_decodes,
+                           max_decode_len, 1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                           decode_partition_size, out, workspace, workspace_bytes, d_status, stream, nullptr, nullptr,
+                           decode_items, decode_grid, chunks > 0);
+}
+
 }  // extern "C"
 
 namespace pkv {
@@ -940,7 +976,8 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs, int max_seq_len, int q_len,
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                 void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items, int grid_items) {
+                 void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items, int grid_items,
+                 bool skip_dependency_wait) {
   cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   Plan plan;
   const int checked = decode_check(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -1036,6 +1073,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   p.scale_log2 = scale * kLog2e;
   p.num_seqs = num_seqs;
   if (items) p.items = reinterpret_cast<const int4 *>(items);  // q_len == 1, grid_items >= 1 (entry checks)
+  p.skip_dependency_wait = skip_dependency_wait ? 1 : 0;
   if (nt) {
     p.k_new = static_cast<const uint4 *>(nt->k);
     p.v_new = static_cast<const uint4 *>(nt->v);

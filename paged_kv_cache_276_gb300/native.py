@@ -89,6 +89,9 @@ SIGNATURES = {
     "paged_attention_prefill_ex": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                                             _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
+    "paged_attention_mixed": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                       _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -388,6 +391,35 @@ def paged_attention_prefill_ex(q, k_cache, v_cache, block_tables, seq_lens, q_st
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
         _ptr(q_start), B, total_q, Hq, Hkv, d, bs, NB, float(scale), int(max_seq_len), int(partition_size),
         _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_prefill_ex")
+
+
+def paged_attention_mixed(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, num_decodes,
+                          decode_items, max_decode_len, decode_partition_size=0, workspace=None, prefill_ctas=0,
+                          decode_grid=None, d_status=None, stream=None):
+    """One step of decodes (the first ``num_decodes`` sequences, query rows
+    0..num_decodes-1) and prompt chunks (the rest), as paged_attention_prefill
+    over the whole batch; ``decode_items`` (device) from pkv_decode_items over the
+    decodes' lengths and tables."""
+    dev = k_cache.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (seq_lens, "seq_lens", torch.int32), (q_start, "q_start", torch.int32),
+                     (out, "out", torch.bfloat16), (decode_items, "decode_items", torch.int32)):
+        _need(t, dt, n, dev)
+    total_q, Hq, d = q.shape
+    NB, Hkv, bs, d2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if d2 != d or out.shape != q.shape or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or seq_lens.shape != (B,) or q_start.shape != (B + 1,) or decode_items.dim() != 2 \
+            or decode_items.shape[1] != 4:
+        raise ValueError("shape mismatch")
+    grid = decode_items.shape[0] - 1 if decode_grid is None else int(decode_grid)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().paged_attention_mixed(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        _ptr(q_start), B, total_q, int(num_decodes), Hq, Hkv, d, bs, NB, float(scale), int(max_decode_len),
+        int(decode_partition_size), _ptr(decode_items), grid, int(prefill_ctas), _ptr(out), _ptr(workspace),
+        ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_mixed")
 
 
 def _swap_check(k_cache, v_cache, block_ids, host_k, host_v):

@@ -231,6 +231,24 @@ def causal_visible_keys(lens, chunks) -> int:
     return total
 
 
+# Rates of the two halves of a mixed step, measured alone on one GB300 (whole
+# GPU): chunked prefill on the tensor cores and the decode kernel's streaming.
+PREFILL_FLOPS_PER_S = 1.25e15
+DECODE_BYTES_PER_S = 5.0e12
+
+
+def mixed_prefill_ctas(case, sms: int = 152) -> int:
+    """SMs for the chunks of a mixed step: their share of the step's time when
+    each half runs alone at its measured rate (at least 8, at most sms - 8)."""
+    nd = case.num_decodes
+    flops_chunks = 4 * case.d * case.Hq * causal_visible_keys(case.lens[nd:], case.chunks[nd:])
+    bytes_dec = int(case.lens[:nd].astype(np.int64).sum()) * 2 * case.Hkv * case.d * 2
+    tc, td = flops_chunks / PREFILL_FLOPS_PER_S, bytes_dec / DECODE_BYTES_PER_S
+    if tc + td <= 0:
+        return 0
+    return int(min(sms - 8, max(8, round(sms * tc / (tc + td)))))
+
+
 class PrefillCase:
     """One chunked-prefill batch resident on the device.
 
@@ -275,8 +293,40 @@ class PrefillCase:
         native.paged_attention_prefill(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
                                        self.d_q_start, self.scale, self.out, d_status, stream)
 
-    def step(self, d_status=None, stream=None):
+    # A batch whose leading sequences are single-token decodes (rows 0..nd-1)
+    # can run as one mixed step: the decodes over their work list beside the chunks.
+    @property
+    def num_decodes(self) -> int:
+        nd = 0
+        while nd < self.B and int(self.chunks[nd]) == 1 and int(self.q_start[nd]) == nd:
+            nd += 1
+        return nd
+
+    def prepare_mixed(self, prefill_ctas=None, partition_size=0):
+        """Work list and workspace of the leading decodes; the chunks' grid cap
+        (default: mixed_prefill_ctas)."""
+        nd = self.num_decodes
+        self.mixed_nd = nd
+        self.mixed_max_len = int(self.lens[:nd].max()) if nd else 0
+        self.mixed_part = partition_size
+        self.mixed_items = torch.as_tensor(native.pkv_decode_items(self.lens[:nd], self.tables[:nd], self.Hkv,
+                                                                   self.bs, partition_size), device=self.device)
+        n = native.paged_attention_workspace_size(nd, 1, self.Hq, self.d, self.mixed_max_len, partition_size)
+        self.mixed_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+        self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
+
+    def attend_mixed(self, d_status=None, stream=None):
+        native.paged_attention_mixed(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens, self.d_q_start,
+                                     self.scale, self.out, self.mixed_nd, self.mixed_items, self.mixed_max_len,
+                                     self.mixed_part, self.mixed_ws, self.mixed_ctas, d_status=d_status,
+                                     stream=stream)
+
+    def write(self, d_status=None, stream=None):
+        """The chunk tokens' keys and values into their slots."""
         native.pkv_write(self.chunk_k, self.chunk_v, self.slots, self.k_cache, self.v_cache, d_status, stream)
+
+    def step(self, d_status=None, stream=None):
+        self.write(d_status, stream)
         self.attend(d_status, stream)
 
     def flops(self) -> int:

@@ -243,8 +243,9 @@ def test_mixed_step_of_decodes_and_a_prefill_chunk():
     assert torch.allclose(dec[:, 0].float(), out[:n_dec].float(), atol=1e-2, rtol=1e-2)
 
 
-@pytest.mark.parametrize("tag", ["prefill_long_context", "prefill_prompts", "prefill_mixed"])
-def test_prefill_workloads_every_sequence(tag):
+@pytest.mark.parametrize("tag,mixed", [("prefill_long_context", False), ("prefill_prompts", False),
+                                       ("prefill_mixed", False), ("prefill_mixed", True)])
+def test_prefill_workloads_every_sequence(tag, mixed):
     """The benchmark's prefill workloads at full size, in the benchmark's launch
     configuration.  Every sequence is compared with the oracle on whole query
     tiles (128 / G tokens x the G heads of each KV head, the unit the kernel
@@ -253,7 +254,12 @@ def test_prefill_workloads_every_sequence(tag):
     from paged_kv_cache_276_gb300.workloads import PrefillCase
     case = PrefillCase(inputs.PREFILL_WORKLOADS[tag], "cuda")
     st = status_tensor()
-    case.attend(st)
+    if mixed:  # the benchmark's launch: decodes over their work list beside the chunks
+        case.prepare_mixed()
+        assert case.mixed_nd == 256 and 8 <= case.mixed_ctas <= 144
+        case.attend_mixed(st)
+    else:
+        case.attend(st)
     torch.cuda.synchronize()
     assert st.item() == 0
     kb, vb = bits(case.k_cache), bits(case.v_cache)
@@ -424,3 +430,36 @@ def test_prefill_split_of_a_short_chunk_behind_a_long_context():
                                  np.array([L - c + lo + 16], dtype=np.int32), num_q_heads=Hq, num_kv_heads=Hkv,
                                  head_dim=d, block_size=bs, scale=scale, q_len=16)
         assert_attention_close(out[lo:lo + 16], ref[0], f"tile at row {lo}")
+
+
+@pytest.mark.parametrize("ctas", [0, 24, 100])
+def test_mixed_step_entry_matches_the_oracle(ctas):
+    """paged_attention_mixed: 40 single-token decodes (rows 0..39, over their
+    work list) beside two prompt chunks whose grid is capped at `ctas` CTAs
+    (0: every SM).  The result is that of paged_attention_prefill over the
+    whole batch, and matches the oracle."""
+    rng = np.random.default_rng(23)
+    n_dec = 40
+    lens = [int(x) for x in rng.integers(1, 3000, size=n_dec)] + [2600, 900]
+    chunks = [1] * n_dec + [512, 300]
+    Hq, Hkv, bs, d = 32, 8, 16, 128
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=23)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    dev = kc.device
+    items = torch.as_tensor(native.pkv_decode_items(np.asarray(lens[:n_dec], dtype=np.int32), tables[:n_dec], Hkv, bs,
+                                                    512), device=dev)
+    n = native.paged_attention_workspace_size(n_dec, 1, Hq, d, max(lens[:n_dec]), 512)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    out.view(torch.int16).fill_(CANARY)
+    st = status_tensor()
+    native.paged_attention_mixed(q, kc, vc, torch.as_tensor(np.asarray(tables, dtype=np.int32), device=dev),
+                                 torch.as_tensor(np.asarray(lens, dtype=np.int32), device=dev),
+                                 torch.as_tensor(q_start, device=dev), scale, out, n_dec, items, max(lens[:n_dec]),
+                                 512, ws, ctas, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(out, ref, f"mixed step, chunks on {ctas or 'all'} CTAs")
+    whole = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    assert torch.allclose(out.float(), whole.float(), atol=1e-2, rtol=1e-2)
