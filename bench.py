@@ -262,7 +262,7 @@ class Runner:
                         native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
                                                             sess.v_caches[l], p.tables, p.lens, p.max_len,
                                                             sess.scale, out, p.items, workspace=ws,
-                                                            partition_size=sess.partition_size, d_status=status,
+                                                            partition_size=p.partition, d_status=status,
                                                             stream=stream)
                     else:
                         native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
@@ -272,7 +272,7 @@ class Runner:
                                                       stream)
                     d1.record(stream)
                     dec.append((d0, d1))
-                    nparts = math.ceil(p.max_len / (sess.partition_size or DEFAULT_PARTITION)) if p.max_len else 1
+                    nparts = math.ceil(p.max_len / (p.partition or DEFAULT_PARTITION)) if p.max_len else 1
                     # (write,) decode, cross-partition combine
                     launches += (i >= warmup) * ((1 if fused else 2) + (nparts > 1))
                 s1.record(stream)
@@ -298,7 +298,7 @@ class Runner:
                         native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
                                                             sess.v_caches[l], p.tables, p.lens, p.max_len,
                                                             sess.scale, out, p.items, workspace=ws,
-                                                            partition_size=sess.partition_size, d_status=status,
+                                                            partition_size=p.partition, d_status=status,
                                                             stream=stream, main_done_event=dm)
                     else:
                         native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)

@@ -234,8 +234,8 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
  * The pages have no counterpart to this call; it moves the decode's schedule
  * to the host, which knows every length when it builds the step (the
  * allocator's append and table fill).  Each sequence's keys are split into
- * partitions of partition_size tokens (0: 768) as paged_attention_decode
- * splits them, and every (partition, KV head) becomes one item:
+ * partitions of partition_size tokens as paged_attention_decode splits them,
+ * and every (partition, KV head) becomes one item:
  *   {sequence, KV head | partition << 16, length, physical block of the
  *    partition's first logical block (-1 if block_tables is NULL or the
  *    partition is empty)}
@@ -243,26 +243,34 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
  * and head order), so the CTAs that start first carry the most keys and the
  * shortest partitions fill the end of the grid.  A sequence of length 0 gets
  * one empty item per KV head (its output rows are zeros).
+ * partition_size 0 lets the call choose among 768, 1024, 1536 and 2048 tokens
+ * (those that are multiples of block_size) the one a schedule model of the
+ * decode kernel on a GB300 predicts fastest for these lengths: more, shorter
+ * partitions balance the grid's end, fewer longer ones save each CTA's start.
+ * A workspace sized for partition 768 (paged_attention_workspace_size with
+ * partition_size 0) fits every choice.
  *   seq_lens      host, [num_seqs] int32, each in [0, max_blocks_per_seq *
  *                 block_size] (else PKV_ERR_RANGE)
  *   block_tables  host, [num_seqs][max_blocks_per_seq] int32, or NULL
- *   items_out     host, [1 + max_items][4] int32: row 0 = {count, 0, 0, 0},
- *                 rows 1..count the items
+ *   items_out     host, [1 + max_items][4] int32: row 0 = {count, partition
+ *                 size used, 0, 0}, rows 1..count the items.  Pass row 0's
+ *                 partition size to paged_attention_decode_items.
  * *num_items receives the count (also when it exceeds max_items, which
- * returns PKV_ERR_RANGE and writes no item).  partition_size must be a
- * multiple of block_size (PKV_ERR_ARG).
+ * returns PKV_ERR_RANGE and writes no item).  A partition_size that is not a
+ * multiple of block_size returns PKV_ERR_ARG.
  */
 int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int max_blocks_per_seq,
-                     int num_seqs, int num_kv_heads, int block_size, int partition_size,
-                     int32_t *items_out, int max_items, int *num_items);
+                     int num_seqs, int num_kv_heads, int head_dim, int block_size,
+                     int partition_size, int32_t *items_out, int max_items, int *num_items);
 
 /*
  * paged_attention_decode_items -- the single-token decode over a work list:
  * paged_attention_decode_write (or, with k_new, v_new and slot_mapping all
  * NULL, paged_attention_decode with q_len = 1), one CTA per item.
  *   items       device, 16-byte aligned, [1 + grid_items][4] int32: the rows
- *               pkv_decode_items wrote for these seq_lens, block_tables and
- *               partition_size (row 0 holds the count)
+ *               pkv_decode_items wrote for these seq_lens and block_tables
+ *               (row 0 holds the count); partition_size must be the size the
+ *               list was built for (row 0's second entry)
  *   grid_items  CTAs to launch, >= the count in row 0 (CTAs past the count do
  *               nothing), so a CUDA graph can be captured for a bound
  * Every other argument and the result are those of paged_attention_decode_write.

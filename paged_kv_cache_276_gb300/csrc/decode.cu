@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <functional>
 #include <cstdint>
 #include <mutex>
 #include <utility>
@@ -818,22 +819,91 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                            out, workspace, workspace_bytes, d_status, stream, main_done_event, &nt);
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+// Predicted time of a decode work list with partitions of `part` tokens, from a
+// model of one GB300 running the decode kernel: 152 SMs x 3 resident CTAs, the
+// CTAs that stream at once share ~6.45 TB/s of HBM, one CTA alone streams at
+// most ~28 GB/s, and a CTA spends ~2.4 us before its first tile lands.  Items
+// go to the CTA slots longest first (as launched); every streaming CTA
+// progresses at the same rate, so the slots' finishing order in bytes gives
+// the number of CTAs streaming at each point and the time is the integral of
+// bytes over rate.  Only the comparison between partition sizes is used.
+double predict_list_time(const int32_t *lens, int num_seqs, int num_kv_heads, int head_dim, int part,
+                         std::vector<double> &rest, std::vector<double> &slot) {
+  constexpr int kSlots = 456;
+  constexpr double kBw = 6.45e3;  // bytes per ns, every streaming CTA together
+  constexpr double kRmax = 28.0;  // bytes per ns, one CTA
+  constexpr double kStartNs = 2400.0;
+  const double per_tok = 4.0 * head_dim, start = kStartNs * kBw / kSlots;
+  // Whole partitions all cost the same and come first (the longest), so they
+  // go round the slots; then the sequences' last, shorter partitions (and the
+  // empty sequences), longest first, each to the least loaded slot.
+  long long full = 0;
+  rest.clear();
+  for (int i = 0; i < num_seqs; ++i) {
+    const int L = lens[i];
+    full += L / part;
+    if (L % part != 0 || L == 0) rest.push_back((L % part) * per_tok + start);
+  }
+  const long long nfull = full * num_kv_heads;
+  const double cfull = part * per_tok + start;
+  slot.assign(kSlots, static_cast<double>(nfull / kSlots) * cfull);
+  for (long long i = 0; i < nfull % kSlots; ++i) slot[i] += cfull;
+  std::make_heap(slot.begin(), slot.end(), std::greater<double>());
+  std::sort(rest.begin(), rest.end(), std::greater<double>());
+  for (double c : rest)
+    for (int h = 0; h < num_kv_heads; ++h) {
+      std::pop_heap(slot.begin(), slot.end(), std::greater<double>());
+      slot.back() += c;
+      std::push_heap(slot.begin(), slot.end(), std::greater<double>());
+    }
+  std::sort(slot.begin(), slot.end());
+  double t = 0.0, u = 0.0;
+  for (int i = 0; i < kSlots; ++i) {
+    const int busy = kSlots - i;
+    t += (slot[i] - u) / std::min(kRmax, kBw / busy);
+    u = slot[i];
+  }
+  return t;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
 // Host: the work list of a single-token decode batch (see pkv.h).
 int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int max_blocks_per_seq, int num_seqs,
-                     int num_kv_heads, int block_size, int partition_size, int32_t *items_out, int max_items,
-                     int *num_items) {
+                     int num_kv_heads, int head_dim, int block_size, int partition_size, int32_t *items_out,
+                     int max_items, int *num_items) {
   if (!num_items) return PKV_ERR_ARG;
   *num_items = 0;
   if (num_seqs < 0 || num_kv_heads < 1 || num_kv_heads > 65535 || block_size < 1 || max_blocks_per_seq < 0 ||
-      max_items < 0 || partition_size < 0 || (num_seqs > 0 && !seq_lens) || !items_out)
+      max_items < 0 || partition_size < 0 || head_dim < 1 || (num_seqs > 0 && !seq_lens) || !items_out)
     return PKV_ERR_ARG;
-  const int part = partition_size == 0 ? pkv::kDefaultPartition : partition_size;
-  if (part % block_size != 0) return PKV_ERR_ARG;
+  if (partition_size % block_size != 0) return PKV_ERR_ARG;
   const long long cap = static_cast<long long>(max_blocks_per_seq) * block_size;
+  for (int i = 0; i < num_seqs; ++i)
+    if (seq_lens[i] < 0 || seq_lens[i] > cap) return PKV_ERR_RANGE;
+  int part = partition_size;
+  if (part == 0) {  // the candidate the schedule model predicts fastest (ties: the smaller)
+    double best = 0.0;
+    std::vector<double> rest, slot;
+    rest.reserve(static_cast<size_t>(num_seqs));
+    for (int cand : {768, 1024, 1536, 2048}) {
+      if (cand % block_size != 0) continue;
+      const double t = pkv::predict_list_time(seq_lens, num_seqs, num_kv_heads, head_dim, cand, rest, slot);
+      if (part == 0 || t < best) part = cand, best = t;
+    }
+    if (part == 0) part = pkv::kDefaultPartition;
+  }
   long long count = 0;
   for (int i = 0; i < num_seqs; ++i) {
     const int L = seq_lens[i];
-    if (L < 0 || L > cap) return PKV_ERR_RANGE;
     const long long np = L > 0 ? (static_cast<long long>(L) + part - 1) / part : 1;
     if (np > 65535) return PKV_ERR_UNSUPPORTED;
     count += np * num_kv_heads;
@@ -859,7 +929,8 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
   std::stable_sort(pieces.begin(), pieces.end(), [](const Piece &a, const Piece &b) { return a.ntok > b.ntok; });
   int32_t *o = items_out;
   o[0] = static_cast<int32_t>(count);
-  o[1] = o[2] = o[3] = 0;
+  o[1] = part;  // the partition the list was built for: pass it to the decode
+  o[2] = o[3] = 0;
   o += 4;
   const long long part_blocks = part / block_size;
   for (const Piece &pc : pieces) {

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <map>
 #include <new>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -21,6 +22,7 @@
 namespace {
 
 constexpr int kMaxGraphs = 32;
+constexpr int kRepick = 64;  // steps between two picks of the work list's partition
 constexpr int kDefaultPartition = 768;  // paged_attention_decode's default
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -50,7 +52,8 @@ struct pkv_step {
   cudaStream_t cap = nullptr;
   cudaEvent_t done = nullptr;
   bool pending = false;
-  std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
+  std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;  // (n, partitions, partition size)
+  int auto_part = 0, auto_n = 0, auto_age = 0;  // the work list's partition pick, kept between steps
 };
 
 namespace {
@@ -62,7 +65,7 @@ void drop_graphs(pkv_step *s) {
 
 // Copy in, every layer's write and decode, copy out, on `st`.  q_len 1: the
 // decode runs grid_items CTAs over the work list in the staging buffer.
-int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items) {
+int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items, int partition) {
   const pkv_step_config &c = s->cfg;
   const pkv_step_layout &L = s->lay;
   cudaError_t e = cudaMemcpyAsync(s->ds, s->hs, L.stage_bytes, cudaMemcpyHostToDevice, st);
@@ -80,7 +83,7 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items
       const auto *items = reinterpret_cast<const int32_t *>(s->ds + L.items_offset);
       rc = paged_attention_decode_items(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
                                         max_seq_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
-                                        c.num_blocks, c.scale, c.partition_size, items, grid_items, out, s->ws,
+                                        c.num_blocks, c.scale, partition, items, grid_items, out, s->ws,
                                         s->ws_bytes, s->status, st, nullptr);
     } else {
       rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
@@ -97,7 +100,7 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items
   return PKV_OK;
 }
 
-int capture(pkv_step *s, int n, int max_seq_len, int grid_items, cudaGraphExec_t *exec) {
+int capture(pkv_step *s, int n, int max_seq_len, int grid_items, int partition, cudaGraphExec_t *exec) {
   cudaError_t e;
   if (!s->cap && (e = cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking)) != cudaSuccess)
     return pkv::set_cuda_error(e), PKV_ERR_CUDA;
@@ -105,7 +108,7 @@ int capture(pkv_step *s, int n, int max_seq_len, int grid_items, cudaGraphExec_t
   // entry points while the stream is being captured.
   if ((e = cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeRelaxed)) != cudaSuccess)
     return pkv::set_cuda_error(e), PKV_ERR_CUDA;
-  const int rc = enqueue(s, s->cap, n, max_seq_len, grid_items);
+  const int rc = enqueue(s, s->cap, n, max_seq_len, grid_items, partition);
   cudaGraph_t g = nullptr;
   e = cudaStreamEndCapture(s->cap, &g);
   if (rc != PKV_OK || e != cudaSuccess) {
@@ -238,43 +241,68 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
     if (len + c.q_len > cap) return PKV_ERR_RANGE;
     max_len = len + c.q_len > max_len ? static_cast<int>(len + c.q_len) : max_len;
   }
+  // The work list (q_len 1) depends on the lengths after the append, which the
+  // checks above already know; its partition size keys the graphs.
+  auto *items = reinterpret_cast<int32_t *>(s->hs + s->lay.items_offset);
+  auto *tables = reinterpret_cast<int32_t *>(s->hs + s->lay.tables_offset);
+  auto *lens = reinterpret_cast<int32_t *>(s->hs + s->lay.lens_offset);
+  int count = 0, partition = c.partition_size;
+  if (c.q_len == 1) {
+    for (int i = 0; i < n; ++i) lens[i] = static_cast<int32_t>(pkv_seq_len(s->alloc, seq_ids[i]) + c.q_len);
+    // With partition_size 0 the list picks its partition from a schedule model;
+    // the lengths move by one token a step, so the pick is kept for a while
+    // and made again every kRepick steps or when the batch size changes.
+    int want = c.partition_size;
+    if (want == 0 && s->auto_part > 0 && s->auto_n == n && s->auto_age < kRepick) want = s->auto_part;
+    // cannot fail: the lengths fit the tables and the list its segment (partitions of at least 768 tokens)
+    if ((rc = pkv_decode_items(lens, nullptr, c.max_blocks_per_seq, n, c.num_kv_heads, c.head_dim, c.block_size,
+                               want, items, s->lay.max_items, &count)) != PKV_OK)
+      return rc;
+    partition = items[1];
+    if (c.partition_size == 0) {
+      s->auto_age = want == 0 ? 0 : s->auto_age + 1;
+      s->auto_part = partition;
+      s->auto_n = n;
+    }
+  }
   // Everything that can fail without a CUDA fault (a graph capture included)
   // happens before the allocator changes; the append is the last host step.
   cudaStream_t st = pkv::as_stream(stream);
   cudaGraphExec_t exec = nullptr;
+  const int part = partition > 0 ? partition : s->part;
   if (c.use_graph) {
-    const int parts = max_len > 0 ? (max_len + s->part - 1) / s->part : 1;
-    const auto key = std::make_pair(n, parts);
+    const int parts = max_len > 0 ? (max_len + part - 1) / part : 1;
+    const auto key = std::make_tuple(n, parts, part);
     auto it = s->graphs.find(key);
     if (it == s->graphs.end()) {
       if (static_cast<int>(s->graphs.size()) >= kMaxGraphs) drop_graphs(s);
-      const long long bound = static_cast<long long>(parts) * s->part;
+      const long long bound = static_cast<long long>(parts) * part;
       // the work list of any step with this key has at most n x KV heads x parts items
       const int grid_items = c.q_len == 1 ? n * c.num_kv_heads * parts : 0;
-      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), grid_items, &exec);
+      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), grid_items, partition, &exec);
       if (rc != PKV_OK) return rc;
       it = s->graphs.emplace(key, exec).first;
     }
     exec = it->second;
   }
   auto *slots = reinterpret_cast<int64_t *>(s->hs + s->lay.slots_offset);
-  auto *tables = reinterpret_cast<int32_t *>(s->hs + s->lay.tables_offset);
-  auto *lens = reinterpret_cast<int32_t *>(s->hs + s->lay.lens_offset);
   if ((rc = pkv_seq_append_batch(s->alloc, seq_ids, n, c.q_len, slots)) != PKV_OK) return rc;
   // cannot fail: every id is resident (the append took it) and its table has room (checked above)
   if ((rc = pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, lens)) != PKV_OK) return rc;
-  int count = 0;
-  if (c.q_len == 1) {  // cannot fail either: the lengths fit the tables and the list its segment
-    auto *items = reinterpret_cast<int32_t *>(s->hs + s->lay.items_offset);
-    if ((rc = pkv_decode_items(lens, tables, c.max_blocks_per_seq, n, c.num_kv_heads, c.block_size,
-                               c.partition_size, items, s->lay.max_items, &count)) != PKV_OK)
-      return rc;
+  if (c.q_len == 1) {  // the first blocks of the items, now that the tables are filled
+    const int part_blocks = partition / c.block_size;
+    for (int i = 1; i <= count; ++i) {
+      int32_t *it = items + 4 * i;
+      const int seq = it[0], pt = static_cast<int>(static_cast<uint32_t>(it[1]) >> 16);
+      const long long e = static_cast<long long>(pt) * part_blocks;
+      it[3] = it[2] > 0 && e < c.max_blocks_per_seq ? tables[static_cast<size_t>(seq) * c.max_blocks_per_seq + e] : -1;
+    }
   }
 
   if (exec) {
     const cudaError_t e = cudaGraphLaunch(exec, st);
     if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
-  } else if ((rc = enqueue(s, st, n, max_len, count)) != PKV_OK) {
+  } else if ((rc = enqueue(s, st, n, max_len, count, partition)) != PKV_OK) {
     return rc;
   }
   const cudaError_t e = cudaEventRecord(s->done, st);

@@ -79,8 +79,8 @@ SIGNATURES = {
     "paged_attention_decode_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
                                               _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_float, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr, _c_ptr]),
-    "pkv_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int,
-                                  ctypes.POINTER(_c_int)]),
+    "pkv_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr,
+                                  _c_int, ctypes.POINTER(_c_int)]),
     "paged_attention_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
                                               _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_float, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
@@ -277,25 +277,27 @@ def paged_attention_decode_write(q, k_new, v_new, slot_mapping, k_cache, v_cache
         None if ev is None else ctypes.c_void_p(ev)), "paged_attention_decode_write")
 
 
-def pkv_decode_items(seq_lens, block_tables, num_kv_heads, block_size, partition_size=0, out=None):
+def pkv_decode_items(seq_lens, block_tables, num_kv_heads, block_size, partition_size=0, head_dim=128, out=None):
     """Host work list of a single-token decode batch (numpy int32 lengths [B] and
-    tables [B, max_blocks], or None): returns int32 [1 + count, 4], row 0 = {count, 0, 0, 0}.
+    tables [B, max_blocks], or None): returns int32 [1 + count, 4], row 0 =
+    {count, partition size used, 0, 0}.  partition_size 0: the library picks it.
     ``out`` (int32 [1 + n, 4], C-contiguous) is filled in place when it has room."""
     import numpy as np
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     tbl = None if block_tables is None else np.ascontiguousarray(block_tables, dtype=np.int32)
     B = lens.shape[0]
-    maxb = 0 if tbl is None else tbl.shape[1]
     if tbl is None:
         maxb = int(-(-int(lens.max(initial=0)) // block_size))
     elif tbl.shape[0] != B:
         raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    else:
+        maxb = tbl.shape[1]
     n = ctypes.c_int(0)
     buf = out if out is not None else np.empty((1, 4), dtype=np.int32)
     for _ in range(2):
         rc = lib().pkv_decode_items(lens.ctypes.data, None if tbl is None else tbl.ctypes.data, maxb, B,
-                                    int(num_kv_heads), int(block_size), int(partition_size), buf.ctypes.data,
-                                    buf.shape[0] - 1, ctypes.byref(n))
+                                    int(num_kv_heads), int(head_dim), int(block_size), int(partition_size),
+                                    buf.ctypes.data, buf.shape[0] - 1, ctypes.byref(n))
         if rc == PKV_ERR_RANGE and n.value > buf.shape[0] - 1 and out is None:
             buf = np.empty((1 + n.value, 4), dtype=np.int32)
             continue

@@ -49,6 +49,7 @@ class StepInputs:
     host_tables: np.ndarray
     host_lens: np.ndarray
     items: torch.Tensor | None = None  # single-token steps: the decode's work list [1 + n, 4] int32, device
+    partition: int = 0                 # the partition size that list was built for
 
 
 class DecodeSession:
@@ -150,13 +151,13 @@ class DecodeSession:
         lens = np.asarray(lens, dtype=np.int32)
         dev = self.device
         cow = torch.as_tensor(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), device=dev) if pairs else None
-        items = None
+        items, partition = None, self.partition_size
         if self.q_len == 1:  # the host knows every length: the decode's longest-first work list
-            items = torch.as_tensor(native.pkv_decode_items(lens, tables, self.Hkv, self.bs, self.partition_size),
-                                    device=dev)
+            host_items = native.pkv_decode_items(lens, tables, self.Hkv, self.bs, self.partition_size, self.d)
+            items, partition = torch.as_tensor(host_items, device=dev), int(host_items[0, 1])
         return StepInputs(torch.as_tensor(slots, device=dev), torch.as_tensor(tables, device=dev),
                           torch.as_tensor(lens, device=dev), int(lens.max()) if len(lens) else 0, cow,
-                          tables, lens, items)
+                          tables, lens, items, partition)
 
     def plan_steps(self, n: int):
         return [self.plan_step() for _ in range(n)]
@@ -199,7 +200,7 @@ class DecodeSession:
             if fused and planned:
                 native.paged_attention_decode_items(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
                                                     step.tables, step.lens, step.max_len, self.scale, o, step.items,
-                                                    workspace=workspace, partition_size=self.partition_size,
+                                                    workspace=workspace, partition_size=step.partition,
                                                     d_status=d_status, stream=stream)
                 continue
             if fused:
@@ -238,15 +239,17 @@ DECODE_BYTES_PER_S = 5.0e12
 
 
 def mixed_prefill_ctas(case, sms: int = 152) -> int:
-    """SMs for the chunks of a mixed step: their share of the step's time when
-    each half runs alone at its measured rate (at least 8, at most sms - 8)."""
+    """SMs for the chunks of a mixed step.  The decodes saturate HBM on about
+    half the SMs, so the chunks get their share of the two halves' times with
+    the decodes' time counted half (at least half the SMs): measured on the
+    mixed workload, 88 to 152 chunk CTAs all give 0.62-0.63 ms, 64 gives 0.76."""
     nd = case.num_decodes
     flops_chunks = 4 * case.d * case.Hq * causal_visible_keys(case.lens[nd:], case.chunks[nd:])
     bytes_dec = int(case.lens[:nd].astype(np.int64).sum()) * 2 * case.Hkv * case.d * 2
     tc, td = flops_chunks / PREFILL_FLOPS_PER_S, bytes_dec / DECODE_BYTES_PER_S
     if tc + td <= 0:
         return 0
-    return int(min(sms - 8, max(8, round(sms * tc / (tc + td)))))
+    return int(min(sms, max(sms // 2, round(sms * tc / (tc + td / 2)))))
 
 
 class PrefillCase:
@@ -308,10 +311,11 @@ class PrefillCase:
         nd = self.num_decodes
         self.mixed_nd = nd
         self.mixed_max_len = int(self.lens[:nd].max()) if nd else 0
-        self.mixed_part = partition_size
-        self.mixed_items = torch.as_tensor(native.pkv_decode_items(self.lens[:nd], self.tables[:nd], self.Hkv,
-                                                                   self.bs, partition_size), device=self.device)
-        n = native.paged_attention_workspace_size(nd, 1, self.Hq, self.d, self.mixed_max_len, partition_size)
+        host_items = native.pkv_decode_items(self.lens[:nd], self.tables[:nd], self.Hkv, self.bs, partition_size,
+                                             self.d)
+        self.mixed_part = int(host_items[0, 1])
+        self.mixed_items = torch.as_tensor(host_items, device=self.device)
+        n = native.paged_attention_workspace_size(nd, 1, self.Hq, self.d, self.mixed_max_len, self.mixed_part)
         self.mixed_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
         self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
 

@@ -452,7 +452,7 @@ def test_decode_work_list_is_longest_first_and_complete(native):
     tables[2, :63] = np.arange(100, 163)
     tables[3, :48] = np.arange(200, 248)
     items = native.pkv_decode_items(lens, tables, num_kv_heads=2, block_size=16, partition_size=768)
-    assert items[0].tolist() == [10, 0, 0, 0]
+    assert items[0].tolist() == [10, 768, 0, 0]
 
     def it(seq, part, h, L, b0):
         return [seq, h | (part << 16), L, b0]
@@ -462,19 +462,35 @@ def test_decode_work_list_is_longest_first_and_complete(native):
             it(1, 0, 0, 5, 7), it(1, 0, 1, 5, 7),             # 5 tokens
             it(0, 0, 0, 0, -1), it(0, 0, 1, 0, -1)]           # empty: zeros
     assert items[1:].tolist() == want
-    # without tables the first block is unknown (-1); the default partition is 768
-    assert native.pkv_decode_items(lens, None, 2, 16)[1:, 3].tolist() == [-1] * 10
+    # without tables the first block is unknown (-1)
+    assert native.pkv_decode_items(lens, None, 2, 16, 768)[1:, 3].tolist() == [-1] * 10
     # a length past the table, a partition that is not a multiple of the block, no room
     lib = native.lib()
     n = ctypes.c_int(0)
     buf = np.zeros((11, 4), dtype=np.int32)
     bad = np.array([16 * 70 + 1], dtype=np.int32)
-    assert lib.pkv_decode_items(bad.ctypes.data, None, 70, 1, 2, 16, 0, buf.ctypes.data, 10,
+    assert lib.pkv_decode_items(bad.ctypes.data, None, 70, 1, 2, 128, 16, 0, buf.ctypes.data, 10,
                                 ctypes.byref(n)) == native.PKV_ERR_RANGE
-    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 16, 24, buf.ctypes.data, 10,
+    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 128, 16, 24, buf.ctypes.data, 10,
                                 ctypes.byref(n)) == native.PKV_ERR_ARG
-    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 16, 768, buf.ctypes.data, 9,
+    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 128, 16, 768, buf.ctypes.data, 9,
                                 ctypes.byref(n)) == native.PKV_ERR_RANGE and n.value == 10
+
+
+def test_decode_work_list_chooses_its_partition():
+    """partition_size 0: the list is built for one of 768 / 1024 / 1536 / 2048
+    tokens (a multiple of the block), reported in row 0, and is the list an
+    explicit request for that size gives."""
+    from paged_kv_cache_276_gb300 import build, native as nat
+    build.build()
+    rng = np.random.default_rng(4)
+    for B, hi, bs in ((32, 4096, 16), (256, 8192, 16), (3, 300, 128), (64, 20000, 32)):
+        lens = rng.integers(0, hi, size=B).astype(np.int32)
+        auto = nat.pkv_decode_items(lens, None, 8, bs, 0)
+        part = int(auto[0, 1])
+        assert part in (768, 1024, 1536, 2048) and part % bs == 0
+        assert np.array_equal(auto, nat.pkv_decode_items(lens, None, 8, bs, part))
+        assert auto[0, 0] == sum(max(1, -(-int(L) // part)) for L in lens) * 8
 
 
 def test_decode_items_rejects_bad_arguments_before_launch(native):

@@ -803,8 +803,8 @@ def test_decode_items_equals_the_grid_decode_bit_exact(d, bs, Hq, Hkv, part):
     max_len = max(lens)
     n = native.paged_attention_workspace_size(B, 1, Hq, d, max_len, part)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
-    items = native.pkv_decode_items(np.asarray(lens, dtype=np.int32), tables, Hkv, bs, part)
-    count = int(items[0, 0])
+    items = native.pkv_decode_items(np.asarray(lens, dtype=np.int32), tables, Hkv, bs, part, d)
+    count, part = int(items[0, 0]), int(items[0, 1])  # part 0: the size the list chose
     padded = np.zeros((1 + count + 37, 4), dtype=np.int32)  # a grid of count + 37 CTAs
     padded[:1 + count] = items
     items_d = torch.as_tensor(padded, device="cuda")
@@ -838,7 +838,7 @@ def test_decode_items_built_for_other_lengths_is_reported():
     d, bs, Hq, Hkv = 128, 16, 32, 8
     lens = [900, 40, 2000]
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=97)
-    items = native.pkv_decode_items(np.asarray([900, 40, 1990], dtype=np.int32), tables, Hkv, bs, 512)
+    items = native.pkv_decode_items(np.asarray([900, 40, 1990], dtype=np.int32), tables, Hkv, bs, 512, d)
     st = status_tensor()
     out = torch.empty_like(q)
     n = native.paged_attention_workspace_size(3, 1, Hq, d, 2000, 512)

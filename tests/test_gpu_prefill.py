@@ -256,7 +256,7 @@ def test_prefill_workloads_every_sequence(tag, mixed):
     st = status_tensor()
     if mixed:  # the benchmark's launch: decodes over their work list beside the chunks
         case.prepare_mixed()
-        assert case.mixed_nd == 256 and 8 <= case.mixed_ctas <= 144
+        assert case.mixed_nd == 256 and 76 <= case.mixed_ctas <= 152
         case.attend_mixed(st)
     else:
         case.attend(st)
@@ -447,7 +447,7 @@ def test_mixed_step_entry_matches_the_oracle(ctas):
     scale = float(np.float32(1 / math.sqrt(d)))
     dev = kc.device
     items = torch.as_tensor(native.pkv_decode_items(np.asarray(lens[:n_dec], dtype=np.int32), tables[:n_dec], Hkv, bs,
-                                                    512), device=dev)
+                                                    512, d), device=dev)
     n = native.paged_attention_workspace_size(n_dec, 1, Hq, d, max(lens[:n_dec]), 512)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
