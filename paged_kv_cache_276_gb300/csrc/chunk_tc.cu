@@ -783,10 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item &x = sc.x;
         const int L = lens[x.seq];
         const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
-        if (kP2 && set == 1 && !x.has_b) {  // the pair has no second query tile
-          g += ntile;  // the tiles still pass through the rings: stage and phase follow them
-          continue;
-        }
+        if (kP2 && set == 1 && !x.has_b) continue;  // the pair has no second query tile
         if (x.skip) continue;                        // an empty partition: nothing to compute or store
         if (x.run_begin) {
           m = -INFINITY;
