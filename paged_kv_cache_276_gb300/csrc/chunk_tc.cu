@@ -413,12 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) prefix[0] = 0;
   }
   if (threadIdx.x == 32 * kKWarp) {
-    // over pairs of query tiles each query tile has its own issuer, and both
-    // release the queries, key stages and value stages they read
-    constexpr int kReaders = kP2 ? 2 : 1;
     for (int i = 0; i < kQBufs; ++i) {
       mbar_init(bar(B_Q_FULL0 + i), 1);
-      mbar_init(bar(B_Q_FREE0 + i), kReaders);
+      mbar_init(bar(B_Q_FREE0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {  // decode chunk: index 0 only; prefill: one per query tile of the pair
       mbar_init(bar(B_O_FULL + i), 1);
@@ -435,9 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_K_FULL0 + s), 1);
-      mbar_init(bar(B_K_EMPTY0 + s), kReaders);
+      mbar_init(bar(B_K_EMPTY0 + s), 1);
       mbar_init(bar(B_V_FULL0 + s), 1);
-      mbar_init(bar(B_V_EMPTY0 + s), kReaders);
+      mbar_init(bar(B_V_EMPTY0 + s), 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -573,85 +570,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int qi = tpieces > kQBufs ? tpieces - kQBufs : 0; qi < tpieces; ++qi)
             mbar_wait_sleep(bar(B_Q_FULL0 + qi % kQBufs), (qi / kQBufs) & 1);
       }
-    } else if (kP2 && (warp == kMmaWarp || warp == kPvWarp)) {
-      // ------------------------------- pairs: one issuer per query tile
-      // Warp 9 issues query tile A's products, warp 10 query tile B's: per key
-      // tile the score product S_q = Q_q K^T (after the set's previous P V
-      // product, whose P lives over S), then, once the set's softmax has
-      // written P, O_q += P_q V.  Each set's chain depends only on its own
-      // softmax, so one set's products run while the other set computes its
-      // weights.  Both issuers release the queries, key and value stages
-      // (barriers with two arrivals); an issuer whose pair has no tile B
-      // still waits for each stage before it counts in, so neither runs more
-      // than one stage phase ahead.
-      if (lane == 0) {
-        constexpr uint32_t kIdS = tc::idesc_bf16(kRows, kTileKeys, false, false);
-        constexpr uint32_t kIdO = tc::idesc_bf16(kRows, D, false, true);
-        constexpr int kSteps = kTileKeys / 16;  // 16 keys = 8 packed columns of P
-        const int q = warp == kMmaWarp ? 0 : 1;
-        const uint32_t sq = sQ + q * kQBytes, tSq = tS0 + q * kTileKeys;
-        const uint32_t pa = tP0 + q * Lay::kPStride, acc = tmem + q * D;
-        Sched<kPrefill, kP2> sc;
-        sc.begin(p, tab, I);
-        int g = 0, tpieces = 0, n = 0, items = 0;
-        bool ok = true;
-        for (; sc.valid() && ok; sc.advance(p, tab)) {
-          const Item &x = sc.x;
-          const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
-          if (ntile == 0) continue;
-          const bool mine = q == 0 || x.has_b;
-          const int qi = tpieces++;
-          if (!mbar_wait(bar(B_Q_FULL0), qi & 1)) { ok = false; break; }
-          if (mine) ++items;
-          for (int t = 0; t < ntile && ok; ++t, ++g) {
-            const int s = g % kStages;
-            if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            if (mine) {
-              if (n > 0 && !mbar_wait(bar(B_PV_DONE0 + q), (n - 1) & 1)) { ok = false; break; }
-              tc::fence_after();
-              const uint32_t kb = sK + s * kKVBytes;
-#pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks)
-                tc::mma(tSq, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
-                        tc::desc_sw128(kb + (ks >> 2) * Lay::kKVHalf + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
-              tc::commit(bar(B_S_FULL0 + q));
-              tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by this product
-              if (t == ntile - 1) tc::commit(bar(B_Q_FREE0));
-            } else {
-              mbar_arrive(bar(B_K_EMPTY0 + s));
-              if (t == ntile - 1) mbar_arrive(bar(B_Q_FREE0));
-            }
-            if (!mbar_wait(bar(B_V_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
-            if (!mine) {
-              mbar_arrive(bar(B_V_EMPTY0 + s));
-              continue;
-            }
-            // keys kTK/2.. first (P_FULL), keys 0.. once weighted (P_LO)
-            if (!mbar_wait(bar(B_P_FULL0 + q), n & 1)) { ok = false; break; }
-            // the item's first product overwrites the accumulator: the previous epilogue must have read it
-            if (t == 0 && items > 1 && !mbar_wait(bar(B_O_FREE + q), (items - 2) & 1)) { ok = false; break; }
-            tc::fence_after();
-            const uint32_t vb = sV + s * kKVBytes;
-#pragma unroll
-            for (int ks = kSteps / 2; ks < kSteps; ++ks)
-              tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
-                         !(t == 0 && ks == kSteps / 2));
-            if (!mbar_wait(bar(B_P_LO0 + q), n & 1)) { ok = false; break; }
-            tc::fence_after();
-#pragma unroll
-            for (int ks = 0; ks < kSteps / 2; ++ks)
-              tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO, true);
-            tc::commit(bar(B_PV_DONE0 + q));
-            if (t == ntile - 1) tc::commit(bar(B_O_FULL + q));
-            tc::commit(bar(B_V_EMPTY0 + s));
-            ++n;
-          }
-        }
-        if (!ok) {
-          if (p.status) atomicOr(p.status, PKV_STATUS_TIMEOUT);
-          *abort_flag = 1;
-        }
-      }
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------- S = Q K^T issuer
       // A score product waits for its key stage and for its S buffer: in
@@ -666,10 +584,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0;
         bool ok = true;
+        int na = 0, nb = 0;  // prefill: score products of each query tile of the pair so far
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
           if (ntile == 0) continue;
+          if constexpr (kP2) {
+            // both query tiles of the pair against each key tile: tile A into
+            // S buffer 0, tile B into buffer 1; each buffer holds its tile's
+            // previous P until that P V product completes
+            const int qi = tpieces++;
+            if (!mbar_wait(bar(B_Q_FULL0), qi & 1)) { ok = false; break; }
+            for (int t = 0; t < ntile && ok; ++t, ++g) {
+              const int s = g % kStages;
+              if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
+              const uint32_t kb = sK + s * kKVBytes;
+              for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
+                int &n = q ? nb : na;
+                if (n > 0 && !mbar_wait(bar(B_PV_DONE0 + q), (n - 1) & 1)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t sq = sQ + q * kQBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                  tc::mma(tS0 + q * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
+                          tc::desc_sw128(kb + (ks >> 2) * Lay::kKVHalf + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
+                tc::commit(bar(B_S_FULL0 + q));
+                ++n;
+              }
+              if (!ok) break;
+              tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by these products only
+              if (t == ntile - 1) tc::commit(bar(B_Q_FREE0));
+            }
+            continue;
+          }
           int qb = (tpieces > 0 ? tpieces - 1 : 0) % kQBufs;
           if (x.run_begin) {
             const int qi = tpieces++;
@@ -711,11 +658,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         Sched<kPrefill, kP2> sc;
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0, run_g0 = 0;
+        int na = 0, nb = 0, ia = 0, ib = 0;  // prefill: P V products and items of each query tile of the pair
         bool ok = true;
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
           if (ntile == 0) continue;
+          if constexpr (kP2) {
+            // per key tile: tile A's product, then tile B's (so that B's
+            // product follows A's zeroing of the value rows past the end)
+            ++ia;
+            if (x.has_b) ++ib;
+            for (int t = 0; t < ntile && ok; ++t, ++g) {
+              const int vs = g % kStages;
+              if (!mbar_wait(bar(B_V_FULL0 + vs), (g / kStages) & 1)) { ok = false; break; }
+              const uint32_t vb = sV + vs * kKVBytes;
+              constexpr int kSteps = kTileKeys / 16;  // 16 keys = 8 packed columns of P
+              for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
+                int &n = q ? nb : na;
+                const int items = q ? ib : ia;
+                if (!mbar_wait(bar(B_P_FULL0 + q), n & 1)) { ok = false; break; }
+                // the item's first product overwrites the accumulator: the previous epilogue must have read it
+                if (t == 0 && items > 1 && !mbar_wait(bar(B_O_FREE + q), (items - 2) & 1)) { ok = false; break; }
+                tc::fence_after();
+                const uint32_t pa = tP0 + q * Lay::kPStride, acc = tmem + q * D;
+                // keys kTK/2.. first (P_FULL), keys 0.. once weighted (P_LO)
+#pragma unroll
+                for (int ks = kSteps / 2; ks < kSteps; ++ks)
+                  tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO,
+                             !(t == 0 && ks == kSteps / 2));
+                if (!mbar_wait(bar(B_P_LO0 + q), n & 1)) { ok = false; break; }
+                tc::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < kSteps / 2; ++ks)
+                  tc::mma_ta(acc, pa + ks * 8, tc::desc_sw128(vb + ks * 2048, Lay::kKVHalf, 1024), kIdO, true);
+                tc::commit(bar(B_PV_DONE0 + q));
+                if (t == ntile - 1) tc::commit(bar(B_O_FULL + q));
+                ++n;
+              }
+              if (!ok) break;
+              tc::commit(bar(B_V_EMPTY0 + vs));
+            }
+            continue;
+          }
           if (x.run_begin) {
             ++tpieces;
             run_g0 = g;
@@ -865,10 +850,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // before any P V product of this tile reads the stage
           auto zero_tail_values = [&]() {
             const int exist = L - k0;
-            // over pairs each set zeroes the rows before its own P V product
-            // (the same zeros, so a product of the other set reading them
-            // meanwhile sees zeros either way)
-            if (exist >= kTileKeys) return true;
+            // prefill: query tile A's set zeroes; B's P V product is issued after A's
+            if (exist >= kTileKeys || (kP2 && set == 1)) return true;
             const int s = g % kStages;
             if (!wait_warp(bar(B_V_FULL0 + s), (g / kStages) & 1)) return false;
             const uint32_t vb = sV + s * kKVBytes;
