@@ -652,9 +652,12 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
             # a batch led by single-token decodes runs as one mixed step: the
             # decodes over their work list beside the chunks on the tensor cores
             mixed = 0 < case.num_decodes < case.B
+            split = pw.extra.get("split", 0)
             if mixed:
                 case.prepare_mixed()
-            attend = case.attend_mixed if mixed else case.attend
+            if split:
+                case.prepare_split(split)
+            attend = case.attend_mixed if mixed else case.attend_split if split else case.attend
             status = torch.zeros(1, dtype=torch.int32, device=device)
             pool = []
             for _ in range(4 * (warmup + steps)):  # created and recorded once, before the timed loop
@@ -689,20 +692,35 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
             tf = fl / (am * 1e-3) / 1e12
             kv_gbs = case.kv_bytes() / (am * 1e-3) / 1e9
             hbm_peak, hbm_kind = measured_hbm_peak()
+            traffic = kernel_traffic("chunk_tc_kernel_traffic.txt", tag)
+            if mixed:  # the call's two kernels: the chunks' and the decodes' launches
+                tc_part = kernel_traffic("chunk_tc_kernel_traffic.txt", tag + "_chunks")
+                dec_part = kernel_traffic("decode_kernel_traffic.txt", tag + "_decodes")
+                traffic = tc_part + dec_part if tc_part is not None and dec_part is not None else None
             if case.kv_bytes() / (hbm_peak * 1e9) > fl / (peak * 1e12):
                 # more time in moving K/V than in the products at the peaks: bandwidth-bound
                 roof = {"bound": "hbm", "achieved": round(kv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                         "frac": round(kv_gbs / hbm_peak, 4), "peak_kind": f"{hbm_kind} hbm_gbs",
-                        "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag),
-                        "tflops": round(tf, 1)}
+                        "traffic": traffic, "tflops": round(tf, 1)}
             else:
                 roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                        "frac": round(tf / peak, 4), "peak_kind": peak_kind,
-                        "traffic": kernel_traffic("chunk_tc_kernel_traffic.txt", tag)}
+                        "frac": round(tf / peak, 4), "peak_kind": peak_kind, "traffic": traffic}
             res[tag] = {"ms": round(am, 5), "roofline": roof, "kv_gbs": round(kv_gbs, 1),
                         "rows_s": round(case.total_q / (sm * 1e-3), 1), "step_ms": round(sm, 5)}
             if mixed:
                 res[tag]["call"] = f"paged_attention_mixed ({case.mixed_nd} decodes, chunks on {case.mixed_ctas} CTAs)"
+            if split:  # the same call without the split, for comparison
+                res[tag]["call"] = f"paged_attention_prefill_ex (keys split into {split}-token partitions)"
+                us = []
+                for i in range(steps):
+                    flush.fill_(float(i) + 0.25)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    case.attend(status, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    us.append(e0.elapsed_time(e1))
+                res[tag]["unsplit_ms"] = round(sum(us) / len(us), 5)
             if not compact:
                 res[tag].update(
                     workload=f"{pw.name}: {case.B} seqs, (L, chunk) = "
@@ -766,7 +784,7 @@ def main():
                     help="time only this secondary workload (for profiling runs; no headline line)")
     ap.add_argument("--swap", action="store_true", help="bandwidth of the block swap-out / swap-in copies")
     ap.add_argument("--prefill", nargs="?", const="all", default=None,
-                    choices=["all", "prefill_long_context", "prefill_prompts", "prefill_mixed"],
+                    choices=["all", "prefill_long_context", "prefill_prompts", "prefill_mixed", "prefill_short_chunk"],
                     help="chunked prefill only (all workloads, or the one named)")
     ap.add_argument("--block-sweep", action="store_true",
                     help="block-size trade-off: decode GB/s at block 16..128 and the memory simulation")

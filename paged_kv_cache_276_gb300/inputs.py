@@ -30,6 +30,9 @@ length L including its chunk, chunk length c)):
   prefill_mixed         one scheduler step: 256 single-token decodes with
                         L ~ U{1..4096} and two 1,024-token prompt chunks at
                         L 8192 and 16384, block 16, 32 q / 8 KV heads, d 128
+  prefill_short_chunk   one 128-token chunk behind 32,640 cached tokens
+                        (L 32768, c 128), block 16, 64 q / 8 KV heads, d 128,
+                        its keys split into 2048-token partitions
 """
 from __future__ import annotations
 
@@ -100,6 +103,11 @@ PREFILL_WORKLOADS = {
     "prefill_mixed": PrefillWorkload("prefill_mixed", "256 decodes + two 1,024-token prompt chunks in one call",
                                      16, 32, 8, 128, 2003,
                                      extra={"decodes": 256, "len_max": 4096, "chunks": ((8192, 1024), (16384, 1024))}),
+    # one short chunk behind a long context: 8 query tiles x 8 KV heads, fewer units
+    # of work than SMs unless the keys are split (partitions of 2048 keys)
+    "prefill_short_chunk": PrefillWorkload("prefill_short_chunk", "one 128-token chunk behind a 32,640-token context",
+                                           16, 64, 8, 128, 2004,
+                                           extra={"seqs": 1, "len": 32768, "chunk": 128, "split": 2048}),
 }
 
 

@@ -319,6 +319,19 @@ class PrefillCase:
         self.mixed_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
         self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
 
+    def prepare_split(self, partition_size: int):
+        """Workspace of the prefill split over keys into partition_size-token partitions."""
+        self.split_part = partition_size
+        self.split_max_len = int(self.lens.max())
+        n = native.paged_attention_prefill_workspace_size(self.total_q, self.Hq, self.d, self.split_max_len,
+                                                          partition_size)
+        self.split_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+
+    def attend_split(self, d_status=None, stream=None):
+        native.paged_attention_prefill_ex(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens,
+                                          self.d_q_start, self.scale, self.out, self.split_max_len, self.split_part,
+                                          self.split_ws, d_status, stream)
+
     def attend_mixed(self, d_status=None, stream=None):
         native.paged_attention_mixed(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens, self.d_q_start,
                                      self.scale, self.out, self.mixed_nd, self.mixed_items, self.mixed_max_len,

@@ -243,9 +243,10 @@ def test_mixed_step_of_decodes_and_a_prefill_chunk():
     assert torch.allclose(dec[:, 0].float(), out[:n_dec].float(), atol=1e-2, rtol=1e-2)
 
 
-@pytest.mark.parametrize("tag,mixed", [("prefill_long_context", False), ("prefill_prompts", False),
-                                       ("prefill_mixed", False), ("prefill_mixed", True)])
-def test_prefill_workloads_every_sequence(tag, mixed):
+@pytest.mark.parametrize("tag,mode", [("prefill_long_context", "plain"), ("prefill_prompts", "plain"),
+                                      ("prefill_mixed", "plain"), ("prefill_mixed", "mixed"),
+                                      ("prefill_short_chunk", "plain"), ("prefill_short_chunk", "split")])
+def test_prefill_workloads_every_sequence(tag, mode):
     """The benchmark's prefill workloads at full size, in the benchmark's launch
     configuration.  Every sequence is compared with the oracle on whole query
     tiles (128 / G tokens x the G heads of each KV head, the unit the kernel
@@ -254,10 +255,13 @@ def test_prefill_workloads_every_sequence(tag, mixed):
     from paged_kv_cache_276_gb300.workloads import PrefillCase
     case = PrefillCase(inputs.PREFILL_WORKLOADS[tag], "cuda")
     st = status_tensor()
-    if mixed:  # the benchmark's launch: decodes over their work list beside the chunks
+    if mode == "mixed":  # the benchmark's launch: decodes over their work list beside the chunks
         case.prepare_mixed()
         assert case.mixed_nd == 256 and 76 <= case.mixed_ctas <= 152
         case.attend_mixed(st)
+    elif mode == "split":  # the benchmark's launch: the keys split into partitions
+        case.prepare_split(inputs.PREFILL_WORKLOADS[tag].extra["split"])
+        case.attend_split(st)
     else:
         case.attend(st)
     torch.cuda.synchronize()
