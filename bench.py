@@ -79,9 +79,11 @@ def _source_sha(parts):
 
 
 HOST_MARK = b"// ------------------------------------------------------------------ host"
-# the device code each traffic record covers
+COMBINE_MARK = b"// ---------------------------------------------- cross-partition combine"
+# the device code each traffic record covers (the decode record: decode.cu up to
+# its split-K merge kernel, whose code does not change the main kernel's traffic)
 TRAFFIC_SOURCES = {
-    "decode_kernel_traffic.txt": [("decode.cu", HOST_MARK), ("attend.cuh", None), ("ptx.cuh", None)],
+    "decode_kernel_traffic.txt": [("decode.cu", COMBINE_MARK), ("attend.cuh", None), ("ptx.cuh", None)],
     "chunk_tc_kernel_traffic.txt": [("chunk_tc.cu", HOST_MARK), ("tc.cuh", None), ("ptx.cuh", None)],
 }
 

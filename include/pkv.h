@@ -253,11 +253,14 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
  *                 block_size] (else PKV_ERR_RANGE)
  *   block_tables  host, [num_seqs][max_blocks_per_seq] int32, or NULL
  *   items_out     host, [1 + max_items][4] int32: row 0 = {count, partition
- *                 size used, 0, 0}, rows 1..count the items.  Pass row 0's
- *                 partition size to paged_attention_decode_items.
- * *num_items receives the count (also when it exceeds max_items, which
- * returns PKV_ERR_RANGE and writes no item).  A partition_size that is not a
- * multiple of block_size returns PKV_ERR_ARG.
+ *                 size used, m, 1 + count}, rows 1..count the items, then
+ *                 the m sequences with more than one partition (those the
+ *                 split-K merge combines), four to a row, -1 after the last.
+ *                 Pass row 0's partition size to paged_attention_decode_items.
+ * *num_items receives the rows after the header, count + ceil(m / 4) (also
+ * when they exceed max_items, which returns PKV_ERR_RANGE and writes
+ * nothing).  A partition_size that is not a multiple of block_size returns
+ * PKV_ERR_ARG.
  */
 int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int max_blocks_per_seq,
                      int num_seqs, int num_kv_heads, int head_dim, int block_size,
@@ -267,12 +270,14 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
  * paged_attention_decode_items -- the single-token decode over a work list:
  * paged_attention_decode_write (or, with k_new, v_new and slot_mapping all
  * NULL, paged_attention_decode with q_len = 1), one CTA per item.
- *   items       device, 16-byte aligned, [1 + grid_items][4] int32: the rows
- *               pkv_decode_items wrote for these seq_lens and block_tables
- *               (row 0 holds the count); partition_size must be the size the
- *               list was built for (row 0's second entry)
+ *   items       device, 16-byte aligned, [1 + grid_items][4] int32 (at least
+ *               the rows pkv_decode_items wrote for these seq_lens and
+ *               block_tables); partition_size must be the size the list was
+ *               built for (row 0's second entry).  The split-K merge runs over
+ *               the list's merge rows only.
  *   grid_items  CTAs to launch, >= the count in row 0 (CTAs past the count do
- *               nothing), so a CUDA graph can be captured for a bound
+ *               nothing; the rows after the header are a valid choice), so a
+ *               CUDA graph can be captured for a bound
  * Every other argument and the result are those of paged_attention_decode_write.
  * An item naming a sequence, head or partition out of range, a length other
  * than seq_lens[sequence], or a first block other than the table's sets

@@ -587,14 +587,33 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
 }
 
 // ---------------------------------------------- cross-partition combine
-// One warp per (sequence, query row): the exact merge of its partitions.
+// One warp per (sequence, query row): the exact merge of its partitions.  Over
+// a work list only the sequences the list names (those with more than one
+// partition) are merged, by a grid of a few CTAs per SM looping over their rows.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const Params p, int block_size, int total_rows,
                                                       int rows) {
   grid_launch_dependents();
   grid_dependency_wait();  // the partials come from the grid launched just before
-  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (p.items) {
+    const int4 hdr = p.items[0];
+    const int *list = reinterpret_cast<const int *>(p.items + hdr.w);
+    const long long n = static_cast<long long>(hdr.z) * rows;
+    for (long long w = blockIdx.x * 4ll + (threadIdx.x >> 5); w < n; w += gridDim.x * 4ll) {
+      const int k = static_cast<int>(w / rows), r = static_cast<int>(w - static_cast<long long>(k) * rows);
+      const int seq = list[k];
+      if (seq < 0 || seq >= p.num_seqs) continue;
+      const int L = clamp_len(p, seq, block_size, false);
+      const int part_tokens = p.part_blocks * block_size;
+      const int nparts = L > 0 ? (L + part_tokens - 1) / part_tokens : 1;
+      if (nparts <= 1) continue;
+      const size_t wg = static_cast<size_t>(seq) * rows + r;
+      merge_partials<D>(p.ws_ml + wg * p.max_parts, p.ws_o + wg * p.max_parts * D, nparts, p.out + wg * D, lane);
+    }
+    return;
+  }
+  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (wg >= total_rows) return;
   const int seq = wg / rows;
   const int L = clamp_len(p, seq, block_size, false);
@@ -721,7 +740,9 @@ int launch(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p, int 
   if (p.max_parts <= 1) return PKV_OK;
   const int rows = q_len * p.num_q_heads;
   const int total = num_seqs * rows;
-  e = launch_pdl(combine_kernel<D>, dim3((total + 3) / 4), dim3(128), 0, stream, p, BS, total, rows);
+  // over a work list the merge loops over the listed sequences' rows: a few CTAs per SM at most
+  const int ctas = p.items ? std::min((total + 3) / 4, 2 * num_sms()) : (total + 3) / 4;
+  e = launch_pdl(combine_kernel<D>, dim3(ctas), dim3(128), 0, stream, p, BS, total, rows);
   if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
   return PKV_OK;
 }
@@ -901,16 +922,19 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
     }
     if (part == 0) part = pkv::kDefaultPartition;
   }
-  long long count = 0;
+  long long count = 0, merges = 0;
   for (int i = 0; i < num_seqs; ++i) {
     const int L = seq_lens[i];
     const long long np = L > 0 ? (static_cast<long long>(L) + part - 1) / part : 1;
     if (np > 65535) return PKV_ERR_UNSUPPORTED;
     count += np * num_kv_heads;
+    merges += np > 1;
   }
-  if (count > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
-  *num_items = static_cast<int>(count);
-  if (count > max_items) return PKV_ERR_RANGE;
+  // rows after the header: the items, then the merge list, four sequences a row
+  const long long rows = count + (merges + 3) / 4;
+  if (rows > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
+  *num_items = static_cast<int>(rows);
+  if (rows > max_items) return PKV_ERR_RANGE;
   struct Piece {
     int ntok, seq, part, len;
   };
@@ -930,7 +954,8 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
   int32_t *o = items_out;
   o[0] = static_cast<int32_t>(count);
   o[1] = part;  // the partition the list was built for: pass it to the decode
-  o[2] = o[3] = 0;
+  o[2] = static_cast<int32_t>(merges);      // sequences whose partitions the merge combines
+  o[3] = static_cast<int32_t>(1 + count);   // the row where their list starts
   o += 4;
   const long long part_blocks = part / block_size;
   for (const Piece &pc : pieces) {
@@ -945,6 +970,9 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
       o[3] = b0;
     }
   }
+  for (long long i = 0; i < (merges + 3) / 4 * 4; ++i) o[i] = -1;
+  for (int i = 0, k = 0; i < num_seqs; ++i)
+    if (seq_lens[i] > part) o[k++] = i;
   return PKV_OK;
 }
 

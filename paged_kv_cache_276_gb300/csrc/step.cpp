@@ -155,7 +155,9 @@ int pkv_step_layout_of(const pkv_step_config *c, pkv_step_layout *o) {
   o->stage_bytes = after_lens;
   if (c->q_len == 1) {  // the decode's work list: at most every sequence's partitions x KV heads
     const int part = c->partition_size > 0 ? c->partition_size : kDefaultPartition;
-    const long long items = static_cast<long long>(c->max_seqs) * c->num_kv_heads * ((cap + part - 1) / part);
+    // rows after the list's header: every sequence's partitions x KV heads, then the merge list
+    const long long items = static_cast<long long>(c->max_seqs) * c->num_kv_heads * ((cap + part - 1) / part) +
+                            (c->max_seqs + 3) / 4;
     if (items > 0x7ffffffell) return PKV_ERR_ARG;
     o->items_offset = after_lens;
     o->max_items = static_cast<int>(items);
@@ -259,6 +261,7 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
                                want, items, s->lay.max_items, &count)) != PKV_OK)
       return rc;
     partition = items[1];
+    count = items[0];  // the merge list follows the items; the decode's grid is the items
     if (c.partition_size == 0) {
       s->auto_age = want == 0 ? 0 : s->auto_age + 1;
       s->auto_part = partition;

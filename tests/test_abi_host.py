@@ -452,7 +452,8 @@ def test_decode_work_list_is_longest_first_and_complete(native):
     tables[2, :63] = np.arange(100, 163)
     tables[3, :48] = np.arange(200, 248)
     items = native.pkv_decode_items(lens, tables, num_kv_heads=2, block_size=16, partition_size=768)
-    assert items[0].tolist() == [10, 768, 0, 0]
+    # header: 10 items, partition 768, one sequence to merge, its list at row 11
+    assert items[0].tolist() == [10, 768, 1, 11] and items.shape == (12, 4)
 
     def it(seq, part, h, L, b0):
         return [seq, h | (part << 16), L, b0]
@@ -461,9 +462,10 @@ def test_decode_work_list_is_longest_first_and_complete(native):
             it(2, 1, 0, 1000, 148), it(2, 1, 1, 1000, 148),   # 232 tokens, from logical block 48
             it(1, 0, 0, 5, 7), it(1, 0, 1, 5, 7),             # 5 tokens
             it(0, 0, 0, 0, -1), it(0, 0, 1, 0, -1)]           # empty: zeros
-    assert items[1:].tolist() == want
+    assert items[1:11].tolist() == want
+    assert items[11].tolist() == [2, -1, -1, -1]  # sequence 2 spans two partitions
     # without tables the first block is unknown (-1)
-    assert native.pkv_decode_items(lens, None, 2, 16, 768)[1:, 3].tolist() == [-1] * 10
+    assert native.pkv_decode_items(lens, None, 2, 16, 768)[1:11, 3].tolist() == [-1] * 10
     # a length past the table, a partition that is not a multiple of the block, no room
     lib = native.lib()
     n = ctypes.c_int(0)
@@ -473,8 +475,8 @@ def test_decode_work_list_is_longest_first_and_complete(native):
                                 ctypes.byref(n)) == native.PKV_ERR_RANGE
     assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 128, 16, 24, buf.ctypes.data, 10,
                                 ctypes.byref(n)) == native.PKV_ERR_ARG
-    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 128, 16, 768, buf.ctypes.data, 9,
-                                ctypes.byref(n)) == native.PKV_ERR_RANGE and n.value == 10
+    assert lib.pkv_decode_items(lens.ctypes.data, None, 70, 4, 2, 128, 16, 768, buf.ctypes.data, 10,
+                                ctypes.byref(n)) == native.PKV_ERR_RANGE and n.value == 11  # items + merge row
 
 
 def test_decode_work_list_chooses_its_partition():

@@ -805,8 +805,8 @@ def test_decode_items_equals_the_grid_decode_bit_exact(d, bs, Hq, Hkv, part):
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
     items = native.pkv_decode_items(np.asarray(lens, dtype=np.int32), tables, Hkv, bs, part, d)
     count, part = int(items[0, 0]), int(items[0, 1])  # part 0: the size the list chose
-    padded = np.zeros((1 + count + 37, 4), dtype=np.int32)  # a grid of count + 37 CTAs
-    padded[:1 + count] = items
+    padded = np.zeros((items.shape[0] + 37, 4), dtype=np.int32)  # room for a grid of 37 more CTAs
+    padded[:items.shape[0]] = items
     items_d = torch.as_tensor(padded, device="cuda")
     st = status_tensor()
     kc2, vc2 = kc.clone(), vc.clone()
@@ -826,7 +826,8 @@ def test_decode_items_equals_the_grid_decode_bit_exact(d, bs, Hq, Hkv, part):
     native.paged_attention_decode(q, kc, vc, tables_d, lens_d, max_len, 0.09, ref2, ws, part, st)
     got2 = torch.full_like(q, float("nan"))
     native.paged_attention_decode_items(q, None, None, None, kc, vc, tables_d, lens_d, max_len, 0.09, got2, items_d,
-                                        grid_items=count + 37, workspace=ws, partition_size=part, d_status=st)
+                                        grid_items=padded.shape[0] - 1, workspace=ws, partition_size=part,
+                                        d_status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert torch.equal(got2.view(torch.int16), ref2.view(torch.int16))
