@@ -583,16 +583,19 @@ int pkv_refcount(const pkv_alloc *a, int block);
  *       layout.stage_bytes each, 16-byte aligned.  The caller writes each
  *       step's inputs into host_stage; the runner writes the slots, tables and
  *       lengths into it and copies all of it to dev_stage in one copy.
- *       Segments (byte offsets; every segment starts on a 256-byte boundary):
- *         queries of layer l  q_offset + l * q_layer_bytes,
- *                             [max_seqs][q_len][num_q_heads][head_dim] bf16
- *         new keys of layer l k_offset + l * kv_layer_bytes,
- *         new values          v_offset + l * kv_layer_bytes,
- *                             [max_seqs * q_len][num_kv_heads][head_dim] bf16
+ *       Segments (byte offsets; every segment starts on a 256-byte boundary),
+ *       first those every layer reads, then the layers one after the other:
  *         slots               slots_offset, [max_seqs * q_len] int64
  *         block tables        tables_offset, [max_seqs][max_blocks_per_seq] int32
  *         lengths             lens_offset, [max_seqs] int32
  *         work list (q_len 1) items_offset, [1 + max_items][4] int32
+ *         queries of layer l  q_offset + l * layer_stride,
+ *                             [max_seqs][q_len][num_q_heads][head_dim] bf16
+ *                             (q_layer_bytes)
+ *         new keys of layer l k_offset + l * layer_stride,
+ *         new values          v_offset + l * layer_stride,
+ *                             [max_seqs * q_len][num_kv_heads][head_dim] bf16
+ *                             (kv_layer_bytes each)
  *       A run over n sequences uses the first n rows of each segment; the
  *       runner writes the work list itself.
  *   dev_out / host_out      device and page-locked host memory of
@@ -634,6 +637,7 @@ typedef struct {
   size_t workspace_bytes;
   size_t items_offset;     /* q_len 1: the decode's work list (pkv_decode_items), 0 otherwise */
   int max_items;           /* rows of that list after its header */
+  size_t layer_stride;     /* bytes from one layer's queries, keys, values to the next layer's */
 } pkv_step_layout;
 
 typedef struct pkv_step pkv_step;
@@ -664,10 +668,16 @@ void pkv_step_destroy(pkv_step *s);
  *   3. pkv_seq_append_batch of q_len tokens each (its errors are returned and
  *      change nothing), slots into host_stage; pkv_block_table of the n
  *      sequences into host_stage;
- *   4. enqueue on `stream`: host_stage -> dev_stage, for each layer l the
- *      pkv_write of its n * q_len new keys and values and the
+ *   4. enqueue: the common segments and layer 0's inputs host_stage ->
+ *      dev_stage, then each further layer's inputs, on a copy stream of the
+ *      runner's own; on `stream`, for each layer l once its inputs have
+ *      landed, the pkv_write of its n * q_len new keys and values and the
  *      paged_attention_decode of its n query rows (q_len = 1: both as one
- *      paged_attention_decode_write), dev_out -> host_out.
+ *      paged_attention_decode_items over the step's work list); each layer's
+ *      output dev_out -> host_out on the copy stream as soon as its kernels
+ *      finish.  The copies of one layer overlap the kernels of the others;
+ *      `stream` waits for the last output copy, so the step is complete on
+ *      `stream` (for events or graphs) as before.
  * Returns after the enqueue.  The caller writes the step's queries, keys and
  * values for rows 0..n-1 into host_stage before the call, and may touch
  * host_stage and host_out again only after pkv_step_wait (or a synchronisation

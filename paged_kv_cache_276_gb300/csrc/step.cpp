@@ -50,7 +50,10 @@ struct pkv_step {
   int32_t *status = nullptr;
   int part = kDefaultPartition;
   cudaStream_t cap = nullptr;
+  cudaStream_t copy = nullptr;  // the step's host <-> device copies, beside the kernels
   cudaEvent_t done = nullptr;
+  cudaEvent_t start = nullptr, copied_out = nullptr;
+  std::vector<cudaEvent_t> layer_in, layer_done;  // per layer: its inputs landed, its kernels finished
   bool pending = false;
   std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;  // (n, partitions, partition size)
   int auto_part = 0, auto_n = 0, auto_age = 0;  // the work list's partition pick, kept between steps
@@ -63,21 +66,38 @@ void drop_graphs(pkv_step *s) {
   s->graphs.clear();
 }
 
-// Copy in, every layer's write and decode, copy out, on `st`.  q_len 1: the
-// decode runs grid_items CTAs over the work list in the staging buffer.
+// One step on `st`: the common inputs (slots, tables, lengths, work list) and
+// each layer's queries, keys and values go to the device on the runner's copy
+// stream, layer after layer, while the kernels of the layers already copied run
+// on `st`; each layer's output goes back as soon as its kernels finish.  So the
+// copies overlap the kernels instead of preceding and following all of them.
+// q_len 1: the decode runs grid_items CTAs over the work list in the staging buffer.
 int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items, int partition) {
   const pkv_step_config &c = s->cfg;
   const pkv_step_layout &L = s->lay;
-  cudaError_t e = cudaMemcpyAsync(s->ds, s->hs, L.stage_bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  cudaError_t e;
+  auto fail = [](cudaError_t err) { return pkv::set_cuda_error(err), PKV_ERR_CUDA; };
+  // the copies may overwrite the staging buffers only after the work before this step
+  if ((e = cudaEventRecord(s->start, st)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(s->copy, s->start, 0)) != cudaSuccess) return fail(e);
+  for (int l = 0; l < c.num_layers; ++l) {
+    // layer 0 comes with the common segment in front of it
+    const size_t lo = l == 0 ? 0 : L.q_offset + l * L.layer_stride;
+    const size_t hi = L.q_offset + (l + 1) * L.layer_stride;
+    if ((e = cudaMemcpyAsync(s->ds + lo, s->hs + lo, hi - lo, cudaMemcpyHostToDevice, s->copy)) != cudaSuccess)
+      return fail(e);
+    if ((e = cudaEventRecord(s->layer_in[l], s->copy)) != cudaSuccess) return fail(e);
+  }
   const auto *slots = reinterpret_cast<const int64_t *>(s->ds + L.slots_offset);
   const auto *tables = reinterpret_cast<const int32_t *>(s->ds + L.tables_offset);
   const auto *lens = reinterpret_cast<const int32_t *>(s->ds + L.lens_offset);
   for (int l = 0; l < c.num_layers; ++l) {
-    const auto *q = reinterpret_cast<const pkv_bf16 *>(s->ds + L.q_offset + l * L.q_layer_bytes);
-    const auto *kn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.k_offset + l * L.kv_layer_bytes);
-    const auto *vn = reinterpret_cast<const pkv_bf16 *>(s->ds + L.v_offset + l * L.kv_layer_bytes);
+    const char *layer = s->ds + L.q_offset + l * L.layer_stride;
+    const auto *q = reinterpret_cast<const pkv_bf16 *>(layer);
+    const auto *kn = reinterpret_cast<const pkv_bf16 *>(layer + (L.k_offset - L.q_offset));
+    const auto *vn = reinterpret_cast<const pkv_bf16 *>(layer + (L.v_offset - L.q_offset));
     auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
+    if ((e = cudaStreamWaitEvent(st, s->layer_in[l], 0)) != cudaSuccess) return fail(e);
     int rc;
     if (c.q_len == 1) {  // the allocator's slots are the newest tokens' table positions: one grid
       const auto *items = reinterpret_cast<const int32_t *>(s->ds + L.items_offset);
@@ -94,9 +114,15 @@ int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items
                                   c.scale, c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
     }
     if (rc != PKV_OK) return rc;
+    if ((e = cudaEventRecord(s->layer_done[l], st)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(s->copy, s->layer_done[l], 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaMemcpyAsync(s->hout + l * L.out_layer_bytes, s->dout + l * L.out_layer_bytes, L.out_layer_bytes,
+                             cudaMemcpyDeviceToHost, s->copy)) != cudaSuccess)
+      return fail(e);
   }
-  e = cudaMemcpyAsync(s->hout, s->dout, L.out_bytes, cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+  // the step ends on `st` once its last output has landed
+  if ((e = cudaEventRecord(s->copied_out, s->copy)) != cudaSuccess) return fail(e);
+  if ((e = cudaStreamWaitEvent(st, s->copied_out, 0)) != cudaSuccess) return fail(e);
   return PKV_OK;
 }
 
@@ -143,26 +169,28 @@ int pkv_step_layout_of(const pkv_step_config *c, pkv_step_layout *o) {
   const size_t qb = up256(r * c->num_q_heads * c->head_dim * 2);
   const size_t kvb = up256(r * c->num_kv_heads * c->head_dim * 2);
   std::memset(o, 0, sizeof(*o));
-  o->q_offset = 0;
-  o->q_layer_bytes = qb;
-  o->kv_layer_bytes = kvb;
-  o->k_offset = o->q_offset + c->num_layers * qb;
-  o->v_offset = o->k_offset + c->num_layers * kvb;
-  o->slots_offset = o->v_offset + c->num_layers * kvb;
+  // the segments every layer reads come first, then each layer's queries, keys and values
+  o->slots_offset = 0;
   o->tables_offset = o->slots_offset + up256(r * sizeof(int64_t));
   o->lens_offset = o->tables_offset + up256(static_cast<size_t>(c->max_seqs) * c->max_blocks_per_seq * 4);
-  const size_t after_lens = o->lens_offset + up256(static_cast<size_t>(c->max_seqs) * 4);
-  o->stage_bytes = after_lens;
+  size_t common = o->lens_offset + up256(static_cast<size_t>(c->max_seqs) * 4);
   if (c->q_len == 1) {  // the decode's work list: at most every sequence's partitions x KV heads
     const int part = c->partition_size > 0 ? c->partition_size : kDefaultPartition;
     // rows after the list's header: every sequence's partitions x KV heads, then the merge list
     const long long items = static_cast<long long>(c->max_seqs) * c->num_kv_heads * ((cap + part - 1) / part) +
                             (c->max_seqs + 3) / 4;
     if (items > 0x7ffffffell) return PKV_ERR_ARG;
-    o->items_offset = after_lens;
+    o->items_offset = common;
     o->max_items = static_cast<int>(items);
-    o->stage_bytes = after_lens + up256(static_cast<size_t>(items + 1) * 16);
+    common += up256(static_cast<size_t>(items + 1) * 16);
   }
+  o->q_layer_bytes = qb;
+  o->kv_layer_bytes = kvb;
+  o->layer_stride = qb + 2 * kvb;
+  o->q_offset = common;
+  o->k_offset = o->q_offset + qb;
+  o->v_offset = o->k_offset + kvb;
+  o->stage_bytes = common + c->num_layers * o->layer_stride;
   o->out_layer_bytes = qb;
   o->out_bytes = c->num_layers * qb;
   o->workspace_bytes = paged_attention_workspace_size(c->max_seqs, c->q_len, c->num_q_heads, c->head_dim,
@@ -203,10 +231,20 @@ int pkv_step_create(const pkv_step_config *cfg, pkv_alloc *alloc, pkv_bf16 *cons
   s->ws_bytes = workspace_bytes;
   s->status = d_status;
   s->part = cfg->partition_size > 0 ? cfg->partition_size : kDefaultPartition;
-  const cudaError_t e = cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming);
+  cudaError_t e = cudaEventCreateWithFlags(&s->done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->copied_out, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
+  s->layer_in.assign(cfg->num_layers, nullptr);
+  s->layer_done.assign(cfg->num_layers, nullptr);
+  for (int l = 0; l < cfg->num_layers && e == cudaSuccess; ++l) {
+    e = cudaEventCreateWithFlags(&s->layer_in[l], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->layer_done[l], cudaEventDisableTiming);
+  }
   if (e != cudaSuccess) {
-    delete s;
-    return pkv::set_cuda_error(e), PKV_ERR_CUDA;
+    pkv::set_cuda_error(e);
+    pkv_step_destroy(s);
+    return PKV_ERR_CUDA;
   }
   *out = s;
   return PKV_OK;
@@ -226,7 +264,13 @@ void pkv_step_destroy(pkv_step *s) {
   pkv_step_wait(s);
   drop_graphs(s);
   if (s->cap) cudaStreamDestroy(s->cap);
-  if (s->done) cudaEventDestroy(s->done);
+  if (s->copy) cudaStreamDestroy(s->copy);
+  for (cudaEvent_t ev : {s->done, s->start, s->copied_out})
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : s->layer_in)
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : s->layer_done)
+    if (ev) cudaEventDestroy(ev);
   delete s;
 }
 

@@ -50,7 +50,7 @@ class StepLayout(ctypes.Structure):
     _fields_ = [(n, _c_size) for n in ("q_offset", "q_layer_bytes", "k_offset", "v_offset", "kv_layer_bytes",
                                        "slots_offset", "tables_offset", "lens_offset", "stage_bytes",
                                        "out_layer_bytes", "out_bytes", "workspace_bytes", "items_offset")] \
-        + [("max_items", _c_int)]
+        + [("max_items", _c_int), ("layer_stride", _c_size)]
 
 
 # name -> (restype, argtypes); mirrors include/pkv.h
@@ -657,15 +657,15 @@ class DecodeStep:
         return buf[off:off + n * torch.empty((), dtype=dtype).element_size()].view(dtype).view(shape)
 
     def q(self, layer):
-        return self._view(self.host_stage, self.layout.q_offset + layer * self.layout.q_layer_bytes,
+        return self._view(self.host_stage, self.layout.q_offset + layer * self.layout.layer_stride,
                           torch.bfloat16, self._q_shape)
 
     def k(self, layer):
-        return self._view(self.host_stage, self.layout.k_offset + layer * self.layout.kv_layer_bytes,
+        return self._view(self.host_stage, self.layout.k_offset + layer * self.layout.layer_stride,
                           torch.bfloat16, self._kv_shape)
 
     def v(self, layer):
-        return self._view(self.host_stage, self.layout.v_offset + layer * self.layout.kv_layer_bytes,
+        return self._view(self.host_stage, self.layout.v_offset + layer * self.layout.layer_stride,
                           torch.bfloat16, self._kv_shape)
 
     def out(self, layer):

@@ -384,14 +384,21 @@ def test_step_layout_host_only(native):
     assert native.lib().pkv_step_layout_of(ctypes.byref(cfg), ctypes.byref(lay)) == native.PKV_OK
     up = lambda x: -(-x // 256) * 256  # noqa: E731
     assert lay.q_layer_bytes == up(B * ql * Hq * d * 2) and lay.kv_layer_bytes == up(B * ql * Hkv * d * 2)
-    segs = [(lay.q_offset, L * lay.q_layer_bytes), (lay.k_offset, L * lay.kv_layer_bytes),
-            (lay.v_offset, L * lay.kv_layer_bytes), (lay.slots_offset, B * ql * 8),
-            (lay.tables_offset, B * mb * 4), (lay.lens_offset, B * 4)]
+    # the segments every layer reads, then each layer's queries, keys and values
+    segs = [(lay.slots_offset, B * ql * 8), (lay.tables_offset, B * mb * 4), (lay.lens_offset, B * 4),
+            (lay.items_offset, (1 + lay.max_items) * 16)]
+    for l in range(L):
+        segs += [(lay.q_offset + l * lay.layer_stride, lay.q_layer_bytes),
+                 (lay.k_offset + l * lay.layer_stride, lay.kv_layer_bytes),
+                 (lay.v_offset + l * lay.layer_stride, lay.kv_layer_bytes)]
     end = 0
     for off, size in segs:  # in order, 256-byte aligned, not overlapping
         assert off % 256 == 0 and off >= end
         end = off + size
     assert lay.stage_bytes >= end and lay.stage_bytes % 256 == 0
+    assert lay.layer_stride == lay.q_layer_bytes + 2 * lay.kv_layer_bytes
+    # the work list holds every sequence's partitions x KV heads and the merge list
+    assert lay.max_items == B * Hkv * -(-(mb * 16) // 768) + -(-B // 4)
     assert lay.out_layer_bytes == lay.q_layer_bytes and lay.out_bytes == L * lay.q_layer_bytes
     assert lay.workspace_bytes == native.paged_attention_workspace_size(B, ql, Hq, d, mb * 16, 768)
     for field, bad in (("num_layers", 0), ("max_seqs", 0), ("q_len", 0), ("block_size", 0),
