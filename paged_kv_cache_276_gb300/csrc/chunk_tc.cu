@@ -308,17 +308,20 @@ __device__ __forceinline__ float extreme64(const uint32_t (&v)[64], bool neg) {
 }
 
 // Weights of 64 raw scores, p = 2^(s * scale * log2e - m), two at a time with a
-// packed fp32 FMA, packed to bf16 pairs; returns the sum of the rounded
-// weights (the P V product uses the same rounded values).  Masked keys hold
-// -inf (or +inf for a negative scale): their weight is 2^-inf = 0.
+// packed fp32 FMA, packed to bf16 pairs; returns the sum of the weights before
+// their rounding to bf16 (the rounding errors, at most 2^-9 of each weight and
+// of either sign, leave the sum's relative error far below the output's bf16
+// step).  Masked keys hold -inf (or +inf for a negative scale): their weight
+// is 2^-inf = 0.
 __device__ __forceinline__ float weights64(const uint32_t (&v)[64], uint64_t ks2, uint64_t nm2, uint32_t (&pk)[32]) {
   uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (0 bits = +0.0)
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     float x0, x1;
     f32x2_split(ffma2(f32x2_bits(v[2 * c], v[2 * c + 1]), ks2, nm2), x0, x1);
-    pk[c] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-    ls[c & 3] = fadd2(ls[c & 3], bf16x2_to_f32x2(pk[c]));
+    const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+    pk[c] = pack_bf16x2(e0, e1);
+    ls[c & 3] = fadd2(ls[c & 3], f32x2_bits(__float_as_uint(e0), __float_as_uint(e1)));
   }
   float a0, a1, b0, b1, c0, c1, d0, d1;
   f32x2_split(ls[0], a0, a1);
@@ -891,44 +894,80 @@ __global__ void __launch_bounds__(kThreads, 1)
               publish(B_P_FULL0 + sb);
               mbar_arrive(bar(B_P_LO0 + sb));
             } else {
-              uint32_t sv[64];
-              // pass 1: the row's extreme raw score, 64 columns at a time
-              float rm = neg ? INFINITY : -INFINITY;
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+              if constexpr (kP2) {
+                // the row's 128 scores in one load round; once all are in
+                // registers the weights may go over the buffer's upper half
+                uint32_t sl[64], sh[64];
+                tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sl[0]));
+                tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sl[32]));
+                tc::ld32(tSb + 64, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
+                tc::ld32(tSb + 96, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
                 tc::wait_ld();
-                mask(sv, hh * 64);
-                const float e = extreme64(sv, neg);
-                rm = neg ? fminf(rm, e) : fmaxf(rm, e);
+                mask(sl, 0);
+                mask(sh, 64);
+                const float el = extreme64(sl, neg), eh = extreme64(sh, neg);
+                const float msub = new_reference(neg ? fminf(el, eh) : fmaxf(el, eh));
+                const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+                const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
+                // keys 64..127 first: their P V product starts while keys
+                // 0..63 are weighted
+                uint32_t pk[32];
+                float lsum = weights64(sh, ks2, nm2, pk);
+                tc::st32(tPb + 32, pk);
+                // the set's previous P V product completed before this tile's
+                // score product was issued (the score product waited for it), and
+                // none of this tile's is issued before P_FULL: the accumulator
+                // holds its final value and may be rescaled here
+                rescale_o();
+                if (!zero_tail_values()) { ok = false; break; }
+                publish(B_P_FULL0 + sb);
+                lsum += weights64(sl, ks2, nm2, pk);
+                tc::st32(tPb, pk);
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(bar(B_P_LO0 + sb));
+                l += lsum;
+              } else {
+                // two load rounds (fewer registers, for the single-tile
+                // schedule): the maximum over both halves, then the weights of
+                // keys 64..127 from the scores still in registers and of keys
+                // 0..63 after reloading them
+                uint32_t sv[64];
+                // pass 1: the row's extreme raw score, 64 columns at a time
+                float rm = neg ? INFINITY : -INFINITY;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  tc::ld32(tSb + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                  tc::ld32(tSb + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                  tc::wait_ld();
+                  mask(sv, hh * 64);
+                  const float e = extreme64(sv, neg);
+                  rm = neg ? fminf(rm, e) : fmaxf(rm, e);
+                }
+                const float msub = new_reference(rm);
+                const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
+                const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
+                // pass 2, keys 64..127 first (their scores are still in
+                // registers): weights over score columns 96..127, already read;
+                // their P V product starts while keys 0..63 are weighted
+                uint32_t pk[32];
+                float lsum = weights64(sv, ks2, nm2, pk);
+                tc::st32(tPb + 32, pk);
+                rescale_o();
+                if (!zero_tail_values()) { ok = false; break; }
+                publish(B_P_FULL0 + sb);
+                // keys 0..63: weights over score columns 64..95
+                tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                tc::wait_ld();
+                mask(sv, 0);
+                lsum += weights64(sv, ks2, nm2, pk);
+                tc::st32(tPb, pk);
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(bar(B_P_LO0 + sb));
+                l += lsum;
               }
-              const float msub = new_reference(rm);
-              const uint64_t ks2 = f32x2_bits(__float_as_uint(p.scale_log2), __float_as_uint(p.scale_log2));
-              const uint64_t nm2 = f32x2_bits(__float_as_uint(-msub), __float_as_uint(-msub));
-              // pass 2, keys 64..127 first (their scores are still in
-              // registers): weights over score columns 96..127, already read;
-              // their P V product starts while keys 0..63 are weighted
-              uint32_t pk[32];
-              float lsum = weights64(sv, ks2, nm2, pk);
-              tc::st32(tPb + 32, pk);
-              // the set's previous P V product completed before this tile's
-              // score product was issued (the score product waited for it), and
-              // none of this tile's is issued before P_FULL: the accumulator is still
-              rescale_o();
-              if (!zero_tail_values()) { ok = false; break; }
-              publish(B_P_FULL0 + sb);
-              // keys 0..63: weights over score columns 64..95
-              tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-              tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-              tc::wait_ld();
-              mask(sv, 0);
-              lsum += weights64(sv, ks2, nm2, pk);
-              tc::st32(tPb, pk);
-              tc::wait_st();
-              tc::fence_before();
-              mbar_arrive(bar(B_P_LO0 + sb));
-              l += lsum;
             }
           } else {
             uint32_t pk[32];
