@@ -281,6 +281,14 @@ struct Sched {
   }
 };
 
+// 32 bytes from eight 32-bit registers to global memory in one request
+// (256-bit store, sm_100+); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]),
+               "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // The largest (smallest, for a negative scale) of 64 raw scores: eight short
 // chains of 3-input maxima.
 __device__ __forceinline__ float extreme64(const uint32_t (&v)[64], bool neg) {
@@ -1022,15 +1030,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::wait_ld();
             }
             if (!row_valid) continue;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + ch * 32);
+            // a thread writes its own row: each store instruction touches one
+            // line per lane, so 32-byte stores (when the output allows) halve
+            // the requests of this epilogue, which sits between a set's items
+            __nv_bfloat16 *dst = p.out + orow * D + ch * 32;
+            uint32_t w[16];
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 0]) * inv, __uint_as_float(ov[c8 * 8 + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 2]) * inv, __uint_as_float(ov[c8 * 8 + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 4]) * inv, __uint_as_float(ov[c8 * 8 + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(ov[c8 * 8 + 6]) * inv, __uint_as_float(ov[c8 * 8 + 7]) * inv);
-              dst[c8] = v;
+            for (int c = 0; c < 16; ++c)
+              w[c] = pack_bf16x2(__uint_as_float(ov[2 * c]) * inv, __uint_as_float(ov[2 * c + 1]) * inv);
+            if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
+#pragma unroll
+              for (int h8 = 0; h8 < 2; ++h8) st_global_v8(dst + h8 * 16, &w[8 * h8]);
+            } else {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8)
+                reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
             }
           }
           if (run_has_tiles) {
@@ -1085,15 +1099,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ov[c] = (fa != 0.f ? fa * __uint_as_float(ta[c]) : 0.f) + (fb != 0.f ? fb * __uint_as_float(tb[c]) : 0.f);
           if (!row_valid) continue;  // a spare row of the tile: nothing to store
           if (nparts == 1) {
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D + ch * 32);
+            __nv_bfloat16 *dst = p.out + orow * D + ch * 32;
+            uint32_t w[16];
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint4 v;
-              v.x = pack_bf16x2(ov[c8 * 8 + 0] * inv, ov[c8 * 8 + 1] * inv);
-              v.y = pack_bf16x2(ov[c8 * 8 + 2] * inv, ov[c8 * 8 + 3] * inv);
-              v.z = pack_bf16x2(ov[c8 * 8 + 4] * inv, ov[c8 * 8 + 5] * inv);
-              v.w = pack_bf16x2(ov[c8 * 8 + 6] * inv, ov[c8 * 8 + 7] * inv);
-              dst[c8] = v;
+            for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(ov[2 * c] * inv, ov[2 * c + 1] * inv);
+            if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {  // 32-byte stores, as in the pairs' epilogue
+#pragma unroll
+              for (int h8 = 0; h8 < 2; ++h8) st_global_v8(dst + h8 * 16, &w[8 * h8]);
+            } else {
+#pragma unroll
+              for (int c8 = 0; c8 < 4; ++c8)
+                reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
             }
           } else {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + run_first_part) * D + ch * 32);

@@ -467,3 +467,23 @@ def test_mixed_step_entry_matches_the_oracle(ctas):
     assert_attention_close(out, ref, f"mixed step, chunks on {ctas or 'all'} CTAs")
     whole = run_prefill(q, kc, vc, tables, lens, q_start, scale)
     assert torch.allclose(out.float(), whole.float(), atol=1e-2, rtol=1e-2)
+
+
+def test_prefill_output_on_a_16_byte_boundary_matches_the_aligned_one():
+    """The epilogues write 32 bytes per store when the output is 32-byte
+    aligned and 16 bytes otherwise: an output 16 bytes past an aligned base
+    gets the same bits as the aligned one, for both schedules (pairs of query
+    tiles, and single tiles once empty sequences lower the mean chunk)."""
+    Hq, Hkv, bs, d = 64, 8, 16, 128
+    scale = float(np.float32(1 / math.sqrt(d)))
+    for lens, chunks in (([700, 300], [300, 256]), ([700, 300] + [9] * 40, [300, 256] + [0] * 40)):
+        q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=77)
+        aligned = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+        base = torch.empty(q.numel() + 8, dtype=q.dtype, device=q.device)
+        shifted = base[8:].view(q.shape)
+        assert shifted.data_ptr() % 32 == 16
+        shifted.view(torch.int16).fill_(CANARY)
+        run_prefill(q, kc, vc, tables, lens, q_start, scale, out=shifted)
+        assert torch.equal(aligned.view(torch.int16), shifted.view(torch.int16))
+        ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+        assert_attention_close(shifted, ref, "prefill into a 16-byte-aligned output")
