@@ -368,6 +368,37 @@ int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const
                                size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
+ * pkv_prefill_items -- host-built work list for the prefill's persistent grid:
+ * which of the batch's items (pairs of query tiles, or single tiles, per
+ * sequence and KV head, numbered as the kernel numbers them) each of grid
+ * CTAs takes.
+ *
+ * The pages have no counterpart; it balances the tensor-core work of a few
+ * long chunks over a grid smaller than the GPU (a continuous-batching step,
+ * x321.org "The serving bottleneck is not just FLOPs", section "Continuous
+ * batching is the other half of the story"), where CTA c taking items c,
+ * c + grid, ... can leave some CTAs one item longer than the rest.  Items are
+ * costed by their key tiles (a pair's two query tiles share each key tile)
+ * plus a fixed cost per item, then handed out longest first, each to the
+ * least-loaded CTA.
+ *   seq_lens       host [num_seqs] lengths (negative counts as 0)
+ *   q_start        host [num_seqs + 1] first query row of each sequence
+ *   total_q        the query rows of the call (as paged_attention_prefill;
+ *                  with q_start it decides pairs of query tiles or single ones)
+ *   num_q_heads, num_kv_heads  as paged_attention_prefill (group <= 16)
+ *   grid           CTAs of the launch (>= 1)
+ *   items_out      host [max_ints]: grid, n, the offsets of each CTA's range
+ *                  [grid + 1], then the n item indices
+ *   *num_ints      3 + grid + n
+ * Returns PKV_OK, PKV_ERR_ARG (a null pointer, a count out of range, q_start
+ * out of order or outside [0, total_q]), PKV_ERR_UNSUPPORTED (group > 16) or
+ * PKV_ERR_RANGE (max_ints too small; *num_ints holds the size needed).
+ */
+int pkv_prefill_items(const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
+                      int num_q_heads, int num_kv_heads, int grid, int32_t *items_out, int max_ints,
+                      int *num_ints);
+
+/*
  * paged_attention_mixed -- one continuous-batching step: single-token decodes
  * and prompt chunks in one call, the decodes streamed by the decode kernel
  * while the chunks run on the tensor cores.
@@ -392,6 +423,13 @@ int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const
  *                 SM (0: every SM); the decodes' CTAs take the other SMs from
  *                 the start and every SM the chunks free later.  Size it to the
  *                 chunks' share of the step's work.
+ *   prefill_items device copy of a pkv_prefill_items list built for the chunk
+ *                 sequences (seq_lens + num_decodes, q_start + num_decodes,
+ *                 the same total_q) and grid = prefill_ctas, or NULL: CTA c
+ *                 then takes chunk items c, c + grid, ...  With a list the
+ *                 chunks' grid is prefill_ctas even without decodes.  A list of
+ *                 another grid size, or entries outside the batch, set
+ *                 PKV_STATUS_BAD_ITEM and are skipped (their rows unwritten).
  * Everything else as paged_attention_prefill.  Rows of decodes and chunks must
  * not overlap.  Where the decodes' bound reaches the tensor-core route
  * (max_decode_len >= 16384) the two parts run one after the other.
@@ -402,8 +440,8 @@ int paged_attention_mixed(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                           int num_blocks, float scale, int max_decode_len, int decode_partition_size,
                           const int32_t *decode_items, int decode_grid, int prefill_ctas,
-                          pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
-                          void *stream);
+                          const int32_t *prefill_items, pkv_bf16 *out, void *workspace,
+                          size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
  * paged_attention_decode_static_scratch -- paged_attention_decode without a

@@ -47,9 +47,14 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <cstdint>
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "merge.cuh"
@@ -141,6 +146,9 @@ struct TcParams {
   int tile_tok;            // query tokens per tile: floor(128 / G); rows tile_tok * G .. 127 are spare
   int q_len;               // decode chunk: query tokens per sequence (q_len * G <= 128)
   float scale_log2;
+  // prefill: a host-built list of the items each CTA takes (null: CTA c takes
+  // items c, c + grid, ...): [grid, n, offsets[grid + 1], item indices[n]]
+  const int32_t *work;
 };
 
 // Walks (sequence, KV head, sub-item) in order; the sub-items of a sequence are
@@ -205,12 +213,27 @@ __device__ __forceinline__ int split_parts(const TcParams &p, int L) {
 // kPairs: prefill items are pairs of query tiles.
 template <bool kPrefill, bool kPairs = false>
 struct Sched {
-  int it, end, step;
+  int it, end, step, total;
   ItemWalker w;
   Item x;
 
   __device__ void begin(const TcParams &p, const SeqTab &t, int total_items) {
-    if (kPrefill) {
+    total = total_items;
+    if (kPrefill && p.work) {
+      // this CTA's range of the list; a list built for another grid size, or
+      // a range outside it, is no work and sets PKV_STATUS_BAD_ITEM
+      bool ok = p.work[0] == static_cast<int>(gridDim.x);  // only then are the offsets of this grid there
+      int a = 0, b = 0;
+      if (ok) {
+        a = p.work[2 + blockIdx.x];
+        b = p.work[3 + blockIdx.x];
+        ok = 0 <= a && a <= b && b <= p.work[1];
+      }
+      if (!ok && threadIdx.x == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_ITEM);
+      it = ok ? a : 0;
+      end = ok ? b : 0;
+      step = 1;
+    } else if (kPrefill) {
       it = blockIdx.x;
       end = total_items;
       step = gridDim.x;
@@ -220,17 +243,32 @@ struct Sched {
       step = 1;
     }
     if (it < end) {
-      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
-      fill(p, t, true);
+      if (kPrefill) load(p, t);
+      else {
+        w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
+        fill(p, t, true);
+      }
     }
+  }
+  // prefill: the item at position it (of the list, or of the batch)
+  __device__ void load(const TcParams &p, const SeqTab &t) {
+    const int idx = p.work ? p.work[3 + gridDim.x + it] : it;
+    if (idx < 0 || idx >= total) {  // a list entry outside the batch: nothing to do
+      if ((threadIdx.x & 31) == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_ITEM);
+      x = Item{};
+      x.skip = true;
+      x.run_begin = x.run_end = true;
+      return;
+    }
+    w.seek(t.prefix, p.num_seqs, p.num_kv_heads, idx);
+    fill(p, t, true);
   }
   __device__ bool valid() const { return it < end; }
   __device__ void advance(const TcParams &p, const SeqTab &t) {
     it += step;
     if (it >= end) return;
     if (kPrefill) {
-      w.seek(t.prefix, p.num_seqs, p.num_kv_heads, it);
-      fill(p, t, true);
+      load(p, t);
     } else {
       const int s0 = w.seq, h0 = w.head;
       w.next(t.prefix, p.num_seqs, p.num_kv_heads);
@@ -1301,7 +1339,7 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
                   int max_blocks_per_seq, const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                   int max_seq_len, int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes,
-                  int32_t *d_status, void *stream, int max_ctas) {
+                  int32_t *d_status, void *stream, int max_ctas, const int32_t *work) {
   if (num_seqs < 0 || total_q < 0 || max_blocks_per_seq < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
       num_blocks < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -1327,6 +1365,7 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
   if (static_cast<long long>(max_blocks_per_seq) * block_size >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
   if (plan.ws_bytes() > 0 && (!workspace || workspace_bytes < plan.ws_bytes() || !aligned16(workspace)))
     return PKV_ERR_WORKSPACE;
+  if (work && (plan.part_tokens > 0 || (reinterpret_cast<uintptr_t>(work) & 3u))) return PKV_ERR_ARG;
 
   const int box_rows = block_size < Layout<true, 128>::kTK ? block_size : Layout<true, 128>::kTK;
   CUtensorMap tmq, tmk, tmv;
@@ -1354,6 +1393,7 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
   p.group = group;
   p.tile_tok = tile_tok;
   p.scale_log2 = kernel_scale_log2(scale);
+  p.work = work;
   cudaStream_t st = as_stream(stream);
   if (plan.part_tokens > 0) {
     // split over keys: single query tiles (every partition item has both softmax
@@ -1391,6 +1431,71 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
 
 }  // namespace pkv
 
+// Host-built prefill work list (pkv.h).  The items and their order are the
+// kernel's (Sched::fill): per sequence, per KV head, pairs (or single query
+// tiles) longest first; an item's cost is its key tiles, the tiles of a lone
+// query tile (no pair partner, or the single-tile schedule) weighing about half
+// a pair's, plus a fixed cost per item for its start and its epilogue.
+extern "C" int pkv_prefill_items(const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
+                                 int num_q_heads, int num_kv_heads, int grid, int32_t *items_out, int max_ints,
+                                 int *num_ints) {
+  if (!seq_lens || !q_start || !items_out || !num_ints || num_seqs < 0 || total_q < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || grid < 1 || max_ints < 0)
+    return PKV_ERR_ARG;
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 16) return PKV_ERR_UNSUPPORTED;
+  constexpr double kItemCost = 2.0;    // key-tile periods lost at an item boundary
+  constexpr double kLoneWeight = 0.55;  // a lone query tile's period against a pair's
+  const int tile_tok = pkv::kRows / group;
+  const bool pairs = static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs;  // as prefill_entry
+  const long long span = pairs ? 2 * tile_tok : tile_tok;
+  std::vector<std::pair<double, int>> cost;  // (cost, item index)
+  long long n = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    const long long a = q_start[s], b = q_start[s + 1];
+    if (a < 0 || b < a || b > total_q) return PKV_ERR_ARG;
+    const long long c = b - a, L = seq_lens[s] < 0 ? 0 : seq_lens[s];
+    const long long np = (c + span - 1) / span;
+    n += np * num_kv_heads;
+    if (n > (1ll << 30)) return PKV_ERR_ARG;
+    for (int h = 0; h < num_kv_heads; ++h)
+      for (long long part = 0; part < np; ++part) {
+        const long long qt = np - 1 - part;
+        const long long k_hi = std::min(L, std::max(0ll, L - c + std::min(c, span * (qt + 1))));
+        const bool pair = pairs && (2 * qt + 1) * tile_tok < c;
+        const double tiles = static_cast<double>((k_hi + 127) / 128);
+        cost.emplace_back((pair ? 1.0 : kLoneWeight) * tiles + kItemCost, static_cast<int>(cost.size()));
+      }
+  }
+  const long long need = 3ll + grid + n;
+  *num_ints = need > (1ll << 31) - 1 ? -1 : static_cast<int>(need);
+  if (need > max_ints) return PKV_ERR_RANGE;
+  // longest first (ties in item order), each to the least-loaded CTA
+  std::stable_sort(cost.begin(), cost.end(),
+                   [](const std::pair<double, int> &x, const std::pair<double, int> &y) { return x.first > y.first; });
+  using Load = std::pair<double, int>;  // (load, CTA)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int g = 0; g < grid; ++g) heap.emplace(0.0, g);
+  std::vector<std::vector<int>> lists(grid);
+  for (const auto &it : cost) {
+    Load l = heap.top();
+    heap.pop();
+    lists[l.second].push_back(it.second);
+    l.first += it.first;
+    heap.push(l);
+  }
+  items_out[0] = grid;
+  items_out[1] = static_cast<int32_t>(n);
+  int32_t *off = items_out + 2, *items = items_out + 3 + grid;
+  int32_t pos = 0;
+  for (int g = 0; g < grid; ++g) {
+    off[g] = pos;
+    for (int i : lists[g]) items[pos++] = i;
+  }
+  off[grid] = pos;
+  return PKV_OK;
+}
+
 extern "C" size_t paged_attention_prefill_workspace_size(int total_q, int num_q_heads, int head_dim, int max_seq_len,
                                                          int partition_size) {
   pkv::PrefillPlan plan;
@@ -1405,7 +1510,7 @@ extern "C" int paged_attention_prefill(const pkv_bf16 *q, const pkv_bf16 *k_cach
                                        pkv_bf16 *out, int32_t *d_status, void *stream) {
   return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
                             total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0, 0, out,
-                            nullptr, 0, d_status, stream, 0);
+                            nullptr, 0, d_status, stream, 0, nullptr);
 }
 
 extern "C" int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
@@ -1417,5 +1522,5 @@ extern "C" int paged_attention_prefill_ex(const pkv_bf16 *q, const pkv_bf16 *k_c
                                           void *stream) {
   return pkv::prefill_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, q_start, num_seqs,
                             total_q, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, max_seq_len,
-                            partition_size, out, workspace, workspace_bytes, d_status, stream, 0);
+                            partition_size, out, workspace, workspace_bytes, d_status, stream, 0, nullptr);
 }

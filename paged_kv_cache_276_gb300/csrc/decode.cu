@@ -1004,8 +1004,8 @@ int paged_attention_mixed(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                           const int32_t *q_start, int num_seqs, int total_q, int num_decodes, int num_q_heads,
                           int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                           int max_decode_len, int decode_partition_size, const int32_t *decode_items,
-                          int decode_grid, int prefill_ctas, pkv_bf16 *out, void *workspace,
-                          size_t workspace_bytes, int32_t *d_status, void *stream) {
+                          int decode_grid, int prefill_ctas, const int32_t *prefill_items, pkv_bf16 *out,
+                          void *workspace, size_t workspace_bytes, int32_t *d_status, void *stream) {
   if (num_decodes < 0 || num_decodes > num_seqs || num_decodes > total_q || prefill_ctas < 0 || max_blocks_per_seq < 0)
     return PKV_ERR_ARG;
   const int chunks = num_seqs - num_decodes;
@@ -1017,7 +1017,8 @@ int paged_attention_mixed(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_
                                       max_blocks_per_seq, seq_lens ? seq_lens + num_decodes : nullptr,
                                       q_start ? q_start + num_decodes : nullptr, chunks, total_q, num_q_heads,
                                       num_kv_heads, head_dim, block_size, num_blocks, scale, 0, 0, out, nullptr, 0,
-                                      d_status, stream, num_decodes > 0 ? prefill_ctas : 0);
+                                      d_status, stream, num_decodes > 0 || prefill_items ? prefill_ctas : 0,
+                                      prefill_items);
     if (rc != PKV_OK) return rc;
   }
   if (num_decodes == 0) return PKV_OK;

@@ -36,12 +36,13 @@ bool chunk_tc_supported(int num_seqs, int q_len, int num_q_heads, int num_kv_hea
 int chunk_tc_launch(const ChunkTcArgs &a, cudaStream_t stream);
 
 // Chunked prefill (chunk_tc.cu): paged_attention_prefill_ex with a cap on the
-// persistent grid (max_ctas > 0: at most that many CTAs, one per SM).
+// persistent grid (max_ctas > 0: at most that many CTAs, one per SM) and an
+// optional device copy of a pkv_prefill_items list (work; not with a split).
 int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *seq_lens, const int32_t *q_start, int num_seqs, int total_q,
                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                   int max_seq_len, int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes,
-                  int32_t *d_status, void *stream, int max_ctas);
+                  int32_t *d_status, void *stream, int max_ctas, const int32_t *work);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

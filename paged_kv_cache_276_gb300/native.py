@@ -91,7 +91,9 @@ SIGNATURES = {
                                             _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
     "paged_attention_mixed": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
-                                       _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
+                                       _c_ptr, _c_int, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_ptr]),
+    "pkv_prefill_items": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_int,
+                                   ctypes.POINTER(_c_int)]),
     "paged_attention_decode_static_scratch": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                        _c_int, _c_float, _c_int, _c_ptr, _c_ptr, _c_ptr]),
@@ -395,19 +397,45 @@ def paged_attention_prefill_ex(q, k_cache, v_cache, block_tables, seq_lens, q_st
         _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_prefill_ex")
 
 
+def pkv_prefill_items(seq_lens, q_start, total_q, num_q_heads, num_kv_heads, grid):
+    """Host work list of a prefill launch of ``grid`` CTAs (numpy int32 lengths
+    [B] and q_start [B + 1]): int32 [3 + grid + n] = grid, n, each CTA's range
+    offsets [grid + 1], the item indices."""
+    import numpy as np
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    B = lens.shape[0]
+    if qs.shape != (B + 1,):
+        raise ValueError("q_start must be [num_seqs + 1]")
+    n = ctypes.c_int(0)
+    buf = np.empty(3 + int(grid), dtype=np.int32)
+    for _ in range(2):
+        rc = lib().pkv_prefill_items(lens.ctypes.data, qs.ctypes.data, B, int(total_q), int(num_q_heads),
+                                     int(num_kv_heads), int(grid), buf.ctypes.data, buf.shape[0], ctypes.byref(n))
+        if rc == PKV_ERR_RANGE and n.value > buf.shape[0]:
+            buf = np.empty(n.value, dtype=np.int32)
+            continue
+        _check(rc, "pkv_prefill_items")
+        return buf[:n.value]
+    raise PkvError(PKV_ERR_RANGE, "pkv_prefill_items")
+
+
 def paged_attention_mixed(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, num_decodes,
                           decode_items, max_decode_len, decode_partition_size=0, workspace=None, prefill_ctas=0,
-                          decode_grid=None, d_status=None, stream=None):
+                          decode_grid=None, d_status=None, stream=None, prefill_items=None):
     """One step of decodes (the first ``num_decodes`` sequences, query rows
     0..num_decodes-1) and prompt chunks (the rest), as paged_attention_prefill
     over the whole batch; ``decode_items`` (device) from pkv_decode_items over the
-    decodes' lengths and tables."""
+    decodes' lengths and tables; ``prefill_items`` (device int32, or None) from
+    pkv_prefill_items over the chunks with grid ``prefill_ctas``."""
     dev = k_cache.device
     for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
                      (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
                      (seq_lens, "seq_lens", torch.int32), (q_start, "q_start", torch.int32),
                      (out, "out", torch.bfloat16), (decode_items, "decode_items", torch.int32)):
         _need(t, dt, n, dev)
+    if prefill_items is not None:
+        _need(prefill_items, torch.int32, "prefill_items", dev)
     total_q, Hq, d = q.shape
     NB, Hkv, bs, d2 = k_cache.shape
     B = seq_lens.shape[0]
@@ -420,7 +448,8 @@ def paged_attention_mixed(q, k_cache, v_cache, block_tables, seq_lens, q_start, 
     _check(lib().paged_attention_mixed(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
         _ptr(q_start), B, total_q, int(num_decodes), Hq, Hkv, d, bs, NB, float(scale), int(max_decode_len),
-        int(decode_partition_size), _ptr(decode_items), grid, int(prefill_ctas), _ptr(out), _ptr(workspace),
+        int(decode_partition_size), _ptr(decode_items), grid, int(prefill_ctas), _ptr(prefill_items), _ptr(out),
+        _ptr(workspace),
         ws_bytes, _ptr(d_status), _stream(stream, dev)), "paged_attention_mixed")
 
 

@@ -305,9 +305,10 @@ class PrefillCase:
             nd += 1
         return nd
 
-    def prepare_mixed(self, prefill_ctas=None, partition_size=0):
+    def prepare_mixed(self, prefill_ctas=None, partition_size=0, chunk_list=True):
         """Work list and workspace of the leading decodes; the chunks' grid cap
-        (default: mixed_prefill_ctas)."""
+        (default: mixed_prefill_ctas) and, with chunk_list, their host-built
+        work list for that grid."""
         nd = self.num_decodes
         self.mixed_nd = nd
         self.mixed_max_len = int(self.lens[:nd].max()) if nd else 0
@@ -318,6 +319,11 @@ class PrefillCase:
         n = native.paged_attention_workspace_size(nd, 1, self.Hq, self.d, self.mixed_max_len, self.mixed_part)
         self.mixed_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
         self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
+        self.mixed_chunk_items = None
+        if chunk_list and nd < self.B and self.mixed_ctas > 0:
+            w = native.pkv_prefill_items(self.lens[nd:], self.q_start[nd:], self.total_q, self.Hq, self.Hkv,
+                                         self.mixed_ctas)
+            self.mixed_chunk_items = torch.as_tensor(w, device=self.device)
 
     def prepare_split(self, partition_size: int):
         """Workspace of the prefill split over keys into partition_size-token partitions."""
@@ -336,7 +342,7 @@ class PrefillCase:
         native.paged_attention_mixed(self.q, self.k_cache, self.v_cache, self.d_tables, self.d_lens, self.d_q_start,
                                      self.scale, self.out, self.mixed_nd, self.mixed_items, self.mixed_max_len,
                                      self.mixed_part, self.mixed_ws, self.mixed_ctas, d_status=d_status,
-                                     stream=stream)
+                                     stream=stream, prefill_items=self.mixed_chunk_items)
 
     def write(self, d_status=None, stream=None):
         """The chunk tokens' keys and values into their slots."""

@@ -537,3 +537,68 @@ def test_split_prefill_sizes_and_argument_checks(native):
     assert call() == native.PKV_ERR_WORKSPACE                  # the split needs its workspace
     assert call(ws=fake, wsb=n - 1) == native.PKV_ERR_WORKSPACE
     assert call(ws=ctypes.c_void_p((1 << 20) + 8), wsb=n) == native.PKV_ERR_WORKSPACE  # misaligned
+
+
+def _prefill_item_costs(lens, q_start, total_q, Hq, Hkv):
+    """Items in the kernel's numbering (per sequence, KV head, pair of query
+    tiles or single tile, longest first) and their key tiles."""
+    G = Hq // Hkv
+    tile_tok = 128 // G
+    B = len(lens)
+    pairs = total_q >= 2 * tile_tok * B
+    span = 2 * tile_tok if pairs else tile_tok
+    tiles = []
+    for s in range(B):
+        c, L = int(q_start[s + 1] - q_start[s]), max(0, int(lens[s]))
+        npairs = -(-c // span)
+        for _ in range(Hkv):
+            for part in range(npairs):
+                qt = npairs - 1 - part
+                k_hi = min(L, max(0, L - c + min(c, span * (qt + 1))))
+                tiles.append(-(-k_hi // 128))
+    return np.array(tiles), pairs
+
+
+@pytest.mark.parametrize("grid", [1, 7, 89, 152])
+def test_prefill_items_hand_out_every_item_once(native, grid):
+    """pkv_prefill_items: every item of the batch exactly once, each CTA's
+    range in order, and the longest-first hand-out keeps every CTA within one
+    item of the mean load."""
+    rng = np.random.default_rng(grid)
+    for Hq, Hkv in ((32, 8), (64, 8), (24, 8)):
+        B = 6
+        chunks = rng.integers(0, 1500, B)
+        lens = chunks + rng.integers(0, 9000, B)
+        q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        total_q = int(q_start[-1])
+        w = native.pkv_prefill_items(lens, q_start, total_q, Hq, Hkv, grid)
+        tiles, _ = _prefill_item_costs(lens, q_start, total_q, Hq, Hkv)
+        n = len(tiles)
+        assert w[0] == grid and w[1] == n and len(w) == 3 + grid + n
+        off = w[2:3 + grid]
+        assert off[0] == 0 and off[-1] == n and np.all(np.diff(off) >= 0)
+        items = w[3 + grid:]
+        assert sorted(items.tolist()) == list(range(n))
+        if n:
+            cost = tiles + 2.0  # any positive per-item cost bounds the spread the same way
+            loads = [cost[items[off[g]:off[g + 1]]].sum() for g in range(grid)]
+            assert max(loads) <= cost.sum() / grid + cost.max() + 1e-9
+
+
+def test_prefill_items_rejects_bad_arguments(native):
+    lens = np.array([100, 200], dtype=np.int32)
+    qs = np.array([0, 50, 150], dtype=np.int32)
+    f = native.lib().pkv_prefill_items
+    out = np.zeros(64, dtype=np.int32)
+    n = ctypes.c_int(0)
+    args = lambda **kw: [kw.get("lens", lens.ctypes.data), kw.get("qs", qs.ctypes.data), kw.get("B", 2),
+                         kw.get("total_q", 150), kw.get("Hq", 32), kw.get("Hkv", 8), kw.get("grid", 4),
+                         out.ctypes.data, kw.get("max_ints", 64), ctypes.byref(n)]
+    assert f(*args()) == native.PKV_OK
+    assert f(*args(grid=0)) == native.PKV_ERR_ARG
+    assert f(*args(Hq=30)) == native.PKV_ERR_ARG
+    assert f(*args(Hq=136, Hkv=8)) == native.PKV_ERR_UNSUPPORTED
+    assert f(*args(total_q=100)) == native.PKV_ERR_ARG  # q_start past total_q
+    bad = np.array([0, 80, 60], dtype=np.int32)
+    assert f(*args(qs=bad.ctypes.data)) == native.PKV_ERR_ARG
+    assert f(*args(max_ints=5)) == native.PKV_ERR_RANGE and n.value == 3 + 4 + (1 + 2) * 8  # pairs: 1 + 2 per head

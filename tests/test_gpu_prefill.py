@@ -487,3 +487,54 @@ def test_prefill_output_on_a_16_byte_boundary_matches_the_aligned_one():
         assert torch.equal(aligned.view(torch.int16), shifted.view(torch.int16))
         ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
         assert_attention_close(shifted, ref, "prefill into a 16-byte-aligned output")
+
+
+def test_mixed_step_with_a_host_built_chunk_list():
+    """paged_attention_mixed with the chunks' pkv_prefill_items list: the same
+    bits as without it (each item is computed alike whichever CTA takes it),
+    also with the list and no decodes; a list built for another grid size is
+    reported (PKV_STATUS_BAD_ITEM) and leaves the chunk rows unwritten,
+    without a fault."""
+    rng = np.random.default_rng(31)
+    n_dec = 24
+    lens = [int(x) for x in rng.integers(1, 3000, size=n_dec)] + [2600, 900, 5000]
+    chunks = [1] * n_dec + [512, 300, 1024]
+    Hq, Hkv, bs, d = 32, 8, 16, 128
+    q, kc, vc, tables, q_start = prefill_case(lens, chunks, bs, Hq, Hkv, seed=31)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    dev = kc.device
+    d_tables = torch.as_tensor(np.asarray(tables, dtype=np.int32), device=dev)
+    d_lens = torch.as_tensor(np.asarray(lens, dtype=np.int32), device=dev)
+    d_qs = torch.as_tensor(q_start, device=dev)
+    items = torch.as_tensor(native.pkv_decode_items(np.asarray(lens[:n_dec], dtype=np.int32), tables[:n_dec], Hkv, bs,
+                                                    512, d), device=dev)
+    ws = torch.empty(native.paged_attention_workspace_size(n_dec, 1, Hq, d, max(lens[:n_dec]), 512),
+                     dtype=torch.uint8, device=dev)
+    total_q = int(q_start[-1])
+
+    def mixed(ctas, grid_of_list, nd=n_dec):
+        chunk_list = None
+        if grid_of_list:
+            w = native.pkv_prefill_items(np.asarray(lens[nd:]), q_start[nd:], total_q, Hq, Hkv, grid_of_list)
+            chunk_list = torch.as_tensor(w, device=dev)
+        out = torch.empty_like(q)
+        out.view(torch.int16).fill_(CANARY)
+        st = status_tensor()
+        native.paged_attention_mixed(q, kc, vc, d_tables, d_lens, d_qs, scale, out, nd, items, max(lens[:n_dec]),
+                                     512, ws, ctas, d_status=st, prefill_items=chunk_list)
+        torch.cuda.synchronize()
+        return out, st.item()
+
+    plain, st0 = mixed(37, 0)
+    listed, st1 = mixed(37, 37)
+    assert st0 == 0 and st1 == 0
+    assert torch.equal(plain.view(torch.int16), listed.view(torch.int16))
+    whole = run_prefill(q, kc, vc, tables, lens, q_start, scale)
+    only_chunks, st2 = mixed(23, 23, nd=0)  # no decodes: the list's grid still caps the chunks
+    assert st2 == 0 and torch.equal(only_chunks.view(torch.int16), whole.view(torch.int16))
+    ref = oracle_prefill(q, kc, vc, tables, lens, q_start, Hq, Hkv, bs, scale)
+    assert_attention_close(listed, ref, "mixed step over the chunk list")
+    wrong, st3 = mixed(37, 36)
+    assert st3 & native.PKV_STATUS_BAD_ITEM
+    assert torch.equal(wrong[:n_dec].view(torch.int16), plain[:n_dec].view(torch.int16))  # the decodes still run
+    assert (wrong[n_dec:].view(torch.int16) == CANARY).all()
