@@ -219,6 +219,33 @@ class Runner:
         toks = self.sess.new_token_tensors(n, seed=self.w.seed + 17 * self.rank)
         return steps, toks
 
+    def layer_call(self, p, q, ks, vs, l, out, ws, status, stream, d0=None, dm=None):
+        """One layer of a planned step, as the step runner runs it: the block
+        copies of copy-on-write, then (single tokens) the decode with the new
+        token's store over the host-built work list, overlapping the layer
+        before (independent inputs; not behind this layer's block copies,
+        which it reads), or pkv_write and the decode.  d0 is
+        recorded right before the decode call; dm is recorded by the library
+        right after its main kernel."""
+        from paged_kv_cache_276_gb300 import native
+        sess = self.sess
+        if p.cow_pairs is not None:
+            native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
+        if sess.q_len == 1:
+            if d0 is not None:
+                d0.record(stream)
+            native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l],
+                                                p.tables, p.lens, p.max_len, sess.scale, out, p.items, workspace=ws,
+                                                partition_size=p.partition, d_status=status, stream=stream,
+                                                main_done_event=dm, overlap=p.cow_pairs is None)
+        else:
+            native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
+            if d0 is not None:
+                d0.record(stream)
+            native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens, p.max_len,
+                                          sess.scale, out, ws, sess.partition_size, status, stream,
+                                          main_done_event=dm)
+
     def time_device(self, warmup, steps, world):
         """Per-step CUDA-event times with an L2 flush before every step (outside
         the events); decode launches timed separately for the roofline."""
@@ -252,35 +279,30 @@ class Runner:
                 q, ks, vs = toks[i]
                 flush.fill_(float(i))
                 s0, s1 = ev(), ev()
-                dec = []
                 s0.record(stream)
+                # no event between the layers: one would make each layer's
+                # kernels wait for the previous layer's to finish
                 for l in range(sess.layers):
-                    if p.cow_pairs is not None:
-                        native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
-                        launches += i >= warmup
-                    d0, d1 = ev(), ev()
-                    if fused:  # the new token's store inside the decode's grid, over the host-built work list
-                        d0.record(stream)
-                        native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
-                                                            sess.v_caches[l], p.tables, p.lens, p.max_len,
-                                                            sess.scale, out, p.items, workspace=ws,
-                                                            partition_size=p.partition, d_status=status,
-                                                            stream=stream)
-                    else:
-                        native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
-                        d0.record(stream)
-                        native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
-                                                      p.max_len, sess.scale, out, ws, sess.partition_size, status,
-                                                      stream)
-                    d1.record(stream)
-                    dec.append((d0, d1))
+                    self.layer_call(p, q, ks, vs, l, out, ws, status, stream)
                     nparts = math.ceil(p.max_len / (p.partition or DEFAULT_PARTITION)) if p.max_len else 1
-                    # (write,) decode, cross-partition combine
-                    launches += (i >= warmup) * ((1 if fused else 2) + (nparts > 1))
+                    # (copy,) (write,) decode, cross-partition combine
+                    launches += (i >= warmup) * ((1 if fused else 2) + (nparts > 1) + (p.cow_pairs is not None))
                 s1.record(stream)
                 if i >= warmup:
                     step_ms.append((s0, s1))
-                    dec_ms.extend(dec)
+            torch.cuda.synchronize()
+            # Call pass: the timed steps again (same slots, same values, so the
+            # writes change nothing), an event on each side of every layer's
+            # decode call (the call's time, with its split-K merge)
+            for i in range(warmup, warmup + steps):
+                p = plans[i]
+                q, ks, vs = toks[i]
+                flush.fill_(float(i))
+                for l in range(sess.layers):
+                    d0, d1 = ev(), ev()
+                    self.layer_call(p, q, ks, vs, l, out, ws, status, stream, d0=d0)
+                    d1.record(stream)
+                    dec_ms.append((d0, d1))
             torch.cuda.synchronize()
             # Main-kernel pass: the timed steps again (same slots, same values,
             # so the writes change nothing), each decode call handed an event
@@ -292,22 +314,8 @@ class Runner:
                 q, ks, vs = toks[i]
                 flush.fill_(float(i))
                 for l in range(sess.layers):
-                    if p.cow_pairs is not None:
-                        native.pkv_block_copy(sess.k_caches[l], sess.v_caches[l], p.cow_pairs, status, stream)
                     d0, dm = ev(), ev()
-                    if fused:
-                        d0.record(stream)
-                        native.paged_attention_decode_items(q, ks[l], vs[l], p.slots, sess.k_caches[l],
-                                                            sess.v_caches[l], p.tables, p.lens, p.max_len,
-                                                            sess.scale, out, p.items, workspace=ws,
-                                                            partition_size=p.partition, d_status=status,
-                                                            stream=stream, main_done_event=dm)
-                    else:
-                        native.pkv_write(ks[l], vs[l], p.slots, sess.k_caches[l], sess.v_caches[l], status, stream)
-                        d0.record(stream)
-                        native.paged_attention_decode(q, sess.k_caches[l], sess.v_caches[l], p.tables, p.lens,
-                                                      p.max_len, sess.scale, out, ws, sess.partition_size, status,
-                                                      stream, main_done_event=dm)
+                    self.layer_call(p, q, ks, vs, l, out, ws, status, stream, d0=d0, dm=dm)
                     main_ms.append((d0, dm))
             torch.cuda.synchronize()
         barrier(world)

@@ -285,7 +285,18 @@ int pkv_decode_items(const int32_t *seq_lens, const int32_t *block_tables, int m
  * blocks); a list built for other arguments gives undefined output but never
  * reads or writes out of bounds.  Where the decode runs on the tensor cores
  * (max_seq_len >= 16384) the list is not used.
+ *   flags       0, or PKV_DECODE_OVERLAP: the caller guarantees that nothing
+ *               this call reads (q, k_new, v_new, slot_mapping, the caches,
+ *               tables, lengths, items) and nothing it stores into the caches
+ *               is written or read by the work queued before it on the stream,
+ *               as with the layers of one decode step.  The call then streams
+ *               its keys and values at once and waits for that earlier work
+ *               only before it writes workspace or out, so consecutive calls
+ *               overlap (one workspace may serve them all).  Other bits:
+ *               PKV_ERR_ARG.  Ignored on the tensor-core route.
  */
+#define PKV_DECODE_OVERLAP 1
+
 int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
                                  const int64_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
                                  const int32_t *block_tables, int max_blocks_per_seq,
@@ -294,7 +305,7 @@ int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                                  int num_blocks, float scale, int partition_size,
                                  const int32_t *items, int grid_items, pkv_bf16 *out,
                                  void *workspace, size_t workspace_bytes, int32_t *d_status,
-                                 void *stream, void *main_done_event);
+                                 void *stream, void *main_done_event, int flags);
 
 /*
  * paged_attention_prefill -- attention of a chunk of new tokens per sequence,

@@ -85,6 +85,10 @@ struct Params {
   // chunk kernel of a mixed step), which waited for our inputs before it let
   // this grid start: no wait here, so the two grids run side by side
   int skip_dependency_wait;
+  // nothing this grid reads is written by the kernels launched before it (the
+  // layers of one decode step): it streams at once and waits for them only
+  // before it writes its workspace or outputs, which they may still read
+  int wait_before_writes;
 };
 
 // A block is staged as one or more "units" of consecutive token rows: the
@@ -263,7 +267,8 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   // Let the merge grid queued behind this one become resident now; it still
   // waits for this whole grid's results before it reads anything.
   grid_launch_dependents();
-  if (!p.skip_dependency_wait) grid_dependency_wait();  // inputs may come from the kernel launched just before
+  // inputs may come from the kernel launched just before
+  if (!p.skip_dependency_wait && !p.wait_before_writes) grid_dependency_wait();
   int part, h, seq, L, window0, b0 = -1;
   if (p.items) {
     // a host-built work list: one 16-byte load names this CTA's partition, its
@@ -413,6 +418,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
   }
   __syncthreads();
   if (*abort_flag) return;
+  if (p.wait_before_writes && !p.skip_dependency_wait) grid_dependency_wait();
 
   const int rows = p.num_q_heads;  // q_len == 1
   for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
@@ -788,7 +794,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
                  void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items = nullptr,
-                 int grid_items = 0, bool skip_dependency_wait = false);
+                 int grid_items = 0, bool skip_dependency_wait = false, bool wait_before_writes = false);
 
 }  // namespace pkv
 
@@ -982,7 +988,9 @@ int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const
                                  int num_seqs, int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int num_blocks, float scale, int partition_size,
                                  const int32_t *items, int grid_items, pkv_bf16 *out, void *workspace,
-                                 size_t workspace_bytes, int32_t *d_status, void *stream, void *main_done_event) {
+                                 size_t workspace_bytes, int32_t *d_status, void *stream, void *main_done_event,
+                                 int flags) {
+  if ((flags & ~PKV_DECODE_OVERLAP) != 0) return PKV_ERR_ARG;
   if (num_seqs > 0 && (!items || grid_items < 1 || (reinterpret_cast<uintptr_t>(items) & 15u))) return PKV_ERR_ARG;
   const bool store = k_new || v_new || slot_mapping;
   if (store) {
@@ -994,7 +1002,7 @@ int paged_attention_decode_items(const pkv_bf16 *q, const pkv_bf16 *k_new, const
   return pkv::decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                            1, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
                            out, workspace, workspace_bytes, d_status, stream, main_done_event,
-                           store ? &nt : nullptr, items, grid_items);
+                           store ? &nt : nullptr, items, grid_items, false, (flags & PKV_DECODE_OVERLAP) != 0);
 }
 
 // One continuous-batching step (see pkv.h): the chunks on the tensor cores with
@@ -1077,7 +1085,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
                  int partition_size, pkv_bf16 *out, void *workspace, size_t workspace_bytes, int32_t *d_status,
                  void *stream, void *main_done_event, const NewTokens *nt, const int32_t *items, int grid_items,
-                 bool skip_dependency_wait) {
+                 bool skip_dependency_wait, bool wait_before_writes) {
   cudaEvent_t main_done = static_cast<cudaEvent_t>(main_done_event);
   Plan plan;
   const int checked = decode_check(q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -1174,6 +1182,7 @@ int decode_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_c
   p.num_seqs = num_seqs;
   if (items) p.items = reinterpret_cast<const int4 *>(items);  // q_len == 1, grid_items >= 1 (entry checks)
   p.skip_dependency_wait = skip_dependency_wait ? 1 : 0;
+  p.wait_before_writes = wait_before_writes ? 1 : 0;
   if (nt) {
     p.k_new = static_cast<const uint4 *>(nt->k);
     p.v_new = static_cast<const uint4 *>(nt->v);

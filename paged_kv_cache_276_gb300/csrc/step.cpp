@@ -9,6 +9,7 @@
 // single graph launch captured once per (batch size, partition count).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <map>
 #include <new>
@@ -53,7 +54,7 @@ struct pkv_step {
   cudaStream_t copy = nullptr;  // the step's host <-> device copies, beside the kernels
   cudaEvent_t done = nullptr;
   cudaEvent_t start = nullptr, copied_out = nullptr;
-  std::vector<cudaEvent_t> layer_in, layer_done;  // per layer: its inputs landed, its kernels finished
+  std::vector<cudaEvent_t> layer_in, layer_done;  // per group of layers: its inputs landed, its kernels finished
   bool pending = false;
   std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;  // (n, partitions, partition size)
   int auto_part = 0, auto_n = 0, auto_age = 0;  // the work list's partition pick, kept between steps
@@ -66,58 +67,83 @@ void drop_graphs(pkv_step *s) {
   s->graphs.clear();
 }
 
+// Layers in groups for the copies: 1, 2, 4, then 8 at a time, shrinking again
+// towards the end (never more than half of the layers left), so the first
+// kernels start after a small copy, the last output returns in a small copy,
+// and between groups consecutive layers' kernels overlap (an event between two
+// kernels would make the second wait for the first to finish).  Returns the
+// first layer of each group, then the layer count.
+std::vector<int> layer_groups(int layers) {
+  std::vector<int> first;
+  for (int lo = 0, k = 1; lo < layers; k *= 2) {
+    const int left = layers - lo;
+    const int g = left <= 1 ? left : std::min(std::min(k, 8), std::max(1, left / 2));
+    first.push_back(lo);
+    lo += g;
+  }
+  first.push_back(layers);
+  return first;
+}
+
 // One step on `st`: the common inputs (slots, tables, lengths, work list) and
-// each layer's queries, keys and values go to the device on the runner's copy
-// stream, layer after layer, while the kernels of the layers already copied run
-// on `st`; each layer's output goes back as soon as its kernels finish.  So the
-// copies overlap the kernels instead of preceding and following all of them.
-// q_len 1: the decode runs grid_items CTAs over the work list in the staging buffer.
+// the layers' queries, keys and values go to the device on the runner's copy
+// stream, group after group, while the kernels of the groups already copied
+// run on `st`; each group's outputs go back as soon as its kernels finish.  So
+// the copies overlap the kernels instead of preceding and following all of
+// them.  q_len 1: the decode runs grid_items CTAs over the work list in the
+// staging buffer, each layer overlapping the one before (PKV_DECODE_OVERLAP:
+// the layers' inputs are independent).
 int enqueue(pkv_step *s, cudaStream_t st, int n, int max_seq_len, int grid_items, int partition) {
   const pkv_step_config &c = s->cfg;
   const pkv_step_layout &L = s->lay;
   cudaError_t e;
   auto fail = [](cudaError_t err) { return pkv::set_cuda_error(err), PKV_ERR_CUDA; };
+  const std::vector<int> groups = layer_groups(c.num_layers);
+  const int ng = static_cast<int>(groups.size()) - 1;
   // the copies may overwrite the staging buffers only after the work before this step
   if ((e = cudaEventRecord(s->start, st)) != cudaSuccess) return fail(e);
   if ((e = cudaStreamWaitEvent(s->copy, s->start, 0)) != cudaSuccess) return fail(e);
-  for (int l = 0; l < c.num_layers; ++l) {
-    // layer 0 comes with the common segment in front of it
-    const size_t lo = l == 0 ? 0 : L.q_offset + l * L.layer_stride;
-    const size_t hi = L.q_offset + (l + 1) * L.layer_stride;
+  for (int gi = 0; gi < ng; ++gi) {
+    // the first group comes with the common segment in front of it
+    const size_t lo = gi == 0 ? 0 : L.q_offset + groups[gi] * L.layer_stride;
+    const size_t hi = L.q_offset + groups[gi + 1] * L.layer_stride;
     if ((e = cudaMemcpyAsync(s->ds + lo, s->hs + lo, hi - lo, cudaMemcpyHostToDevice, s->copy)) != cudaSuccess)
       return fail(e);
-    if ((e = cudaEventRecord(s->layer_in[l], s->copy)) != cudaSuccess) return fail(e);
+    if ((e = cudaEventRecord(s->layer_in[gi], s->copy)) != cudaSuccess) return fail(e);
   }
   const auto *slots = reinterpret_cast<const int64_t *>(s->ds + L.slots_offset);
   const auto *tables = reinterpret_cast<const int32_t *>(s->ds + L.tables_offset);
   const auto *lens = reinterpret_cast<const int32_t *>(s->ds + L.lens_offset);
-  for (int l = 0; l < c.num_layers; ++l) {
-    const char *layer = s->ds + L.q_offset + l * L.layer_stride;
-    const auto *q = reinterpret_cast<const pkv_bf16 *>(layer);
-    const auto *kn = reinterpret_cast<const pkv_bf16 *>(layer + (L.k_offset - L.q_offset));
-    const auto *vn = reinterpret_cast<const pkv_bf16 *>(layer + (L.v_offset - L.q_offset));
-    auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
-    if ((e = cudaStreamWaitEvent(st, s->layer_in[l], 0)) != cudaSuccess) return fail(e);
-    int rc;
-    if (c.q_len == 1) {  // the allocator's slots are the newest tokens' table positions: one grid
-      const auto *items = reinterpret_cast<const int32_t *>(s->ds + L.items_offset);
-      rc = paged_attention_decode_items(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
-                                        max_seq_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
-                                        c.num_blocks, c.scale, partition, items, grid_items, out, s->ws,
-                                        s->ws_bytes, s->status, st, nullptr);
-    } else {
-      rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
-                     c.head_dim, s->status, st);
+  for (int gi = 0, l = 0; gi < ng; ++gi) {
+    if ((e = cudaStreamWaitEvent(st, s->layer_in[gi], 0)) != cudaSuccess) return fail(e);
+    for (; l < groups[gi + 1]; ++l) {
+      const char *layer = s->ds + L.q_offset + l * L.layer_stride;
+      const auto *q = reinterpret_cast<const pkv_bf16 *>(layer);
+      const auto *kn = reinterpret_cast<const pkv_bf16 *>(layer + (L.k_offset - L.q_offset));
+      const auto *vn = reinterpret_cast<const pkv_bf16 *>(layer + (L.v_offset - L.q_offset));
+      auto *out = reinterpret_cast<pkv_bf16 *>(s->dout + l * L.out_layer_bytes);
+      int rc;
+      if (c.q_len == 1) {  // the allocator's slots are the newest tokens' table positions: one grid
+        const auto *items = reinterpret_cast<const int32_t *>(s->ds + L.items_offset);
+        rc = paged_attention_decode_items(q, kn, vn, slots, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n,
+                                          max_seq_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size,
+                                          c.num_blocks, c.scale, partition, items, grid_items, out, s->ws,
+                                          s->ws_bytes, s->status, st, nullptr, PKV_DECODE_OVERLAP);
+      } else {
+        rc = pkv_write(kn, vn, slots, n * c.q_len, s->k[l], s->v[l], c.num_blocks, c.block_size, c.num_kv_heads,
+                       c.head_dim, s->status, st);
+        if (rc != PKV_OK) return rc;
+        rc = paged_attention_decode(q, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n, max_seq_len,
+                                    c.q_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks,
+                                    c.scale, c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
+      }
       if (rc != PKV_OK) return rc;
-      rc = paged_attention_decode(q, s->k[l], s->v[l], tables, c.max_blocks_per_seq, lens, n, max_seq_len,
-                                  c.q_len, c.num_q_heads, c.num_kv_heads, c.head_dim, c.block_size, c.num_blocks,
-                                  c.scale, c.partition_size, out, s->ws, s->ws_bytes, s->status, st);
     }
-    if (rc != PKV_OK) return rc;
-    if ((e = cudaEventRecord(s->layer_done[l], st)) != cudaSuccess) return fail(e);
-    if ((e = cudaStreamWaitEvent(s->copy, s->layer_done[l], 0)) != cudaSuccess) return fail(e);
-    if ((e = cudaMemcpyAsync(s->hout + l * L.out_layer_bytes, s->dout + l * L.out_layer_bytes, L.out_layer_bytes,
-                             cudaMemcpyDeviceToHost, s->copy)) != cudaSuccess)
+    // the group's outputs, contiguous in the output buffer
+    const size_t o0 = groups[gi] * L.out_layer_bytes, o1 = groups[gi + 1] * L.out_layer_bytes;
+    if ((e = cudaEventRecord(s->layer_done[gi], st)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(s->copy, s->layer_done[gi], 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaMemcpyAsync(s->hout + o0, s->dout + o0, o1 - o0, cudaMemcpyDeviceToHost, s->copy)) != cudaSuccess)
       return fail(e);
   }
   // the step ends on `st` once its last output has landed

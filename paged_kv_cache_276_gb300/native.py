@@ -34,6 +34,8 @@ PKV_STATUS_TIMEOUT = 8
 PKV_STATUS_BAD_QSTART = 16
 PKV_STATUS_BAD_ITEM = 32
 
+PKV_DECODE_OVERLAP = 1
+
 _c_int, _c_i64, _c_ptr, _c_size, _c_float = (ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_float)
 
@@ -84,7 +86,7 @@ SIGNATURES = {
     "paged_attention_decode_items": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
                                               _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                               _c_float, _c_int, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr,
-                                              _c_ptr, _c_ptr]),
+                                              _c_ptr, _c_ptr, _c_int]),
     "paged_attention_prefill_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "paged_attention_prefill_ex": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
                                             _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
@@ -310,9 +312,11 @@ def pkv_decode_items(seq_lens, block_tables, num_kv_heads, block_size, partition
 
 def paged_attention_decode_items(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens,
                                  max_seq_len, scale, out, items, grid_items=None, workspace=None, partition_size=0,
-                                 d_status=None, stream=None, main_done_event=None):
+                                 d_status=None, stream=None, main_done_event=None, overlap=False):
     """Single-token decode over a work list (device int32 [1 + n, 4] from
-    ``pkv_decode_items``); k_new / v_new / slot_mapping all None: no store."""
+    ``pkv_decode_items``); k_new / v_new / slot_mapping all None: no store.
+    overlap: PKV_DECODE_OVERLAP (nothing this call reads or stores into is
+    touched by the work queued before it, as for the layers of one step)."""
     dev = k_cache.device
     store = k_new is not None or v_new is not None or slot_mapping is not None
     checks = [(q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
@@ -343,7 +347,8 @@ def paged_attention_decode_items(q, k_new, v_new, slot_mapping, k_cache, v_cache
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), B, int(max_seq_len), Hq, Hkv, d, bs, NB, float(scale),
         int(partition_size), _ptr(items), grid, _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_status),
-        _stream(stream, dev), None if ev is None else ctypes.c_void_p(ev)), "paged_attention_decode_items")
+        _stream(stream, dev), None if ev is None else ctypes.c_void_p(ev), PKV_DECODE_OVERLAP if overlap else 0),
+        "paged_attention_decode_items")
 
 
 def paged_attention_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_start, scale, out, d_status=None,

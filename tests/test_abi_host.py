@@ -507,12 +507,13 @@ def test_decode_items_rejects_bad_arguments_before_launch(native):
     fake = ctypes.c_void_p(1 << 20)
     base = [fake, None, None, None, fake, fake, fake, 4, fake, 2, 64, 8, 2, 128, 16, 8, 0.1, 0]
 
-    def call(items=fake, grid=3, **kw):
+    def call(items=fake, grid=3, flags=0, **kw):
         a = list(base)
         for k, v in kw.items():
             a[{"k_new": 1, "slots": 3, "Hq": 11, "d": 13}[k]] = v
-        return lib.paged_attention_decode_items(*a, items, grid, fake, None, 0, None, None, None)
+        return lib.paged_attention_decode_items(*a, items, grid, fake, None, 0, None, None, None, flags)
     assert call(items=None) == native.PKV_ERR_ARG
+    assert call(flags=2) == native.PKV_ERR_ARG                                 # an unknown flag
     assert call(grid=0) == native.PKV_ERR_ARG
     assert call(items=ctypes.c_void_p((1 << 20) + 4)) == native.PKV_ERR_ARG   # items must be 16-byte aligned
     assert call(k_new=fake) == native.PKV_ERR_ARG                             # a store needs k, v and slots

@@ -853,3 +853,52 @@ def test_decode_items_built_for_other_lengths_is_reported():
     # the sequences the list describes correctly are still right
     ref = oracle_decode(q, kc, vc, tables, lens, (Hq, Hkv, d, bs), 0.09)
     assert_attention_close(out[:2], ref[:2], "sequences the list matches")
+
+
+def test_decode_items_overlap_across_layers_is_bit_exact():
+    """PKV_DECODE_OVERLAP: eight "layers" (own caches, queries, new tokens and
+    outputs; shared tables, work list and one workspace) launched back to
+    back, each streaming while the one before finishes and writing only after
+    it: every layer's output and stored token equal those of the same calls
+    without the flag, and a layer matches the oracle."""
+    d, bs, Hq, Hkv = 128, 16, 32, 8
+    lens = [1, 700, 3000, 2047, 64, 4000, 129, 900] * 4
+    B, layers = len(lens), 8
+    q0, kc0, _, tables = random_case(lens, d, bs, Hq, Hkv, seed=300)
+    NB = kc0.shape[0]
+    caches = [(inputs.randn_bf16((NB, Hkv, bs, d), 600 + 2 * l, "cuda"),
+               inputs.randn_bf16((NB, Hkv, bs, d), 601 + 2 * l, "cuda")) for l in range(layers)]
+    qs = [inputs.randn_bf16(tuple(q0.shape), 700 + l, "cuda") for l in range(layers)]
+    knew = [inputs.randn_bf16((B, Hkv, d), 400 + l, "cuda") for l in range(layers)]
+    vnew = [inputs.randn_bf16((B, Hkv, d), 500 + l, "cuda") for l in range(layers)]
+    slots_d = torch.as_tensor(_newest_slots(tables, lens, bs), device="cuda")
+    tables_d = torch.as_tensor(np.asarray(tables, dtype=np.int32), device="cuda")
+    lens_d = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    items = native.pkv_decode_items(np.asarray(lens, dtype=np.int32), tables, Hkv, bs, 1024, d)
+    items_d = torch.as_tensor(items, device="cuda")
+    part = int(items[0, 1])
+    max_len = max(lens)
+    ws = torch.empty(native.paged_attention_workspace_size(B, 1, Hq, d, max_len, part), dtype=torch.uint8,
+                     device="cuda")
+    st = status_tensor()
+
+    def run(overlap):
+        kcs = [(kc.clone(), vc.clone()) for kc, vc in caches]
+        outs = [torch.full_like(qs[0], float("nan")) for _ in range(layers)]
+        for l in range(layers):
+            native.paged_attention_decode_items(qs[l], knew[l], vnew[l], slots_d, kcs[l][0], kcs[l][1], tables_d,
+                                                lens_d, max_len, 0.09, outs[l], items_d, workspace=ws,
+                                                partition_size=part, d_status=st, overlap=overlap)
+        torch.cuda.synchronize()
+        return kcs, outs
+
+    ref_c, ref_o = run(False)
+    for _ in range(3):
+        got_c, got_o = run(True)
+        assert st.item() == 0
+        for l in range(layers):
+            assert torch.equal(got_o[l].view(torch.int16), ref_o[l].view(torch.int16)), f"layer {l}"
+            assert torch.equal(got_c[l][0].view(torch.int16), ref_c[l][0].view(torch.int16))
+            assert torch.equal(got_c[l][1].view(torch.int16), ref_c[l][1].view(torch.int16))
+    ref = oracle_decode(qs[3], got_c[3][0], got_c[3][1], tables, lens, (Hq, Hkv, d, bs), 0.09)
+    assert_attention_close(got_o[3], ref, "an overlapped layer against the oracle")
