@@ -650,12 +650,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t kb = sK + s * kKVBytes;
               for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
                 int &n = q ? nb : na;
-                // Offset tile B's chain by about half a period: its first score
-                // product of the pair goes out once tile A's first weights are
-                // written, so that from then on one set computes its softmax
-                // while the other set's products run (issued in the same order,
-                // the two chains would stay in step, both softmaxes at once).
-                if (q == 1 && t == 0 && !mbar_wait(bar(B_P_FULL0), (na - 1) & 1)) { ok = false; break; }
+                // Offset tile B's chain by about half a period: on the CTA's
+                // first pair, B's first score product goes out once tile A's
+                // first weights are written, so that from then on one set
+                // computes its softmax while the other set's products run
+                // (issued in the same order, the two chains would stay in step,
+                // both softmaxes at once).  Later pairs keep the offset by
+                // themselves; waiting again there only delays B behind A's
+                // epilogue.
+                if (q == 1 && t == 0 && tpieces == 1 && !mbar_wait(bar(B_P_FULL0), (na - 1) & 1)) {
+                  ok = false;
+                  break;
+                }
                 if (n > 0 && !mbar_wait(bar(B_PV_DONE0 + q), (n - 1) & 1)) { ok = false; break; }
                 tc::fence_after();
                 const uint32_t sq = sQ + q * kQBytes;
