@@ -657,11 +657,13 @@ int pkv_refcount(const pkv_alloc *a, int block);
  *       pool per layer, each [num_blocks][num_kv_heads][block_size][head_dim].
  *
  * With use_graph != 0 the device part of a run (copy in, the layers' writes
- * and decodes, copy out) is captured once into a CUDA graph for each pair
- * (n, number of partitions of the longest sequence) and replayed; the decode's
- * max_seq_len is then that number of partitions times partition_size, an upper
- * bound of the lengths (at most 32 graphs are kept; capture happens on a
- * private stream).  With use_graph == 0 the same copies and kernels are
+ * and decodes, copy out) is captured once into a CUDA graph for each key
+ * (n, number of partitions of the longest sequence, partition size, and for
+ * single tokens the work list's item count rounded up to 256: the captured
+ * decode grid, whose CTAs past the count return at once) and replayed; the
+ * decode's max_seq_len is then that number of partitions times the partition
+ * size, an upper bound of the lengths (at most 32 graphs are kept; capture
+ * happens on a private stream).  With use_graph == 0 the same copies and kernels are
  * enqueued one by one on every run, with the exact maximum length.  Graphs
  * save host time when a step has many short kernels (many layers); a step of
  * a few long kernels gains nothing from them.
@@ -712,8 +714,8 @@ void pkv_step_destroy(pkv_step *s);
  *   1. wait until the runner's previous run has finished on the GPU;
  *   2. check that every sequence has room for q_len more tokens in
  *      max_blocks_per_seq blocks (PKV_ERR_RANGE, nothing changed, if not);
- *      with use_graph, capture the step's graph if this (n, partition count)
- *      has none yet (a failed capture returns its error, nothing changed);
+ *      with use_graph, capture the step's graph if its key (above) has none
+ *      yet (a failed capture returns its error, nothing changed);
  *   3. pkv_seq_append_batch of q_len tokens each (its errors are returned and
  *      change nothing), slots into host_stage; pkv_block_table of the n
  *      sequences into host_stage;

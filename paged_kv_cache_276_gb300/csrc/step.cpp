@@ -23,6 +23,7 @@
 namespace {
 
 constexpr int kMaxGraphs = 32;
+constexpr int kGridGranule = 256;  // decode CTAs a captured graph may launch beyond the item count
 constexpr int kRepick = 64;  // steps between two picks of the work list's partition
 constexpr int kDefaultPartition = 768;  // paged_attention_decode's default
 
@@ -56,7 +57,10 @@ struct pkv_step {
   cudaEvent_t start = nullptr, copied_out = nullptr;
   std::vector<cudaEvent_t> layer_in, layer_done;  // per group of layers: its inputs landed, its kernels finished
   bool pending = false;
-  std::map<std::tuple<int, int, int>, cudaGraphExec_t> graphs;  // (n, partitions, partition size)
+  // (n, partitions, partition size, decode grid): the grid is the work list's
+  // item count rounded up to kGridGranule, so a graph launches few idle CTAs
+  // and is captured again only when the count passes its granule
+  std::map<std::tuple<int, int, int, int>, cudaGraphExec_t> graphs;
   int auto_part = 0, auto_n = 0, auto_age = 0;  // the work list's partition pick, kept between steps
 };
 
@@ -345,14 +349,15 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
   const int part = partition > 0 ? partition : s->part;
   if (c.use_graph) {
     const int parts = max_len > 0 ? (max_len + part - 1) / part : 1;
-    const auto key = std::make_tuple(n, parts, part);
+    // the work list of any step with this key has at most n x KV heads x parts items
+    const int most = c.q_len == 1 ? n * c.num_kv_heads * parts : 0;
+    const int grid = c.q_len == 1 ? std::min(most, (count + kGridGranule - 1) / kGridGranule * kGridGranule) : 0;
+    const auto key = std::make_tuple(n, parts, part, grid);
     auto it = s->graphs.find(key);
     if (it == s->graphs.end()) {
       if (static_cast<int>(s->graphs.size()) >= kMaxGraphs) drop_graphs(s);
       const long long bound = static_cast<long long>(parts) * part;
-      // the work list of any step with this key has at most n x KV heads x parts items
-      const int grid_items = c.q_len == 1 ? n * c.num_kv_heads * parts : 0;
-      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), grid_items, partition, &exec);
+      rc = capture(s, n, bound < cap ? static_cast<int>(bound) : static_cast<int>(cap), grid, partition, &exec);
       if (rc != PKV_OK) return rc;
       it = s->graphs.emplace(key, exec).first;
     }
