@@ -191,7 +191,9 @@ class DecodeSession:
                  per_layer_out=None, fused=False, planned=False):
         """One pass of the hot path over every layer.  fused (single-token steps):
         the new tokens' store runs inside the decode grid (paged_attention_decode_write);
-        planned: that grid runs the host-built work list (paged_attention_decode_items)."""
+        planned: that grid runs the host-built work list (paged_attention_decode_items),
+        each layer overlapping the one before (PKV_DECODE_OVERLAP; not behind the
+        layer's copy-on-write copies, which it reads)."""
         fused = fused and self.q_len == 1
         for l in range(self.layers):
             if step.cow_pairs is not None:
@@ -201,7 +203,7 @@ class DecodeSession:
                 native.paged_attention_decode_items(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
                                                     step.tables, step.lens, step.max_len, self.scale, o, step.items,
                                                     workspace=workspace, partition_size=step.partition,
-                                                    d_status=d_status, stream=stream)
+                                                    d_status=d_status, stream=stream, overlap=step.cow_pairs is None)
                 continue
             if fused:
                 native.paged_attention_decode_write(q, ks[l], vs[l], step.slots, self.k_caches[l], self.v_caches[l],
