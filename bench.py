@@ -718,7 +718,8 @@ def prefill_bench(device, steps=10, warmup=3, only=None, cpu=False, compact=Fals
             res[tag] = {"ms": round(am, 5), "roofline": roof, "kv_gbs": round(kv_gbs, 1),
                         "rows_s": round(case.total_q / (sm * 1e-3), 1), "step_ms": round(sm, 5)}
             if mixed:
-                res[tag]["call"] = f"paged_attention_mixed ({case.mixed_nd} decodes, chunks on {case.mixed_ctas} CTAs)"
+                res[tag]["call"] = (f"paged_attention_mixed ({case.mixed_nd} decodes in {case.mixed_part}-token partitions, "
+                                    f"chunks on {case.mixed_ctas} CTAs over their list)")
             if split:  # the same call without the split, for comparison
                 res[tag]["call"] = f"paged_attention_prefill_ex (keys split into {split}-token partitions)"
                 us = []

@@ -429,7 +429,10 @@ int pkv_prefill_items(const int32_t *seq_lens, const int32_t *q_start, int num_s
  *                 paged_attention_decode_items
  *   max_decode_len, decode_partition_size, workspace: as max_seq_len,
  *                 partition_size and workspace of paged_attention_decode for
- *                 the num_decodes decodes (paged_attention_workspace_size)
+ *                 the num_decodes decodes (paged_attention_workspace_size).
+ *                 Beside a long chunk grid the decodes may run unsplit (a
+ *                 partition of at least max_decode_len: no merge, no
+ *                 workspace), since they only need to end before the chunks.
  *   prefill_ctas  the chunks' persistent grid: at most this many CTAs, one per
  *                 SM (0: every SM); the decodes' CTAs take the other SMs from
  *                 the start and every SM the chunks free later.  Size it to the

@@ -254,6 +254,32 @@ def mixed_prefill_ctas(case, sms: int = 152) -> int:
     return int(min(sms, max(sms // 2, round(sms * tc / (tc + td / 2)))))
 
 
+# One decode CTA streams at most this many bytes per second (its ring's bytes
+# in flight over the copy latency; measured by a per-CTA trace of the kernel).
+DECODE_CTA_BYTES_PER_S = 28e9
+
+
+def mixed_decode_partition(case, prefill_ctas: int, sms: int = 152) -> int:
+    """Partition size of the decodes of a mixed step.  Beside a chunk grid the
+    decodes run on the SMs the chunks leave for most of the step, so their
+    longest item only has to end before the chunks do: when one whole decode
+    (a sequence's KV head, unsplit) streams in under half the chunks' estimated
+    time, the decodes run unsplit (no merge kernel, fewer and longer items);
+    otherwise the work list picks its partition (0).  Measured on the mixed
+    workload: unsplit 0.531-0.539 ms at 84-89 chunk CTAs, 2048-token partitions
+    0.551-0.553 ms."""
+    nd = case.num_decodes
+    if nd == 0 or nd == case.B or prefill_ctas <= 0:
+        return 0
+    flops_chunks = 4 * case.d * case.Hq * causal_visible_keys(case.lens[nd:], case.chunks[nd:])
+    t_chunks = flops_chunks / PREFILL_FLOPS_PER_S * sms / min(sms, prefill_ctas)
+    longest = int(case.lens[:nd].max())
+    t_item = longest * 2 * case.d * 2 / DECODE_CTA_BYTES_PER_S
+    if t_item >= t_chunks / 2:
+        return 0
+    return -(-longest // case.bs) * case.bs  # whole blocks: one partition per sequence
+
+
 class PrefillCase:
     """One chunked-prefill batch resident on the device.
 
@@ -308,19 +334,22 @@ class PrefillCase:
         return nd
 
     def prepare_mixed(self, prefill_ctas=None, partition_size=0, chunk_list=True):
-        """Work list and workspace of the leading decodes; the chunks' grid cap
-        (default: mixed_prefill_ctas) and, with chunk_list, their host-built
-        work list for that grid."""
+        """Work list and workspace of the leading decodes (partition_size 0:
+        mixed_decode_partition's choice); the chunks' grid cap (default:
+        mixed_prefill_ctas) and, with chunk_list, their host-built work list
+        for that grid."""
         nd = self.num_decodes
         self.mixed_nd = nd
         self.mixed_max_len = int(self.lens[:nd].max()) if nd else 0
+        self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
+        if partition_size == 0:
+            partition_size = mixed_decode_partition(self, self.mixed_ctas)
         host_items = native.pkv_decode_items(self.lens[:nd], self.tables[:nd], self.Hkv, self.bs, partition_size,
                                              self.d)
         self.mixed_part = int(host_items[0, 1])
         self.mixed_items = torch.as_tensor(host_items, device=self.device)
         n = native.paged_attention_workspace_size(nd, 1, self.Hq, self.d, self.mixed_max_len, self.mixed_part)
         self.mixed_ws = torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
-        self.mixed_ctas = mixed_prefill_ctas(self) if prefill_ctas is None else prefill_ctas
         self.mixed_chunk_items = None
         if chunk_list and nd < self.B and self.mixed_ctas > 0:
             w = native.pkv_prefill_items(self.lens[nd:], self.q_start[nd:], self.total_q, self.Hq, self.Hkv,
