@@ -236,15 +236,16 @@ def causal_visible_keys(lens, chunks) -> int:
 
 # Rates of the two halves of a mixed step, measured alone on one GB300 (whole
 # GPU): chunked prefill on the tensor cores and the decode kernel's streaming.
-PREFILL_FLOPS_PER_S = 1.25e15
+PREFILL_FLOPS_PER_S = 1.4e15
 DECODE_BYTES_PER_S = 5.0e12
 
 
 def mixed_prefill_ctas(case, sms: int = 152) -> int:
     """SMs for the chunks of a mixed step.  The decodes saturate HBM on about
     half the SMs, so the chunks get their share of the two halves' times with
-    the decodes' time counted half (at least half the SMs): measured on the
-    mixed workload, 88 to 152 chunk CTAs all give 0.62-0.63 ms, 64 gives 0.76."""
+    the decodes' time counted half (at least half the SMs).  Measured on the
+    mixed workload with unsplit decodes: 0.531-0.539 ms at 84-89 chunk CTAs,
+    0.549-0.553 ms at 92-104, 0.63-0.64 ms at 76."""
     nd = case.num_decodes
     flops_chunks = 4 * case.d * case.Hq * causal_visible_keys(case.lens[nd:], case.chunks[nd:])
     bytes_dec = int(case.lens[:nd].astype(np.int64).sum()) * 2 * case.Hkv * case.d * 2
