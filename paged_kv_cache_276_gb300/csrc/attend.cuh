@@ -21,12 +21,14 @@ namespace attend {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleSlack = 8.f;  // log2 units: weights stay below 256
 
-// Shared-memory address of the 16-byte chunk `dchunk` of tile row `row`,
-// matching the TMA 128-byte swizzle (chunk index XOR row mod 8 inside each
-// 1024-byte atom; every box starts 1024-byte aligned).
-template <int BS>
+// Shared-memory address of the 16-byte chunk `dchunk` of tile row `row`.  The
+// tile is staged as boxes of R rows, each [64-column half][R rows][128 bytes]
+// (HALVES halves), with the TMA 128-byte swizzle: chunk index XOR row mod 8
+// inside each 1024-byte atom; every box starts 1024-byte aligned.
+template <int R, int HALVES>
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int dchunk) {
-  return base + (dchunk >> 3) * (BS * 128) + row * 128 + ((((dchunk & 7) ^ (row & 7))) << 4);
+  return base + (row / R) * (HALVES * R * 128) + (dchunk >> 3) * (R * 128) + (row % R) * 128 +
+         ((((dchunk & 7) ^ (row & 7))) << 4);
 }
 
 template <int D, int NT>
@@ -88,11 +90,11 @@ __device__ __forceinline__ void online_max_update(WarpAcc<D, NT> &acc, float (&b
   }
 }
 
-// One block of keys for one warp's columns.
+// One staged unit of BS keys (boxes of R rows, see swz) for one warp's columns.
 //   qf:    B fragments of Q^T (column = query row) per n-tile and 16-wide d step
-//   valid: keys of this block that hold tokens (1..BS)
-//   vis:   keys of this block visible to each of the thread's columns
-template <int D, int BS, int NT>
+//   valid: keys of this unit that hold tokens (1..BS)
+//   vis:   keys of this unit visible to each of the thread's columns
+template <int D, int BS, int NT, int R = BS>
 __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
                                              const uint32_t (&qf)[NT][D / 16][2], uint32_t kbase,
                                              uint32_t vbase, int valid, const int (&vis)[NT][2],
@@ -115,7 +117,7 @@ __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       uint32_t a[4];
-      ldsm_x4(swz<BS>(kbase, mt * 16 + r8 + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
+      ldsm_x4(swz<R, D / 64>(kbase, mt * 16 + r8 + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if (ks & 1) mma_bf16_16816(sc2[mt][nt], a, qf[nt][ks][0], qf[nt][ks][1]);
@@ -170,7 +172,7 @@ __device__ __forceinline__ void attend_block(WarpAcc<D, NT> &acc,
 #pragma unroll
     for (int md = 0; md < D / 16; ++md) {
       uint32_t a[4];
-      ldsm_x4_trans(swz<BS>(vbase, kt * 16 + r8 + (mi >> 1) * 8, md * 2 + (mi & 1)), a);
+      ldsm_x4_trans(swz<R, D / 64>(vbase, kt * 16 + r8 + (mi >> 1) * 8, md * 2 + (mi & 1)), a);
       if (tail) {  // slots past the sequence end were never written: keep NaNs out
         a[0] &= m0;
         a[1] &= m0;

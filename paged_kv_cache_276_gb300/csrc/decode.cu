@@ -91,28 +91,40 @@ struct Params {
   int wait_before_writes;
 };
 
-// A block is staged as one or more "units" of consecutive token rows: the
-// whole block for block sizes 16 and 32, 32-row pieces for 64 and 128 (whole
-// tiles would leave too few ring stages for four consumer warps; 32 rows make
-// the same TMA boxes as block 32, which streams best).
+// Keys are staged in "units" of 32 consecutive token rows of one partition,
+// one unit per ring stage: two whole blocks for block size 16, the whole block
+// for 32, 32-row pieces for 64 and 128 (whole tiles would leave too few ring
+// stages for four consumer warps).  A unit is copied as kSub boxes of kBoxRows
+// rows per tensor (one box per block for 16 and 32).  Measured with half the
+// SMs streaming: 16-row units (one block of 16 per stage) 57 GB/s per SM,
+// 32-row units 83.
 template <int BS>
 struct Unit {
   static_assert(BS == 16 || BS == 32 || BS == 64 || BS == 128, "block size 16, 32, 64 or 128");
-  static constexpr int kRows = BS <= 32 ? BS : 32;
-  static constexpr int kPerBlock = BS / kRows;
+  static constexpr int kRows = 32;
+  static constexpr int kBoxRows = BS < 32 ? BS : 32;  // rows of one copy
+  static constexpr int kSub = kRows / kBoxRows;        // copies per unit and tensor
+  static constexpr int kPieces = BS / kBoxRows;        // copies per block
 };
 
-template <int D, int BS>
+// Staged unit in shared memory, per tensor: [sub-box][half][kBoxRows rows][64
+// bf16] with the 128-byte swizzle (R = kBoxRows rows per sub-box; one sub-box
+// unless block 16).
+template <int D, int ROWS, int R>
 struct Tile {
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
-  static_assert(BS % 16 == 0, "block_size must be a multiple of 16");
-  static constexpr int kHalves = D / 64;               // 128-byte-wide TMA boxes per row
-  static constexpr int kBoxBytes = BS * 128;           // one box: BS rows x 64 bf16
-  static constexpr int kTileBytes = kHalves * kBoxBytes;  // K (or V) of one block
+  static_assert(ROWS % R == 0 && R % 16 == 0, "whole boxes of 16-row multiples");
+  static constexpr int kHalves = D / 64;                  // 64-column (128-byte) halves of a row
+  static constexpr int kHalfBytes = R * 128;              // one half of a box's rows
+  static constexpr int kBoxBytes = kHalves * kHalfBytes;  // one copy
+  static constexpr int kTileBytes = (ROWS / R) * kBoxBytes;  // K (or V) of one unit
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kStages = (65536 / kStageBytes) < 8 ? (65536 / kStageBytes) : 8;
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
+
+template <int D, int BS>
+using UnitTile = Tile<D, Unit<BS>::kRows, Unit<BS>::kBoxRows>;
 
 __device__ __forceinline__ int clamp_len(const Params &p, int seq, int block_size, bool report) {
   int L = p.seq_lens[seq];
@@ -189,20 +201,31 @@ __device__ __forceinline__ uint4 new_token_chunk(const Params &p, int seq, int h
 // entry is checked against it afterwards (PKV_STATUS_BAD_ITEM if they differ).
 template <int D, int BS>
 __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p, int seq, int h,
-                        int blk0, int nunit, int window0, int b0, uint32_t ring, uint32_t full0, uint32_t empty0,
+                        int blk0, int ntok, int window0, int b0, uint32_t ring, uint32_t full0, uint32_t empty0,
                         volatile int *abort_flag, int lane) {
   using U = Unit<BS>;
-  using T = Tile<D, U::kRows>;
+  using T = UnitTile<D, BS>;
   constexpr int S = T::kStages;
   const uint64_t pol = l2_policy_evict_first();
   const int32_t *tbl = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
-  const int nblk = (nunit + U::kPerBlock - 1) / U::kPerBlock;
+  const int nunit = (ntok + U::kRows - 1) / U::kRows;
+  const int nbox = (ntok + U::kBoxRows - 1) / U::kBoxRows;  // copies per tensor of this partition
+  const int nblk = (ntok + BS - 1) / BS;                    // its table entries
   int issued = 0;
   int window = lane < nblk ? window0 : -1;
-  for (int j = 0; j < nunit; ++j) {
-    const int e = j / U::kPerBlock, piece = j - e * U::kPerBlock;  // table entry, unit within the block
-    if (piece == 0 && (e & 31) == 0 && e > 0) window = e + lane < nblk ? tbl[e + lane] : -1;
+  // source row of copy q of the partition (past its end: the zero-fill row);
+  // warp-uniform: the lanes hold the current window of 32 table entries
+  auto source_row = [&](int q) {
+    const int e = q / U::kPieces, piece = q - e * U::kPieces;  // table entry, copy within the block
+    if (q < nbox && piece == 0 && (e & 31) == 0 && e > 0) window = e + lane < nblk ? tbl[e + lane] : -1;
     const int b = e == 0 && b0 >= 0 ? b0 : __shfl_sync(0xffffffffu, window, e & 31);
+    if (q >= nbox) return p.oob_row;
+    if (b >= 0 && b < p.num_blocks) return (b * p.num_kv_heads + h) * BS + piece * U::kBoxRows;
+    if (lane == 0 && p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
+    return p.oob_row;  // zero fill
+  };
+  for (int j = 0; j < nunit; ++j) {
+    const int row0 = source_row(j * U::kSub);
     const int s = j % S;
     bool ok = true;
     if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) ok = false;
@@ -214,22 +237,26 @@ __device__ void produce(const CUtensorMap *tmk, const CUtensorMap *tmv, const Pa
       }
       break;
     }
-    if (lane == 0) {
-      int row;
-      if (b >= 0 && b < p.num_blocks) {
-        row = (b * p.num_kv_heads + h) * BS + piece * U::kRows;
-      } else {
-        if (p.status) atomicOr(p.status, PKV_STATUS_BAD_BLOCK);
-        row = p.oob_row;  // zero fill
+    const uint32_t full = full0 + 8 * s;
+    const uint32_t kdst = ring + s * T::kStageBytes;
+    const uint32_t vdst = kdst + T::kTileBytes;
+    if (lane == 0) mbar_arrive_expect_tx(full, T::kStageBytes);
+    // one copy per box: with head_dim 128 the map's box holds both 64-column
+    // halves of its rows, half after half (the layout the consumers read);
+    // fewer, larger copies stream faster per SM than one per half.  A unit's
+    // first copy goes out before the rows of its others are looked up.
+#pragma unroll
+    for (int k = 0; k < U::kSub; ++k) {
+      const int row = k == 0 ? row0 : source_row(j * U::kSub + k);
+      if (lane == 0) {
+        if constexpr (T::kHalves == 2) {
+          tma_load_3d(kdst + k * T::kBoxBytes, tmk, 0, row, 0, full, pol);
+          tma_load_3d(vdst + k * T::kBoxBytes, tmv, 0, row, 0, full, pol);
+        } else {
+          tma_load_2d(kdst + k * T::kBoxBytes, tmk, 0, row, full, pol);
+          tma_load_2d(vdst + k * T::kBoxBytes, tmv, 0, row, full, pol);
+        }
       }
-      const uint32_t full = full0 + 8 * s;
-      mbar_arrive_expect_tx(full, T::kStageBytes);
-      const uint32_t kdst = ring + s * T::kStageBytes;
-      const uint32_t vdst = kdst + T::kTileBytes;
-#pragma unroll
-      for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(kdst + hf * T::kBoxBytes, tmk, hf * 64, row, full, pol);
-#pragma unroll
-      for (int hf = 0; hf < T::kHalves; ++hf) tma_load_2d(vdst + hf * T::kBoxBytes, tmv, hf * 64, row, full, pol);
     }
     ++issued;
   }
@@ -248,13 +275,13 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                   const Params p) {
   using U = Unit<BS>;
-  using T = Tile<D, U::kRows>;
+  using T = UnitTile<D, BS>;
   constexpr int S = T::kStages;
   constexpr int COLS = NT * 8;
   constexpr int DP = D + 4;  // padded row of the merge buffer
   static_assert(kDecodeWarps * COLS * DP * 4 + 2 * kDecodeWarps * COLS * 4 <= T::kRingBytes,
                 "merge buffer must fit in the ring");
-  // Block j goes to stage j % S and to consumer warp j % kDecodeWarps.  Every
+  // Unit j goes to stage j % S and to consumer warp j % kDecodeWarps.  Every
   // use of a stage must go to the same warp, else a warp could wait on a
   // stage two phases ahead of the barrier and pass the parity test early.
   static_assert(S % kDecodeWarps == 0, "ring stages must be a multiple of the consumer warps");
@@ -332,7 +359,7 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
         else p.v_cache[dst * (D / 8) + lane - D / 8] = c;
       }
     }
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, b0, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, ntok, window0, b0, ring, full0, empty0, abort_flag, lane);
   } else {
     const int g4 = lane >> 2, c4 = lane & 3;
     uint32_t qf[NT][D / 16][2];
@@ -369,20 +396,21 @@ __global__ void __launch_bounds__((kDecodeWarps + 1) * 32)
       if (j == patch_unit) {  // 128-byte swizzle: chunk c of row r sits at chunk c ^ (r % 8)
         if (lane < D / 4) {
           const int v = lane >= D / 8, c = v ? lane - D / 8 : lane;
-          const uint32_t dst = ring + s * T::kStageBytes + v * T::kTileBytes + (c >> 3) * T::kBoxBytes +
-                               patch_row * 128 + (((c & 7) ^ (patch_row & 7)) << 4);
+          const int box = patch_row / U::kBoxRows, r = patch_row - box * U::kBoxRows;
+          const uint32_t dst = ring + s * T::kStageBytes + v * T::kTileBytes + box * T::kBoxBytes +
+                               (c >> 3) * T::kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(patch.x), "r"(patch.y),
                        "r"(patch.z), "r"(patch.w)
                        : "memory");
         }
         __syncwarp();
       }
-      const int valid = min(U::kRows, L - (tok0 + j * U::kRows));
+      const int valid = min(U::kRows, ntok - j * U::kRows);  // a partition may end inside a unit
       int vis[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) vis[nt][0] = vis[nt][1] = valid;
       const uint32_t kb = ring + s * T::kStageBytes;
-      attend_block<D, U::kRows, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+      attend_block<D, U::kRows, NT, U::kBoxRows>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
       if (*abort_flag) break;
@@ -452,7 +480,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
     chunk_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Params p) {
   using U = Unit<BS>;
-  using T = Tile<D, U::kRows>;
+  using T = UnitTile<D, BS>;
   constexpr int S = T::kStages;
   constexpr int NT = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -495,7 +523,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
   __syncthreads();
 
   if (warp == kChunkWarps) {
-    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, nunit, window0, -1, ring, full0, empty0, abort_flag, lane);
+    produce<D, BS>(&tmk, &tmv, p, seq, h, blk0, ntok, window0, -1, ring, full0, empty0, abort_flag, lane);
     return;
   }
   if (warp >= p.active_warps) return;
@@ -538,7 +566,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
       break;
     }
     const int key0 = tok0 + j * U::kRows;
-    const int valid = min(U::kRows, L - key0);
+    const int valid = min(U::kRows, ntok - j * U::kRows);  // a partition may end inside a unit
     int vis[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -546,7 +574,7 @@ __global__ void __launch_bounds__((kChunkWarps + 1) * 32)
       vis[nt][1] = min(valid, nvis[nt][1] - key0);
     }
     const uint32_t kb = ring + s * T::kStageBytes;
-    attend_block<D, U::kRows, NT>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
+    attend_block<D, U::kRows, NT, U::kBoxRows>(acc, qf, kb, kb + T::kTileBytes, valid, vis, p.scale_log2, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     if (*abort_flag) {
@@ -652,11 +680,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The cache as a 2-D bf16 tensor: rows = num_blocks * Hkv * block_size, each of
-// head_dim elements; a box is box_rows rows x 64 elements (128 bytes).
+// The cache as a bf16 tensor of rows = num_blocks * Hkv * block_size rows of
+// head_dim elements, read box_rows rows at a time with the 128-byte swizzle
+// (64 elements wide).  head_dim 64: 2-D, a box is box_rows x 64.  head_dim 128:
+// 3-D (64 columns, rows at a 256-byte stride, the two halves of a row at a
+// 128-byte stride), a box is 64 x box_rows x 2, so one copy stages a unit's
+// rows as [half][row][64], the layout of two 2-D boxes side by side.
 bool make_cache_map(CUtensorMap *map, const void *base, int head_dim, int box_rows, long long rows) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  if (head_dim == 128) {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 2};
+    cuuint64_t strides[2] = {256, 128};  // bytes, dimensions 1 and 2
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
@@ -692,7 +733,7 @@ bool make_plan(int num_seqs, int q_len, int num_q_heads, int head_dim, int max_s
 
 template <int D, int BS>
 constexpr size_t smem_bytes() {
-  using T = Tile<D, Unit<BS>::kRows>;
+  using T = UnitTile<D, BS>;
   return T::kRingBytes + 2 * T::kStages * 8 + 16 + 1024;
 }
 

@@ -116,6 +116,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
 // 2-D tiled TMA load of one box into shared memory; completes `bytes` on `bar`.
 // Coordinates are in elements: x = innermost (must be a multiple of 8 for bf16),
 // y = row.  Rows outside the tensor read as zeros.
+__device__ __forceinline__ void tma_load_3d(uint32_t smem_dst, const void *tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void *tmap, int x, int y,
                                             uint32_t bar, uint64_t policy) {
   asm volatile(
