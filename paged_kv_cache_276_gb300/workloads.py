@@ -234,30 +234,72 @@ def causal_visible_keys(lens, chunks) -> int:
     return total
 
 
-# Rates of the two halves of a mixed step, measured alone on one GB300 (whole
-# GPU): chunked prefill on the tensor cores and the decode kernel's streaming.
+# Rates of the two halves of a mixed step on one GB300 (measured): chunked
+# prefill on the tensor cores (whole GPU, and per prefill-list cost unit on one
+# CTA per SM: a pair's 128-key tile, a lone query tile's 0.55, 2 per item), the
+# decode kernel over the whole GPU and per SM when only part of the GPU streams
+# (the rest busy, HBM not saturated).
 PREFILL_FLOPS_PER_S = 1.4e15
-DECODE_BYTES_PER_S = 5.0e12
+CHUNK_UNIT_S = 1.68e-6
+DECODE_BYTES_PER_S = 6.3e12
+DECODE_SM_BYTES_PER_S = 75e9
+
+
+def prefill_item_costs(lens, q_start, total_q: int, num_q_heads: int, num_kv_heads: int) -> np.ndarray:
+    """Cost of every item of a prefill launch, in the kernel's item order, by
+    the model pkv_prefill_items balances: per sequence, per KV head, the pairs
+    of query tiles (or lone tiles) from the last one back; an item costs its
+    128-key tiles (a lone tile's at 0.55 of a pair's) plus 2."""
+    group = num_q_heads // num_kv_heads
+    tile_tok = 128 // group
+    pairs = total_q >= 2 * tile_tok * len(lens)  # the launch's schedule, as prefill_entry picks it
+    span = 2 * tile_tok if pairs else tile_tok
+    out = []
+    for s in range(len(lens)):
+        c, L = int(q_start[s + 1]) - int(q_start[s]), max(0, int(lens[s]))
+        nparts = -(-c // span)
+        qt = np.arange(nparts - 1, -1, -1)
+        k_hi = np.minimum(L, np.maximum(0, L - c + np.minimum(c, span * (qt + 1))))
+        pair = pairs & ((2 * qt + 1) * tile_tok < c)
+        cost = np.where(pair, 1.0, 0.55) * -(-k_hi // 128) + 2.0
+        out.extend([cost] * num_kv_heads)
+    return np.concatenate(out) if out else np.zeros(0)
+
+
+def mixed_step_time(case, prefill_ctas: int, sms: int = 152) -> float:
+    """Estimated seconds of a mixed step with the chunks on a grid of
+    prefill_ctas CTAs over their host-built list: the chunks end with their
+    most loaded CTA; until then the decodes stream on the other SMs, after that
+    on the whole GPU."""
+    nd = case.num_decodes
+    work = native.pkv_prefill_items(case.lens[nd:], case.q_start[nd:], case.total_q, case.Hq, case.Hkv,
+                                    prefill_ctas)
+    cost = prefill_item_costs(case.lens[nd:], case.q_start[nd:], case.total_q, case.Hq, case.Hkv)
+    off = work[2:3 + prefill_ctas]
+    items = work[3 + prefill_ctas:]
+    t_chunks = max(float(cost[items[off[g]:off[g + 1]]].sum()) for g in range(prefill_ctas)) * CHUNK_UNIT_S
+    bytes_dec = float(case.lens[:nd].astype(np.int64).sum()) * 2 * case.Hkv * case.d * 2
+    beside = (sms - prefill_ctas) * DECODE_SM_BYTES_PER_S
+    if beside > 0 and bytes_dec <= beside * t_chunks:
+        return max(t_chunks, bytes_dec / beside)
+    return t_chunks + (bytes_dec - max(0, beside) * t_chunks) / DECODE_BYTES_PER_S
 
 
 def mixed_prefill_ctas(case, sms: int = 152) -> int:
-    """SMs for the chunks of a mixed step.  The decodes saturate HBM on about
-    half the SMs, so the chunks get their share of the two halves' times with
-    the decodes' time counted half (at least half the SMs).  Measured on the
-    mixed workload with unsplit decodes: 0.531-0.539 ms at 84-89 chunk CTAs,
-    0.549-0.553 ms at 92-104, 0.63-0.64 ms at 76."""
+    """Chunk grid of a mixed step: the size from half the SMs up whose
+    estimated step (mixed_step_time) is shortest.  The estimate follows the
+    host list's packing, which moves in steps (the items are few and large
+    against a CTA's share).  Measured on the mixed workload: 0.499 ms at 96
+    CTAs, 0.512 at 104, 0.533 at 112, 0.554 at 90, 0.567 at 84."""
     nd = case.num_decodes
-    flops_chunks = 4 * case.d * case.Hq * causal_visible_keys(case.lens[nd:], case.chunks[nd:])
-    bytes_dec = int(case.lens[:nd].astype(np.int64).sum()) * 2 * case.Hkv * case.d * 2
-    tc, td = flops_chunks / PREFILL_FLOPS_PER_S, bytes_dec / DECODE_BYTES_PER_S
-    if tc + td <= 0:
+    if nd == case.B:
         return 0
-    return int(min(sms, max(sms // 2, round(sms * tc / (tc + td / 2)))))
+    return min(range(sms // 2, sms + 1), key=lambda g: mixed_step_time(case, g, sms))
 
 
 # One decode CTA streams at most this many bytes per second (its ring's bytes
-# in flight over the copy latency; measured by a per-CTA trace of the kernel).
-DECODE_CTA_BYTES_PER_S = 28e9
+# in flight over the copy latency; three CTAs share an SM).
+DECODE_CTA_BYTES_PER_S = 25e9
 
 
 def mixed_decode_partition(case, prefill_ctas: int, sms: int = 152) -> int:
@@ -267,8 +309,8 @@ def mixed_decode_partition(case, prefill_ctas: int, sms: int = 152) -> int:
     (a sequence's KV head, unsplit) streams in under half the chunks' estimated
     time, the decodes run unsplit (no merge kernel, fewer and longer items);
     otherwise the work list picks its partition (0).  Measured on the mixed
-    workload: unsplit 0.531-0.539 ms at 84-89 chunk CTAs, 2048-token partitions
-    0.551-0.553 ms."""
+    workload (decodes staged one 16-row block per stage): unsplit 0.531-0.539
+    ms at 84-89 chunk CTAs, 2048-token partitions 0.551-0.553 ms."""
     nd = case.num_decodes
     if nd == 0 or nd == case.B or prefill_ctas <= 0:
         return 0

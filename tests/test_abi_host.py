@@ -586,6 +586,50 @@ def test_prefill_items_hand_out_every_item_once(native, grid):
             assert max(loads) <= cost.sum() / grid + cost.max() + 1e-9
 
 
+@pytest.mark.parametrize("grid", [7, 89, 152])
+def test_mixed_step_cost_model_prices_the_items_as_the_list_does(native, grid):
+    """workloads.prefill_item_costs (the mixed-step grid policy's cost model)
+    prices every item as pkv_prefill_items balances it: with those costs each
+    CTA's last item went to a least-loaded CTA (the longest-first hand-out's
+    invariant), and its key tiles are the kernel's numbering's."""
+    from paged_kv_cache_276_gb300 import workloads
+    rng = np.random.default_rng(100 + grid)
+    for Hq, Hkv in ((32, 8), (64, 8), (24, 8)):
+        B = 6
+        chunks = rng.integers(0, 1500, B)
+        lens = chunks + rng.integers(0, 9000, B)
+        q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+        total_q = int(q_start[-1])
+        cost = workloads.prefill_item_costs(lens, q_start, total_q, Hq, Hkv)
+        tiles, pairs = _prefill_item_costs(lens, q_start, total_q, Hq, Hkv)
+        assert len(cost) == len(tiles) and np.all(cost >= tiles * 0.55 + 2.0) and np.all(cost <= tiles + 2.0)
+        w = native.pkv_prefill_items(lens, q_start, total_q, Hq, Hkv, grid)
+        off, items = w[2:3 + grid], w[3 + grid:]
+        loads = np.array([cost[items[off[g]:off[g + 1]]].sum() for g in range(grid)])
+        for g in range(grid):
+            if off[g + 1] > off[g]:
+                assert loads[g] - cost[items[off[g + 1] - 1]] <= loads.min() + 1e-6
+
+
+def test_mixed_step_grid_is_the_estimates_minimum(native):
+    """mixed_prefill_ctas on the mixed workload (256 decodes beside two
+    1024-token chunks): at least half the SMs, no estimate below its own."""
+    import types
+    from paged_kv_cache_276_gb300 import inputs, workloads
+    pw = inputs.PREFILL_WORKLOADS["prefill_mixed"]
+    lens, chunks = inputs.prefill_shape(pw)
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    case = types.SimpleNamespace(lens=lens, chunks=chunks, q_start=q_start, total_q=int(q_start[-1]),
+                                 Hq=pw.num_q_heads, Hkv=pw.num_kv_heads, d=pw.head_dim, B=len(lens),
+                                 num_decodes=int((chunks == 1).sum()), bs=pw.block_size)
+    g = workloads.mixed_prefill_ctas(case)
+    assert 76 <= g <= 152
+    t = workloads.mixed_step_time(case, g)
+    assert all(t <= workloads.mixed_step_time(case, x) for x in range(76, 153, 4))
+    # the decodes (up to 4096 tokens) run unsplit beside the chunks
+    assert workloads.mixed_decode_partition(case, g) == 4096
+
+
 def test_prefill_items_rejects_bad_arguments(native):
     lens = np.array([100, 200], dtype=np.int32)
     qs = np.array([0, 50, 150], dtype=np.int32)
