@@ -85,9 +85,12 @@ enum : int {
 
 // Tiles and shared-memory plan of each schedule.
 //  * prefill (compute-bound): 128-key tiles.  S = Q K^T is one N = 128 product
-//    per 16 head dims, and P V one K = 128 product; a set writes its weights P
-//    over its own S buffer, so a score product waits for the set's previous
-//    P V product (which reads that P).  Two key and two value stages.
+//    per 16 head dims, and P V one K = 128 product.  Over single query tiles a
+//    set writes its weights P over its own S buffer, so a score product waits
+//    for the set's previous P V product (which reads that P); over pairs the
+//    two sets share one S buffer and keep their P in columns of their own (the
+//    kernel's tP0), so a score product only waits for the previous one to be
+//    read.  Two key and two value stages.
 //  * decode chunk (bandwidth-bound): 64-key tiles, 4 key and 4 value stages,
 //    and P in its own buffers, so the score products run ahead of the P V
 //    products: finer, deeper rings keep more copies in flight.
@@ -118,7 +121,8 @@ struct Layout {
   // tensor memory: O accumulators at 0 and D, S buffers at 2 D (+kTK); P in
   // the upper half of its S buffer (prefill: keys 0..63 over S columns 64..95,
   // keys 64..127 over 96..127, written after those scores are read) or after
-  // the S buffers
+  // the S buffers.  Prefill over pairs of query tiles uses the first S buffer
+  // only and puts P where the second one starts (the kernel's tP0).
   static constexpr int kTmemS = 2 * D;
   static constexpr int kTmemP = kPOverS ? kTmemS + kTK / 2 : kTmemS + 2 * kTK;
   static constexpr int kPStride = kPOverS ? kTK : kTK / 2;        // columns between the two sets' P
@@ -512,7 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int I = prefix[B];
   const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + Lay::kSmemK), sV = smem_u32(smem + Lay::kSmemV);
   const uint32_t tS0 = tmem + Lay::kTmemS;  // S buffers after the two accumulators
-  const uint32_t tP0 = tmem + Lay::kTmemP;  // P buffers: over the S buffers (prefill) or after them
+  // P buffers: over pairs of query tiles the two sets share one S buffer (a
+  // score product goes out once the previous one has been read) and write
+  // their weights to columns of their own after it; otherwise over the S
+  // buffers (prefill) or after them (decode chunk)
+  const uint32_t tP0 = tmem + (kP2 ? Lay::kTmemS + kTileKeys : Lay::kTmemP);
+  constexpr int kPStr = kP2 ? kTileKeys / 2 : Lay::kPStride;  // columns between the two sets' P
+  static_assert(!kP2 || 2 * D + kTileKeys + 2 * (kTileKeys / 2) <= kTmemCols, "tensor memory");
   const bool has_work = kPrefill ? static_cast<int>(blockIdx.x) < I
                                  : range_first(blockIdx.x, I) < range_first(blockIdx.x + 1, I);
 
@@ -622,9 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
       // ------------------------------------------------- S = Q K^T issuer
       // A score product waits for its key stage and for its S buffer: in
-      // prefill the buffer holds the set's previous P until that tile's P V
-      // product completes; in the decode chunk it is free once the softmax has
-      // read it, so the score products run ahead.  Each releases its key stage
+      // prefill over single query tiles the buffer holds the set's previous P
+      // until that tile's P V product completes; over pairs and in the decode
+      // chunk it is free once the softmax has read it, so the score products
+      // run ahead.  Each releases its key stage
       // when it completes.  The waits are plain try_wait loops (woken on
       // completion), so each issue follows its event closely.
       if (lane == 0) {
@@ -633,15 +644,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc.begin(p, tab, I);
         int g = 0, tpieces = 0;
         bool ok = true;
-        int na = 0, nb = 0;  // prefill: score products of each query tile of the pair so far
+        int ns = 0;  // pairs: score products into the shared S buffer so far
         for (; sc.valid() && ok; sc.advance(p, tab)) {
           const Item &x = sc.x;
           const int ntile = ceil_div(x.k_hi - x.k_lo, kTileKeys);
           if (ntile == 0) continue;
           if constexpr (kP2) {
-            // both query tiles of the pair against each key tile: tile A into
-            // S buffer 0, tile B into buffer 1; each buffer holds its tile's
-            // previous P until that P V product completes
+            // both query tiles of the pair against each key tile, A then B,
+            // into the one S buffer: each product goes out once the set that
+            // owned the previous one has read its scores (the sets' weights
+            // have their own columns), so a set's next score product runs
+            // while it computes its softmax
             const int qi = tpieces++;
             if (!mbar_wait(bar(B_Q_FULL0), qi & 1)) { ok = false; break; }
             for (int t = 0; t < ntile && ok; ++t, ++g) {
@@ -649,28 +662,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!mbar_wait(bar(B_K_FULL0 + s), (g / kStages) & 1)) { ok = false; break; }
               const uint32_t kb = sK + s * kKVBytes;
               for (int q = 0; q < (x.has_b ? 2 : 1); ++q) {
-                int &n = q ? nb : na;
-                // Offset tile B's chain by about half a period: on the CTA's
-                // first pair, B's first score product goes out once tile A's
-                // first weights are written, so that from then on one set
-                // computes its softmax while the other set's products run
-                // (issued in the same order, the two chains would stay in step,
-                // both softmaxes at once).  Later pairs keep the offset by
-                // themselves; waiting again there only delays B behind A's
-                // epilogue.
-                if (q == 1 && t == 0 && tpieces == 1 && !mbar_wait(bar(B_P_FULL0), (na - 1) & 1)) {
-                  ok = false;
-                  break;
-                }
-                if (n > 0 && !mbar_wait(bar(B_PV_DONE0 + q), (n - 1) & 1)) { ok = false; break; }
+                if (ns > 0 && !mbar_wait(bar(B_S_FREE0), (ns - 1) & 1)) { ok = false; break; }
                 tc::fence_after();
                 const uint32_t sq = sQ + q * kQBytes;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                  tc::mma(tS0 + q * kTileKeys, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
+                  tc::mma(tS0, tc::desc_sw128(sq + (ks >> 2) * Lay::kQHalf + (ks & 3) * 32, 16, 1024),
                           tc::desc_sw128(kb + (ks >> 2) * Lay::kKVHalf + (ks & 3) * 32, 16, 1024), kIdS, ks > 0);
                 tc::commit(bar(B_S_FULL0 + q));
-                ++n;
+                ++ns;
               }
               if (!ok) break;
               tc::commit(bar(B_K_EMPTY0 + s));  // the keys are read by these products only
@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the item's first product overwrites the accumulator: the previous epilogue must have read it
                 if (t == 0 && items > 1 && !mbar_wait(bar(B_O_FREE + q), (items - 2) & 1)) { ok = false; break; }
                 tc::fence_after();
-                const uint32_t pa = tP0 + q * Lay::kPStride, acc = tmem + q * D;
+                const uint32_t pa = tP0 + q * kPStr, acc = tmem + q * D;
                 // keys kTK/2.. first (P_FULL), keys 0.. once weighted (P_LO)
 #pragma unroll
                 for (int ks = kSteps / 2; ks < kSteps; ++ks)
@@ -861,8 +861,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar(B_S_FULL0 + sb), sphase)) { ok = false; break; }
           const int k0 = x.k_lo + t * kTileKeys;
           const int vis = min(limit, x.k_hi) - k0;  // keys of this tile the row sees
-          const uint32_t tSb = tS0 + sb * kTileKeys + lane_off;      // this row's scores
-          const uint32_t tPb = tP0 + sb * Lay::kPStride + lane_off;  // this row's weights
+          const uint32_t tSb = tS0 + (kP2 ? 0 : sb * kTileKeys) + lane_off;  // this row's scores
+          const uint32_t tPb = tP0 + sb * kPStr + lane_off;                 // this row's weights
           // no row of this warp sees a key of the tile (rows past a short
           // chunk's end): its weights are zero and nothing else changes
           const bool skip = __all_sync(0xffffffffu, vis <= 0);
@@ -936,7 +936,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after();
           if constexpr (Lay::kPOverS) {
             static_assert(kTileKeys == 128, "two 64-key halves");
+            // pairs: this set's previous P V product must be complete before
+            // its weights' columns and its accumulator are written (the score
+            // product of this tile did not wait for it)
+            auto previous_pv_done = [&]() {
+              if (kP2 && n_set > 1 && !wait_warp(bar(B_PV_DONE0 + sb), (n_set - 2) & 1)) return false;
+              tc::fence_after();
+              return true;
+            };
             if (skip) {
+              if constexpr (kP2) {
+                tc::fence_before();
+                mbar_arrive(bar(B_S_FREE0));  // nothing to read: the next score product may go out
+              }
+              if (!previous_pv_done()) { ok = false; break; }
               uint32_t z[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) z[c] = 0u;
@@ -947,14 +960,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive(bar(B_P_LO0 + sb));
             } else {
               if constexpr (kP2) {
-                // the row's 128 scores in one load round; once all are in
-                // registers the weights may go over the buffer's upper half
+                // the row's 128 scores in one load round; once they are in
+                // registers the other set's score product may overwrite them
                 uint32_t sl[64], sh[64];
                 tc::ld32(tSb, *reinterpret_cast<uint32_t(*)[32]>(&sl[0]));
                 tc::ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(&sl[32]));
                 tc::ld32(tSb + 64, *reinterpret_cast<uint32_t(*)[32]>(&sh[0]));
                 tc::ld32(tSb + 96, *reinterpret_cast<uint32_t(*)[32]>(&sh[32]));
                 tc::wait_ld();
+                tc::fence_before();
+                mbar_arrive(bar(B_S_FREE0));
                 mask(sl, 0);
                 mask(sh, 64);
                 const float el = extreme64(sl, neg), eh = extreme64(sh, neg);
@@ -965,11 +980,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 0..63 are weighted
                 uint32_t pk[32];
                 float lsum = weights64(sh, ks2, nm2, pk);
+                if (!previous_pv_done()) { ok = false; break; }
                 tc::st32(tPb + 32, pk);
-                // the set's previous P V product completed before this tile's
-                // score product was issued (the score product waited for it), and
-                // none of this tile's is issued before P_FULL: the accumulator
-                // holds its final value and may be rescaled here
+                // none of this tile's P V products is issued before P_FULL:
+                // the accumulator holds its final value and may be rescaled here
                 rescale_o();
                 if (!zero_tail_values()) { ok = false; break; }
                 publish(B_P_FULL0 + sb);
