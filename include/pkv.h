@@ -243,12 +243,13 @@ int paged_attention_decode_write(const pkv_bf16 *q, const pkv_bf16 *k_new, const
  * and head order), so the CTAs that start first carry the most keys and the
  * shortest partitions fill the end of the grid.  A sequence of length 0 gets
  * one empty item per KV head (its output rows are zeros).
- * partition_size 0 lets the call choose among 768, 1024, 1536 and 2048 tokens
- * (those that are multiples of block_size) the one a schedule model of the
- * decode kernel on a GB300 predicts fastest for these lengths: more, shorter
- * partitions balance the grid's end, fewer longer ones save each CTA's start.
- * A workspace sized for partition 768 (paged_attention_workspace_size with
- * partition_size 0) fits every choice.
+ * partition_size 0 lets the call choose among 768, 1024, 1536, 2048, 3072 and
+ * 4096 tokens (those that are multiples of block_size; 3072 and 4096 only when
+ * block_tables is given and no physical block serves two sequences) the one a
+ * schedule model of the decode kernel on a GB300 predicts fastest for these
+ * lengths: more, shorter partitions balance the grid's end, fewer longer ones
+ * save each CTA's start and the merge.  A workspace sized for partition 768
+ * (paged_attention_workspace_size with partition_size 0) fits every choice.
  *   seq_lens      host, [num_seqs] int32, each in [0, max_blocks_per_seq *
  *                 block_size] (else PKV_ERR_RANGE)
  *   block_tables  host, [num_seqs][max_blocks_per_seq] int32, or NULL

@@ -488,18 +488,25 @@ def test_decode_work_list_is_longest_first_and_complete(native):
 
 def test_decode_work_list_chooses_its_partition():
     """partition_size 0: the list is built for one of 768 / 1024 / 1536 / 2048
-    tokens (a multiple of the block), reported in row 0, and is the list an
-    explicit request for that size gives."""
+    tokens, or 3072 / 4096 when the tables share no block (a multiple of the
+    block), reported in row 0, and is the list an explicit request for that
+    size gives."""
     from paged_kv_cache_276_gb300 import build, native as nat
     build.build()
     rng = np.random.default_rng(4)
     for B, hi, bs in ((32, 4096, 16), (256, 8192, 16), (3, 300, 128), (64, 20000, 32)):
         lens = rng.integers(0, hi, size=B).astype(np.int32)
-        auto = nat.pkv_decode_items(lens, None, 8, bs, 0)
-        part = int(auto[0, 1])
-        assert part in (768, 1024, 1536, 2048) and part % bs == 0
-        assert np.array_equal(auto, nat.pkv_decode_items(lens, None, 8, bs, part))
-        assert auto[0, 0] == sum(max(1, -(-int(L) // part)) for L in lens) * 8
+        mb = -(-hi // bs)
+        private = np.arange(B * mb, dtype=np.int32).reshape(B, mb)
+        shared = private.copy()
+        shared[:, 0] = 7  # every sequence's first block is the same
+        for tables, allowed in ((None, (768, 1024, 1536, 2048)), (shared, (768, 1024, 1536, 2048)),
+                                (private, (768, 1024, 1536, 2048, 3072, 4096))):
+            auto = nat.pkv_decode_items(lens, tables, 8, bs, 0)
+            part = int(auto[0, 1])
+            assert part in allowed and part % bs == 0
+            assert np.array_equal(auto, nat.pkv_decode_items(lens, tables, 8, bs, part))
+            assert auto[0, 0] == sum(max(1, -(-int(L) // part)) for L in lens) * 8
 
 
 def test_decode_items_rejects_bad_arguments_before_launch(native):
