@@ -1078,6 +1078,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             inv = l > 0.f ? 1.f / l : 0.f;
           }
           const size_t orow = static_cast<size_t>(qs[x.seq] + row_tok) * p.num_q_heads + x.head * p.group + gh;
+          // split over keys: this set's query tile has its own partitions (tile
+          // A may end a partition before tile B); its rows take bf16 output from
+          // their only partition, a partial from each of theirs, and nothing
+          // from a partition past their keys
+          int np_q = 1;
+          if (p.part_tokens > 0) {
+            const int c = qc[x.seq];
+            const int kq = min(L, max(0, L - c + min(c, tile_tok * (2 * x.qt + set + 1))));
+            np_q = max(1, ceil_div(kq, p.part_tokens));
+          }
+          const bool to_out = np_q == 1 && x.part == 0, to_ws = np_q > 1 && x.part < np_q;
 #pragma unroll
           for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t ov[32];
@@ -1088,6 +1099,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::wait_ld();
             }
             if (!row_valid) continue;
+            if (to_ws) {  // the unnormalised partial, against this set's reference m
+              float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (orow * p.max_parts + x.part) * D + ch * 32);
+#pragma unroll
+              for (int c4 = 0; c4 < 8; ++c4)
+                dst[c4] = make_float4(__uint_as_float(ov[c4 * 4]), __uint_as_float(ov[c4 * 4 + 1]),
+                                      __uint_as_float(ov[c4 * 4 + 2]), __uint_as_float(ov[c4 * 4 + 3]));
+              continue;
+            }
+            if (!to_out) continue;
             // a thread writes its own row: each store instruction touches one
             // line per lane, so 32-byte stores (when the output allows) halve
             // the requests of this epilogue, which sits between a set's items
@@ -1109,6 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before();
             mbar_arrive(bar(B_O_FREE + set));
           }
+          if (to_ws && row_valid) p.ws_ml[orow * p.max_parts + x.part] = make_float2(m, l);
           continue;
         }
         const int rp = tpieces & 1;
@@ -1415,12 +1436,18 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
   p.scale_log2 = kernel_scale_log2(scale);
   p.work = work;
   cudaStream_t st = as_stream(stream);
+  // Batches of long chunks run over pairs of query tiles, which share every
+  // key and value tile (half the key / value traffic per product); batches
+  // of mostly short chunks (decodes) split each query tile's keys between the
+  // two softmax sets instead, so that both sets work on every item.
+  const bool pairs = static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs;
   if (plan.part_tokens > 0) {
-    // split over keys: single query tiles (every partition item has both softmax
-    // sets), then the merge of each row's partitions
+    // split over keys: the items of either schedule per key partition, then
+    // the merge of each row's partitions
     p.ws_o = static_cast<float *>(workspace);
     p.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) + plan.ws_o_bytes);
-    const int rc = launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
+    const int rc = pairs ? launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas)
+                         : launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
     if (rc != PKV_OK) return rc;
     const long long warps = static_cast<long long>(total_q) * num_q_heads;
     const dim3 grid(static_cast<unsigned>((warps + 7) / 8));
@@ -1440,12 +1467,7 @@ int prefill_entry(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_
     if (e != cudaSuccess) return set_cuda_error(e), PKV_ERR_CUDA;
     return PKV_OK;
   }
-  // Batches of long chunks run over pairs of query tiles, which share every
-  // key and value tile (half the key / value traffic per product); batches
-  // of mostly short chunks (decodes) split each query tile's keys between the
-  // two softmax sets instead, so that both sets work on every item.
-  if (static_cast<long long>(total_q) >= 2ll * tile_tok * num_seqs)
-    return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
+  if (pairs) return launch_tc<true, true>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
   return launch_tc<true, false>(tmq, tmk, tmv, p, block_size, head_dim, st, max_ctas);
 }
 

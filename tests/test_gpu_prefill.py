@@ -420,20 +420,22 @@ def test_prefill_split_over_keys_matches_the_oracle(d, bs, Hq, Hkv, part):
 
 def test_prefill_split_of_a_short_chunk_behind_a_long_context():
     """One 128-token chunk behind 32k cached tokens (64 query / 8 KV heads):
-    8 query tiles x 8 KV heads = 64 units of work unsplit; split into 2048-key
-    partitions it is 1024 units over every SM.  Sampled tiles match the oracle."""
+    8 query tiles x 8 KV heads = 64 units of work unsplit; split over keys it
+    runs as pairs of query tiles, 4 pairs x 8 KV heads x 16 (or 8) partitions
+    of 2048 (or 4096, the benchmark's) keys.  Sampled tiles match the oracle."""
     L, c = 32768, 128
     Hq, Hkv, bs, d = 64, 8, 16, 128
     q, kc, vc, tables, q_start = prefill_case([L], [c], bs, Hq, Hkv, seed=97, d=d)
     scale = float(np.float32(1 / math.sqrt(d)))
     st = status_tensor()
-    out = run_prefill_split(q, kc, vc, tables, [L], q_start, scale, L, 2048, status=st)
-    assert st.item() == 0
-    for lo in (0, 64, 112):  # whole query tiles of 16 tokens
-        ref = OA.paged_attention(bits(q[lo:lo + 16])[None], bits(kc), bits(vc), tables,
-                                 np.array([L - c + lo + 16], dtype=np.int32), num_q_heads=Hq, num_kv_heads=Hkv,
-                                 head_dim=d, block_size=bs, scale=scale, q_len=16)
-        assert_attention_close(out[lo:lo + 16], ref[0], f"tile at row {lo}")
+    for part in (2048, 4096):
+        out = run_prefill_split(q, kc, vc, tables, [L], q_start, scale, L, part, status=st)
+        assert st.item() == 0
+        for lo in (0, 64, 112):  # whole query tiles of 16 tokens
+            ref = OA.paged_attention(bits(q[lo:lo + 16])[None], bits(kc), bits(vc), tables,
+                                     np.array([L - c + lo + 16], dtype=np.int32), num_q_heads=Hq, num_kv_heads=Hkv,
+                                     head_dim=d, block_size=bs, scale=scale, q_len=16)
+            assert_attention_close(out[lo:lo + 16], ref[0], f"tile at row {lo}, partitions of {part}")
 
 
 @pytest.mark.parametrize("ctas", [0, 24, 100])
