@@ -954,7 +954,10 @@ bool tables_share_blocks(const int32_t *lens, const int32_t *tables, int max_blo
   ids.reserve(static_cast<size_t>(total));
   for (int i = 0; i < num_seqs; ++i) {
     const long long nb = (static_cast<long long>(lens[i]) + block_size - 1) / block_size;
-    for (long long j = 0; j < nb && j < max_blocks; ++j) ids.push_back(tables[static_cast<size_t>(i) * max_blocks + j]);
+    for (long long j = 0; j < nb && j < max_blocks; ++j) {
+      const int32_t b = tables[static_cast<size_t>(i) * max_blocks + j];
+      if (b >= 0) ids.push_back(b);  // -1: an entry past the sequence's blocks
+    }
   }
   std::sort(ids.begin(), ids.end());
   return std::adjacent_find(ids.begin(), ids.end()) != ids.end();

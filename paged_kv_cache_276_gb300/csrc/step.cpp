@@ -330,8 +330,18 @@ int pkv_step_run(pkv_step *s, const int64_t *seq_ids, int n, void *stream) {
     // and made again every kRepick steps or when the batch size changes.
     int want = c.partition_size;
     if (want == 0 && s->auto_part > 0 && s->auto_n == n && s->auto_age < kRepick) want = s->auto_part;
+    // When the model picks, it may go past 2048-token partitions only if no
+    // block serves two sequences: the tables before this step's append tell
+    // (an append never makes a block shared), filled here into the staging
+    // rows that the tables after the append overwrite below.
+    const int32_t *share_tables = nullptr;
+    if (want == 0) {
+      std::vector<int32_t> pre_lens(static_cast<size_t>(n));
+      if (pkv_block_table(s->alloc, seq_ids, n, tables, c.max_blocks_per_seq, pre_lens.data()) == PKV_OK)
+        share_tables = tables;
+    }
     // cannot fail: the lengths fit the tables and the list its segment (partitions of at least 768 tokens)
-    if ((rc = pkv_decode_items(lens, nullptr, c.max_blocks_per_seq, n, c.num_kv_heads, c.head_dim, c.block_size,
+    if ((rc = pkv_decode_items(lens, share_tables, c.max_blocks_per_seq, n, c.num_kv_heads, c.head_dim, c.block_size,
                                want, items, s->lay.max_items, &count)) != PKV_OK)
       return rc;
     partition = items[1];
