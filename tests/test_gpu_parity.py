@@ -276,6 +276,10 @@ def test_decode_over_prefix_cached_blocks_equals_private_storage():
     (128, 64, 32, 8, [1, 63, 64, 65, 700, 2049], 512),    # block 64: staged as 16-row units
     (64, 128, 8, 2, [5, 127, 128, 129, 1500], 256),       # block 128
     (128, 128, 16, 1, [77, 1024, 0], 0),                  # block 128, group 16, default partition
+    # block 16 is staged two blocks per 32-row unit: partitions of an odd number
+    # of blocks end inside a unit, whose second block is then past the partition
+    (128, 16, 32, 8, [1, 15, 16, 17, 47, 48, 49, 1500], 48),
+    (64, 16, 8, 2, [33, 700], 16),
 ])
 def test_decode_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=d + bs + Hq + len(lens))
@@ -294,6 +298,7 @@ def test_decode_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     (128, 16, 16, 8, [530], 64),
     (128, 64, 64, 8, [100, 700, 16], 512),        # block 64: warp-MMA chunk kernel
     (64, 128, 8, 2, [1000, 3], 256),              # block 128
+    (128, 16, 48, 8, [100, 530], 48),             # group 6, block 16: 3-block partitions end inside a unit
 ])
 def test_chunked_causal_query_matches_oracle(d, bs, Hq, Hkv, lens, partition):
     q, kc, vc, tables = random_case(lens, d, bs, Hq, Hkv, seed=3 + d + bs + Hq, q_len=16)
@@ -786,7 +791,8 @@ def test_decode_write_on_the_tensor_core_route_equals_write_then_decode():
 
 # ------------------------------------------------------------------ host-built work list
 @pytest.mark.parametrize("d,bs,Hq,Hkv,part", [(128, 16, 32, 8, 768), (64, 32, 16, 4, 256), (128, 128, 32, 2, 512),
-                                             (128, 64, 8, 8, 128), (64, 16, 64, 4, 0)])
+                                             (128, 64, 8, 8, 128), (64, 16, 64, 4, 0),
+                                             (128, 16, 32, 8, 48)])  # 3-block partitions of 32-row units
 def test_decode_items_equals_the_grid_decode_bit_exact(d, bs, Hq, Hkv, part):
     """paged_attention_decode_items (the host-built, longest-first list) gives the
     same bits as paged_attention_decode_write / paged_attention_decode, with and
