@@ -32,7 +32,7 @@ length L including its chunk, chunk length c)):
                         L 8192 and 16384, block 16, 32 q / 8 KV heads, d 128
   prefill_short_chunk   one 128-token chunk behind 32,640 cached tokens
                         (L 32768, c 128), block 16, 64 q / 8 KV heads, d 128,
-                        its keys split into 4096-token partitions
+                        its keys split into 8192-token partitions
 """
 from __future__ import annotations
 
@@ -104,11 +104,11 @@ PREFILL_WORKLOADS = {
                                      16, 32, 8, 128, 2003,
                                      extra={"decodes": 256, "len_max": 4096, "chunks": ((8192, 1024), (16384, 1024))}),
     # one short chunk behind a long context: 8 query tiles x 8 KV heads, fewer units
-    # of work than SMs unless the keys are split (partitions of 4096 keys: 4 pairs
-    # of query tiles x 8 KV heads x 8 partitions = 256 items over every SM)
+    # of work than SMs unless the keys are split (partitions of 8192 keys: 4 pairs
+    # of query tiles x 8 KV heads x 4 partitions = 128 items, one per CTA)
     "prefill_short_chunk": PrefillWorkload("prefill_short_chunk", "one 128-token chunk behind a 32,640-token context",
                                            16, 64, 8, 128, 2004,
-                                           extra={"seqs": 1, "len": 32768, "chunk": 128, "split": 4096}),
+                                           extra={"seqs": 1, "len": 32768, "chunk": 128, "split": 8192}),
 }
 
 

@@ -421,14 +421,14 @@ def test_prefill_split_over_keys_matches_the_oracle(d, bs, Hq, Hkv, part):
 def test_prefill_split_of_a_short_chunk_behind_a_long_context():
     """One 128-token chunk behind 32k cached tokens (64 query / 8 KV heads):
     8 query tiles x 8 KV heads = 64 units of work unsplit; split over keys it
-    runs as pairs of query tiles, 4 pairs x 8 KV heads x 16 (or 8) partitions
-    of 2048 (or 4096, the benchmark's) keys.  Sampled tiles match the oracle."""
+    runs as pairs of query tiles, 4 pairs x 8 KV heads x 16, 8 or 4 partitions
+    of 2048, 4096 or 8192 (the benchmark's) keys.  Sampled tiles match the oracle."""
     L, c = 32768, 128
     Hq, Hkv, bs, d = 64, 8, 16, 128
     q, kc, vc, tables, q_start = prefill_case([L], [c], bs, Hq, Hkv, seed=97, d=d)
     scale = float(np.float32(1 / math.sqrt(d)))
     st = status_tensor()
-    for part in (2048, 4096):
+    for part in (2048, 4096, 8192):
         out = run_prefill_split(q, kc, vc, tables, [L], q_start, scale, L, part, status=st)
         assert st.item() == 0
         for lo in (0, 64, 112):  # whole query tiles of 16 tokens
